@@ -1,0 +1,511 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE-layer hot path on GB300.
+
+One step = one full layer (router GEMM -> top-K -> permute -> grouped SwiGLU
+expert GEMM -> weighted combine) over one batch of T tokens, through
+``moe_layer``.  Default workload: the Qwen3-30B-A3B-shaped layer (H=2048,
+E=128, K=8, I=768, bf16 experts, softmax top-8 renormalised) at T=2048 tokens,
+synthetic inputs drawn on the device.  Expert weights are 1.2 GB, so every
+step reads inputs larger than L2 (no flush needed).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead (a bounded token sample per step).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload qwen3_30b_a3b] [--T 2048] [--no-sweep]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+METRIC = "MoE-layer tokens/s (and us/layer) vs T; per-stage fraction of HBM/tensor roofline"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ peaks
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            flat = {}
+
+            def walk(o, pre=""):
+                if isinstance(o, dict):
+                    for k, v in o.items():
+                        walk(v, f"{pre}{k}.")
+                else:
+                    flat[pre[:-1]] = o
+            walk(d)
+            hbm = next((v for k, v in flat.items() if k.endswith("hbm_gbs")), None)
+            bf = next((v for k, v in flat.items() if k.endswith("bf16_tflops")), None)
+            bfs = next((v for k, v in flat.items() if k.endswith("bf16_tflops_sustained")), None)
+            if hbm and bf:
+                return {"hbm_gbs": float(hbm), "bf16_tflops": float(bf),
+                        "bf16_tflops_sustained": float(bfs or bf), "source": "measured"}
+        except Exception as e:  # malformed file: fall back, say so
+            log("MEASURED_PEAKS.json unreadable:", e)
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+def tensors_of(spec, d):
+    t = {"x": d["x"], "wg": d["wg"], "gate_bias": d["gate_bias"], "sel_bias": d["sel_bias"]}
+    if spec.wdtype == "fp8":
+        t.update(w1=d["w1_q"], w3=d["w3_q"], w2=d["w2_q"], s1=d["s1"], s3=d["s3"], s2=d["s2"])
+    else:
+        t.update(w1=d["w1"], w3=d["w3"], w2=d["w2"])
+    if spec.has_shared:
+        t.update(sw1=d["sw1"], sw3=d["sw3"], sw2=d["sw2"])
+    return t
+
+
+def launches_per_layer(spec, dispatch=0):
+    """Kernel launches inside one moe_layer call (mirrors the library's
+    launch sequence): router 1, top-K 1, permute 4 (count, scan, scatter,
+    gather), grouped GEMM 1 plan + 4 GEMM (skinny/tile x G1/G2) or 2 GEMM on
+    the CUDA-core path, combine 1; a shared expert adds one grouped GEMM."""
+    simt = dispatch == 2 or spec.wdtype == "fp8"
+    gemm = 1 + (2 if simt else 4)
+    shared = (1 + (2 if dispatch == 2 else 4)) if spec.has_shared else 0
+    return 1 + 1 + 4 + gemm + shared + 1
+
+
+def stage_bytes_flops(spec, T, ids, e_active):
+    """Algorithmic bytes / flops per stage (each tensor read or written once)."""
+    H, E, K, I, G = spec.H, spec.E, spec.K, spec.I, spec.G
+    R = T * K
+    wb = 1 if spec.wdtype == "fp8" else 2
+    sb = 0
+    if spec.wdtype == "fp8":
+        sb = e_active * 4 * 3 * (-(-I // 128)) * (-(-H // 128))
+    st = {
+        "router": {"bytes": 2 * T * H + 4 * G * H + 4 * T * G, "flops": 2 * T * G * H},
+        "topk": {"bytes": 4 * T * G + 8 * T * K + (4 * E if spec.mode == 1 else 0), "flops": 0},
+        "permute": {"bytes": 2 * T * H + 2 * R * H + 12 * R + 4 * (E + 1), "flops": 0},
+        "grouped_gemm": {"bytes": e_active * 3 * H * I * wb + sb + 4 * R * H + 4 * R * I,
+                         "flops": 6 * R * H * I},
+        "unpermute": {"bytes": 2 * R * H + 2 * T * H + 8 * R + (2 * T * H + 4 * T if spec.has_shared else 0),
+                      "flops": 0},
+    }
+    if spec.has_shared:
+        Is = spec.I_shared
+        st["grouped_gemm"]["bytes"] += 3 * H * Is * 2 + 4 * T * H + 4 * T * Is
+        st["grouped_gemm"]["flops"] += 6 * T * H * Is
+    return st
+
+
+def roofline_of(bytes_, flops, seconds, peaks, sustained=False):
+    bw = peaks["hbm_gbs"] * 1e9
+    tc = (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]) * 1e12
+    t_mem, t_tc = bytes_ / bw, flops / tc
+    if t_mem >= t_tc:
+        ach = bytes_ / seconds / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"]}
+    ach = flops / seconds / 1e12
+    pk = tc / 1e12
+    return {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s", "frac": ach / pk}
+
+
+def traffic_record(kernel_file):
+    """Per-launch DRAM traffic from a committed ncu summary, only while the
+    kernel source is unchanged since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        rec = json.load(open(p))
+        src = open(os.path.join(ROOT, "mixture_experts_layer_07_gb300", "csrc", kernel_file), "rb").read()
+        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return rec.get("traffic_bytes_per_step")
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    from mixture_experts_layer_07_gb300 import ops, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks = load_peaks()
+    spec = synth.SPECS[args.workload]
+    T = args.T
+    d = synth.device_inputs(spec, T, seed=rank, device=f"cuda:{local_rank}")
+    t = tensors_of(spec, d)
+    cfg = ops.make_config(T, spec.H, spec.E, spec.K, spec.I, has_shared=spec.has_shared,
+                          I_shared=spec.I_shared, mode=spec.mode, routed_scale=spec.routed_scale,
+                          wdtype=ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16)
+    layer = ops.MoELayer(cfg, t, device=dev)
+    x = d["x"]
+    out = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- device-resident timed region
+    for _ in range(args.warmup):
+        layer(x, out)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        layer(x, out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    st = int(layer.dev_status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+    ms_step = ms / args.steps
+
+    # ---- per-stage times (same workspace, stages called one by one)
+    L = layer.layout
+    ws = layer.workspace
+    E, K, H, I, G = spec.E, spec.K, spec.H, spec.I, spec.G
+    R = T * K
+
+    def v(name, dtype, shape):
+        return layer.view(name, dtype, shape)
+
+    logits = v("logits", torch.float32, (T, G))
+    ids = v("ids", torch.int32, (T, K))
+    wts = v("weights", torch.float32, (T, K))
+    gsh = v("shared_gate", torch.float32, (T,)) if spec.has_shared else None
+    off = v("offsets", torch.int32, (E + 1,))
+    r2f = v("row_to_flat", torch.int32, (R,))
+    f2r = v("flat_to_row", torch.int32, (R,))
+    xp = v("xp", torch.bfloat16, (R, H))
+    hact = v("hact", torch.bfloat16, (R, I))
+    y = v("y", torch.bfloat16, (R, H))
+    pscr = ws[L.permute_scratch:L.gemm_scratch]
+    gscr = ws[L.gemm_scratch:L.shared_gemm_scratch]
+    sh_scr = ws[L.shared_gemm_scratch:L.total]
+    sh_h = v("shared_hact", torch.bfloat16, (T, spec.I_shared)) if spec.has_shared else None
+    sh_y = v("shared_y", torch.bfloat16, (T, H)) if spec.has_shared else None
+    wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
+    names = ["router", "topk", "permute", "grouped_gemm", "unpermute"]
+
+    def stages():
+        yield lambda: ops.router_gemm(x, t["wg"], t["gate_bias"], logits)
+        yield lambda: ops.topk_route(logits, E, K, spec.mode, spec.routed_scale, ids, wts,
+                                     t["sel_bias"], gsh)
+        yield lambda: ops.permute(x, ids, E, off, r2f, f2r, xp, pscr, layer.dev_status)
+
+        def gg():
+            ops.grouped_gemm(xp, off, E, H, I, t["w1"], t["w3"], t["w2"], hact, y, gscr, wdtype=wd,
+                             s1=t.get("s1"), s3=t.get("s3"), s2=t.get("s2"),
+                             dev_status=layer.dev_status)
+            if spec.has_shared:
+                ops.grouped_gemm(x, None, 1, H, spec.I_shared, t["sw1"], t["sw3"], t["sw2"], sh_h,
+                                 sh_y, sh_scr, dev_status=layer.dev_status)
+        yield gg
+        yield lambda: ops.unpermute(y, f2r, wts, T, K, H, out, sh_y, gsh)
+
+    n_stage_steps = max(3, min(args.steps, 20))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_stage_steps)]
+    for s in range(n_stage_steps + 2):
+        rec = s >= 2
+        if rec:
+            evs[s - 2][0].record(stream)
+        for i, fn in enumerate(stages()):
+            fn()
+            if rec:
+                evs[s - 2][i + 1].record(stream)
+    torch.cuda.synchronize()
+    stage_ms = {n: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i, n in enumerate(names)}
+    ids_h = ids.cpu().numpy()
+    e_active = int(len(np.unique(ids_h)))
+    sbf = stage_bytes_flops(spec, T, ids_h, e_active)
+    per_stage = {}
+    for n in names:
+        r = roofline_of(sbf[n]["bytes"], sbf[n]["flops"], stage_ms[n] / 1e3, peaks)
+        per_stage[n] = {"us": round(stage_ms[n] * 1e3, 2), "bound": r["bound"],
+                        "frac": round(r["frac"], 4)}
+    dom = max(names, key=lambda n: stage_ms[n])
+    roof = roofline_of(sbf[dom]["bytes"], sbf[dom]["flops"], stage_ms[dom] / 1e3, peaks)
+    roof = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()}
+    roof["kernel"] = dom
+    roof["peak_source"] = f"of {peaks['source']}"
+    roof["traffic"] = traffic_record("grouped_gemm.cu") if dom == "grouped_gemm" else None
+
+    # ---- end to end through the C ABI with host buffers
+    x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_host.copy_(x)
+    out_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_dev = torch.empty_like(x)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        layer(x_dev, out)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    # ---- T sweep (rank 0 only, short)
+    sweep = None
+    if rank == 0 and args.sweep:
+        sweep = []
+        for Ts in spec.T_sweep:
+            if Ts > T:
+                continue
+            xs = x[:Ts]
+            os_ = out[:Ts]
+            for _ in range(3):
+                layer(xs, os_)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n = 20
+            a.record(stream)
+            for _ in range(n):
+                layer(xs, os_)
+            b.record(stream)
+            torch.cuda.synchronize()
+            us = a.elapsed_time(b) / n * 1e3
+            sweep.append({"T": Ts, "us_per_layer": round(us, 2), "tokens_per_s": round(Ts / us * 1e6, 1)})
+
+    # ---- CPU baseline (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(spec, T, args.cpu_tokens)
+
+    tokens = T * args.steps * world
+    res = {
+        "metric": METRIC,
+        "value": round(tokens / (ms / 1e3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "us_per_layer": round(ms_step * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if spec.wdtype == "bf16" else "bf16 activations, fp8-e4m3 weights",
+        "data": "synthetic (seeded; random-init weights of the named layer shape)",
+        "config": {"workload": f"{spec.name} MoE layer", "T": T, "H": spec.H, "E": spec.E,
+                   "K": spec.K, "I": spec.I, "routing": "softmax top-K renormalised"
+                   if spec.mode == 0 else "sigmoid+bias top-K, scaled-sum", "tokens_per_gpu": T,
+                   "parallelism": f"token-dp replicas x{world}",
+                   "l2": "inputs larger than L2 (expert weights "
+                         f"{spec.E * 3 * spec.H * spec.I * (1 if spec.wdtype == 'fp8' else 2) / 1e9:.2f} GB "
+                         "per layer), no flush"},
+        "roofline": roof,
+        "per_stage": per_stage,
+        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": out.numel() * out.element_size()},
+        "gpu_launches": launches_per_layer(spec) * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    if sweep is not None:
+        res["sweep"] = sweep
+    return res
+
+
+# ------------------------------------------------------------------ oracle arm
+def oracle_sample_time(spec, T_sample, seed=0):
+    """Time the CPU oracle on T_sample tokens of the workload (host draw)."""
+    import oracle
+    from mixture_experts_layer_07_gb300 import synth
+
+    base = synth.host_inputs(spec, T_sample, seed=seed, weights=False)
+    x = oracle.bf16_to_f64(base["x_bits"])
+    lg = oracle.router_logits(x, base["wg"], base["gate_bias"])
+    if spec.mode == 0:
+        ids, _ = oracle.topk_softmax_renorm(lg, spec.E, spec.K)
+    else:
+        ids, _ = oracle.topk_sigmoid_bias(lg.astype(np.float32), base["sel_bias"], spec.E, spec.K,
+                                          spec.routed_scale)
+    inp = synth.host_inputs(spec, T_sample, seed=seed, experts=sorted(set(ids.ravel().tolist())))
+    t0 = time.perf_counter()
+    oracle.moe_layer_from_inputs(inp)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(spec, T, tokens):
+    cores = len(os.sched_getaffinity(0))
+    sec = oracle_sample_time(spec, tokens)
+    return {"value": round(tokens / sec, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{tokens} tokens of the {spec.name} T={T} workload (same shapes, host draw), "
+                      f"float64 numpy oracle, one pass, {sec:.1f} s"}
+
+
+def run_reference(args):
+    from mixture_experts_layer_07_gb300 import synth
+
+    spec = synth.SPECS[args.workload]
+    cores = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup):
+        oracle_sample_time(spec, max(1, args.cpu_tokens // 4), seed=1)
+    total = 0.0
+    for s in range(args.steps):
+        total += oracle_sample_time(spec, args.cpu_tokens, seed=2 + s)
+    tokens = args.cpu_tokens * args.steps
+    val = tokens / total
+    sample = (f"{args.cpu_tokens} tokens per step of the {spec.name} T={args.T} workload "
+              f"(float64 numpy oracle on the host cores)")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(val, 3),
+        "unit": "tokens/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"{spec.name} MoE layer", "T": args.T, "H": spec.H, "E": spec.E,
+                   "K": spec.K, "I": spec.I},
+        "cpu_baseline": {"value": round(val, 3), "unit": "tokens/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(val, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_30b_a3b")
+    ap.add_argument("--T", type=int, default=2048)
+    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        res = run_ours(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

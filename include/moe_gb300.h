@@ -1,0 +1,282 @@
+/*
+ * moe_gb300.h -- C ABI of the GB300 (sm_103a) MoE-layer hot path.
+ *
+ *   router GEMM -> top-K routing -> permute -> grouped SwiGLU expert GEMM
+ *   -> weighted unpermute / combine
+ *
+ * Pages the operations come from (titles shortened):
+ *   [dispatch] "vLLM CPU MoE: dynamic GEMM dispatch beyond a fixed threshold"
+ *              (vllm PR #50949), sections "1. gemm.h", "2. moe_fp8.cpp"
+ *   [router]   "vLLM MiniMax-M2 MoE gate optimisation: fused FP32 kernel"
+ *              (vllm PR #38445), sections "1. Python layer", "2. CUDA kernel"
+ *   [shared]   "vLLM fused shared-expert gate GEMM path on ROCm"
+ *              (vllm PR #54185), section "code analysis"
+ *   [permute]  "vLLM MoE permute optimisation: buffer pre-allocation"
+ *              (vllm PR #43014), sections "1. C++ kernel level", "2. Python layer"
+ *   [routing]  "FlashInfer MoE routing optimisation" (flashinfer PR #4152),
+ *              sections "1. routing_custom.cu", "2. routing_common.cu"
+ *
+ * Conventions for every entry point:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  Inputs are
+ *     const and never written.  The library never allocates device memory,
+ *     never frees, never synchronises: all work is queued on `stream`
+ *     (a cudaStream_t; NULL = legacy default stream).  Caller scratch and
+ *     workspace follow [permute] "1. C++ kernel level": buffers are allocated
+ *     once by the caller and reused on every call.
+ *   - Layouts are dense row-major with the last index contiguous.
+ *   - bf16 tensors are IEEE bfloat16; FP8 weights are OCP e4m3 ("fn") codes
+ *     with one fp32 scale per 128 x 128 block (the last block of a dimension
+ *     may be narrower); scales are laid out [E][ceil(rows/128)][ceil(cols/128)].
+ *   - Errors found on the host (null pointer, bad size, misalignment, short
+ *     scratch) return a status != MOE_OK before anything is queued.  A failed
+ *     launch returns MOE_ERR_CUDA.  Errors found by a kernel (an expert id out
+ *     of range, a bounded wait that ran out) are written to *dev_status, a
+ *     device int32 the caller zeroes; the first error written wins.  The
+ *     caller reads it whenever it chooses.
+ *   - Alignment: bf16 activation/weight pointers 16-byte aligned, fp32 and
+ *     int32 pointers 4-byte aligned, scratch/workspace 256-byte aligned.
+ *   - Sizes: 1 <= K <= E <= 1024, H % 16 == 0, I % 16 == 0, T >= 0
+ *     (T == 0 is a no-op that returns MOE_OK).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, size out of range */
+  MOE_ERR_UNSUPPORTED = 2,   /* combination the kernels do not implement */
+  MOE_ERR_WORKSPACE = 3,     /* scratch / workspace too small */
+  MOE_ERR_MISALIGNED = 4,    /* pointer alignment rule broken */
+  MOE_ERR_CUDA = 5,          /* a CUDA call or launch failed */
+  MOE_ERR_DEVICE_STATUS = 6  /* reserved for callers that fold *dev_status in */
+} moe_status_t;
+
+/* codes a kernel writes to *dev_status */
+#define MOE_DEV_OK 0
+#define MOE_DEV_BAD_EXPERT_ID 1  /* permute saw an id outside [0, E) */
+#define MOE_DEV_WAIT_TIMEOUT 2   /* a bounded wait inside the expert GEMM ran out */
+
+typedef enum {
+  MOE_SCORE_SOFTMAX_RENORM = 0,      /* softmax over E, top-K, weights sum to 1 */
+  MOE_SCORE_SIGMOID_BIAS_SCALED = 1  /* key sigmoid(l)+bias, weights scale*s/sum s */
+} moe_score_mode_t;
+
+typedef enum {
+  MOE_W_BF16 = 0,         /* expert weights bf16 */
+  MOE_W_FP8E4M3_B128 = 1  /* expert weights e4m3 + fp32 128x128 block scales */
+} moe_wdtype_t;
+
+/* How the grouped GEMM picks a kernel variant for each expert block. */
+typedef enum {
+  MOE_DISPATCH_PER_BLOCK = 0,  /* from the block's own m_size ([dispatch] after) */
+  MOE_DISPATCH_GLOBAL_AVG = 1, /* from max(1, R/E) for every block ([dispatch] before) */
+  MOE_DISPATCH_SIMT = 2        /* every block on the CUDA-core kernel (cross-check) */
+} moe_dispatch_t;
+
+/* Variant codes reported per expert block. */
+#define MOE_VARIANT_SKIP 0    /* m_size == 0: no work */
+#define MOE_VARIANT_SKINNY 1  /* small block: narrow token tile */
+#define MOE_VARIANT_TILE 2    /* large block: wide tensor-core tile */
+#define MOE_VARIANT_SIMT 3    /* CUDA-core kernel (MOE_DISPATCH_SIMT) */
+
+typedef struct {
+  int T_max;           /* largest T the workspace must hold */
+  int H;               /* hidden size */
+  int E;               /* routed experts */
+  int K;               /* experts per token */
+  int I;               /* routed expert intermediate size */
+  int has_shared;      /* 1: gate has E+1 rows, row E gates a shared expert */
+  int I_shared;        /* shared expert intermediate size (has_shared) */
+  int mode;            /* moe_score_mode_t */
+  float routed_scale;  /* ScaledSumNormalize factor (mode 1); ignored in mode 0 */
+  int wdtype;          /* moe_wdtype_t of the routed experts */
+  int m_skinny;        /* blocks with m_size <= m_skinny use the skinny variant;
+                          -1 = library default (moe_default_m_skinny()) */
+  int dispatch;        /* moe_dispatch_t */
+} moe_config_t;
+
+typedef struct {
+  const float* wg;         /* [G, H] fp32 gate weight, G = E + has_shared */
+  const float* gate_bias;  /* [G] fp32 added to the logits, or NULL */
+  const float* sel_bias;   /* [E] fp32 selection bias (mode 1), or NULL = 0 */
+  const void* w1;          /* [E, I, H] gate projection (bf16 or e4m3) */
+  const void* w3;          /* [E, I, H] up projection */
+  const void* w2;          /* [E, H, I] down projection */
+  const float* s1;         /* FP8 block scales of w1 / w3 / w2, else NULL */
+  const float* s3;
+  const float* s2;
+  const void* sw1;         /* shared expert bf16 [I_shared, H], or NULL */
+  const void* sw3;         /* [I_shared, H] */
+  const void* sw2;         /* [H, I_shared] */
+} moe_weights_t;
+
+/* Text for a status code (static storage). */
+const char* moe_status_string(moe_status_t status);
+
+/* Default skinny/tile threshold on m_size used when m_skinny == -1. */
+int moe_default_m_skinny(void);
+
+/*
+ * Variant a block of m_size rows takes, as the grouped GEMM decides it on the
+ * device ([dispatch] "2. moe_fp8.cpp": m_size = offsets[e+1] - offsets[e], a
+ * block with m_size == 0 returns at once, the kernel is chosen per block;
+ * "1. gemm.h": the large-tile kernel is used above a small-M threshold).
+ * R = total rows, E = number of blocks (used by MOE_DISPATCH_GLOBAL_AVG, which
+ * decides from max(1, R / E) for every non-empty block).  Host-callable copy
+ * of the device predicate; returns a MOE_VARIANT_* code.
+ */
+int moe_block_variant(int64_t m_size, int64_t R, int E, int m_skinny, int dispatch);
+
+/*
+ * R: router (gate) GEMM.   logits[t, g] = sum_h fp32(x[t, h]) * wg[g, h] (+ gate_bias[g])
+ * [router] "2. CUDA kernel": bf16 activations are loaded 8 at a time (16 bytes)
+ * and widened to fp32 in registers, so no fp32 copy of x is written; the
+ * products accumulate in fp32 on the CUDA cores.  [shared] "code analysis":
+ * with a fused shared-expert gate, G = E + 1.
+ *   x         [T, H] bf16, 16-byte aligned, H % 8 == 0
+ *   wg        [G, H] fp32 (nn.Linear layout), 16-byte aligned
+ *   gate_bias [G] fp32 or NULL
+ *   logits    [T, G] fp32 output
+ * Deterministic: the summation order depends only on (T, H, G).
+ */
+moe_status_t moe_router_gemm(const void* x, const float* wg, const float* gate_bias,
+                             float* logits, int T, int H, int G, moe_stream_t stream);
+
+/*
+ * K: top-K routing, one warp per token.  [routing] "1. routing_custom.cu":
+ * every lane keeps its own sorted top-K candidates (from the experts it
+ * reads) and the warp merges the lane heads K times with shuffles; "2.
+ * routing_common.cu": E = 896 has its own tier (28 experts per lane) instead
+ * of running as 1024.
+ *   mode MOE_SCORE_SOFTMAX_RENORM: select the K largest logits among columns
+ *     [0, E); weights = softmax over the selected logits (sum 1).
+ *   mode MOE_SCORE_SIGMOID_BIAS_SCALED: s = sigmoid(l) in a fixed float32
+ *     formula (Cody-Waite exp + degree-7 Taylor, each step one correctly
+ *     rounded operation), key = s + sel_bias[e]; select the K largest keys;
+ *     weights = scale * s / sum_selected s.
+ *   Equal keys: the lower expert index wins.  Outputs are in selection order
+ *   (key descending).
+ *   logits       [T, ld_logits] fp32, ld_logits >= E
+ *   sel_bias     [E] fp32 or NULL (mode 1 only)
+ *   ids          [T, K] int32 output;  weights [T, K] fp32 output
+ *   shared_gate  [T] fp32 output sigmoid(logits[t, E]) or NULL (needs
+ *                ld_logits >= E + 1)
+ */
+moe_status_t moe_topk_route(const float* logits, int ld_logits, const float* sel_bias,
+                            int T, int E, int K, int mode, float scale,
+                            int32_t* ids, float* weights, float* shared_gate,
+                            moe_stream_t stream);
+
+/* Scratch bytes moe_permute needs for (T, E, K). */
+moe_status_t moe_permute_scratch_bytes(int T, int E, int K, size_t* bytes);
+
+/*
+ * P: permute.  Replica f = t*K + k of token t, routed to expert e = ids[f],
+ * goes to row offsets[e] + (number of replicas f' < f routed to e): a stable
+ * counting sort ([permute] "1. C++ kernel level" permutes the replicas into
+ * expert order; [dispatch] "2. moe_fp8.cpp" reads each block's size as
+ * offsets[e+1] - offsets[e]).  Done as a per-chunk histogram, a scan and a
+ * stable scatter (warp match + popcount), then a row gather.
+ *   x            [T, H] bf16 (may be NULL when xp is NULL)
+ *   ids          [T, K] int32 in [0, E); an id outside it sets
+ *                MOE_DEV_BAD_EXPERT_ID and that replica is dropped
+ *                (flat_to_row = -1)
+ *   offsets      [E + 1] int32 output, offsets[0] = 0
+ *   row_to_flat  [T*K] int32 output;  flat_to_row [T*K] int32 output
+ *   xp           [T*K, H] bf16 output, xp[row] = x[row_to_flat[row] / K];
+ *                NULL skips the gather
+ *   scratch      >= moe_permute_scratch_bytes(T, E, K) bytes, 256-byte aligned
+ */
+moe_status_t moe_permute(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                         int32_t* offsets, int32_t* row_to_flat, int32_t* flat_to_row,
+                         void* xp, void* scratch, size_t scratch_bytes,
+                         int32_t* dev_status, moe_stream_t stream);
+
+/* Scratch bytes moe_grouped_gemm needs for R rows in E_blocks blocks. */
+moe_status_t moe_grouped_gemm_scratch_bytes(int R, int E_blocks, size_t* bytes);
+
+/*
+ * G1 + G2: grouped SwiGLU expert GEMM over expert-contiguous row blocks.
+ *   for every block e with m_e = offsets[e+1] - offsets[e] > 0, rows r in it:
+ *     hact[r] = bf16( silu(xp[r] . W1[e]^T) * (xp[r] . W3[e]^T) )   (fp32 accumulate)
+ *     y[r]    = bf16( hact[r] . W2[e]^T )
+ * The kernel variant is chosen on the device for each block from its own m_e
+ * (moe_block_variant), never from a global average unless dispatch asks for
+ * it ([dispatch] "2. moe_fp8.cpp").  Both variants run tcgen05 tensor-core
+ * MMAs fed by TMA with TMEM accumulators: the skinny variant uses a 16-row
+ * token tile, the tile variant a 128-row token tile.
+ *   xp        [R, H] bf16, 16-byte aligned
+ *   offsets   [E_blocks + 1] int32 (device), or NULL for one block [0, R)
+ *   w1, w3    [E_blocks, I, H]; w2 [E_blocks, H, I]; bf16 or e4m3 per wdtype
+ *   s1, s3    [E_blocks, ceil(I/128), ceil(H/128)] fp32; s2 [E_blocks, ceil(H/128), ceil(I/128)]
+ *             (wdtype MOE_W_FP8E4M3_B128 only, else NULL)
+ *   hact      [R, I] bf16 output;  y [R, H] bf16 output (rows outside every
+ *             block are left untouched)
+ *   block_variant  [E_blocks] int32 output of MOE_VARIANT_* codes, or NULL
+ *   scratch   >= moe_grouped_gemm_scratch_bytes(R, E_blocks), 256-byte aligned
+ */
+moe_status_t moe_grouped_gemm(const void* xp, const int32_t* offsets, int E_blocks, int R,
+                              int H, int I, int wdtype,
+                              const void* w1, const void* w3, const void* w2,
+                              const float* s1, const float* s3, const float* s2,
+                              void* hact, void* y, int m_skinny, int dispatch,
+                              int32_t* block_variant, void* scratch, size_t scratch_bytes,
+                              int32_t* dev_status, moe_stream_t stream);
+
+/*
+ * U: weighted unpermute / combine ([permute] introduction: the inverse of
+ * permute that returns expert outputs to token order and combines them).
+ *   out[t] = bf16( sum_{k=0..K-1} weights[t,k] * y[flat_to_row[t*K+k]]
+ *                  + shared_gate[t] * shared_y[t] )
+ *   summed in fp32 in k order, one rounding to bf16 at the end.  A replica
+ *   with flat_to_row < 0 contributes nothing.
+ *   y [T*K, H] bf16; flat_to_row [T*K] int32; weights [T, K] fp32
+ *   shared_y [T, H] bf16 and shared_gate [T] fp32: both or neither (NULL)
+ *   out [T, H] bf16 output
+ */
+moe_status_t moe_unpermute(const void* y, const int32_t* flat_to_row, const float* weights,
+                           int T, int K, int H, const void* shared_y,
+                           const float* shared_gate, void* out, moe_stream_t stream);
+
+/* Workspace bytes moe_layer needs for cfg (sized for cfg->T_max). */
+moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes);
+
+/*
+ * The whole layer on one stream, no host synchronisation:
+ *   R -> K -> P -> G1/G2 (+ shared expert) -> U.
+ *   x    [T, H] bf16 input, out [T, H] bf16 output, T <= cfg->T_max
+ *   workspace  >= moe_workspace_bytes(cfg), 256-byte aligned; holds every
+ *              intermediate (logits, ids, weights, offsets, permuted rows,
+ *              expert activations and outputs, plans)
+ */
+moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_weights_t* w,
+                       void* out, void* workspace, size_t workspace_bytes,
+                       int32_t* dev_status, moe_stream_t stream);
+
+/*
+ * Byte offsets of the intermediates inside a moe_layer workspace, for callers
+ * that inspect them (tests, profilers).  Filled for cfg and T_max.
+ */
+typedef struct {
+  size_t logits, ids, weights, shared_gate, offsets, row_to_flat, flat_to_row,
+      xp, hact, y, shared_hact, shared_y, block_variant, permute_scratch, gemm_scratch,
+      shared_gemm_scratch, total;
+} moe_workspace_layout_t;
+
+moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_workspace_layout_t* layout);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

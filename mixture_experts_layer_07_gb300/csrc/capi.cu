@@ -1,0 +1,264 @@
+// C ABI of the MoE-layer library: argument checks, workspace layout, launches.
+// Every entry point validates on the host first (nothing is queued when a
+// check fails), then queues kernels on the caller's stream and returns.  No
+// allocation, no synchronisation -- the caller-scratch convention of "vLLM MoE
+// permute optimisation: buffer pre-allocation" (vllm PR #43014), "1. C++
+// kernel level": scratch is allocated once by the owner and reused, and each
+// reused buffer's size is checked before use.
+#include <stdio.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+bool misaligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status_t check_dims(int T, int H, int E, int K) {
+  if (T < 0 || H <= 0 || E <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (H % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (E > 1024 || K > E || K > 32) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t check_cfg(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  moe_status_t s = check_dims(c->T_max, c->H, c->E, c->K);
+  if (s != MOE_OK) return s;
+  if (c->I <= 0 || c->I % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->mode != MOE_SCORE_SOFTMAX_RENORM && c->mode != MOE_SCORE_SIGMOID_BIAS_SCALED)
+    return MOE_ERR_INVALID_ARG;
+  if (c->wdtype != MOE_W_BF16 && c->wdtype != MOE_W_FP8E4M3_B128) return MOE_ERR_UNSUPPORTED;
+  if (c->dispatch < MOE_DISPATCH_PER_BLOCK || c->dispatch > MOE_DISPATCH_SIMT)
+    return MOE_ERR_INVALID_ARG;
+  if (c->m_skinny < -1) return MOE_ERR_INVALID_ARG;
+  if (c->has_shared && (c->I_shared <= 0 || c->I_shared % 16 != 0)) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)c->T_max * c->K > 0x7fffffff / 2) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+void layout_of(const moe_config_t* c, moe_workspace_layout_t* L) {
+  const int G = c->E + (c->has_shared ? 1 : 0);
+  const size_t Tm = (size_t)c->T_max, R = Tm * c->K;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = moe_align_up(off + bytes, 256);
+    return o;
+  };
+  L->logits = take(Tm * G * 4);
+  L->ids = take(R * 4);
+  L->weights = take(R * 4);
+  L->shared_gate = take(Tm * 4);
+  L->offsets = take((size_t)(c->E + 1) * 4);
+  L->row_to_flat = take(R * 4);
+  L->flat_to_row = take(R * 4);
+  L->xp = take(R * c->H * 2);
+  L->hact = take(R * c->I * 2);
+  L->y = take(R * c->H * 2);
+  L->shared_hact = take(c->has_shared ? Tm * c->I_shared * 2 : 0);
+  L->shared_y = take(c->has_shared ? Tm * c->H * 2 : 0);
+  L->block_variant = take((size_t)c->E * 4);
+  L->permute_scratch = take(permute_scratch_bytes(c->T_max, c->E, c->K));
+  L->gemm_scratch = take(grouped_gemm_scratch_bytes((int)R, c->E));
+  L->shared_gemm_scratch = take(c->has_shared ? grouped_gemm_scratch_bytes(c->T_max, 1) : 0);
+  L->total = off;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported combination";
+    case MOE_ERR_WORKSPACE: return "scratch or workspace too small";
+    case MOE_ERR_MISALIGNED: return "misaligned pointer";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_STATUS: return "device status error";
+  }
+  return "unknown status";
+}
+
+int moe_default_m_skinny(void) { return MOE_DEFAULT_M_SKINNY; }
+
+int moe_block_variant(int64_t m_size, int64_t R, int E, int m_skinny, int dispatch) {
+  if (m_skinny < 0) m_skinny = MOE_DEFAULT_M_SKINNY;
+  return moe_variant_of(m_size, R, E, m_skinny, dispatch);
+}
+
+moe_status_t moe_router_gemm(const void* x, const float* wg, const float* gate_bias,
+                             float* logits, int T, int H, int G, moe_stream_t stream) {
+  if (T < 0 || H <= 0 || G <= 0 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !wg || !logits) return MOE_ERR_INVALID_ARG;
+  if (misaligned(x, 16) || misaligned(wg, 16) || misaligned(logits, 4) ||
+      (gate_bias && misaligned(gate_bias, 4)))
+    return MOE_ERR_MISALIGNED;
+  return cuda_status(launch_router_gemm(x, wg, gate_bias, logits, T, H, G, stream));
+}
+
+moe_status_t moe_topk_route(const float* logits, int ld_logits, const float* sel_bias, int T,
+                            int E, int K, int mode, float scale, int32_t* ids, float* weights,
+                            float* shared_gate, moe_stream_t stream) {
+  if (T < 0 || E <= 0 || E > 1024 || K <= 0 || K > E || K > 32) return MOE_ERR_INVALID_ARG;
+  if (ld_logits < E || (shared_gate && ld_logits < E + 1)) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_SCORE_SOFTMAX_RENORM && mode != MOE_SCORE_SIGMOID_BIAS_SCALED)
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!logits || !ids || !weights) return MOE_ERR_INVALID_ARG;
+  if (misaligned(logits, 4) || misaligned(ids, 4) || misaligned(weights, 4) ||
+      (sel_bias && misaligned(sel_bias, 4)) || (shared_gate && misaligned(shared_gate, 4)))
+    return MOE_ERR_MISALIGNED;
+  return cuda_status(launch_topk_route(logits, ld_logits, sel_bias, T, E, K, mode, scale, ids,
+                                       weights, shared_gate, stream));
+}
+
+moe_status_t moe_permute_scratch_bytes(int T, int E, int K, size_t* bytes) {
+  if (!bytes || T < 0 || E <= 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  *bytes = permute_scratch_bytes(T, E, K);
+  return MOE_OK;
+}
+
+moe_status_t moe_permute(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                         int32_t* offsets, int32_t* row_to_flat, int32_t* flat_to_row, void* xp,
+                         void* scratch, size_t scratch_bytes, int32_t* dev_status,
+                         moe_stream_t stream) {
+  moe_status_t s = check_dims(T, H, E, K);
+  if (s != MOE_OK) return s;
+  if (!offsets || !scratch) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!ids || !row_to_flat || !flat_to_row || (xp && !x))) return MOE_ERR_INVALID_ARG;
+  if (scratch_bytes < permute_scratch_bytes(T, E, K)) return MOE_ERR_WORKSPACE;
+  if (misaligned(scratch, 256) || misaligned(offsets, 4) || (ids && misaligned(ids, 4)) ||
+      (row_to_flat && misaligned(row_to_flat, 4)) || (flat_to_row && misaligned(flat_to_row, 4)) ||
+      (xp && (misaligned(xp, 16) || misaligned(x, 16))))
+    return MOE_ERR_MISALIGNED;
+  return cuda_status(launch_permute(x, ids, T, H, E, K, offsets, row_to_flat, flat_to_row, xp,
+                                    scratch, dev_status, stream));
+}
+
+moe_status_t moe_grouped_gemm_scratch_bytes(int R, int E_blocks, size_t* bytes) {
+  if (!bytes || R < 0 || E_blocks <= 0) return MOE_ERR_INVALID_ARG;
+  *bytes = grouped_gemm_scratch_bytes(R, E_blocks);
+  return MOE_OK;
+}
+
+moe_status_t moe_grouped_gemm(const void* xp, const int32_t* offsets, int E_blocks, int R, int H,
+                              int I, int wdtype, const void* w1, const void* w3, const void* w2,
+                              const float* s1, const float* s3, const float* s2, void* hact,
+                              void* y, int m_skinny, int dispatch, int32_t* block_variant,
+                              void* scratch, size_t scratch_bytes, int32_t* dev_status,
+                              moe_stream_t stream) {
+  if (E_blocks <= 0 || R < 0 || m_skinny < -1) return MOE_ERR_INVALID_ARG;
+  if (dispatch < MOE_DISPATCH_PER_BLOCK || dispatch > MOE_DISPATCH_SIMT) return MOE_ERR_INVALID_ARG;
+  const int chk = grouped_gemm_check(H, I, wdtype);
+  if (chk != MOE_OK) return (moe_status_t)chk;
+  if (!w1 || !w3 || !w2 || !scratch) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!xp || !hact || !y)) return MOE_ERR_INVALID_ARG;
+  if (wdtype == MOE_W_FP8E4M3_B128 && (!s1 || !s3 || !s2)) return MOE_ERR_INVALID_ARG;
+  if (scratch_bytes < grouped_gemm_scratch_bytes(R, E_blocks)) return MOE_ERR_WORKSPACE;
+  if (misaligned(scratch, 256) || misaligned(w1, 16) || misaligned(w3, 16) || misaligned(w2, 16) ||
+      (xp && misaligned(xp, 16)) || (hact && misaligned(hact, 16)) || (y && misaligned(y, 16)) ||
+      (offsets && misaligned(offsets, 4)) || (block_variant && misaligned(block_variant, 4)))
+    return MOE_ERR_MISALIGNED;
+  return cuda_status(launch_grouped_gemm(xp, offsets, E_blocks, R, H, I, wdtype, w1, w3, w2, s1,
+                                         s3, s2, hact, y, m_skinny, dispatch, block_variant,
+                                         scratch, dev_status, stream));
+}
+
+moe_status_t moe_unpermute(const void* y, const int32_t* flat_to_row, const float* weights, int T,
+                           int K, int H, const void* shared_y, const float* shared_gate,
+                           void* out, moe_stream_t stream) {
+  if (T < 0 || K <= 0 || H <= 0 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if ((shared_y == nullptr) != (shared_gate == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!y || !flat_to_row || !weights || !out) return MOE_ERR_INVALID_ARG;
+  if (misaligned(y, 16) || misaligned(out, 16) || misaligned(flat_to_row, 4) ||
+      misaligned(weights, 4) || (shared_y && (misaligned(shared_y, 16) || misaligned(shared_gate, 4))))
+    return MOE_ERR_MISALIGNED;
+  return cuda_status(
+      launch_unpermute(y, flat_to_row, weights, T, K, H, shared_y, shared_gate, out, stream));
+}
+
+moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_workspace_layout_t* layout) {
+  const moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!layout) return MOE_ERR_INVALID_ARG;
+  layout_of(cfg, layout);
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  moe_workspace_layout_t L;
+  const moe_status_t s = moe_workspace_layout(cfg, &L);
+  if (s != MOE_OK) return s;
+  *bytes = L.total;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_weights_t* w,
+                       void* out, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                       moe_stream_t stream) {
+  moe_status_t s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (T < 0 || T > cfg->T_max) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w || !out || !workspace || !w->wg || !w->w1 || !w->w3 || !w->w2)
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->wdtype == MOE_W_FP8E4M3_B128 && (!w->s1 || !w->s3 || !w->s2)) return MOE_ERR_INVALID_ARG;
+  if (cfg->has_shared && (!w->sw1 || !w->sw3 || !w->sw2)) return MOE_ERR_INVALID_ARG;
+  moe_workspace_layout_t L;
+  layout_of(cfg, &L);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (misaligned(workspace, 256) || misaligned(x, 16) || misaligned(out, 16) ||
+      misaligned(w->wg, 16) || misaligned(w->w1, 16) || misaligned(w->w3, 16) ||
+      misaligned(w->w2, 16) ||
+      (cfg->has_shared && (misaligned(w->sw1, 16) || misaligned(w->sw3, 16) || misaligned(w->sw2, 16))))
+    return MOE_ERR_MISALIGNED;
+
+  char* ws = static_cast<char*>(workspace);
+  float* logits = reinterpret_cast<float*>(ws + L.logits);
+  int32_t* ids = reinterpret_cast<int32_t*>(ws + L.ids);
+  float* wts = reinterpret_cast<float*>(ws + L.weights);
+  float* gsh = reinterpret_cast<float*>(ws + L.shared_gate);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* r2f = reinterpret_cast<int32_t*>(ws + L.row_to_flat);
+  int32_t* f2r = reinterpret_cast<int32_t*>(ws + L.flat_to_row);
+  void* xp = ws + L.xp;
+  void* hact = ws + L.hact;
+  void* y = ws + L.y;
+  const int E = cfg->E, K = cfg->K, H = cfg->H;
+  const int G = E + (cfg->has_shared ? 1 : 0);
+  const int R = T * K;
+
+  cudaError_t e = launch_router_gemm(x, w->wg, w->gate_bias, logits, T, H, G, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_topk_route(logits, G, w->sel_bias, T, E, K, cfg->mode, cfg->routed_scale, ids, wts,
+                        cfg->has_shared ? gsh : nullptr, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_permute(x, ids, T, H, E, K, offsets, r2f, f2r, xp, ws + L.permute_scratch, dev_status,
+                     stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_grouped_gemm(xp, offsets, E, R, H, cfg->I, cfg->wdtype, w->w1, w->w3, w->w2, w->s1,
+                          w->s3, w->s2, hact, y, cfg->m_skinny, cfg->dispatch,
+                          reinterpret_cast<int32_t*>(ws + L.block_variant), ws + L.gemm_scratch,
+                          dev_status, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  void* sh_y = nullptr;
+  if (cfg->has_shared) {
+    sh_y = ws + L.shared_y;
+    e = launch_grouped_gemm(x, nullptr, 1, T, H, cfg->I_shared, MOE_W_BF16, w->sw1, w->sw3, w->sw2,
+                            nullptr, nullptr, nullptr, ws + L.shared_hact, sh_y, cfg->m_skinny,
+                            cfg->dispatch, nullptr, ws + L.shared_gemm_scratch, dev_status, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  e = launch_unpermute(y, f2r, wts, T, K, H, sh_y, cfg->has_shared ? gsh : nullptr, out, stream);
+  return cuda_status(e);
+}
+
+}  // extern "C"

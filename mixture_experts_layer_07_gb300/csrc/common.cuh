@@ -1,0 +1,58 @@
+// Shared device helpers of the MoE-layer library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_gb300.h"
+
+#define MOE_DEVICE __device__ __forceinline__
+
+// Skinny/tile threshold on m_size used when the caller passes -1.  The
+// skinny variant's token tile is 16 rows, so blocks that fit one skinny tile
+// take it.
+#define MOE_DEFAULT_M_SKINNY 16
+
+// Variant predicate shared by the host mirror and the plan kernel.
+//   m_size == 0                      -> skip (no work for the block)
+//   dispatch SIMT                    -> CUDA-core kernel
+//   m (per block, or max(1, R/E))    -> skinny if m <= m_skinny else tile
+__host__ __device__ __forceinline__ int moe_variant_of(int64_t m_size, int64_t R, int E,
+                                                      int m_skinny, int dispatch) {
+  if (m_size <= 0) return MOE_VARIANT_SKIP;
+  if (dispatch == MOE_DISPATCH_SIMT) return MOE_VARIANT_SIMT;
+  int64_t m = m_size;
+  if (dispatch == MOE_DISPATCH_GLOBAL_AVG) {
+    int64_t avg = E > 0 ? R / E : R;
+    m = avg < 1 ? 1 : avg;
+  }
+  return m <= (int64_t)m_skinny ? MOE_VARIANT_SKINNY : MOE_VARIANT_TILE;
+}
+
+// First error wins.
+MOE_DEVICE void moe_set_status(int32_t* dev_status, int32_t code) {
+  if (dev_status) atomicCAS(dev_status, 0, code);
+}
+
+MOE_DEVICE float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+MOE_DEVICE float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// 8 bf16 packed in a uint4 -> 8 fp32 (exact widening)
+MOE_DEVICE void bf16x8_to_f32(const uint4& v, float* f) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+MOE_DEVICE uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+MOE_DEVICE int lane_id() { return threadIdx.x & 31; }
+MOE_DEVICE int warp_id() { return threadIdx.x >> 5; }
+
+static inline size_t moe_align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ static inline int moe_cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }

@@ -1,0 +1,563 @@
+// G1 + G2: grouped SwiGLU expert GEMM over expert-contiguous row blocks.
+//
+//   hact[r] = bf16( silu(xp[r] . W1[e]^T) * (xp[r] . W3[e]^T) )     (G1, N = I, K = H)
+//   y[r]    = bf16( hact[r] . W2[e]^T )                             (G2, N = H, K = I)
+//
+// Kernel choice per expert block, on the device.  "vLLM CPU MoE: dynamic GEMM
+// dispatch beyond a fixed threshold" (vllm PR #50949), "2. moe_fp8.cpp":
+// the variant used to be fixed for all experts from the global average
+// avg_M = max(1, M*topk/E); it is now chosen inside the per-expert loop from
+// that block's own m_size = offsets[mb+1] - offsets[mb], and a block with
+// m_size == 0 returns at once; "1. gemm.h": the high-throughput kernel is
+// taken above a small-M threshold.  Here a one-CTA plan kernel reads the
+// offsets on the device (the host never learns m_size, so nothing syncs),
+// applies that predicate per block and writes two work lists:
+//   skinny -- blocks with m_size <= m_skinny, 16-row token tiles
+//   tile   -- larger blocks, 128-row token tiles
+// Both lists run on the same tensor-core kernel template, instantiated for the
+// two token-tile widths, so small blocks do not pay for a 128-row tile.
+//
+// Tensor-core kernel (sm_100 family: tcgen05 + TMEM + TMA), "swap-AB" form:
+// the MMA's M side is 128 rows of the expert weight (output features), its N
+// side is the token tile, so even a one-token block fills the 128-row MMA and
+// the accumulator's TMEM lane is the output feature -- the epilogue's thread
+// i owns feature i and walks the tokens, and the 32 threads of a warp store
+// 32 consecutive features of one token row.
+//   warp 0     TMA producer: weight tiles [128 x 64] (W1 and W3 for G1) and
+//              the activation tile [BN x 64], 128-byte swizzled, into a ring
+//              of stages guarded by full/empty mbarriers
+//   warp 1     allocates TMEM, one thread issues tcgen05.mma (K = 16 per
+//              instruction, 4 per stage) and commits each stage back to the
+//              producer and the finished accumulator to the epilogue
+//   warps 2-5  epilogue: tcgen05.ld the fp32 accumulators (TMEM lanes are
+//              split by warp % 4), SwiGLU, bf16 store masked to the block
+// Persistent: one CTA per SM walks (item, 128-feature block) work units.
+// Every mbarrier wait is bounded; a wait that runs out sets
+// MOE_DEV_WAIT_TIMEOUT, the CTA drains its own in-flight copies and MMAs
+// (again bounded), frees its TMEM and returns.
+//
+// A CUDA-core kernel (MOE_DISPATCH_SIMT, and the FP8 weight format for now)
+// runs the same work list with plain FMA; it is the cross-check of the
+// tensor-core path and the FP8 (e4m3 + 128x128 block scale) path.
+#include <cuda.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace {
+
+using namespace moe_ptx;
+
+constexpr int kBnSkinny = 16;
+constexpr int kBnTile = 128;
+constexpr int kBM = 128;  // weight rows per MMA (output features)
+constexpr int kBK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// scratch layout
+struct PlanView {
+  int32_t* counts;  // [0] skinny items, [1] tile items
+  int4* items_s;    // {block, first row, rows, 0}
+  int4* items_t;
+  int cap_s, cap_t;
+};
+
+inline PlanView plan_view(void* scratch, int R, int E_blocks) {
+  PlanView v;
+  char* p = static_cast<char*>(scratch);
+  v.counts = reinterpret_cast<int32_t*>(p);
+  v.cap_s = moe_cdiv(R, kBnSkinny) + E_blocks;
+  v.cap_t = moe_cdiv(R, kBnTile) + E_blocks;
+  v.items_s = reinterpret_cast<int4*>(p + 256);
+  v.items_t = reinterpret_cast<int4*>(p + 256 + moe_align_up((size_t)v.cap_s * sizeof(int4), 256));
+  return v;
+}
+
+// ---------------------------------------------------------------- plan
+__global__ void __launch_bounds__(1024)
+gemm_plan_kernel(const int32_t* __restrict__ offsets, int E_blocks, int R, int m_skinny,
+                 int dispatch, int32_t* __restrict__ counts, int4* __restrict__ items_s,
+                 int4* __restrict__ items_t, int32_t* __restrict__ block_variant) {
+  __shared__ int ws[32], wt[32];
+  __shared__ int carry_s, carry_t;
+  const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
+  if (tid == 0) { carry_s = 0; carry_t = 0; }
+  const int64_t total_rows = offsets ? offsets[E_blocks] : R;
+  __syncthreads();
+  for (int base = 0; base < E_blocks; base += 1024) {
+    const int e = base + tid;
+    int lo = 0, m = 0;
+    if (e < E_blocks) {
+      lo = offsets ? offsets[e] : 0;
+      m = (offsets ? offsets[e + 1] : R) - lo;
+    }
+    const int v = e < E_blocks ? moe_variant_of(m, total_rows, E_blocks, m_skinny, dispatch)
+                               : MOE_VARIANT_SKIP;
+    const int ns = (v == MOE_VARIANT_SKINNY || v == MOE_VARIANT_SIMT) ? moe_cdiv(m, kBnSkinny) : 0;
+    const int nt = v == MOE_VARIANT_TILE ? moe_cdiv(m, kBnTile) : 0;
+    // block-wide exclusive scans of ns and nt
+    int is = ns, it = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, is, o);
+      const int b = __shfl_up_sync(0xffffffffu, it, o);
+      if (lane >= o) { is += a; it += b; }
+    }
+    if (lane == 31) { ws[warp] = is; wt[warp] = it; }
+    __syncthreads();
+    if (warp == 0) {
+      int a = ws[lane], b = wt[lane];
+      int sa = a, sb = b;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, sa, o);
+        const int y = __shfl_up_sync(0xffffffffu, sb, o);
+        if (lane >= o) { sa += x; sb += y; }
+      }
+      ws[lane] = sa - a;
+      wt[lane] = sb - b;
+    }
+    __syncthreads();
+    const int ps = carry_s + ws[warp] + is - ns;
+    const int pt = carry_t + wt[warp] + it - nt;
+    for (int i = 0; i < ns; ++i) {
+      const int r0 = i * kBnSkinny;
+      items_s[ps + i] = make_int4(e, lo + r0, min(kBnSkinny, m - r0), 0);
+    }
+    for (int i = 0; i < nt; ++i) {
+      const int r0 = i * kBnTile;
+      items_t[pt + i] = make_int4(e, lo + r0, min(kBnTile, m - r0), 0);
+    }
+    if (block_variant && e < E_blocks) block_variant[e] = v;
+    __syncthreads();
+    if (tid == 1023) { carry_s = ps + ns; carry_t = pt + nt; }
+    __syncthreads();
+  }
+  if (tid == 0) { counts[0] = carry_s; counts[1] = carry_t; }
+}
+
+// ---------------------------------------------------------------- tensor cores
+template <int BN, bool SWIGLU>
+struct TcCfg {
+  static constexpr int kNA = SWIGLU ? 2 : 1;
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kNA * kABytes + kBBytes;
+  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kAccCols = kNA * BN;
+  static constexpr int kTmemCols = kAccCols <= 32 ? 32 : kAccCols <= 64 ? 64
+                                 : kAccCols <= 128 ? 128 : kAccCols <= 256 ? 256 : 512;
+  static constexpr int kBarBytes = (2 * kStages + 3) * 8 + 16;
+  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+  static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+};
+
+MOE_DEVICE float silu_f(float g) { return g / (1.f + __expf(-g)); }
+
+template <int BN, bool SWIGLU>
+__global__ void __launch_bounds__(192, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wb,
+               const __grid_constant__ CUtensorMap tm_act, const int32_t* __restrict__ counts,
+               int list, const int4* __restrict__ items, int N, int Kdim,
+               __nv_bfloat16* __restrict__ out, int32_t* dev_status) {
+  using C = TcCfg<BN, SWIGLU>;
+  const int nblk = (N + kBM - 1) / kBM;
+  const int total = counts[list] * nblk;
+  if ((int)blockIdx.x >= total) return;
+  const int nk = (Kdim + kBK - 1) / kBK;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  const uint32_t sbase = smem_u32(smem);
+  uint8_t* bar_area = smem + (size_t)C::kStages * C::kStageBytes;
+  const uint32_t bar0 = smem_u32(bar_area);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
+  const uint32_t acc_full = bar0 + 8u * (2 * C::kStages);
+  const uint32_t acc_empty = acc_full + 8u;
+  const uint32_t drain_bar = acc_full + 16u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::kStages + 3));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 128);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_wa);
+    if (SWIGLU) prefetch_tmap(&tm_wb);
+    prefetch_tmap(&tm_act);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    moe_set_status(dev_status, MOE_DEV_WAIT_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        const int4 it = items[w / nblk];
+        const int nb = w % nblk;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            fail();
+            ok = false;
+            break;
+          }
+          const uint32_t st = sbase + stage * C::kStageBytes;
+          mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
+          tma_load_3d(st, &tm_wa, full_bar(stage), kb * kBK, nb * kBM, it.x);
+          if (SWIGLU) tma_load_3d(st + C::kABytes, &tm_wb, full_bar(stage), kb * kBK, nb * kBM, it.x);
+          tma_load_2d(st + C::kNA * C::kABytes, &tm_act, full_bar(stage), kb * kBK, it.y);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // every copy this thread started has landed before the CTA moves on
+      for (int s = 0; s < C::kStages; ++s)
+        if (armed & (1u << s))
+          if (!mbar_wait_bounded(full_bar(s), (armed_parity >> s) & 1u, nullptr, kWaitLimitNs)) fail();
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true, issued = false;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, kWaitLimitNs)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = sbase + stage * C::kStageBytes;
+          const uint32_t sa = st, sb3 = st + C::kABytes, sx = st + C::kNA * C::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint32_t acc = (kb | kk) != 0;
+            const uint64_t bdesc = sdesc_k128_sw128(sx + kk * 32);
+            tc_mma_f16(tmem, sdesc_k128_sw128(sa + kk * 32), bdesc, C::kIdesc, acc);
+            if (SWIGLU) tc_mma_f16(tmem + BN, sdesc_k128_sw128(sb3 + kk * 32), bdesc, C::kIdesc, acc);
+          }
+          issued = true;
+          tc_commit(empty_bar(stage));
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(acc_full);
+        acc_phase ^= 1u;
+      }
+      if (issued) {
+        // all MMAs of this thread complete before TMEM is released
+        tc_commit(drain_bar);
+        if (!mbar_wait_bounded(drain_bar, 0, nullptr, kWaitLimitNs)) fail();
+      }
+    }
+  } else {
+    // ---------------- epilogue, warps 2..5
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    uint32_t acc_phase = 0;
+    for (int w = blockIdx.x; w < total; w += gridDim.x) {
+      const int4 it = items[w / nblk];
+      const int nb = w % nblk;
+      if (!mbar_wait_bounded(acc_full, acc_phase, abort_flag, kWaitLimitNs)) {
+        fail();
+        break;
+      }
+      tc_fence_after();
+      const int n = nb * kBM + row;
+      const int m = it.z;
+      for (int c0 = 0; c0 < BN && c0 < m; c0 += 16) {
+        uint32_t g[16], u[16];
+        tc_ld_32x32b_x16(t_lane + c0, g);
+        if (SWIGLU) tc_ld_32x32b_x16(t_lane + BN + c0, u);
+        tc_wait_ld();
+        if (n < N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tok = c0 + j;
+            if (tok < m) {
+              const float gv = __uint_as_float(g[j]);
+              const float v = SWIGLU ? silu_f(gv) * __uint_as_float(u[j]) : gv;
+              out[(size_t)(it.y + tok) * N + n] = __float2bfloat16_rn(v);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty);
+      acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- CUDA cores
+// One CTA = one skinny item (<= 16 rows) x 64 output features, 256 threads:
+// thread = feature (tid % 64) x 4 rows (tid / 64).  Weights and activations
+// are staged per 64-wide K chunk in shared memory as fp32.
+constexpr int kSimtN = 64;
+constexpr int kSimtK = 64;
+
+template <bool FP8>
+MOE_DEVICE float load_w(const void* w, const float* s, int e, int n, int k, int N, int Kdim) {
+  const size_t idx = ((size_t)e * N + n) * Kdim + k;
+  if (FP8) {
+    const uint8_t code = static_cast<const uint8_t*>(w)[idx];
+    const __half_raw hr = __nv_cvt_fp8_to_halfraw(code, __NV_E4M3);
+    const int rb = (N + 127) / 128, cb = (Kdim + 127) / 128;
+    const float sc = s[((size_t)e * rb + n / 128) * cb + k / 128];
+    return __half2float(__half(hr)) * sc;
+  } else {
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(w)[idx]);
+  }
+}
+
+template <bool SWIGLU, bool FP8>
+__global__ void __launch_bounds__(256)
+gemm_simt_kernel(const __nv_bfloat16* __restrict__ act, const void* __restrict__ wa,
+                 const void* __restrict__ wb, const float* __restrict__ sa,
+                 const float* __restrict__ sb, const int32_t* __restrict__ counts, int list,
+                 const int4* __restrict__ items, int N, int Kdim, __nv_bfloat16* __restrict__ out) {
+  __shared__ float As[kBnSkinny][kSimtK];
+  __shared__ float Wa[kSimtN][kSimtK + 1];
+  __shared__ float Wb[SWIGLU ? kSimtN : 1][kSimtK + 1];
+  const int n_items = counts[list];
+  for (int item = blockIdx.y; item < n_items; item += gridDim.y) {
+  const int4 it = items[item];
+  const int e = it.x, r0 = it.y, m = it.z;
+  const int n0 = blockIdx.x * kSimtN;
+  const int tid = threadIdx.x, fl = tid % kSimtN, tg = tid / kSimtN;
+  float ga[4] = {0.f, 0.f, 0.f, 0.f}, gb[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int k0 = 0; k0 < Kdim; k0 += kSimtK) {
+    for (int i = tid; i < kBnSkinny * kSimtK; i += 256) {
+      const int r = i / kSimtK, k = k0 + i % kSimtK;
+      As[r][i % kSimtK] = (r < m && k < Kdim) ? __bfloat162float(act[(size_t)(r0 + r) * Kdim + k]) : 0.f;
+    }
+    for (int i = tid; i < kSimtN * kSimtK; i += 256) {
+      const int r = i / kSimtK, k = k0 + i % kSimtK, n = n0 + r;
+      const bool in = n < N && k < Kdim;
+      Wa[r][i % kSimtK] = in ? load_w<FP8>(wa, sa, e, n, k, N, Kdim) : 0.f;
+      if (SWIGLU) Wb[r][i % kSimtK] = in ? load_w<FP8>(wb, sb, e, n, k, N, Kdim) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int k = 0; k < kSimtK; ++k) {
+      const float w1 = Wa[fl][k];
+      const float w3 = SWIGLU ? Wb[fl][k] : 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = As[tg * 4 + i][k];
+        ga[i] = fmaf(a, w1, ga[i]);
+        if (SWIGLU) gb[i] = fmaf(a, w3, gb[i]);
+      }
+    }
+    __syncthreads();
+  }
+  const int n = n0 + fl;
+  if (n < N) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = tg * 4 + i;
+      if (r < m) {
+        const float v = SWIGLU ? silu_f(ga[i]) * gb[i] : ga[i];
+        out[(size_t)(r0 + r) * N + n] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// [E][N][Kdim] bf16 weights, box 64 (K) x 128 (N) x 1
+bool make_weight_map(CUtensorMap* m, const void* w, int E, int N, int Kdim) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)Kdim, (cuuint64_t)N, (cuuint64_t)E};
+  cuuint64_t strides[2] = {(cuuint64_t)Kdim * 2, (cuuint64_t)N * Kdim * 2};
+  cuuint32_t box[3] = {kBK, kBM, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [R][Kdim] bf16 activations, box 64 (K) x bn (rows)
+bool make_act_map(CUtensorMap* m, const void* a, int R, int Kdim, int bn) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)Kdim, (cuuint64_t)R};
+  cuuint64_t strides[1] = {(cuuint64_t)Kdim * 2};
+  cuuint32_t box[2] = {kBK, (cuuint32_t)bn};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  static int n[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 148;
+  }
+  return n[dev];
+}
+
+template <int BN, bool SWIGLU>
+cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorMap& act,
+                   const int32_t* counts, int list, const int4* items, int cap, int N, int Kdim,
+                   void* out, int32_t* dev_status, cudaStream_t stream) {
+  using C = TcCfg<BN, SWIGLU>;
+  static bool attr_set = false;  // per process; the attribute is per function, all devices
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, SWIGLU>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const long long work = (long long)cap * moe_cdiv(N, kBM);
+  const int grid = (int)(work < num_sms() ? work : num_sms());
+  if (grid <= 0) return cudaSuccess;
+  gemm_tc_kernel<BN, SWIGLU><<<grid, 192, C::kSmemBytes, stream>>>(
+      wa, wb, act, counts, list, items, N, Kdim, static_cast<__nv_bfloat16*>(out), dev_status);
+  return cudaGetLastError();
+}
+
+template <bool SWIGLU>
+cudaError_t run_simt(bool fp8, const void* act, const void* wa, const void* wb, const float* sa,
+                     const float* sb, const int32_t* counts, const int4* items, int cap, int N,
+                     int Kdim, void* out, cudaStream_t stream) {
+  if (cap <= 0) return cudaSuccess;
+  dim3 grid(moe_cdiv(N, kSimtN), cap < 32768 ? cap : 32768);
+  const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(act);
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+  if (fp8)
+    gemm_simt_kernel<SWIGLU, true><<<grid, 256, 0, stream>>>(a, wa, wb, sa, sb, counts, 0, items, N, Kdim, o);
+  else
+    gemm_simt_kernel<SWIGLU, false><<<grid, 256, 0, stream>>>(a, wa, wb, sa, sb, counts, 0, items, N, Kdim, o);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t grouped_gemm_scratch_bytes(int R, int E_blocks) {
+  const int cap_s = moe_cdiv(R, kBnSkinny) + E_blocks;
+  const int cap_t = moe_cdiv(R, kBnTile) + E_blocks;
+  return 256 + moe_align_up((size_t)cap_s * sizeof(int4), 256) +
+         moe_align_up((size_t)cap_t * sizeof(int4), 256);
+}
+
+int grouped_gemm_check(int H, int I, int wdtype) {
+  if (H % 16 != 0 || I % 16 != 0) return MOE_ERR_INVALID_ARG;
+  if (wdtype != MOE_W_BF16 && wdtype != MOE_W_FP8E4M3_B128) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_blocks, int R,
+                                int H, int I, int wdtype, const void* w1, const void* w3,
+                                const void* w2, const float* s1, const float* s3,
+                                const float* s2, void* hact, void* y, int m_skinny,
+                                int dispatch, int32_t* block_variant, void* scratch,
+                                int32_t* dev_status, cudaStream_t stream) {
+  if (m_skinny < 0) m_skinny = MOE_DEFAULT_M_SKINNY;
+  const bool fp8 = wdtype == MOE_W_FP8E4M3_B128;
+  // the FP8 weight format runs on the CUDA-core kernel for now
+  const bool simt = dispatch == MOE_DISPATCH_SIMT || fp8;
+  const int plan_dispatch = simt ? MOE_DISPATCH_SIMT : dispatch;
+  PlanView pv = plan_view(scratch, R, E_blocks);
+  gemm_plan_kernel<<<1, 1024, 0, stream>>>(offsets, E_blocks, R, m_skinny, plan_dispatch,
+                                           pv.counts, pv.items_s, pv.items_t, block_variant);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess || R == 0) return err;
+
+  if (simt) {
+    err = run_simt<true>(fp8, xp, w1, w3, s1, s3, pv.counts, pv.items_s, pv.cap_s, I, H, hact, stream);
+    if (err != cudaSuccess) return err;
+    return run_simt<false>(fp8, hact, w2, nullptr, s2, nullptr, pv.counts, pv.items_s, pv.cap_s, H,
+                           I, y, stream);
+  }
+
+  CUtensorMap m_w1, m_w3, m_w2, m_x16, m_x128, m_h16, m_h128;
+  if (!make_weight_map(&m_w1, w1, E_blocks, I, H) || !make_weight_map(&m_w3, w3, E_blocks, I, H) ||
+      !make_weight_map(&m_w2, w2, E_blocks, H, I) || !make_act_map(&m_x16, xp, R, H, kBnSkinny) ||
+      !make_act_map(&m_x128, xp, R, H, kBnTile) || !make_act_map(&m_h16, hact, R, I, kBnSkinny) ||
+      !make_act_map(&m_h128, hact, R, I, kBnTile))
+    return cudaErrorInvalidValue;
+
+  err = run_tc<kBnSkinny, true>(m_w1, m_w3, m_x16, pv.counts, 0, pv.items_s, pv.cap_s, I, H, hact,
+                                dev_status, stream);
+  if (err != cudaSuccess) return err;
+  err = run_tc<kBnTile, true>(m_w1, m_w3, m_x128, pv.counts, 1, pv.items_t, pv.cap_t, I, H, hact,
+                              dev_status, stream);
+  if (err != cudaSuccess) return err;
+  err = run_tc<kBnSkinny, false>(m_w2, m_w2, m_h16, pv.counts, 0, pv.items_s, pv.cap_s, H, I, y,
+                                 dev_status, stream);
+  if (err != cudaSuccess) return err;
+  return run_tc<kBnTile, false>(m_w2, m_w2, m_h128, pv.counts, 1, pv.items_t, pv.cap_t, H, I, y,
+                                dev_status, stream);
+}

@@ -1,0 +1,32 @@
+// Launchers shared between the C-ABI layer and the kernel translation units.
+// Every launcher queues work on `stream` and returns cudaGetLastError().
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+cudaError_t launch_router_gemm(const void* x, const float* wg, const float* gate_bias,
+                               float* logits, int T, int H, int G, cudaStream_t stream);
+
+cudaError_t launch_topk_route(const float* logits, int ld, const float* sel_bias, int T, int E,
+                              int K, int mode, float scale, int32_t* ids, float* weights,
+                              float* shared_gate, cudaStream_t stream);
+
+size_t permute_scratch_bytes(int T, int E, int K);
+cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                           int32_t* offsets, int32_t* row_to_flat, int32_t* flat_to_row,
+                           void* xp, void* scratch, int32_t* dev_status, cudaStream_t stream);
+
+size_t grouped_gemm_scratch_bytes(int R, int E_blocks);
+int grouped_gemm_check(int H, int I, int wdtype);  // 0 ok, else a moe_status_t
+cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_blocks, int R,
+                                int H, int I, int wdtype, const void* w1, const void* w3,
+                                const void* w2, const float* s1, const float* s3,
+                                const float* s2, void* hact, void* y, int m_skinny,
+                                int dispatch, int32_t* block_variant, void* scratch,
+                                int32_t* dev_status, cudaStream_t stream);
+
+cudaError_t launch_unpermute(const void* y, const int32_t* flat_to_row, const float* weights,
+                             int T, int K, int H, const void* shared_y, const float* shared_gate,
+                             void* out, cudaStream_t stream);

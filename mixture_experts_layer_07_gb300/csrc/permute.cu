@@ -1,0 +1,179 @@
+// P: stable permute of token replicas into expert-contiguous row blocks.
+//
+// "vLLM MoE permute optimisation: buffer pre-allocation" (vllm PR #43014),
+// "1. C++ kernel level": the permute works in caller-owned scratch that is
+// allocated once and reused instead of being allocated on every call.  The
+// block boundaries are the per-expert offsets whose differences are the
+// m_size of "vLLM CPU MoE: dynamic GEMM dispatch" (vllm PR #50949),
+// "2. moe_fp8.cpp".
+//
+// Replica f = t*K + k goes to row offsets[e] + rank, rank = number of
+// replicas f' < f with the same expert, so the result is unique and the
+// kernels need no sort and no cross-CTA waits:
+//   1. count   one warp per 256-replica chunk: per-chunk expert histogram
+//   2. scan    one CTA: per expert, exclusive scan over chunks; then an
+//              exclusive scan over experts gives offsets[E+1]
+//   3. scatter one warp per chunk, 32 replicas per step in order: lanes with
+//              the same expert find each other with __match_any_sync, the
+//              rank is the running count plus the popcount of lower lanes
+//   4. gather  xp[row] = x[row_to_flat[row] / K], 16-byte vectors
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int kChunk = 256;        // replicas per warp chunk
+constexpr int kWarpsPerCta = 8;
+
+// scratch: int32 counts[nchunks][E] (turned into per-chunk bases by the scan)
+inline int num_chunks(int R) { return moe_cdiv(R, kChunk); }
+
+__global__ void __launch_bounds__(32 * kWarpsPerCta)
+permute_count_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunks,
+                     int32_t* __restrict__ counts, int32_t* dev_status) {
+  extern __shared__ int32_t hist[];  // [kWarpsPerCta][E]
+  const int w = warp_id(), lane = lane_id();
+  const int chunk = blockIdx.x * kWarpsPerCta + w;
+  int32_t* h = hist + w * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  if (chunk < nchunks) {
+    const int f0 = chunk * kChunk;
+    for (int i = lane; i < kChunk; i += 32) {
+      const int f = f0 + i;
+      if (f < R) {
+        const int e = ids[f];
+        if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+        else moe_set_status(dev_status, MOE_DEV_BAD_EXPERT_ID);
+      }
+    }
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) counts[(size_t)chunk * E + e] = h[e];
+  }
+}
+
+__global__ void __launch_bounds__(1024)
+permute_scan_kernel(int32_t* __restrict__ counts, int E, int nchunks,
+                    int32_t* __restrict__ offsets) {
+  __shared__ int32_t warp_tot[32];
+  const int e = threadIdx.x;
+  int32_t run = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int32_t v = counts[(size_t)c * E + e];
+      counts[(size_t)c * E + e] = run;
+      run += v;
+    }
+  }
+  // exclusive scan of the per-expert totals across the block
+  int32_t incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane_id() >= o) incl += n;
+  }
+  if (lane_id() == 31) warp_tot[warp_id()] = incl;
+  __syncthreads();
+  if (warp_id() == 0) {
+    int32_t v = warp_tot[lane_id()];
+    int32_t s = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t n = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane_id() >= o) s += n;
+    }
+    warp_tot[lane_id()] = s - v;  // exclusive prefix of the warps
+  }
+  __syncthreads();
+  const int32_t excl = incl - run + warp_tot[warp_id()];
+  if (e < E) offsets[e] = excl;
+  if (e == E - 1) offsets[E] = excl + run;
+}
+
+__global__ void __launch_bounds__(32 * kWarpsPerCta)
+permute_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunks,
+                       const int32_t* __restrict__ bases, const int32_t* __restrict__ offsets,
+                       int32_t* __restrict__ row_to_flat, int32_t* __restrict__ flat_to_row) {
+  extern __shared__ int32_t cnt_all[];  // [kWarpsPerCta][E]
+  const int w = warp_id(), lane = lane_id();
+  const int chunk = blockIdx.x * kWarpsPerCta + w;
+  if (chunk >= nchunks) return;
+  int32_t* cnt = cnt_all + w * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = offsets[e] + bases[(size_t)chunk * E + e];
+  __syncwarp();
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int f0 = chunk * kChunk;
+  for (int s = 0; s < kChunk; s += 32) {
+    const int f = f0 + s + lane;
+    int e = -1;
+    if (f < R) {
+      e = ids[f];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    const int leader = __ffs(peers) - 1;
+    int base = 0;
+    if (e >= 0) base = cnt[e];
+    __syncwarp();
+    if (e >= 0 && lane == leader) cnt[e] = base + __popc(peers);
+    __syncwarp();
+    if (f < R) {
+      if (e >= 0) {
+        const int row = base + rank;
+        row_to_flat[row] = f;
+        flat_to_row[f] = row;
+      } else {
+        flat_to_row[f] = -1;
+      }
+    }
+  }
+}
+
+// one warp per row, 16-byte vectors
+__global__ void __launch_bounds__(256)
+permute_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_to_flat,
+                      const int32_t* __restrict__ offsets, int E, int K, int H8,
+                      uint4* __restrict__ xp) {
+  const int nrows = offsets[E];
+  const int lane = lane_id();
+  for (int row = blockIdx.x * 8 + warp_id(); row < nrows; row += gridDim.x * 8) {
+    const int t = row_to_flat[row] / K;
+    const uint4* src = x + (size_t)t * H8;
+    uint4* dst = xp + (size_t)row * H8;
+    for (int c = lane; c < H8; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
+}  // namespace
+
+size_t permute_scratch_bytes(int T, int E, int K) {
+  const int R = T * K;
+  return moe_align_up((size_t)num_chunks(R) * E * sizeof(int32_t) + 256, 256);
+}
+
+cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                           int32_t* offsets, int32_t* row_to_flat, int32_t* flat_to_row,
+                           void* xp, void* scratch, int32_t* dev_status, cudaStream_t stream) {
+  const int R = T * K;
+  const int nch = num_chunks(R);
+  int32_t* counts = static_cast<int32_t*>(scratch);
+  const size_t smem = (size_t)kWarpsPerCta * E * sizeof(int32_t);
+  const int ctas = moe_cdiv(nch, kWarpsPerCta);
+  if (R > 0) {
+    permute_count_kernel<<<ctas, 32 * kWarpsPerCta, smem, stream>>>(ids, R, E, nch, counts,
+                                                                     dev_status);
+  }
+  permute_scan_kernel<<<1, 1024, 0, stream>>>(counts, E, nch, offsets);
+  if (R > 0) {
+    permute_scatter_kernel<<<ctas, 32 * kWarpsPerCta, smem, stream>>>(
+        ids, R, E, nch, counts, offsets, row_to_flat, flat_to_row);
+    if (xp) {
+      const int grid = moe_cdiv(R, 8) < 152 * 16 ? moe_cdiv(R, 8) : 152 * 16;
+      permute_gather_kernel<<<grid, 256, 0, stream>>>(
+          static_cast<const uint4*>(x), row_to_flat, offsets, E, K, H / 8,
+          static_cast<uint4*>(xp));
+    }
+  }
+  return cudaGetLastError();
+}

@@ -1,0 +1,64 @@
+// U: weighted unpermute / combine.
+//
+// "vLLM MoE permute optimisation: buffer pre-allocation" (vllm PR #43014),
+// introduction: unpermute is the inverse of permute; it brings every expert
+// output row back to its token and combines the K rows of a token.  Fused
+// here into one gather-multiply-add pass:
+//   out[t] = bf16( sum_{k=0..K-1} w[t,k] * y[flat_to_row[t*K+k]] + g[t] * sh[t] )
+// with fp32 sums in k order and one rounding at the end.  Each thread owns 8
+// consecutive columns (one 16-byte vector per source row); a CTA covers one
+// token and 1024 columns.
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int kThreads = 128;
+
+__global__ void __launch_bounds__(kThreads)
+unpermute_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ flat_to_row,
+                 const float* __restrict__ weights, int K, int H8,
+                 const uint4* __restrict__ shared_y, const float* __restrict__ shared_gate,
+                 uint4* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int c = blockIdx.y * kThreads + threadIdx.x;
+  if (c >= H8) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int k = 0; k < K; ++k) {
+    const int row = __ldg(flat_to_row + (size_t)t * K + k);
+    if (row < 0) continue;
+    const float w = __ldg(weights + (size_t)t * K + k);
+    float f[8];
+    bf16x8_to_f32(__ldg(y + (size_t)row * H8 + c), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+  }
+  if (shared_y) {
+    const float g = __ldg(shared_gate + t);
+    float f[8];
+    bf16x8_to_f32(__ldg(shared_y + (size_t)t * H8 + c), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  out[(size_t)t * H8 + c] = o;
+}
+
+}  // namespace
+
+cudaError_t launch_unpermute(const void* y, const int32_t* flat_to_row, const float* weights,
+                             int T, int K, int H, const void* shared_y, const float* shared_gate,
+                             void* out, cudaStream_t stream) {
+  const int H8 = H / 8;
+  dim3 grid(T, moe_cdiv(H8, kThreads));
+  unpermute_kernel<<<grid, kThreads, 0, stream>>>(
+      static_cast<const uint4*>(y), flat_to_row, weights, K, H8,
+      static_cast<const uint4*>(shared_y), shared_gate, static_cast<uint4*>(out));
+  return cudaGetLastError();
+}

@@ -115,38 +115,37 @@ def _normal(seed, tid, sub, shape, std) -> np.ndarray:
 def quantize_fp8_block(w: np.ndarray):
     """Quantise one [rows, cols] float32 matrix to e4m3 codes + fp32 block scales.
 
-    Uses torch's float8_e4m3fn cast (round to nearest even) on the host.  Returns
+    scale = amax(block) / 448 (1 for an all-zero block); code = e4m3(w / scale)
+    by torch's float8_e4m3fn cast (round to nearest even) on the host.  Returns
     (codes uint8 [rows, cols], scales float32 [ceil(rows/128), ceil(cols/128)]).
     """
     import torch
 
     rows, cols = w.shape
     rb, cb = math.ceil(rows / FP8_BLOCK), math.ceil(cols / FP8_BLOCK)
-    scales = np.empty((rb, cb), dtype=np.float32)
-    codes = np.empty((rows, cols), dtype=np.uint8)
-    for i in range(rb):
-        for j in range(cb):
-            blk = w[i * FP8_BLOCK:(i + 1) * FP8_BLOCK, j * FP8_BLOCK:(j + 1) * FP8_BLOCK]
-            amax = float(np.max(np.abs(blk))) if blk.size else 0.0
-            s = np.float32(amax / FP8_MAX) if amax > 0 else np.float32(1.0)
-            scales[i, j] = s
-            q = torch.from_numpy(np.ascontiguousarray(blk / s, dtype=np.float32))
-            q = q.clamp_(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
-            codes[i * FP8_BLOCK:(i + 1) * FP8_BLOCK, j * FP8_BLOCK:(j + 1) * FP8_BLOCK] = q.numpy()
-    return codes, scales
+    pad = np.zeros((rb * FP8_BLOCK, cb * FP8_BLOCK), dtype=np.float32)
+    pad[:rows, :cols] = w
+    blk = pad.reshape(rb, FP8_BLOCK, cb, FP8_BLOCK)
+    amax = np.abs(blk).max(axis=(1, 3))
+    scales = np.where(amax > 0, (amax / np.float32(FP8_MAX)).astype(np.float32),
+                      np.float32(1.0)).astype(np.float32)
+    q = (blk / scales[:, None, :, None]).astype(np.float32)
+    q = np.clip(q, -FP8_MAX, FP8_MAX).reshape(rb * FP8_BLOCK, cb * FP8_BLOCK)[:rows, :cols]
+    codes = torch.from_numpy(np.ascontiguousarray(q)).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.numpy(), scales
 
 
 # ----------------------------------------------------------------------------
 # host back end (numpy Philox)
 # ----------------------------------------------------------------------------
 
-def host_inputs(spec: LayerSpec, T: int, seed: int = 0, experts=None) -> dict:
+def host_inputs(spec: LayerSpec, T: int, seed: int = 0, experts=None, weights: bool = True) -> dict:
     """Draw every tensor of one layer on the host.
 
     ``experts`` restricts the expert weights to that list of expert indices (the
-    other experts' slots stay absent); by default all E experts are drawn.  Each
+    other experts' slots stay zero); by default all E experts are drawn.  Each
     expert matrix has its own Philox key, so a subset equals the same slices of
-    the full draw.
+    the full draw.  ``weights=False`` draws only x, the gate and the biases.
 
     Returned keys (numpy):
       x_bits [T,H] u16 | wg [G,H] f32 | gate_bias [G] f32 or None |
@@ -172,6 +171,8 @@ def host_inputs(spec: LayerSpec, T: int, seed: int = 0, experts=None) -> dict:
 
     ex = list(range(E)) if experts is None else list(experts)
     out["experts"] = ex
+    if not weights:
+        return out
     std1, std2 = 1.0 / math.sqrt(H), 1.0 / math.sqrt(I)
     if spec.wdtype == "bf16":
         for key, tid, shp, std in (("w1_bits", TID_W1, (I, H), std1),

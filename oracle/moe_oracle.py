@@ -300,14 +300,34 @@ def unpermute(y, flat_to_row, weights, T: int, K: int, shared_y=None, g_sh=None)
 # ----------------------------------------------------------------------------
 
 
+class ExpertBank:
+    """Read-only [E, rows, cols] view of stored expert weights that decodes one
+    expert to float64 when it is indexed (bf16 codes widened, or e4m3 codes
+    dequantised by block), so a layer with many large experts never holds all
+    of them in float64 at once."""
+
+    def __init__(self, codes, scales=None):
+        self.codes = codes
+        self.scales = scales
+        self.shape = tuple(codes.shape)
+
+    def __getitem__(self, e):
+        if self.scales is None:
+            return bf16_to_f64(self.codes[e])
+        return dequant_fp8_block(self.codes[e], self.scales[e])
+
+    def __len__(self):
+        return self.shape[0]
+
+
 def layer_weights_f64(inp: dict):
     """Expert weights of an input dict (see the package's ``synth`` module) as
-    float64: bf16 codes widened, or e4m3 codes dequantised by block."""
+    three ``ExpertBank``s: W1 [E, I, H], W3 [E, I, H], W2 [E, H, I]."""
     if "w1_bits" in inp:
-        return (bf16_to_f64(inp["w1_bits"]), bf16_to_f64(inp["w3_bits"]),
-                bf16_to_f64(inp["w2_bits"]))
-    return (dequant_fp8_block(inp["w1_q"], inp["s1"]), dequant_fp8_block(inp["w3_q"], inp["s3"]),
-            dequant_fp8_block(inp["w2_q"], inp["s2"]))
+        return (ExpertBank(inp["w1_bits"]), ExpertBank(inp["w3_bits"]),
+                ExpertBank(inp["w2_bits"]))
+    return (ExpertBank(inp["w1_q"], inp["s1"]), ExpertBank(inp["w3_q"], inp["s3"]),
+            ExpertBank(inp["w2_q"], inp["s2"]))
 
 
 def moe_layer(x, wg, gate_bias, sel_bias, w1, w3, w2, *, E: int, K: int, mode: int,

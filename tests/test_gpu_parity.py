@@ -1,0 +1,370 @@
+"""GPU parity: every stage of the CUDA path through the C ABI, element by
+element against the CPU oracle on the same seeded inputs (tolerances in
+tests/gpu_util.py).  Sizes span several tiles and a ragged tail; full-size
+workloads are checked on sampled tokens in test_gpu_fullsize.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_layer_07_gb300 import synth
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+SPECS = synth.SPECS
+
+
+@pytest.fixture(scope="module")
+def ops():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from mixture_experts_layer_07_gb300 import build
+    build.build()
+    from mixture_experts_layer_07_gb300 import ops as o
+    return o
+
+
+def sync():
+    torch.cuda.synchronize()
+
+
+def i32(n):
+    return torch.empty(n, dtype=torch.int32, device="cuda")
+
+
+# ---------------------------------------------------------------- R
+ROUTER_CASES = [("tiny", 16), ("qwen3_30b_a3b", 1), ("qwen3_30b_a3b", 8),
+                ("qwen3_30b_a3b", 17), ("qwen3_30b_a3b", 256), ("gpt_oss_20b", 32),
+                ("shared_gate", 4), ("shared_gate", 131), ("high_expert", 512)]
+
+
+@pytest.mark.parametrize("name,T", ROUTER_CASES)
+def test_router_gemm(ops, name, T):
+    spec = SPECS[name]
+    inp = synth.host_inputs(spec, T, seed=1, weights=False)
+    logits = torch.full((T, spec.G), float("nan"), device="cuda")
+    ops.router_gemm(U.bf16_dev(inp["x_bits"]), U.dev(inp["wg"]), U.dev(inp["gate_bias"]), logits)
+    sync()
+    U.assert_router_close(U.f64(logits), oracle.bf16_to_f64(inp["x_bits"]), inp["wg"],
+                          inp["gate_bias"])
+
+
+# ---------------------------------------------------------------- K
+TOPK_CASES = [  # E, K, mode, T, shared
+    (8, 2, 0, 16, False), (128, 8, 0, 1, False), (128, 8, 0, 2048, False),
+    (32, 4, 0, 517, False), (512, 10, 0, 64, True), (896, 16, 1, 512, False),
+    (512, 9, 1, 512, False), (1024, 16, 1, 512, False), (1024, 9, 1, 37, False),
+    (8, 8, 0, 5, False), (64, 32, 0, 3, False), (33, 3, 1, 70, True), (1, 1, 0, 4, False)]
+
+
+def run_topk(ops, logits, E, K, mode, scale, sel_bias, shared):
+    T = logits.shape[0]
+    ids = i32((T, K))
+    w = torch.empty(T, K, device="cuda")
+    gsh = torch.empty(T, device="cuda") if shared else None
+    ops.topk_route(U.dev(logits), E, K, mode, scale, ids, w, U.dev(sel_bias), gsh)
+    sync()
+    return ids.cpu().numpy(), w.cpu().numpy(), None if gsh is None else gsh.cpu().numpy()
+
+
+@pytest.mark.parametrize("E,K,mode,T,shared", TOPK_CASES)
+def test_topk_route(ops, E, K, mode, T, shared):
+    G = E + int(shared)
+    lg = synth.random_logits(T, G, seed=E * 31 + K)
+    scale = 2.5 if mode else 1.0
+    bias = synth._normal(7, 9, E, (E,), 0.1 ** 0.5) if mode else None
+    ids, w, gsh = run_topk(ops, lg, E, K, mode, scale, bias, shared)
+    if mode == 0:
+        rid, rw = oracle.topk_softmax_renorm(lg.astype(np.float64), E, K)
+    else:
+        rid, rw = oracle.topk_sigmoid_bias(lg, bias, E, K, scale)
+    assert np.array_equal(ids, rid)
+    U.assert_weights_close(w, rw)
+    if shared:
+        U.assert_weights_close(gsh, oracle.shared_gate(lg.astype(np.float64), E))
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_topk_heavy_ties(ops, mode):
+    # logits from a 3-value set: most keys tie, the index rule decides
+    T, E, K = 300, 128, 8
+    r = np.random.default_rng(3)
+    lg = r.choice(np.float32([-1.0, 0.0, 1.0]), size=(T, E)).astype(np.float32)
+    lg[0] = 0.5                                   # one all-equal row
+    lg[1] = -0.0
+    lg[1, ::2] = 0.0                              # -0 and +0 are equal keys
+    bias = np.zeros(E, np.float32) if mode else None
+    ids, w, _ = run_topk(ops, lg, E, K, mode, 2.5 if mode else 1.0, bias, False)
+    if mode == 0:
+        rid, rw = oracle.topk_softmax_renorm(lg.astype(np.float64), E, K)
+    else:
+        rid, rw = oracle.topk_sigmoid_bias(lg, bias, E, K, 2.5)
+    assert np.array_equal(ids, rid)
+    assert ids[0].tolist() == list(range(K)) and ids[1].tolist() == list(range(K))
+    U.assert_weights_close(w, rw)
+
+
+def test_sigmoid_key_matches_oracle_bits(ops):
+    # the selection key is one specified float32 formula on both sides: compare
+    # its bits through a K = E route where weights = scale * s / sum(s) and the
+    # selection order is the key order
+    E = 32
+    lg = np.linspace(-95, 95, 32 * 4001, dtype=np.float32).reshape(-1, E)
+    ids, _, _ = run_topk(ops, lg, E, E, 1, 1.0, np.zeros(E, np.float32), False)
+    rid, _ = oracle.topk_sigmoid_bias(lg, np.zeros(E, np.float32), E, E, 1.0)
+    assert np.array_equal(ids, rid)
+    # sigmoid_f32 agrees with CUDA's expf-based sigmoid to a few ulp
+    t = torch.from_numpy(lg).cuda()
+    ref = (1.0 / (1.0 + torch.exp(-t))).cpu().numpy()
+    mine = oracle.sigmoid_f32(lg)
+    ok = ref > 1e-30
+    assert (np.abs(mine[ok] - ref[ok]) <= 4 * np.spacing(ref[ok])).all()
+
+
+# ---------------------------------------------------------------- P
+PERMUTE_CASES = [(16, 2, 8, 256), (1, 8, 128, 2048), (37, 8, 128, 2048), (2048, 8, 128, 2048),
+                 (4096, 4, 32, 2880), (512, 16, 896, 64), (512, 16, 1024, 64), (64, 10, 512, 2048),
+                 (33, 1, 3, 16)]
+
+
+def run_permute(ops, x, ids, E, want_xp=True):
+    T, K = ids.shape
+    R = T * K
+    H = x.shape[1]
+    off, r2f, f2r = i32(E + 1), i32(R), i32(R)
+    xp = torch.empty(R, H, dtype=torch.bfloat16, device="cuda") if want_xp else None
+    scratch = torch.empty(ops.permute_scratch_bytes(T, E, K), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.permute(x, ids, E, off, r2f, f2r, xp, scratch, st)
+    sync()
+    return off, r2f, f2r, xp, int(st.item())
+
+
+@pytest.mark.parametrize("T,K,E,H", PERMUTE_CASES)
+def test_permute(ops, T, K, E, H):
+    ids = synth.random_ids(T, K, E, seed=T + E)
+    x_bits = synth.f32_to_bf16_bits(synth._normal(0, 1, T, (T, H), 1.0))
+    x = U.bf16_dev(x_bits)
+    off, r2f, f2r, xp, st = run_permute(ops, x, torch.from_numpy(ids).cuda(), E)
+    ro, rr, rf = oracle.permute(ids, E)
+    assert st == 0
+    assert np.array_equal(off.cpu().numpy(), ro)
+    assert np.array_equal(r2f.cpu().numpy(), rr)
+    assert np.array_equal(f2r.cpu().numpy(), rf)
+    got = xp.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, x_bits[rr // K])
+
+
+def test_permute_concentrated_with_empty_experts(ops):
+    T, K, E, H = 300, 4, 32, 64
+    r = np.random.default_rng(5)
+    ids = np.stack([r.choice([0, 1, 2, 3, 9], size=K, replace=False) for _ in range(T)]).astype(np.int32)
+    x = torch.randn(T, H, device="cuda").to(torch.bfloat16)
+    off, r2f, f2r, _, st = run_permute(ops, x, torch.from_numpy(ids).cuda(), E)
+    ro, rr, rf = oracle.permute(ids, E)
+    assert st == 0 and np.array_equal(off.cpu().numpy(), ro)
+    assert np.array_equal(r2f.cpu().numpy(), rr) and np.array_equal(f2r.cpu().numpy(), rf)
+
+
+def test_permute_flags_out_of_range_ids(ops):
+    T, K, E = 50, 2, 16
+    ids = synth.random_ids(T, K, E, seed=1)
+    ids[7, 1] = E        # out of range
+    ids[20, 0] = -3
+    x = torch.randn(T, 32, device="cuda").to(torch.bfloat16)
+    off, r2f, f2r, _, st = run_permute(ops, x, torch.from_numpy(ids).cuda(), E)
+    assert st == ops.DEV_BAD_EXPERT_ID
+    f2r = f2r.cpu().numpy()
+    assert f2r[7 * K + 1] == -1 and f2r[20 * K] == -1
+    assert off.cpu().numpy()[-1] == T * K - 2
+    valid = np.ones(T * K, bool)
+    valid[[7 * K + 1, 20 * K]] = False
+    ro, rr, _ = oracle.permute(np.where(valid, ids.ravel(), E), E + 1)
+    assert np.array_equal(off.cpu().numpy(), ro[:E + 1])
+    assert np.array_equal(r2f.cpu().numpy()[:T * K - 2], rr[:T * K - 2])
+
+
+def test_permute_then_unpermute_is_identity(ops):
+    T, H, E = 129, 256, 8
+    x_bits = synth.f32_to_bf16_bits(synth._normal(0, 1, 5, (T, H), 1.0))
+    x = U.bf16_dev(x_bits)
+    # K = 1 and weight 1: bit-exact round trip
+    ids = torch.from_numpy(synth.random_ids(T, 1, E, seed=2)).cuda()
+    _, _, f2r, xp, _ = run_permute(ops, x, ids, E)
+    out = torch.empty_like(x)
+    ops.unpermute(xp, f2r, torch.ones(T, 1, device="cuda"), T, 1, H, out)
+    sync()
+    assert torch.equal(out.view(torch.int16), x.view(torch.int16))
+    # K = 4 with weights summing to 1: within one bf16 rounding
+    ids = torch.from_numpy(synth.random_ids(T, 4, E, seed=3)).cuda()
+    _, _, f2r, xp, _ = run_permute(ops, x, ids, E)
+    w = torch.rand(T, 4, device="cuda")
+    w = w / w.sum(1, keepdim=True)
+    ops.unpermute(xp, f2r, w, T, 4, H, out)
+    sync()
+    ref = oracle.bf16_to_f64(x_bits)
+    assert (np.abs(U.f64(out) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30).all()
+
+
+# ---------------------------------------------------------------- G
+def concentrated_ids(T, K, E, seed):
+    """Most tokens pick from a few hot experts (big blocks); the rest spread
+    over all experts (small blocks); unpicked experts stay empty."""
+    r = np.random.default_rng(seed)
+    hot = np.arange(min(E, K + 2))
+    rows = [r.choice(hot, K, replace=False) if r.random() < 0.7 else r.choice(E, K, replace=False)
+            for _ in range(T)]
+    return np.stack(rows).astype(np.int32)
+
+
+def gemm_case(spec, T, seed, concentrated=False):
+    """Host inputs + oracle permute for a grouped-GEMM case."""
+    K, E = spec.K, spec.E
+    ids = concentrated_ids(T, K, E, seed) if concentrated else synth.random_ids(T, K, E, seed=seed)
+    inp = synth.host_inputs(spec, T, seed=seed, experts=sorted(set(ids.ravel().tolist())))
+    off, r2f, f2r = oracle.permute(ids, E)
+    return inp, ids, off, r2f, f2r
+
+
+def run_gemm(ops, spec, inp, off, r2f, K, dispatch=0, m_skinny=-1):
+    T = inp["x_bits"].shape[0]
+    R = T * K
+    E, H, I = spec.E, spec.H, spec.I
+    xp_bits = inp["x_bits"][r2f // K]
+    t = U.layer_tensors(inp, inp["experts"])
+    hact = torch.full((R, I), float("nan"), device="cuda").to(torch.bfloat16)
+    y = torch.full((R, H), float("nan"), device="cuda").to(torch.bfloat16)
+    scratch = torch.empty(ops.grouped_gemm_scratch_bytes(R, E), dtype=torch.uint8, device="cuda")
+    bv = i32(E)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.grouped_gemm(U.bf16_dev(xp_bits), torch.from_numpy(off).cuda(), E, H, I, t["w1"], t["w3"],
+                     t["w2"], hact, y, scratch, wdtype=ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16,
+                     s1=t.get("s1"), s3=t.get("s3"), s2=t.get("s2"), m_skinny=m_skinny,
+                     dispatch=dispatch, block_variant=bv, dev_status=st)
+    sync()
+    return hact, y, bv.cpu().numpy(), int(st.item()), xp_bits
+
+
+GEMM_CASES = [  # spec name, overrides, T, concentrated, dispatch, m_skinny, both variants
+    ("tiny", {}, 16, False, 0, -1, False),
+    ("tiny", {}, 16, False, 2, -1, False),
+    ("qwen3_30b_a3b", {}, 8, False, 0, -1, False),
+    ("qwen3_30b_a3b", {}, 256, False, 0, -1, True),
+    ("qwen3_30b_a3b", {}, 300, True, 0, -1, True),
+    ("qwen3_30b_a3b", {}, 300, True, 1, -1, False),
+    ("qwen3_30b_a3b", {}, 300, True, 2, -1, False),
+    ("qwen3_30b_a3b", {}, 300, True, 0, 4, True),
+    ("tiny", {"H": 2880, "I": 2880, "E": 4}, 40, False, 0, 8, False),
+    ("tiny", {"H": 2880, "I": 2880, "E": 4}, 40, False, 0, 64, False),
+    ("tiny", {"H": 320, "I": 192, "E": 6}, 200, True, 0, -1, False),
+    ("tiny", {"H": 160, "I": 144, "E": 5, "wdtype": "fp8"}, 50, True, 0, -1, False),
+    ("gpt_oss_20b", {"E": 6}, 40, True, 0, -1, False),
+]
+
+
+@pytest.mark.parametrize("name,over,T,conc,dispatch,m_skinny,both", GEMM_CASES)
+def test_grouped_gemm(ops, name, over, T, conc, dispatch, m_skinny, both):
+    spec = SPECS[name].with_(**over)
+    inp, ids, off, r2f, f2r = gemm_case(spec, T, seed=T + spec.E, concentrated=conc)
+    hact, y, bv, st, xp_bits = run_gemm(ops, spec, inp, off, r2f, spec.K, dispatch, m_skinny)
+    assert st == 0
+    w1, w3, w2 = oracle.layer_weights_f64(inp)
+    rh, ry = oracle.grouped_gemm(oracle.bf16_to_f64(xp_bits), off, w1, w3, w2)
+    rel = 5e-2 if spec.wdtype == "fp8" else 2e-2
+    U.assert_bf16_close(U.f64(hact), rh, rel, "hact")
+    U.assert_bf16_close(U.f64(y), ry, rel, "y")
+    R = T * spec.K
+    m = np.diff(off)
+    want_bv = [ops.block_variant(int(mm), R, spec.E, m_skinny,
+                                 ops.DISPATCH_SIMT if spec.wdtype == "fp8" else dispatch) for mm in m]
+    assert bv.tolist() == want_bv
+    if both:  # skinny and tile blocks in the same call
+        assert {ops.VARIANT_SKINNY, ops.VARIANT_TILE} <= set(bv.tolist())
+
+
+def test_grouped_gemm_single_block_without_offsets(ops):
+    # offsets == NULL runs one block [0, R) -- the shared-expert form
+    spec = SPECS["tiny"].with_(E=1, H=512, I=256)
+    for T in (3, 16, 17, 200):
+        inp = synth.host_inputs(spec, T, seed=T)
+        t = U.layer_tensors(inp)
+        hact = torch.empty(T, spec.I, dtype=torch.bfloat16, device="cuda")
+        y = torch.empty(T, spec.H, dtype=torch.bfloat16, device="cuda")
+        scratch = torch.empty(ops.grouped_gemm_scratch_bytes(T, 1), dtype=torch.uint8, device="cuda")
+        ops.grouped_gemm(t["x"], None, 1, spec.H, spec.I, t["w1"], t["w3"], t["w2"], hact, y, scratch)
+        sync()
+        w1, w3, w2 = oracle.layer_weights_f64(inp)
+        rh, ry = oracle.expert_swiglu(oracle.bf16_to_f64(inp["x_bits"]), w1[0], w3[0], w2[0])
+        U.assert_bf16_close(U.f64(hact), rh, what=f"hact T={T}")
+        U.assert_bf16_close(U.f64(y), ry, what=f"y T={T}")
+
+
+# ---------------------------------------------------------------- U
+@pytest.mark.parametrize("T,K,H,shared", [(16, 2, 256, False), (1, 8, 2048, False),
+                                          (333, 8, 2048, False), (64, 10, 2048, True),
+                                          (7, 16, 7168, False)])
+def test_unpermute(ops, T, K, H, shared):
+    E = 64
+    ids = synth.random_ids(T, K, E, seed=T)
+    _, _, f2r = oracle.permute(ids, E)
+    y_bits = synth.f32_to_bf16_bits(synth._normal(3, 1, T, (T * K, H), 1.0))
+    w = np.random.default_rng(T).random((T, K)).astype(np.float32)
+    sh_bits = synth.f32_to_bf16_bits(synth._normal(3, 2, T, (T, H), 1.0)) if shared else None
+    g = np.random.default_rng(1).random(T).astype(np.float32) if shared else None
+    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    ops.unpermute(U.bf16_dev(y_bits), torch.from_numpy(f2r).cuda(), U.dev(w), T, K, H, out,
+                  None if sh_bits is None else U.bf16_dev(sh_bits), U.dev(g))
+    sync()
+    ref = oracle.unpermute(oracle.bf16_to_f64(y_bits), f2r, w, T, K,
+                           None if sh_bits is None else oracle.bf16_to_f64(sh_bits), g)
+    # only the final bf16 rounding (+ fp32 sums): 2^-8 relative to the magnitude sum
+    mag = oracle.unpermute(np.abs(oracle.bf16_to_f64(y_bits)), f2r, np.abs(w), T, K,
+                           None if sh_bits is None else np.abs(oracle.bf16_to_f64(sh_bits)), g)
+    assert (np.abs(U.f64(out) - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6 * mag + 1e-30).all()
+
+
+# ---------------------------------------------------------------- whole layer
+LAYER_CASES = [("tiny", {}, 16), ("tiny", {}, 1), ("qwen3_30b_a3b", {}, 1),
+               ("qwen3_30b_a3b", {}, 2), ("qwen3_30b_a3b", {}, 8), ("qwen3_30b_a3b", {}, 32),
+               ("qwen3_30b_a3b", {}, 256), ("gpt_oss_20b", {}, 32), ("shared_gate", {}, 4),
+               ("shared_gate", {}, 64), ("high_expert", {}, 2),
+               ("high_expert", {"E": 512, "K": 9}, 2), ("high_expert", {"E": 1024}, 1)]
+
+
+def oracle_routing(spec, inp):
+    x = oracle.bf16_to_f64(inp["x_bits"])
+    logits = oracle.router_logits(x, inp["wg"], inp["gate_bias"])
+    if spec.mode == 0:
+        ids, _ = oracle.topk_softmax_renorm(logits, spec.E, spec.K)
+        keys = logits[:, :spec.E]
+    else:
+        ids, _ = oracle.topk_sigmoid_bias(logits.astype(np.float32), inp["sel_bias"], spec.E,
+                                          spec.K, spec.routed_scale)
+        s = oracle.sigmoid_f32(logits.astype(np.float32)[:, :spec.E])
+        keys = (s + inp["sel_bias"][None, :]).astype(np.float64)
+    srt = -np.sort(-keys, axis=1)
+    margin = srt[:, spec.K - 1] - srt[:, spec.K] if spec.K < spec.E else np.full(len(ids), np.inf)
+    return logits, ids, margin
+
+
+@pytest.mark.parametrize("name,over,T", LAYER_CASES)
+def test_layer(ops, name, over, T):
+    spec = SPECS[name].with_(**over)
+    base = synth.host_inputs(spec, T, seed=11, weights=False)
+    logits, ids, margin = oracle_routing(spec, base)
+    inp = synth.host_inputs(spec, T, seed=11, experts=sorted(set(ids.ravel().tolist())))
+    t = U.layer_tensors(inp, inp["experts"])
+    layer = ops.MoELayer(U.config_for(ops, spec, T_max=max(T, 4)), t)
+    out = layer(t["x"])
+    sync()
+    assert int(layer.dev_status.item()) == 0
+    res = oracle.moe_layer_from_inputs(inp)
+    # intermediates
+    U.assert_router_close(U.f64(layer.view("logits", torch.float32, (T, spec.G))),
+                          oracle.bf16_to_f64(inp["x_bits"]), inp["wg"], inp["gate_bias"])
+    gid = layer.view("ids", torch.int32, (T, spec.K)).cpu().numpy()
+    clear = margin > 1e-4          # fp32 router vs fp64 oracle: near ties may route either way
+    assert clear.mean() > 0.9
+    assert np.array_equal(gid[clear], res["ids"][clear])
+    rel = 5e-2 if spec.wdtype == "fp8" else 2e-2
+    U.assert_bf16_close(U.f64(out)[clear], res["out"][clear], rel, "layer out")

@@ -343,7 +343,7 @@ def test_layer_matches_brute_force(mode, shared):
     inp = synth.host_inputs(spec, T=6, seed=13)
     res = oracle.moe_layer_from_inputs(inp)
     x = oracle.bf16_to_f64(inp["x_bits"])
-    w1, w3, w2 = oracle.layer_weights_f64(inp)
+    w1, w3, w2 = (np.stack([b[e] for e in range(spec.E)]) for b in oracle.layer_weights_f64(inp))
     sh = None
     if shared:
         sh = tuple(oracle.bf16_to_f64(inp[k]).tolist() for k in ("sw1_bits", "sw3_bits", "sw2_bits"))
@@ -358,7 +358,7 @@ def test_layer_fp8_equals_bf16_path_on_dequantised_weights():
     spec = synth.LayerSpec("pin8", H=160, E=3, K=2, I=136, wdtype="fp8")
     inp = synth.host_inputs(spec, T=5, seed=14)
     res = oracle.moe_layer_from_inputs(inp)
-    w1, w3, w2 = oracle.layer_weights_f64(inp)
+    w1, w3, w2 = (np.stack([b[e] for e in range(3)]) for b in oracle.layer_weights_f64(inp))
     res2 = oracle.moe_layer(oracle.bf16_to_f64(inp["x_bits"]), inp["wg"], None, None, w1, w3, w2,
                             E=3, K=2, mode=0)
     assert np.array_equal(res["out"], res2["out"])
