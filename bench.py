@@ -407,31 +407,30 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------------------ oracle arm
-def oracle_sample_time(spec, T_sample, seed=0):
-    """Time the CPU oracle on T_sample tokens of the workload (host draw)."""
-    import oracle
+def host_workload(spec, T, seed=0):
+    """The workload drawn on the host (tokens + every expert's weights)."""
     from mixture_experts_layer_07_gb300 import synth
+    return synth.host_inputs(spec, T, seed=seed)
 
-    base = synth.host_inputs(spec, T_sample, seed=seed, weights=False)
-    x = oracle.bf16_to_f64(base["x_bits"])
-    lg = oracle.router_logits(x, base["wg"], base["gate_bias"])
-    if spec.mode == 0:
-        ids, _ = oracle.topk_softmax_renorm(lg, spec.E, spec.K)
-    else:
-        ids, _ = oracle.topk_sigmoid_bias(lg.astype(np.float32), base["sel_bias"], spec.E, spec.K,
-                                          spec.routed_scale)
-    inp = synth.host_inputs(spec, T_sample, seed=seed, experts=sorted(set(ids.ravel().tolist())))
-    t0 = time.perf_counter()
-    oracle.moe_layer_from_inputs(inp)
-    return time.perf_counter() - t0
+
+def oracle_time(inp, t0, n):
+    """Seconds the CPU oracle takes for tokens [t0, t0 + n) of ``inp``."""
+    import oracle
+    sub = dict(inp)
+    sub["x_bits"] = inp["x_bits"][t0:t0 + n]
+    sub["T"] = n
+    start = time.perf_counter()
+    oracle.moe_layer_from_inputs(sub)
+    return time.perf_counter() - start
 
 
 def cpu_baseline(spec, T, tokens):
     cores = len(os.sched_getaffinity(0))
-    sec = oracle_sample_time(spec, tokens)
+    inp = host_workload(spec, tokens, seed=0)
+    sec = oracle_time(inp, 0, tokens)
     return {"value": round(tokens / sec, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{tokens} tokens of the {spec.name} T={T} workload (same shapes, host draw), "
-                      f"float64 numpy oracle, one pass, {sec:.1f} s"}
+            "sample": f"{tokens} tokens of the {spec.name} workload (same shapes, all {spec.E} "
+                      f"experts, host draw), float64 numpy oracle, one pass, {sec:.1f} s"}
 
 
 def run_reference(args):
@@ -439,15 +438,17 @@ def run_reference(args):
 
     spec = synth.SPECS[args.workload]
     cores = len(os.sched_getaffinity(0))
-    for _ in range(args.warmup):
-        oracle_sample_time(spec, max(1, args.cpu_tokens // 4), seed=1)
+    n = max(1, args.ref_tokens)
+    inp = host_workload(spec, n * (args.steps + args.warmup), seed=1)
+    for w in range(args.warmup):
+        oracle_time(inp, w * n, n)
     total = 0.0
     for s in range(args.steps):
-        total += oracle_sample_time(spec, args.cpu_tokens, seed=2 + s)
-    tokens = args.cpu_tokens * args.steps
+        total += oracle_time(inp, (args.warmup + s) * n, n)
+    tokens = n * args.steps
     val = tokens / total
-    sample = (f"{args.cpu_tokens} tokens per step of the {spec.name} T={args.T} workload "
-              f"(float64 numpy oracle on the host cores)")
+    sample = (f"{n} tokens per step of the {spec.name} workload (T={args.T} batch shape, all "
+              f"{spec.E} experts), float64 numpy oracle on the host cores")
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -479,7 +480,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_30b_a3b")
     ap.add_argument("--T", type=int, default=2048)
-    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--ref-tokens", type=int, default=16)
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
