@@ -202,6 +202,31 @@ moe_status_t moe_permute(const void* x, const int32_t* ids, int T, int H, int E,
                          void* xp, void* scratch, size_t scratch_bytes,
                          int32_t* dev_status, moe_stream_t stream);
 
+/*
+ * moe_permute without caller scratch (the pages have no counterpart; this is a
+ * convenience of this library).  For callers that cannot allocate device
+ * memory at all -- e.g. code whose device memory is owned entirely by a fixed
+ * pool or arena set up at start-up, or hooks that are not allowed to call
+ * cudaMalloc -- and so have no scratch buffer to pass.  Same arguments,
+ * results and errors as moe_permute, minus scratch / scratch_bytes.
+ *   - The scratch is a fixed array of MOE_PERMUTE_STATIC_SCRATCH_BYTES inside
+ *     the library, held on every GPU that loads the library until the process
+ *     exits.  Sizes whose moe_permute_scratch_bytes(T, E, K) exceeds it return
+ *     MOE_ERR_WORKSPACE before anything is queued (1 MiB covers, e.g.,
+ *     T*K up to 32768 at E = 1024, or up to 262144 at E = 128).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.  No cudaMalloc, cudaFree or allocating routine is called.
+ *   - Every call shares the array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls whose kernels may overlap
+ *     on the GPU -- on different streams without ordering, or from different
+ *     host threads -- race on it: order them on one stream.
+ */
+#define MOE_PERMUTE_STATIC_SCRATCH_BYTES (1u << 20)
+moe_status_t moe_permute_static(const void* x, const int32_t* ids, int T, int H, int E, int K,
+                                int32_t* offsets, int32_t* row_to_flat, int32_t* flat_to_row,
+                                void* xp, int32_t* dev_status, moe_stream_t stream);
+
 /* Scratch bytes moe_grouped_gemm needs for R rows in E_blocks blocks. */
 moe_status_t moe_grouped_gemm_scratch_bytes(int R, int E_blocks, size_t* bytes);
 

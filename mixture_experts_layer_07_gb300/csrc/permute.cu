@@ -177,3 +177,65 @@ cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int 
   }
   return cudaGetLastError();
 }
+
+// ---------------------------------------------------------------- static scratch
+// A variant of moe_permute for callers that may not allocate device memory at
+// all: its per-chunk counts live in a fixed array compiled into this library,
+// so the caller passes only inputs and outputs.  The array is shared by every
+// call on a device and keeps the previous call's contents; the count kernel
+// overwrites every entry it later reads, so nothing needs clearing.  Two calls
+// whose kernels overlap on the GPU (different streams, no ordering) race on it.
+#include <mutex>
+
+static __device__ __align__(256) unsigned char g_permute_static_scratch[MOE_PERMUTE_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+// Device address of the array, looked up once per device with that device
+// current (in host code the symbol is only a host-side stand-in).
+void* static_scratch_address(cudaError_t* err) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_permute_static_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+bool unaligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+}  // namespace
+
+extern "C" moe_status_t moe_permute_static(const void* x, const int32_t* ids, int T, int H, int E,
+                                           int K, int32_t* offsets, int32_t* row_to_flat,
+                                           int32_t* flat_to_row, void* xp, int32_t* dev_status,
+                                           moe_stream_t stream) {
+  if (T < 0 || H <= 0 || H % 16 != 0 || E <= 0 || E > 1024 || K <= 0 || K > E || K > 32)
+    return MOE_ERR_INVALID_ARG;
+  if (!offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!ids || !row_to_flat || !flat_to_row || (xp && !x))) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)T * K > 0x3fffffff) return MOE_ERR_INVALID_ARG;
+  if (permute_scratch_bytes(T, E, K) > (size_t)MOE_PERMUTE_STATIC_SCRATCH_BYTES)
+    return MOE_ERR_WORKSPACE;
+  if (unaligned(offsets, 4) || (ids && unaligned(ids, 4)) ||
+      (row_to_flat && unaligned(row_to_flat, 4)) || (flat_to_row && unaligned(flat_to_row, 4)) ||
+      (xp && (unaligned(xp, 16) || unaligned(x, 16))))
+    return MOE_ERR_MISALIGNED;
+  cudaError_t err;
+  void* scratch = static_scratch_address(&err);
+  if (!scratch) return MOE_ERR_CUDA;
+  err = launch_permute(x, ids, T, H, E, K, offsets, row_to_flat, flat_to_row, xp, scratch,
+                       dev_status, stream);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -29,7 +29,9 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTS = ["moe_status_string", "moe_default_m_skinny", "moe_block_variant", "moe_router_gemm",
            "moe_topk_route", "moe_permute_scratch_bytes", "moe_permute",
            "moe_grouped_gemm_scratch_bytes", "moe_grouped_gemm", "moe_unpermute",
-           "moe_workspace_bytes", "moe_layer", "moe_workspace_layout"]
+           "moe_workspace_bytes", "moe_layer", "moe_workspace_layout", "moe_permute_static"]
+
+PERMUTE_STATIC_SCRATCH_BYTES = 1 << 20
 
 
 class MoEError(RuntimeError):
@@ -82,6 +84,7 @@ def _lib():
             "moe_topk_route": [_P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P],
             "moe_permute_scratch_bytes": [_I, _I, _I, ctypes.POINTER(_S)],
             "moe_permute": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P, _P],
+            "moe_permute_static": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
             "moe_grouped_gemm_scratch_bytes": [_I, _I, ctypes.POINTER(_S)],
             "moe_grouped_gemm": [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I,
                                  _I, _P, _P, _S, _P, _P],
@@ -195,6 +198,17 @@ def permute(x, ids, E, offsets, row_to_flat, flat_to_row, xp, scratch, dev_statu
     _check(_lib().moe_permute(_p(x), _p(ids), T, H, E, K, _p(offsets), _p(row_to_flat),
                               _p(flat_to_row), _p(xp), _p(scratch), scratch.numel(),
                               _p(dev_status), _stream(stream)), "moe_permute")
+
+
+def permute_static(x, ids, E, offsets, row_to_flat, flat_to_row, xp, dev_status=None,
+                   stream=None, H=None):
+    """moe_permute_static: moe_permute with the library's built-in scratch, for
+    callers that cannot allocate device memory (see the header)."""
+    T, K = ids.shape
+    H = x.shape[1] if x is not None else H
+    _check(_lib().moe_permute_static(_p(x), _p(ids), T, H, E, K, _p(offsets), _p(row_to_flat),
+                                     _p(flat_to_row), _p(xp), _p(dev_status), _stream(stream)),
+           "moe_permute_static")
 
 
 def grouped_gemm(xp, offsets, E_blocks, H, I, w1, w3, w2, hact, y, scratch, *, wdtype=W_BF16,
