@@ -34,6 +34,8 @@ import torch  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# FP32 FMA peak from unit counts and clock: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 METRIC = "MoE-layer tokens/s (and us/layer) vs T; per-stage fraction of HBM/tensor roofline"
 
 
@@ -168,17 +170,27 @@ def stage_bytes_flops(spec, T, ids, e_active):
     return st
 
 
-def roofline_of(bytes_, flops, seconds, peaks, sustained=False):
+def roofline_of(bytes_, flops, seconds, peaks, compute="tensor", sustained=False):
+    """Fraction of the binding roofline: HBM bytes vs. the stage's compute
+    ceiling (bf16 tensor cores for the expert GEMM, FP32 FMA pipes for the
+    router); whichever takes longer at its peak is the bound."""
     bw = peaks["hbm_gbs"] * 1e9
-    tc = (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]) * 1e12
-    t_mem, t_tc = bytes_ / bw, flops / tc
-    if t_mem >= t_tc:
+    if compute == "alu":
+        cpk = FP32_ALU_TFLOPS * 1e12
+    else:
+        cpk = (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]) * 1e12
+    t_mem, t_c = bytes_ / bw, flops / cpk
+    if t_mem >= t_c:
         ach = bytes_ / seconds / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"]}
     ach = flops / seconds / 1e12
-    pk = tc / 1e12
-    return {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s", "frac": ach / pk}
+    pk = cpk / 1e12
+    return {"bound": compute, "achieved": ach, "peak": pk, "unit": "TFLOP/s", "frac": ach / pk}
+
+
+STAGE_COMPUTE = {"router": "alu", "topk": "alu", "permute": "alu", "grouped_gemm": "tensor",
+                 "unpermute": "alu"}
 
 
 def traffic_record(kernel_file):
@@ -220,13 +232,20 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             torch.distributed.barrier()
 
-    # ---- device-resident timed region
-    for _ in range(args.warmup):
-        layer(x, out)
-    torch.cuda.synchronize()
-    barrier()
+    # ---- device-resident timed region.  The clock sampler starts with the
+    # warm-up, which runs for at least one second, so its samples cover the GPU
+    # under this load right up to and through the timed steps.
     clocks = ClockSampler(local_rank)
     clocks.start()
+    t_start = time.perf_counter()
+    n_w = 0
+    while n_w < args.warmup or time.perf_counter() - t_start < 1.0:
+        layer(x, out)
+        n_w += 1
+        if n_w % 50 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
@@ -244,6 +263,36 @@ def run_ours(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status {st}")
     ms_step = ms / args.steps
+
+    # ---- the same layer captured once as a CUDA graph and replayed
+    graph_ms = None
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            layer(x, out)
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            layer(x, out)
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = g0.elapsed_time(g1)
+        if world > 1:
+            tt = torch.tensor([graph_ms], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            graph_ms = float(tt.item())
+        del g
+    except Exception as e:  # report, do not hide: the stream number stands
+        log("graph capture failed:", repr(e))
 
     # ---- per-stage times (same workspace, stages called one by one)
     L = layer.layout
@@ -306,11 +355,12 @@ def run_ours(args, rank, world, local_rank):
     sbf = stage_bytes_flops(spec, T, ids_h, e_active)
     per_stage = {}
     for n in names:
-        r = roofline_of(sbf[n]["bytes"], sbf[n]["flops"], stage_ms[n] / 1e3, peaks)
+        r = roofline_of(sbf[n]["bytes"], sbf[n]["flops"], stage_ms[n] / 1e3, peaks, STAGE_COMPUTE[n])
         per_stage[n] = {"us": round(stage_ms[n] * 1e3, 2), "bound": r["bound"],
                         "frac": round(r["frac"], 4)}
     dom = max(names, key=lambda n: stage_ms[n])
-    roof = roofline_of(sbf[dom]["bytes"], sbf[dom]["flops"], stage_ms[dom] / 1e3, peaks)
+    roof = roofline_of(sbf[dom]["bytes"], sbf[dom]["flops"], stage_ms[dom] / 1e3, peaks,
+                       STAGE_COMPUTE[dom])
     roof = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()}
     roof["kernel"] = dom
     roof["peak_source"] = f"of {peaks['source']}"
@@ -343,7 +393,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(tt.item())
 
-    # ---- T sweep (rank 0 only, short)
+    # ---- T sweep (rank 0 only, short): stream launches and graph replay
     sweep = None
     if rank == 0 and args.sweep:
         sweep = []
@@ -355,15 +405,33 @@ def run_ours(args, rank, world, local_rank):
             for _ in range(3):
                 layer(xs, os_)
             torch.cuda.synchronize()
+            n = 50
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            n = 20
             a.record(stream)
             for _ in range(n):
                 layer(xs, os_)
             b.record(stream)
             torch.cuda.synchronize()
             us = a.elapsed_time(b) / n * 1e3
-            sweep.append({"T": Ts, "us_per_layer": round(us, 2), "tokens_per_s": round(Ts / us * 1e6, 1)})
+            row = {"T": Ts, "us_per_layer": round(us, 2), "tokens_per_s": round(Ts / us * 1e6, 1)}
+            try:
+                gs = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gs):
+                    layer(xs, os_)
+                for _ in range(3):
+                    gs.replay()
+                torch.cuda.synchronize()
+                a.record(stream)
+                for _ in range(n):
+                    gs.replay()
+                b.record(stream)
+                torch.cuda.synchronize()
+                ug = a.elapsed_time(b) / n * 1e3
+                row.update(graph_us_per_layer=round(ug, 2), graph_tokens_per_s=round(Ts / ug * 1e6, 1))
+                del gs
+            except Exception as e:
+                log("graph capture failed:", repr(e))
+            sweep.append(row)
 
     # ---- CPU baseline (rank 0, N=1 only)
     cpu = None
@@ -394,6 +462,10 @@ def run_ours(args, rank, world, local_rank):
                          "per layer), no flush"},
         "roofline": roof,
         "per_stage": per_stage,
+        "graph": None if graph_ms is None else {
+            "value": round(tokens / (graph_ms / 1e3), 1), "unit": "tokens/s",
+            "us_per_layer": round(graph_ms / args.steps * 1e3, 2),
+            "note": "same layer captured once as a CUDA graph, replayed K times"},
         "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": out.numel() * out.element_size()},
@@ -480,8 +552,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_30b_a3b")
     ap.add_argument("--T", type=int, default=2048)
-    ap.add_argument("--cpu-tokens", type=int, default=256)
-    ap.add_argument("--ref-tokens", type=int, default=16)
+    ap.add_argument("--cpu-tokens", type=int, default=32768)
+    ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -145,16 +145,21 @@ struct TcCfg {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kNA * kABytes + kBBytes;
-  static constexpr int kStagesRaw = (200 * 1024) / kStageBytes;
+  static constexpr int kEpiBytes = 4 * 16 * 32 * 2;  // per epilogue warp: 16 tokens x 32 features
+  static constexpr int kStagesRaw = (200 * 1024 - kEpiBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-  static constexpr int kAccCols = kNA * BN;
-  static constexpr int kTmemCols = kAccCols <= 32 ? 32 : kAccCols <= 64 ? 64
-                                 : kAccCols <= 128 ? 128 : kAccCols <= 256 ? 256 : 512;
-  static constexpr int kBarBytes = (2 * kStages + 3) * 8 + 16;
-  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
+  static constexpr int kAccCols = kNA * BN;                  // columns of one accumulator set
+  static constexpr int kAccStages = 2 * kAccCols <= 512 ? 2 : 1;
+  static constexpr int kTmemNeed = kAccStages * kAccCols;
+  static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
+                                 : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
+  static constexpr int kBarBytes = (2 * kStages + 2 * kAccStages + 1) * 8 + 16;
+  static constexpr size_t kSmemBytes =
+      1024 + (size_t)kStages * kStageBytes + kEpiBytes + kBarBytes;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+  static_assert(kTmemNeed <= 512, "TMEM holds 512 columns");
 };
 
 MOE_DEVICE float silu_f(float g) { return g / (1.f + __expf(-g)); }
@@ -175,21 +180,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
-  uint8_t* bar_area = smem + (size_t)C::kStages * C::kStageBytes;
+  uint16_t* epi = reinterpret_cast<uint16_t*>(smem + (size_t)C::kStages * C::kStageBytes);
+  uint8_t* bar_area = smem + (size_t)C::kStages * C::kStageBytes + C::kEpiBytes;
   const uint32_t bar0 = smem_u32(bar_area);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
-  const uint32_t acc_full = bar0 + 8u * (2 * C::kStages);
-  const uint32_t acc_empty = acc_full + 8u;
-  const uint32_t drain_bar = acc_full + 16u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::kStages + 3));
+  auto acc_full = [&](uint32_t a) { return bar0 + 8u * (2 * C::kStages + a); };
+  auto acc_empty = [&](uint32_t a) { return bar0 + 8u * (2 * C::kStages + C::kAccStages + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 2 * C::kAccStages);
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::kStages + 2 * C::kAccStages + 1));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    for (int a = 0; a < C::kAccStages; ++a) { mbar_init(acc_full(a), 1); mbar_init(acc_empty(a), 128); }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -212,6 +218,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
     moe_set_status(dev_status, MOE_DEV_WAIT_TIMEOUT);
     *abort_flag = 1;
   };
+  // accumulator set and the parity of its barriers for the i-th unit of this CTA
+  auto acc_set = [](uint32_t i) { return C::kAccStages == 2 ? (i & 1u) : 0u; };
+  auto acc_par = [](uint32_t i) { return (C::kAccStages == 2 ? (i >> 1) : i) & 1u; };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -247,14 +256,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
     if (lane == 0) {
       // ---------------- MMA issuer
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      uint32_t phase = 0, unit = 0;
       bool ok = true, issued = false;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-        if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++unit) {
+        const uint32_t a = acc_set(unit);
+        if (!mbar_wait_bounded(acc_empty(a), acc_par(unit) ^ 1u, abort_flag, kWaitLimitNs)) {
           fail();
           break;
         }
         tc_fence_after();
+        const uint32_t d = tmem + a * C::kAccCols;
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, kWaitLimitNs)) {
             fail();
@@ -268,16 +279,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t acc = (kb | kk) != 0;
             const uint64_t bdesc = sdesc_k128_sw128(sx + kk * 32);
-            tc_mma_f16(tmem, sdesc_k128_sw128(sa + kk * 32), bdesc, C::kIdesc, acc);
-            if (SWIGLU) tc_mma_f16(tmem + BN, sdesc_k128_sw128(sb3 + kk * 32), bdesc, C::kIdesc, acc);
+            tc_mma_f16(d, sdesc_k128_sw128(sa + kk * 32), bdesc, C::kIdesc, acc);
+            if (SWIGLU) tc_mma_f16(d + BN, sdesc_k128_sw128(sb3 + kk * 32), bdesc, C::kIdesc, acc);
           }
           issued = true;
           tc_commit(empty_bar(stage));
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        tc_commit(acc_full);
-        acc_phase ^= 1u;
+        tc_commit(acc_full(a));
       }
       if (issued) {
         // all MMAs of this thread complete before TMEM is released
@@ -287,40 +297,49 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
     }
   } else {
     // ---------------- epilogue, warps 2..5
+    // TMEM lane quarter = warp % 4 = 32 output features; each 16-token chunk
+    // is staged in shared memory and written back as 16-byte row segments.
     const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint32_t acc_phase = 0;
-    for (int w = blockIdx.x; w < total; w += gridDim.x) {
+    uint16_t* stg = epi + quarter * (16 * 32);
+    uint32_t unit = 0;
+    for (int w = blockIdx.x; w < total; w += gridDim.x, ++unit) {
       const int4 it = items[w / nblk];
       const int nb = w % nblk;
-      if (!mbar_wait_bounded(acc_full, acc_phase, abort_flag, kWaitLimitNs)) {
+      const uint32_t a = acc_set(unit);
+      if (!mbar_wait_bounded(acc_full(a), acc_par(unit), abort_flag, kWaitLimitNs)) {
         fail();
         break;
       }
       tc_fence_after();
-      const int n = nb * kBM + row;
+      const uint32_t tacc = t_lane + a * C::kAccCols;
       const int m = it.z;
       for (int c0 = 0; c0 < BN && c0 < m; c0 += 16) {
         uint32_t g[16], u[16];
-        tc_ld_32x32b_x16(t_lane + c0, g);
-        if (SWIGLU) tc_ld_32x32b_x16(t_lane + BN + c0, u);
+        tc_ld_32x32b_x16(tacc + c0, g);
+        if (SWIGLU) tc_ld_32x32b_x16(tacc + BN + c0, u);
         tc_wait_ld();
-        if (n < N) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int tok = c0 + j;
-            if (tok < m) {
-              const float gv = __uint_as_float(g[j]);
-              const float v = SWIGLU ? silu_f(gv) * __uint_as_float(u[j]) : gv;
-              out[(size_t)(it.y + tok) * N + n] = __float2bfloat16_rn(v);
-            }
+        for (int j = 0; j < 16; ++j) {
+          const float gv = __uint_as_float(g[j]);
+          const float v = SWIGLU ? silu_f(gv) * __uint_as_float(u[j]) : gv;
+          stg[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        }
+        __syncwarp();
+        // 16 token rows x 64 bytes: lane -> (row lane/4 (+8), 16-byte chunk lane%4)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int r = (lane >> 2) + 8 * i;
+          const int n0 = nb * kBM + quarter * 32 + (lane & 3) * 8;
+          if (c0 + r < m && n0 < N) {
+            const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 32 + (lane & 3) * 8);
+            *reinterpret_cast<uint4*>(out + (size_t)(it.y + c0 + r) * N + n0) = v;
           }
         }
+        __syncwarp();
       }
       tc_fence_before();
-      mbar_arrive(acc_empty);
-      acc_phase ^= 1u;
+      mbar_arrive(acc_empty(a));
     }
   }
 

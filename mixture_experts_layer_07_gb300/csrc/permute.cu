@@ -11,7 +11,7 @@
 // replicas f' < f with the same expert, so the result is unique and the
 // kernels need no sort and no cross-CTA waits:
 //   1. count   one warp per 256-replica chunk: per-chunk expert histogram
-//   2. scan    one CTA: per expert, exclusive scan over chunks; then an
+//   2. scan    one CTA: a warp per expert scans its chunk counts; then an
 //              exclusive scan over experts gives offsets[E+1]
 //   3. scatter one warp per chunk, 32 replicas per step in order: lanes with
 //              the same expert find each other with __match_any_sync, the
@@ -25,7 +25,7 @@ namespace {
 constexpr int kChunk = 256;        // replicas per warp chunk
 constexpr int kWarpsPerCta = 8;
 
-// scratch: int32 counts[nchunks][E] (turned into per-chunk bases by the scan)
+// scratch: int32 counts[E][nchunks] (turned into per-chunk bases by the scan)
 inline int num_chunks(int R) { return moe_cdiv(R, kChunk); }
 
 __global__ void __launch_bounds__(32 * kWarpsPerCta)
@@ -48,46 +48,61 @@ permute_count_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunks,
       }
     }
     __syncwarp();
-    for (int e = lane; e < E; e += 32) counts[(size_t)chunk * E + e] = h[e];
+    for (int e = lane; e < E; e += 32) counts[(size_t)e * nchunks + chunk] = h[e];
   }
 }
 
+// counts[e][c] -> exclusive prefix over chunks (in place), one warp per expert
+// (32 chunks per step, warp scan), then an exclusive scan of the per-expert
+// totals over the block gives offsets[E+1].
 __global__ void __launch_bounds__(1024)
 permute_scan_kernel(int32_t* __restrict__ counts, int E, int nchunks,
                     int32_t* __restrict__ offsets) {
+  __shared__ int32_t tot[1024];
   __shared__ int32_t warp_tot[32];
-  const int e = threadIdx.x;
-  int32_t run = 0;
-  if (e < E) {
-    for (int c = 0; c < nchunks; ++c) {
-      const int32_t v = counts[(size_t)c * E + e];
-      counts[(size_t)c * E + e] = run;
-      run += v;
+  const int lane = lane_id(), warp = warp_id();
+  for (int e = warp; e < E; e += 32) {
+    int32_t* row = counts + (size_t)e * nchunks;
+    int32_t run = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int32_t v = c < nchunks ? row[c] : 0;
+      int32_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (c < nchunks) row[c] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (lane == 0) tot[e] = run;
   }
-  // exclusive scan of the per-expert totals across the block
-  int32_t incl = run;
+  __syncthreads();
+  const int e = threadIdx.x;
+  const int32_t mine = e < E ? tot[e] : 0;
+  int32_t incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane_id() >= o) incl += n;
+    if (lane >= o) incl += n;
   }
-  if (lane_id() == 31) warp_tot[warp_id()] = incl;
+  if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
-  if (warp_id() == 0) {
-    int32_t v = warp_tot[lane_id()];
-    int32_t s = v;
+  if (warp == 0) {
+    const int32_t v = warp_tot[lane];
+    int32_t sc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int32_t n = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane_id() >= o) s += n;
+      const int32_t n = __shfl_up_sync(0xffffffffu, sc, o);
+      if (lane >= o) sc += n;
     }
-    warp_tot[lane_id()] = s - v;  // exclusive prefix of the warps
+    warp_tot[lane] = sc - v;
   }
   __syncthreads();
-  const int32_t excl = incl - run + warp_tot[warp_id()];
+  const int32_t excl = incl - mine + warp_tot[warp];
   if (e < E) offsets[e] = excl;
-  if (e == E - 1) offsets[E] = excl + run;
+  if (e == E - 1) offsets[E] = excl + mine;
 }
 
 __global__ void __launch_bounds__(32 * kWarpsPerCta)
@@ -99,7 +114,7 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunk
   const int chunk = blockIdx.x * kWarpsPerCta + w;
   if (chunk >= nchunks) return;
   int32_t* cnt = cnt_all + w * E;
-  for (int e = lane; e < E; e += 32) cnt[e] = offsets[e] + bases[(size_t)chunk * E + e];
+  for (int e = lane; e < E; e += 32) cnt[e] = offsets[e] + bases[(size_t)e * nchunks + chunk];
   __syncwarp();
   const unsigned lt_mask = (1u << lane) - 1u;
   const int f0 = chunk * kChunk;

@@ -8,13 +8,17 @@
 // the gate must stay in fp32 precision, so tensor cores (tf32) are not used.
 //
 // Two kernels:
-//  * decode (T <= 16): bound by reading wg once (4*G*H bytes).  A CTA owns ROWS
+//  * decode (T <= 32): bound by reading wg once (4*G*H bytes).  A CTA owns ROWS
 //    gate rows; its 256 threads split H in 8-element chunks, accumulate all
 //    tokens of an 8-token group, and reduce across the block in a fixed tree.
-//  * prefill (T > 16): FP32-FMA bound (2*T*G*H flops).  A 64x64 output tile per
-//    CTA, bf16 tile widened while it is staged into shared memory, 4x4
-//    register micro-tile per thread.
+//  * prefill (T > 32): FP32-FMA bound (2*T*G*H flops).  64x64 output tiles,
+//    the bf16 tile widened while it is staged into shared memory, an 8x4
+//    register micro-tile per thread, and H split across the CTAs of a
+//    thread-block cluster (reduced through distributed shared memory) so that
+//    small T x G still fills the GPU.
 // Both are deterministic: the order of the sums depends only on the sizes.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -22,6 +26,7 @@ namespace {
 
 constexpr int kSmallThreads = 256;
 constexpr int kSmallTok = 8;
+constexpr int kSmallMaxT = 32;  // up to here the gate-weight stream dominates
 
 template <int ROWS>
 __global__ void __launch_bounds__(kSmallThreads)
@@ -93,73 +98,120 @@ router_small_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict
 constexpr int kBM = 64;  // tokens per tile
 constexpr int kBN = 64;  // gate rows per tile
 constexpr int kBK = 32;  // H per stage
+constexpr int kTiledThreads = 128;
 
-__global__ void __launch_bounds__(256)
-router_tiled_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wg,
-                    const float* __restrict__ bias, float* __restrict__ logits, int T, int H,
-                    int G) {
-  // transposed tiles, padded so the transposing stores are conflict free
-  __shared__ float xs[kBK][kBM + 1];
-  __shared__ float ws[kBK][kBN + 1];
+// One CTA computes a 64x64 logit tile over its slice of H; the `splits` CTAs
+// of a thread-block cluster take consecutive slices and the partial tiles are
+// summed through distributed shared memory in rank order (deterministic, no
+// global scratch, no atomics).  Thread (ty, tx) owns tokens 8ty..8ty+7 and
+// gate rows 4tx..4tx+3; operands are staged transposed so that each k step is
+// two 16-byte loads of x (a broadcast across the warp) and one of wg.
+__global__ void __launch_bounds__(kTiledThreads)
+router_cluster_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wg,
+                      const float* __restrict__ bias, float* __restrict__ logits, int T, int H,
+                      int G, int kchunk) {
+  __shared__ __align__(16) float xs[kBK][kBM + 4];
+  __shared__ __align__(16) float ws[kBK][kBN + 4];
+  __shared__ __align__(16) float part[kBM][kBN + 4];
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int splits = (int)cluster.num_blocks();
   const int tid = threadIdx.x;
+  const int ty = tid / 16, tx = tid % 16;
   const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
-  const int ty = tid / 16, tx = tid % 16;  // token m = ty + 16 i, gate n = tx + 16 j
-  float acc[4][4];
+  const int k_lo = rank * kchunk;
+  const int k_hi = min(H, k_lo + kchunk);
+
+  float acc[8][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 
-  // x tile: 64 rows x 32 bf16 = 256 uint4, one per thread
-  const int xr = tid / 4, xc = (tid % 4) * 8;
-  for (int k0 = 0; k0 < H; k0 += kBK) {
-    {
-      float f[8];
-      if (m0 + xr < T && k0 + xc < H) {
-        uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(m0 + xr) * H + k0 + xc));
-        bf16x8_to_f32(v, f);
-      } else {
+  uint4 xr[2];
+  float4 wr[4];
+  auto load = [&](int k0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) xs[xc + i][xr] = f[i];
+    for (int q = 0; q < 2; ++q) {  // 64 rows x 32 bf16 = 256 vectors
+      const int idx = tid + q * kTiledThreads;
+      const int r = idx / 4, c = (idx % 4) * 8;
+      xr[q] = (m0 + r < T && k0 + c < k_hi)
+                  ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(m0 + r) * H + k0 + c))
+                  : make_uint4(0u, 0u, 0u, 0u);
     }
-    // wg tile: 64 rows x 32 fp32 = 512 float4, two per thread
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // 64 rows x 32 fp32 = 512 vectors
+      const int idx = tid + q * kTiledThreads;
+      const int r = idx / 8, c = (idx % 8) * 4;
+      wr[q] = (n0 + r < G && k0 + c < k_hi)
+                  ? __ldg(reinterpret_cast<const float4*>(wg + (size_t)(n0 + r) * H + k0 + c))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  auto stage = [&]() {
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const int idx = tid + q * 256;
-      const int wr = idx / 8, wc = (idx % 8) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (n0 + wr < G && k0 + wc < H)
-        v = __ldg(reinterpret_cast<const float4*>(wg + (size_t)(n0 + wr) * H + k0 + wc));
-      ws[wc + 0][wr] = v.x; ws[wc + 1][wr] = v.y; ws[wc + 2][wr] = v.z; ws[wc + 3][wr] = v.w;
+      const int idx = tid + q * kTiledThreads;
+      const int r = idx / 4, c = (idx % 4) * 8;
+      float f[8];
+      bf16x8_to_f32(xr[q], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[c + i][r] = f[i];
     }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int idx = tid + q * kTiledThreads;
+      const int r = idx / 8, c = (idx % 8) * 4;
+      ws[c + 0][r] = wr[q].x; ws[c + 1][r] = wr[q].y; ws[c + 2][r] = wr[q].z; ws[c + 3][r] = wr[q].w;
+    }
+  };
+
+  if (k_lo < k_hi) load(k_lo);
+  for (int k0 = k_lo; k0 < k_hi; k0 += kBK) {
+    stage();
     __syncthreads();
+    if (k0 + kBK < k_hi) load(k0 + kBK);  // next tile's loads overlap this tile's math
 #pragma unroll 8
     for (int k = 0; k < kBK; ++k) {
-      float a[4], b[4];
+      const float4 a0 = *reinterpret_cast<const float4*>(&xs[k][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&xs[k][ty * 8 + 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[k][tx * 4]);
+      const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = xs[k][ty + 16 * i];
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = ws[k][tx + 16 * j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty + 16 * i;
-    if (m >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx + 16 * j;
-      if (n < G) logits[(size_t)m * G + n] = acc[i][j] + (bias ? bias[n] : 0.f);
-    }
+  for (int i = 0; i < 8; ++i)
+    *reinterpret_cast<float4*>(&part[ty * 8 + i][tx * 4]) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+  cluster.sync();
+  // rank r sums rows [r*64/splits, (r+1)*64/splits) of the tile over the cluster
+  const int rows = kBM / splits;
+  for (int e = tid; e < rows * kBN; e += kTiledThreads) {
+    const int r = rank * rows + e / kBN, c = e % kBN;
+    float sum = 0.f;
+    for (int q = 0; q < splits; ++q) sum += cluster.map_shared_rank(&part[r][c], q)[0];
+    const int m = m0 + r, n = n0 + c;
+    if (m < T && n < G) logits[(size_t)m * G + n] = sum + (bias ? bias[n] : 0.f);
   }
+  cluster.sync();  // keep this CTA's partial tile alive until every rank has read it
+}
+
+int num_sms_router() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0, v = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n = v > 0 ? v : 148;
+  }
+  return n;
 }
 
 }  // namespace
@@ -167,7 +219,7 @@ router_tiled_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict
 cudaError_t launch_router_gemm(const void* x, const float* wg, const float* gate_bias,
                                float* logits, int T, int H, int G, cudaStream_t stream) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  if (T <= 16) {
+  if (T <= kSmallMaxT) {
     if (G <= 256) {
       router_small_kernel<1><<<G, kSmallThreads, 0, stream>>>(xb, wg, gate_bias, logits, T, H, G);
     } else if (G <= 512) {
@@ -178,8 +230,27 @@ cudaError_t launch_router_gemm(const void* x, const float* wg, const float* gate
                                                                           logits, T, H, G);
     }
   } else {
-    dim3 grid(moe_cdiv(G, kBN), moe_cdiv(T, kBM));
-    router_tiled_kernel<<<grid, 256, 0, stream>>>(xb, wg, gate_bias, logits, T, H, G);
+    // split H over a cluster until there are about two CTAs per SM
+    const int tiles = moe_cdiv(G, kBN) * moe_cdiv(T, kBM);
+    int splits = 1;
+    while (splits < 8 && tiles * splits < 2 * num_sms_router() && H / (splits * 2) >= 2 * kBK)
+      splits *= 2;
+    const int kchunk = moe_cdiv(moe_cdiv(H, splits), kBK) * kBK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(moe_cdiv(G, kBN), moe_cdiv(T, kBM), splits);
+    cfg.blockDim = dim3(kTiledThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = splits;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, router_cluster_kernel, xb, wg, gate_bias, logits, T,
+                                       H, G, kchunk);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
