@@ -140,7 +140,7 @@ def launches_per_layer(spec, dispatch=0):
     launch sequence): router 1, top-K 1, permute 4 (count, scan, scatter,
     gather), grouped GEMM 1 plan + 4 GEMM (skinny/tile x G1/G2) or 2 GEMM on
     the CUDA-core path, combine 1; a shared expert adds one grouped GEMM."""
-    simt = dispatch == 2 or spec.wdtype == "fp8"
+    simt = dispatch == 2
     gemm = 1 + (2 if simt else 4)
     shared = (1 + (2 if dispatch == 2 else 4)) if spec.has_shared else 0
     return 1 + 1 + 4 + gemm + shared + 1

@@ -36,9 +36,8 @@
 // MOE_DEV_WAIT_TIMEOUT, the CTA drains its own in-flight copies and MMAs
 // (again bounded), frees its TMEM and returns.
 //
-// A CUDA-core kernel (MOE_DISPATCH_SIMT, and the FP8 weight format for now)
-// runs the same work list with plain FMA; it is the cross-check of the
-// tensor-core path and the FP8 (e4m3 + 128x128 block scale) path.
+// A CUDA-core kernel (MOE_DISPATCH_SIMT) runs the same work list with plain
+// FMA, bf16 or e4m3 weights; it is the cross-check of the tensor-core path.
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -139,38 +138,65 @@ gemm_plan_kernel(const int32_t* __restrict__ offsets, int E_blocks, int R, int m
 }
 
 // ---------------------------------------------------------------- tensor cores
-template <int BN, bool SWIGLU>
+// WFP8: expert weights are e4m3 with one fp32 scale per 128 x 128 block.  TMA
+// brings the e4m3 tile [128 rows x 64 K] in unswizzled; a converter warpgroup
+// turns it into bf16 (e4m3 -> f16 is exact, times the block's scale, rounded
+// once to bf16) written straight into the 128-byte-swizzled K-major layout the
+// MMA reads, in a small ring of its own.  The 128-row weight tile is exactly
+// one scale row block and a 64-wide K stage lies inside one scale column
+// block, so each converted tile needs a single scale.
+template <int BN, bool SWIGLU, bool WFP8>
 struct TcCfg {
   static constexpr int kNA = SWIGLU ? 2 : 1;
-  static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
-  static constexpr int kStageBytes = kNA * kABytes + kBBytes;
+  static constexpr int kABytes = kBM * kBK * 2;             // bf16 weight tile
+  static constexpr int kQBytes = kBM * kBK;                 // e4m3 weight tile
+  static constexpr int kBBytes = BN * kBK * 2;              // bf16 activation tile
+  static constexpr int kStageBytes = kNA * (WFP8 ? kQBytes : kABytes) + kBBytes;
+  static constexpr int kConvStages = WFP8 ? 2 : 0;
+  static constexpr int kConvBytes = kNA * kABytes;
   static constexpr int kEpiBytes = 4 * 16 * 32 * 2;  // per epilogue warp: 16 tokens x 32 features
-  static constexpr int kStagesRaw = (200 * 1024 - kEpiBytes) / kStageBytes;
+  static constexpr int kStagesRaw =
+      (200 * 1024 - kEpiBytes - kConvStages * kConvBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kAccCols = kNA * BN;                  // columns of one accumulator set
   static constexpr int kAccStages = 2 * kAccCols <= 512 ? 2 : 1;
   static constexpr int kTmemNeed = kAccStages * kAccCols;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
                                  : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
-  static constexpr int kBarBytes = (2 * kStages + 2 * kAccStages + 1) * 8 + 16;
-  static constexpr size_t kSmemBytes =
-      1024 + (size_t)kStages * kStageBytes + kEpiBytes + kBarBytes;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 1 + 2 * kConvStages;
+  static constexpr int kBarBytes = kNumBars * 8 + 16;
+  static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes +
+                                       (size_t)kConvStages * kConvBytes + kEpiBytes + kBarBytes;
+  static constexpr int kThreads = WFP8 ? 320 : 192;  // + one converter warpgroup
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(kTmemNeed <= 512, "TMEM holds 512 columns");
+  static_assert(kStages >= 2, "pipeline needs two stages");
 };
 
 MOE_DEVICE float silu_f(float g) { return g / (1.f + __expf(-g)); }
 
-template <int BN, bool SWIGLU>
-__global__ void __launch_bounds__(192, 1)
+MOE_DEVICE void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// two e4m3 codes (low byte first) -> two bf16 of code * scale, packed low first
+MOE_DEVICE uint32_t e4m3x2_to_bf16x2(uint32_t two, float sc) {
+  const __half2_raw hr =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  return pack_bf16x2(f.x * sc, f.y * sc);
+}
+
+template <int BN, bool SWIGLU, bool WFP8>
+__global__ void __launch_bounds__(TcCfg<BN, SWIGLU, WFP8>::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wb,
-               const __grid_constant__ CUtensorMap tm_act, const int32_t* __restrict__ counts,
-               int list, const int4* __restrict__ items, int N, int Kdim,
-               __nv_bfloat16* __restrict__ out, int32_t* dev_status) {
-  using C = TcCfg<BN, SWIGLU>;
+               const __grid_constant__ CUtensorMap tm_act, const float* __restrict__ sa,
+               const float* __restrict__ sb, const int32_t* __restrict__ counts, int list,
+               const int4* __restrict__ items, int N, int Kdim, __nv_bfloat16* __restrict__ out,
+               int32_t* dev_status) {
+  using C = TcCfg<BN, SWIGLU, WFP8>;
   const int nblk = (N + kBM - 1) / kBM;
   const int total = counts[list] * nblk;
   if ((int)blockIdx.x >= total) return;
@@ -180,16 +206,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
   const uint32_t sbase = smem_u32(smem);
-  uint16_t* epi = reinterpret_cast<uint16_t*>(smem + (size_t)C::kStages * C::kStageBytes);
-  uint8_t* bar_area = smem + (size_t)C::kStages * C::kStageBytes + C::kEpiBytes;
+  uint8_t* conv = smem + (size_t)C::kStages * C::kStageBytes;
+  const uint32_t cbase = smem_u32(conv);
+  uint16_t* epi = reinterpret_cast<uint16_t*>(conv + (size_t)C::kConvStages * C::kConvBytes);
+  uint8_t* bar_area = reinterpret_cast<uint8_t*>(epi) + C::kEpiBytes;
   const uint32_t bar0 = smem_u32(bar_area);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
   auto acc_full = [&](uint32_t a) { return bar0 + 8u * (2 * C::kStages + a); };
   auto acc_empty = [&](uint32_t a) { return bar0 + 8u * (2 * C::kStages + C::kAccStages + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 2 * C::kAccStages);
-  uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(bar_area + 8 * (2 * C::kStages + 2 * C::kAccStages + 1));
+  auto conv_full = [&](int c) { return drain_bar + 8u * (1 + c); };
+  auto conv_empty = [&](int c) { return drain_bar + 8u * (1 + C::kConvStages + c); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
@@ -197,6 +226,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
     for (int s = 0; s < C::kStages; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
     for (int a = 0; a < C::kAccStages; ++a) { mbar_init(acc_full(a), 1); mbar_init(acc_empty(a), 128); }
     mbar_init(drain_bar, 1);
+    for (int c = 0; c < C::kConvStages; ++c) { mbar_init(conv_full(c), 128); mbar_init(conv_empty(c), 1); }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -221,6 +251,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
   // accumulator set and the parity of its barriers for the i-th unit of this CTA
   auto acc_set = [](uint32_t i) { return C::kAccStages == 2 ? (i & 1u) : 0u; };
   auto acc_par = [](uint32_t i) { return (C::kAccStages == 2 ? (i >> 1) : i) & 1u; };
+  constexpr int kWeightBytes = WFP8 ? C::kQBytes : C::kABytes;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -240,8 +271,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
           const uint32_t st = sbase + stage * C::kStageBytes;
           mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
           tma_load_3d(st, &tm_wa, full_bar(stage), kb * kBK, nb * kBM, it.x);
-          if (SWIGLU) tma_load_3d(st + C::kABytes, &tm_wb, full_bar(stage), kb * kBK, nb * kBM, it.x);
-          tma_load_2d(st + C::kNA * C::kABytes, &tm_act, full_bar(stage), kb * kBK, it.y);
+          if (SWIGLU) tma_load_3d(st + kWeightBytes, &tm_wb, full_bar(stage), kb * kBK, nb * kBM, it.x);
+          tma_load_2d(st + C::kNA * kWeightBytes, &tm_act, full_bar(stage), kb * kBK, it.y);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -255,8 +286,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      int stage = 0;
-      uint32_t phase = 0, unit = 0;
+      int stage = 0, cs = 0;
+      uint32_t phase = 0, cphase = 0, unit = 0;
       bool ok = true, issued = false;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++unit) {
         const uint32_t a = acc_set(unit);
@@ -267,23 +298,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
         tc_fence_after();
         const uint32_t d = tmem + a * C::kAccCols;
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, kWaitLimitNs)) {
+          if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, kWaitLimitNs) ||
+              (WFP8 && !mbar_wait_bounded(conv_full(cs), cphase, abort_flag, kWaitLimitNs))) {
             fail();
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t st = sbase + stage * C::kStageBytes;
-          const uint32_t sa = st, sb3 = st + C::kABytes, sx = st + C::kNA * C::kABytes;
+          const uint32_t wa_s = WFP8 ? cbase + cs * C::kConvBytes : st;
+          const uint32_t wb_s = wa_s + C::kABytes;
+          const uint32_t sx = st + C::kNA * kWeightBytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint32_t acc = (kb | kk) != 0;
             const uint64_t bdesc = sdesc_k128_sw128(sx + kk * 32);
-            tc_mma_f16(d, sdesc_k128_sw128(sa + kk * 32), bdesc, C::kIdesc, acc);
-            if (SWIGLU) tc_mma_f16(d + BN, sdesc_k128_sw128(sb3 + kk * 32), bdesc, C::kIdesc, acc);
+            tc_mma_f16(d, sdesc_k128_sw128(wa_s + kk * 32), bdesc, C::kIdesc, acc);
+            if (SWIGLU) tc_mma_f16(d + BN, sdesc_k128_sw128(wb_s + kk * 32), bdesc, C::kIdesc, acc);
           }
           issued = true;
           tc_commit(empty_bar(stage));
+          if (WFP8) {
+            tc_commit(conv_empty(cs));
+            if (++cs == C::kConvStages) { cs = 0; cphase ^= 1u; }
+          }
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -295,7 +333,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
         if (!mbar_wait_bounded(drain_bar, 0, nullptr, kWaitLimitNs)) fail();
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ---------------- epilogue, warps 2..5
     // TMEM lane quarter = warp % 4 = 32 output features; each 16-token chunk
     // is staged in shared memory and written back as 16-byte row segments.
@@ -340,6 +378,54 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
       }
       tc_fence_before();
       mbar_arrive(acc_empty(a));
+    }
+  } else if (WFP8) {
+    // ---------------- e4m3 -> bf16 converters, warps 6..9
+    const int ct = threadIdx.x - 192;
+    const int rb = (N + 127) / 128, cb = (Kdim + 127) / 128;
+    int stage = 0, cs = 0;
+    uint32_t phase = 0, cphase = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      const int4 it = items[w / nblk];
+      const int nb = w % nblk;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, kWaitLimitNs) ||
+            !mbar_wait_bounded(conv_empty(cs), cphase ^ 1u, abort_flag, kWaitLimitNs)) {
+          fail();
+          ok = false;
+          break;
+        }
+        const size_t sidx = ((size_t)it.x * rb + nb) * cb + (kb * kBK) / 128;
+        const float scl[2] = {__ldg(sa + sidx), SWIGLU ? __ldg(sb + sidx) : 0.f};
+#pragma unroll
+        for (int t = 0; t < C::kNA; ++t) {
+          const uint8_t* src = smem + (size_t)stage * C::kStageBytes + t * C::kQBytes;
+          uint8_t* dst = conv + (size_t)cs * C::kConvBytes + t * C::kABytes;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int q = ct + 128 * i;  // 16-byte e4m3 chunk: row q/4, K 16*(q%4) .. +15
+            const int r = q >> 2, j = q & 3;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + j * 16);
+            uint4 lo, hi;
+            lo.x = e4m3x2_to_bf16x2(v.x & 0xFFFFu, scl[t]);
+            lo.y = e4m3x2_to_bf16x2(v.x >> 16, scl[t]);
+            lo.z = e4m3x2_to_bf16x2(v.y & 0xFFFFu, scl[t]);
+            lo.w = e4m3x2_to_bf16x2(v.y >> 16, scl[t]);
+            hi.x = e4m3x2_to_bf16x2(v.z & 0xFFFFu, scl[t]);
+            hi.y = e4m3x2_to_bf16x2(v.z >> 16, scl[t]);
+            hi.z = e4m3x2_to_bf16x2(v.w & 0xFFFFu, scl[t]);
+            hi.w = e4m3x2_to_bf16x2(v.w >> 16, scl[t]);
+            // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
+            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * j) ^ (r & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
+          }
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+        mbar_arrive(conv_full(cs));
+        if (++cs == C::kConvStages) { cs = 0; cphase ^= 1u; }
+        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+      }
     }
   }
 
@@ -447,16 +533,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [E][N][Kdim] bf16 weights, box 64 (K) x 128 (N) x 1
-bool make_weight_map(CUtensorMap* m, const void* w, int E, int N, int Kdim) {
+// [E][N][Kdim] weights, box 64 (K) x 128 (N) x 1: bf16 in the 128-byte swizzle
+// the MMA reads, or e4m3 bytes unswizzled (the converters re-lay them out)
+bool make_weight_map(CUtensorMap* m, const void* w, int E, int N, int Kdim, bool fp8 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  const int eb = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)Kdim, (cuuint64_t)N, (cuuint64_t)E};
-  cuuint64_t strides[2] = {(cuuint64_t)Kdim * 2, (cuuint64_t)N * Kdim * 2};
+  cuuint64_t strides[2] = {(cuuint64_t)Kdim * eb, (cuuint64_t)N * Kdim * eb};
   cuuint32_t box[3] = {kBK, kBM, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(w), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+             const_cast<void*>(w), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -486,14 +575,15 @@ int num_sms() {
   return n[dev];
 }
 
-template <int BN, bool SWIGLU>
+template <int BN, bool SWIGLU, bool WFP8>
 cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorMap& act,
-                   const int32_t* counts, int list, const int4* items, int cap, int N, int Kdim,
-                   void* out, int32_t* dev_status, cudaStream_t stream) {
-  using C = TcCfg<BN, SWIGLU>;
+                   const float* sa, const float* sb, const int32_t* counts, int list,
+                   const int4* items, int cap, int N, int Kdim, void* out, int32_t* dev_status,
+                   cudaStream_t stream) {
+  using C = TcCfg<BN, SWIGLU, WFP8>;
   static bool attr_set = false;  // per process; the attribute is per function, all devices
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, SWIGLU>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, SWIGLU, WFP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -502,9 +592,36 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
   const long long work = (long long)cap * moe_cdiv(N, kBM);
   const int grid = (int)(work < num_sms() ? work : num_sms());
   if (grid <= 0) return cudaSuccess;
-  gemm_tc_kernel<BN, SWIGLU><<<grid, 192, C::kSmemBytes, stream>>>(
-      wa, wb, act, counts, list, items, N, Kdim, static_cast<__nv_bfloat16*>(out), dev_status);
+  gemm_tc_kernel<BN, SWIGLU, WFP8><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
+      wa, wb, act, sa, sb, counts, list, items, N, Kdim, static_cast<__nv_bfloat16*>(out),
+      dev_status);
   return cudaGetLastError();
+}
+
+template <bool WFP8>
+cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const void* w1,
+                       const void* w3, const void* w2, const float* s1, const float* s3,
+                       const float* s2, void* hact, void* y, const PlanView& pv,
+                       int32_t* dev_status, cudaStream_t stream) {
+  CUtensorMap m_w1, m_w3, m_w2, m_x16, m_x128, m_h16, m_h128;
+  if (!make_weight_map(&m_w1, w1, E_blocks, I, H, WFP8) ||
+      !make_weight_map(&m_w3, w3, E_blocks, I, H, WFP8) ||
+      !make_weight_map(&m_w2, w2, E_blocks, H, I, WFP8) ||
+      !make_act_map(&m_x16, xp, R, H, kBnSkinny) || !make_act_map(&m_x128, xp, R, H, kBnTile) ||
+      !make_act_map(&m_h16, hact, R, I, kBnSkinny) || !make_act_map(&m_h128, hact, R, I, kBnTile))
+    return cudaErrorInvalidValue;
+  cudaError_t err;
+  err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x16, s1, s3, pv.counts, 0, pv.items_s,
+                                      pv.cap_s, I, H, hact, dev_status, stream);
+  if (err != cudaSuccess) return err;
+  err = run_tc<kBnTile, true, WFP8>(m_w1, m_w3, m_x128, s1, s3, pv.counts, 1, pv.items_t,
+                                    pv.cap_t, I, H, hact, dev_status, stream);
+  if (err != cudaSuccess) return err;
+  err = run_tc<kBnSkinny, false, WFP8>(m_w2, m_w2, m_h16, s2, s2, pv.counts, 0, pv.items_s,
+                                       pv.cap_s, H, I, y, dev_status, stream);
+  if (err != cudaSuccess) return err;
+  return run_tc<kBnTile, false, WFP8>(m_w2, m_w2, m_h128, s2, s2, pv.counts, 1, pv.items_t,
+                                      pv.cap_t, H, I, y, dev_status, stream);
 }
 
 template <bool SWIGLU>
@@ -545,12 +662,10 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 int32_t* dev_status, cudaStream_t stream) {
   if (m_skinny < 0) m_skinny = MOE_DEFAULT_M_SKINNY;
   const bool fp8 = wdtype == MOE_W_FP8E4M3_B128;
-  // the FP8 weight format runs on the CUDA-core kernel for now
-  const bool simt = dispatch == MOE_DISPATCH_SIMT || fp8;
-  const int plan_dispatch = simt ? MOE_DISPATCH_SIMT : dispatch;
+  const bool simt = dispatch == MOE_DISPATCH_SIMT;
   PlanView pv = plan_view(scratch, R, E_blocks);
-  gemm_plan_kernel<<<1, 1024, 0, stream>>>(offsets, E_blocks, R, m_skinny, plan_dispatch,
-                                           pv.counts, pv.items_s, pv.items_t, block_variant);
+  gemm_plan_kernel<<<1, 1024, 0, stream>>>(offsets, E_blocks, R, m_skinny, dispatch, pv.counts,
+                                           pv.items_s, pv.items_t, block_variant);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess || R == 0) return err;
 
@@ -560,23 +675,9 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
     return run_simt<false>(fp8, hact, w2, nullptr, s2, nullptr, pv.counts, pv.items_s, pv.cap_s, H,
                            I, y, stream);
   }
-
-  CUtensorMap m_w1, m_w3, m_w2, m_x16, m_x128, m_h16, m_h128;
-  if (!make_weight_map(&m_w1, w1, E_blocks, I, H) || !make_weight_map(&m_w3, w3, E_blocks, I, H) ||
-      !make_weight_map(&m_w2, w2, E_blocks, H, I) || !make_act_map(&m_x16, xp, R, H, kBnSkinny) ||
-      !make_act_map(&m_x128, xp, R, H, kBnTile) || !make_act_map(&m_h16, hact, R, I, kBnSkinny) ||
-      !make_act_map(&m_h128, hact, R, I, kBnTile))
-    return cudaErrorInvalidValue;
-
-  err = run_tc<kBnSkinny, true>(m_w1, m_w3, m_x16, pv.counts, 0, pv.items_s, pv.cap_s, I, H, hact,
-                                dev_status, stream);
-  if (err != cudaSuccess) return err;
-  err = run_tc<kBnTile, true>(m_w1, m_w3, m_x128, pv.counts, 1, pv.items_t, pv.cap_t, I, H, hact,
-                              dev_status, stream);
-  if (err != cudaSuccess) return err;
-  err = run_tc<kBnSkinny, false>(m_w2, m_w2, m_h16, pv.counts, 0, pv.items_s, pv.cap_s, H, I, y,
-                                 dev_status, stream);
-  if (err != cudaSuccess) return err;
-  return run_tc<kBnTile, false>(m_w2, m_w2, m_h128, pv.counts, 1, pv.items_t, pv.cap_t, H, I, y,
-                                dev_status, stream);
+  if (fp8)
+    return run_tc_all<true>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
+                            stream);
+  return run_tc_all<false>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
+                           stream);
 }

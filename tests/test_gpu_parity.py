@@ -258,7 +258,10 @@ GEMM_CASES = [  # spec name, overrides, T, concentrated, dispatch, m_skinny, bot
     ("tiny", {"H": 2880, "I": 2880, "E": 4}, 40, False, 0, 64, False),
     ("tiny", {"H": 320, "I": 192, "E": 6}, 200, True, 0, -1, False),
     ("tiny", {"H": 160, "I": 144, "E": 5, "wdtype": "fp8"}, 50, True, 0, -1, False),
-    ("gpt_oss_20b", {"E": 6}, 40, True, 0, -1, False),
+    ("tiny", {"H": 160, "I": 144, "E": 5, "wdtype": "fp8"}, 50, True, 2, -1, False),
+    ("gpt_oss_20b", {}, 40, True, 0, -1, True),
+    ("gpt_oss_20b", {"E": 6}, 40, True, 2, -1, False),
+    ("gpt_oss_20b", {"E": 4}, 300, True, 0, -1, False),
 ]
 
 
@@ -275,8 +278,7 @@ def test_grouped_gemm(ops, name, over, T, conc, dispatch, m_skinny, both):
     U.assert_bf16_close(U.f64(y), ry, rel, "y")
     R = T * spec.K
     m = np.diff(off)
-    want_bv = [ops.block_variant(int(mm), R, spec.E, m_skinny,
-                                 ops.DISPATCH_SIMT if spec.wdtype == "fp8" else dispatch) for mm in m]
+    want_bv = [ops.block_variant(int(mm), R, spec.E, m_skinny, dispatch) for mm in m]
     assert bv.tolist() == want_bv
     if both:  # skinny and tile blocks in the same call
         assert {ops.VARIANT_SKINNY, ops.VARIANT_TILE} <= set(bv.tolist())
