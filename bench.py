@@ -123,6 +123,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(ms, world, device=None):
+    """Slowest rank's time: every rank passes its own, all get the max."""
+    if world <= 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank_step, steps, world, max_ms):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time
+    (token data-parallel replicas, weak scaling)."""
+    return tokens_per_rank_step * steps * world / (max_ms / 1e3)
+
+
 # ------------------------------------------------------------------ workload
 def tensors_of(spec, d):
     t = {"x": d["x"], "wg": d["wg"], "gate_bias": d["gate_bias"], "sel_bias": d["sel_bias"]}
@@ -254,11 +270,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     st = int(layer.dev_status.item())
     if st != 0:
         raise RuntimeError(f"device status {st}")
@@ -285,11 +297,7 @@ def run_ours(args, rank, world, local_rank):
             g.replay()
         g1.record(stream)
         torch.cuda.synchronize()
-        graph_ms = g0.elapsed_time(g1)
-        if world > 1:
-            tt = torch.tensor([graph_ms], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            graph_ms = float(tt.item())
+        graph_ms = max_over_ranks(g0.elapsed_time(g1), world, dev)
         del g
     except Exception as e:  # report, do not hide: the stream number stands
         log("graph capture failed:", repr(e))
@@ -387,11 +395,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
     # ---- T sweep (rank 0 only, short): stream launches and graph replay
     sweep = None
@@ -441,7 +445,7 @@ def run_ours(args, rank, world, local_rank):
     tokens = T * args.steps * world
     res = {
         "metric": METRIC,
-        "value": round(tokens / (ms / 1e3), 1),
+        "value": round(job_throughput(T, args.steps, world, ms), 1),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -475,6 +479,110 @@ def run_ours(args, rank, world, local_rank):
     }
     if sweep is not None:
         res["sweep"] = sweep
+    if rank == 0 and args.extra:
+        res["stage_sweep_large_T"] = stage_sweep(spec, (16384, 65536, 262144), peaks, dev)
+        res["prefill_grouped_gemm"] = prefill_points(peaks, dev)
+    return res
+
+
+# ------------------------------------------------------------------ extra sweeps
+def _time(fn, n, stream):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n / 1e3  # seconds
+
+
+def stage_sweep(spec, Ts, peaks, dev):
+    """R, K, P, U alone at large T (the sizes where their bytes, not launch
+    latency, set the time); each against its own roofline."""
+    from mixture_experts_layer_07_gb300 import ops, synth
+
+    stream = torch.cuda.current_stream()
+    out = []
+    H, E, K, G = spec.H, spec.E, spec.K, spec.G
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    wg = (torch.randn(G, H, device=dev, generator=gen) / H ** 0.5).contiguous()
+    for T in Ts:
+        R = T * K
+        x = torch.randn(T, H, device=dev, generator=gen).to(torch.bfloat16)
+        logits = torch.empty(T, G, device=dev)
+        ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+        w = torch.empty(T, K, device=dev)
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        r2f = torch.empty(R, dtype=torch.int32, device=dev)
+        f2r = torch.empty(R, dtype=torch.int32, device=dev)
+        xp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+        scratch = torch.empty(ops.permute_scratch_bytes(T, E, K), dtype=torch.uint8, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        o = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        sel_bias = torch.zeros(E, device=dev) if spec.mode == 1 else None
+        sb = stage_bytes_flops(spec, T, None, 0)
+        row = {"T": T}
+        t = _time(lambda: ops.router_gemm(x, wg, None, logits), 5, stream)
+        r = roofline_of(sb["router"]["bytes"], sb["router"]["flops"], t, peaks, "alu")
+        row["router"] = {"us": round(t * 1e6, 1), "bound": r["bound"], "frac": round(r["frac"], 3)}
+        t = _time(lambda: ops.topk_route(logits, E, K, spec.mode, spec.routed_scale, ids, w,
+                                         sel_bias), 10, stream)
+        r = roofline_of(sb["topk"]["bytes"], 0, t, peaks, "alu")
+        row["topk"] = {"us": round(t * 1e6, 1), "GB/s": round(r["achieved"], 1), "frac": round(r["frac"], 3)}
+        t = _time(lambda: ops.permute(x, ids, E, off, r2f, f2r, xp, scratch, st), 5, stream)
+        r = roofline_of(sb["permute"]["bytes"], 0, t, peaks, "alu")
+        row["permute"] = {"us": round(t * 1e6, 1), "GB/s": round(r["achieved"], 1), "frac": round(r["frac"], 3)}
+        t = _time(lambda: ops.unpermute(xp, f2r, w, T, K, H, o), 5, stream)
+        r = roofline_of(sb["unpermute"]["bytes"], 0, t, peaks, "alu")
+        row["unpermute"] = {"us": round(t * 1e6, 1), "GB/s": round(r["achieved"], 1), "frac": round(r["frac"], 3)}
+        out.append(row)
+        del x, logits, ids, w, off, r2f, f2r, xp, scratch, o
+        torch.cuda.empty_cache()
+    return out
+
+
+def prefill_points(peaks, dev):
+    """The grouped GEMM stage on prefill shapes where it is tensor-bound."""
+    from mixture_experts_layer_07_gb300 import ops, synth
+
+    stream = torch.cuda.current_stream()
+    res = []
+    for name, T in (("qwen3_30b_a3b", 16384), ("gpt_oss_20b", 4096)):
+        spec = synth.SPECS[name]
+        d = synth.device_inputs(spec, T, seed=3, device=dev)
+        t = tensors_of(spec, d)
+        cfg = ops.make_config(T, spec.H, spec.E, spec.K, spec.I,
+                              wdtype=ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16)
+        layer = ops.MoELayer(cfg, t, device=dev)
+        layer(d["x"])
+        torch.cuda.synchronize()
+        E, K, H, I = spec.E, spec.K, spec.H, spec.I
+        R = T * K
+        off = layer.view("offsets", torch.int32, (E + 1,))
+        xp = layer.view("xp", torch.bfloat16, (R, H))
+        hact = layer.view("hact", torch.bfloat16, (R, I))
+        y = layer.view("y", torch.bfloat16, (R, H))
+        L = layer.layout
+        gscr = layer.workspace[L.gemm_scratch:L.shared_gemm_scratch]
+        wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
+        sec = _time(lambda: ops.grouped_gemm(xp, off, E, H, I, t["w1"], t["w3"], t["w2"], hact, y,
+                                             gscr, wdtype=wd, s1=t.get("s1"), s3=t.get("s3"),
+                                             s2=t.get("s2")), 10, stream)
+        ids = layer.view("ids", torch.int32, (T, K)).cpu().numpy()
+        e_act = int(len(np.unique(ids)))
+        sb = stage_bytes_flops(spec, T, ids, e_act)["grouped_gemm"]
+        r = roofline_of(sb["bytes"], sb["flops"], sec, peaks, "tensor")
+        hot = float(np.isin(ids, list(spec.hot_experts)).mean()) if spec.hot_experts else None
+        res.append({"workload": name, "T": T, "us": round(sec * 1e6, 1), "bound": r["bound"],
+                    "achieved": round(r["achieved"], 1), "unit": r["unit"],
+                    "frac": round(r["frac"], 3), "tflops": round(sb["flops"] / sec / 1e12, 1),
+                    "hot_expert_share": hot})
+        del layer, d, t
+        torch.cuda.empty_cache()
     return res
 
 
@@ -556,6 +664,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra", action="store_true",
+                    help="also time R/K/P/U at large T and the grouped GEMM on prefill shapes")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

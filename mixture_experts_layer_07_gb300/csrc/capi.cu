@@ -247,14 +247,15 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
   e = launch_grouped_gemm(xp, offsets, E, R, H, cfg->I, cfg->wdtype, w->w1, w->w3, w->w2, w->s1,
                           w->s3, w->s2, hact, y, cfg->m_skinny, cfg->dispatch,
                           reinterpret_cast<int32_t*>(ws + L.block_variant), ws + L.gemm_scratch,
-                          dev_status, stream);
+                          dev_status, stream, /*max_rows=*/T);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   void* sh_y = nullptr;
   if (cfg->has_shared) {
     sh_y = ws + L.shared_y;
     e = launch_grouped_gemm(x, nullptr, 1, T, H, cfg->I_shared, MOE_W_BF16, w->sw1, w->sw3, w->sw2,
                             nullptr, nullptr, nullptr, ws + L.shared_hact, sh_y, cfg->m_skinny,
-                            cfg->dispatch, nullptr, ws + L.shared_gemm_scratch, dev_status, stream);
+                            cfg->dispatch, nullptr, ws + L.shared_gemm_scratch, dev_status, stream,
+                            /*max_rows=*/T);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   e = launch_unpermute(y, f2r, wts, T, K, H, sh_y, cfg->has_shared ? gsh : nullptr, out, stream);

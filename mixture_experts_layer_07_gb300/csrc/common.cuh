@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_gb300.h"
 
 #define MOE_DEVICE __device__ __forceinline__
@@ -56,3 +58,37 @@ MOE_DEVICE int warp_id() { return threadIdx.x >> 5; }
 
 static inline size_t moe_align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 __host__ __device__ static inline int moe_cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// Programmatic dependent launch.  Every kernel of the layer is launched with
+// programmatic stream serialisation: the next kernel's grid may be scheduled
+// while this one runs, and each kernel waits here for its predecessor's
+// completion (and memory) before reading anything the predecessor wrote.
+MOE_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_DEVICE void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// cudaLaunchKernelEx with programmatic stream serialisation (and an optional
+// cluster of `cluster_z` CTAs along z).
+template <typename... KArgs, typename... Args>
+static inline cudaError_t moe_launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t stream, int cluster_z, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_z > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = cluster_z;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}

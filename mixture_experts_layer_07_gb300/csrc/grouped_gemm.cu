@@ -81,9 +81,11 @@ gemm_plan_kernel(const int32_t* __restrict__ offsets, int E_blocks, int R, int m
                  int4* __restrict__ items_t, int32_t* __restrict__ block_variant) {
   __shared__ int ws[32], wt[32];
   __shared__ int carry_s, carry_t;
+  pdl_wait();
+  pdl_trigger();
   const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
   if (tid == 0) { carry_s = 0; carry_t = 0; }
-  const int64_t total_rows = offsets ? offsets[E_blocks] : R;
+  const int64_t total_rows = R;  // the global average divides all R replicas by E
   __syncthreads();
   for (int base = 0; base < E_blocks; base += 1024) {
     const int e = base + tid;
@@ -147,6 +149,7 @@ gemm_plan_kernel(const int32_t* __restrict__ offsets, int E_blocks, int R, int m
 // block, so each converted tile needs a single scale.
 template <int BN, bool SWIGLU, bool WFP8>
 struct TcCfg {
+  static constexpr int kMaxScaleCols = 64;  // FP8: K up to 8192 (64 scale columns of 128)
   static constexpr int kNA = SWIGLU ? 2 : 1;
   static constexpr int kABytes = kBM * kBK * 2;             // bf16 weight tile
   static constexpr int kQBytes = kBM * kBK;                 // e4m3 weight tile
@@ -163,11 +166,13 @@ struct TcCfg {
   static constexpr int kTmemNeed = kAccStages * kAccCols;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
                                  : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
-  static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 1 + 2 * kConvStages;
-  static constexpr int kBarBytes = kNumBars * 8 + 16;
+  static constexpr int kScaleBufs = WFP8 ? 3 : 0;  // per-unit scale rows, reused every 3 units
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 1 + 2 * kConvStages + kScaleBufs;
+  static constexpr int kBarBytes = kNumBars * 8 + 16 + kScaleBufs * 2 * kMaxScaleCols * 4;
   static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes +
                                        (size_t)kConvStages * kConvBytes + kEpiBytes + kBarBytes;
-  static constexpr int kThreads = WFP8 ? 320 : 192;  // + one converter warpgroup
+  static constexpr int kConvThreads = WFP8 ? 256 : 0;  // eight converter warps
+  static constexpr int kThreads = 192 + kConvThreads;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
@@ -197,6 +202,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
                const int4* __restrict__ items, int N, int Kdim, __nv_bfloat16* __restrict__ out,
                int32_t* dev_status) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
+  pdl_wait();
+  pdl_trigger();
   const int nblk = (N + kBM - 1) / kBM;
   const int total = counts[list] * nblk;
   if ((int)blockIdx.x >= total) return;
@@ -218,15 +225,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
   const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 2 * C::kAccStages);
   auto conv_full = [&](int c) { return drain_bar + 8u * (1 + c); };
   auto conv_empty = [&](int c) { return drain_bar + 8u * (1 + C::kConvStages + c); };
+  auto scale_bar = [&](int b) { return drain_bar + 8u * (1 + 2 * C::kConvStages + b); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* scale_rows = reinterpret_cast<float*>(tmem_slot + 4);  // FP8: [3][2][kMaxScaleCols]
 
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
     for (int a = 0; a < C::kAccStages; ++a) { mbar_init(acc_full(a), 1); mbar_init(acc_empty(a), 128); }
     mbar_init(drain_bar, 1);
-    for (int c = 0; c < C::kConvStages; ++c) { mbar_init(conv_full(c), 128); mbar_init(conv_empty(c), 1); }
+    for (int c = 0; c < C::kConvStages; ++c) {
+      mbar_init(conv_full(c), C::kConvThreads);
+      mbar_init(conv_empty(c), 1);
+    }
+    for (int b = 0; b < C::kScaleBufs; ++b) mbar_init(scale_bar(b), C::kConvThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -380,15 +393,32 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
       mbar_arrive(acc_empty(a));
     }
   } else if (WFP8) {
-    // ---------------- e4m3 -> bf16 converters, warps 6..9
+    // ---------------- e4m3 -> bf16 converters, warps 6..13
+    // At the start of each work unit the converters stage that unit's row of
+    // block scales (one per 128-wide K block) in shared memory, so the
+    // per-stage scale is a shared-memory read, not a global load.  Rows rotate
+    // through three buffers: a converter can run at most two stages ahead of
+    // the slowest one, so a buffer is never rewritten while still being read.
     const int ct = threadIdx.x - 192;
     const int rb = (N + 127) / 128, cb = (Kdim + 127) / 128;
     int stage = 0, cs = 0;
-    uint32_t phase = 0, cphase = 0;
+    uint32_t phase = 0, cphase = 0, unit = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++unit) {
       const int4 it = items[w / nblk];
       const int nb = w % nblk;
+      const int buf = (int)(unit % 3u);
+      float* scale_row = scale_rows + buf * 2 * C::kMaxScaleCols;
+      const size_t row = ((size_t)it.x * rb + nb) * cb;
+      for (int c = ct; c < cb; c += C::kConvThreads) {
+        scale_row[c] = __ldg(sa + row + c);
+        scale_row[C::kMaxScaleCols + c] = SWIGLU ? __ldg(sb + row + c) : 0.f;
+      }
+      mbar_arrive(scale_bar(buf));
+      if (!mbar_wait_bounded(scale_bar(buf), (unit / 3u) & 1u, abort_flag, kWaitLimitNs)) {
+        fail();
+        break;
+      }
       for (int kb = 0; kb < nk; ++kb) {
         if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, kWaitLimitNs) ||
             !mbar_wait_bounded(conv_empty(cs), cphase ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -396,26 +426,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
           ok = false;
           break;
         }
-        const size_t sidx = ((size_t)it.x * rb + nb) * cb + (kb * kBK) / 128;
-        const float scl[2] = {__ldg(sa + sidx), SWIGLU ? __ldg(sb + sidx) : 0.f};
+        const int sc = (kb * kBK) / 128;
 #pragma unroll
         for (int t = 0; t < C::kNA; ++t) {
+          const float scl = scale_row[t * C::kMaxScaleCols + sc];
           const uint8_t* src = smem + (size_t)stage * C::kStageBytes + t * C::kQBytes;
           uint8_t* dst = conv + (size_t)cs * C::kConvBytes + t * C::kABytes;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int q = ct + 128 * i;  // 16-byte e4m3 chunk: row q/4, K 16*(q%4) .. +15
+          for (int i = 0; i < 512 / C::kConvThreads; ++i) {
+            const int q = ct + C::kConvThreads * i;  // 16-byte e4m3 chunk: row q/4, K 16*(q%4)..+15
             const int r = q >> 2, j = q & 3;
             const uint4 v = *reinterpret_cast<const uint4*>(src + r * kBK + j * 16);
             uint4 lo, hi;
-            lo.x = e4m3x2_to_bf16x2(v.x & 0xFFFFu, scl[t]);
-            lo.y = e4m3x2_to_bf16x2(v.x >> 16, scl[t]);
-            lo.z = e4m3x2_to_bf16x2(v.y & 0xFFFFu, scl[t]);
-            lo.w = e4m3x2_to_bf16x2(v.y >> 16, scl[t]);
-            hi.x = e4m3x2_to_bf16x2(v.z & 0xFFFFu, scl[t]);
-            hi.y = e4m3x2_to_bf16x2(v.z >> 16, scl[t]);
-            hi.z = e4m3x2_to_bf16x2(v.w & 0xFFFFu, scl[t]);
-            hi.w = e4m3x2_to_bf16x2(v.w >> 16, scl[t]);
+            lo.x = e4m3x2_to_bf16x2(v.x & 0xFFFFu, scl);
+            lo.y = e4m3x2_to_bf16x2(v.x >> 16, scl);
+            lo.z = e4m3x2_to_bf16x2(v.y & 0xFFFFu, scl);
+            lo.w = e4m3x2_to_bf16x2(v.y >> 16, scl);
+            hi.x = e4m3x2_to_bf16x2(v.z & 0xFFFFu, scl);
+            hi.y = e4m3x2_to_bf16x2(v.z >> 16, scl);
+            hi.z = e4m3x2_to_bf16x2(v.w & 0xFFFFu, scl);
+            hi.w = e4m3x2_to_bf16x2(v.w >> 16, scl);
             // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
             *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * j) ^ (r & 7)) << 4)) = lo;
             *reinterpret_cast<uint4*>(dst + r * 128 + (((2 * j + 1) ^ (r & 7)) << 4)) = hi;
@@ -468,6 +498,8 @@ gemm_simt_kernel(const __nv_bfloat16* __restrict__ act, const void* __restrict__
   __shared__ float As[kBnSkinny][kSimtK];
   __shared__ float Wa[kSimtN][kSimtK + 1];
   __shared__ float Wb[SWIGLU ? kSimtN : 1][kSimtK + 1];
+  pdl_wait();
+  pdl_trigger();
   const int n_items = counts[list];
   for (int item = blockIdx.y; item < n_items; item += gridDim.y) {
   const int4 it = items[item];
@@ -592,17 +624,16 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
   const long long work = (long long)cap * moe_cdiv(N, kBM);
   const int grid = (int)(work < num_sms() ? work : num_sms());
   if (grid <= 0) return cudaSuccess;
-  gemm_tc_kernel<BN, SWIGLU, WFP8><<<grid, C::kThreads, C::kSmemBytes, stream>>>(
-      wa, wb, act, sa, sb, counts, list, items, N, Kdim, static_cast<__nv_bfloat16*>(out),
-      dev_status);
-  return cudaGetLastError();
+  return moe_launch(gemm_tc_kernel<BN, SWIGLU, WFP8>, dim3(grid), dim3(C::kThreads),
+                    C::kSmemBytes, stream, 1, wa, wb, act, sa, sb, counts, list, items, N, Kdim,
+                    static_cast<__nv_bfloat16*>(out), dev_status);
 }
 
 template <bool WFP8>
 cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const void* w1,
                        const void* w3, const void* w2, const float* s1, const float* s3,
                        const float* s2, void* hact, void* y, const PlanView& pv,
-                       int32_t* dev_status, cudaStream_t stream) {
+                       int32_t* dev_status, cudaStream_t stream, bool any_skinny, bool any_tile) {
   CUtensorMap m_w1, m_w3, m_w2, m_x16, m_x128, m_h16, m_h128;
   if (!make_weight_map(&m_w1, w1, E_blocks, I, H, WFP8) ||
       !make_weight_map(&m_w3, w3, E_blocks, I, H, WFP8) ||
@@ -610,18 +641,23 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
       !make_act_map(&m_x16, xp, R, H, kBnSkinny) || !make_act_map(&m_x128, xp, R, H, kBnTile) ||
       !make_act_map(&m_h16, hact, R, I, kBnSkinny) || !make_act_map(&m_h128, hact, R, I, kBnTile))
     return cudaErrorInvalidValue;
-  cudaError_t err;
-  err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x16, s1, s3, pv.counts, 0, pv.items_s,
-                                      pv.cap_s, I, H, hact, dev_status, stream);
+  cudaError_t err = cudaSuccess;
+  if (any_skinny)
+    err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x16, s1, s3, pv.counts, 0, pv.items_s,
+                                        pv.cap_s, I, H, hact, dev_status, stream);
   if (err != cudaSuccess) return err;
-  err = run_tc<kBnTile, true, WFP8>(m_w1, m_w3, m_x128, s1, s3, pv.counts, 1, pv.items_t,
-                                    pv.cap_t, I, H, hact, dev_status, stream);
+  if (any_tile)
+    err = run_tc<kBnTile, true, WFP8>(m_w1, m_w3, m_x128, s1, s3, pv.counts, 1, pv.items_t,
+                                      pv.cap_t, I, H, hact, dev_status, stream);
   if (err != cudaSuccess) return err;
-  err = run_tc<kBnSkinny, false, WFP8>(m_w2, m_w2, m_h16, s2, s2, pv.counts, 0, pv.items_s,
-                                       pv.cap_s, H, I, y, dev_status, stream);
+  if (any_skinny)
+    err = run_tc<kBnSkinny, false, WFP8>(m_w2, m_w2, m_h16, s2, s2, pv.counts, 0, pv.items_s,
+                                         pv.cap_s, H, I, y, dev_status, stream);
   if (err != cudaSuccess) return err;
-  return run_tc<kBnTile, false, WFP8>(m_w2, m_w2, m_h128, s2, s2, pv.counts, 1, pv.items_t,
-                                      pv.cap_t, H, I, y, dev_status, stream);
+  if (any_tile)
+    err = run_tc<kBnTile, false, WFP8>(m_w2, m_w2, m_h128, s2, s2, pv.counts, 1, pv.items_t,
+                                       pv.cap_t, H, I, y, dev_status, stream);
+  return err;
 }
 
 template <bool SWIGLU>
@@ -633,10 +669,10 @@ cudaError_t run_simt(bool fp8, const void* act, const void* wa, const void* wb, 
   const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(act);
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
   if (fp8)
-    gemm_simt_kernel<SWIGLU, true><<<grid, 256, 0, stream>>>(a, wa, wb, sa, sb, counts, 0, items, N, Kdim, o);
-  else
-    gemm_simt_kernel<SWIGLU, false><<<grid, 256, 0, stream>>>(a, wa, wb, sa, sb, counts, 0, items, N, Kdim, o);
-  return cudaGetLastError();
+    return moe_launch(gemm_simt_kernel<SWIGLU, true>, grid, dim3(256), 0, stream, 1, a, wa, wb, sa,
+                      sb, counts, 0, items, N, Kdim, o);
+  return moe_launch(gemm_simt_kernel<SWIGLU, false>, grid, dim3(256), 0, stream, 1, a, wa, wb, sa,
+                    sb, counts, 0, items, N, Kdim, o);
 }
 
 }  // namespace
@@ -651,6 +687,8 @@ size_t grouped_gemm_scratch_bytes(int R, int E_blocks) {
 int grouped_gemm_check(int H, int I, int wdtype) {
   if (H % 16 != 0 || I % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (wdtype != MOE_W_BF16 && wdtype != MOE_W_FP8E4M3_B128) return MOE_ERR_UNSUPPORTED;
+  // FP8: each work unit stages its row of 128-wide K-block scales (<= 64)
+  if (wdtype == MOE_W_FP8E4M3_B128 && (H > 8192 || I > 8192)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -659,14 +697,14 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 const void* w2, const float* s1, const float* s3,
                                 const float* s2, void* hact, void* y, int m_skinny,
                                 int dispatch, int32_t* block_variant, void* scratch,
-                                int32_t* dev_status, cudaStream_t stream) {
+                                int32_t* dev_status, cudaStream_t stream, int max_rows) {
   if (m_skinny < 0) m_skinny = MOE_DEFAULT_M_SKINNY;
   const bool fp8 = wdtype == MOE_W_FP8E4M3_B128;
   const bool simt = dispatch == MOE_DISPATCH_SIMT;
   PlanView pv = plan_view(scratch, R, E_blocks);
-  gemm_plan_kernel<<<1, 1024, 0, stream>>>(offsets, E_blocks, R, m_skinny, dispatch, pv.counts,
-                                           pv.items_s, pv.items_t, block_variant);
-  cudaError_t err = cudaGetLastError();
+  cudaError_t err = moe_launch(gemm_plan_kernel, dim3(1), dim3(1024), 0, stream, 1, offsets,
+                               E_blocks, R, m_skinny, dispatch, pv.counts, pv.items_s, pv.items_t,
+                               block_variant);
   if (err != cudaSuccess || R == 0) return err;
 
   if (simt) {
@@ -675,9 +713,21 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
     return run_simt<false>(fp8, hact, w2, nullptr, s2, nullptr, pv.counts, pv.items_s, pv.cap_s, H,
                            I, y, stream);
   }
+  // Which lists can be non-empty, from what the host knows without reading
+  // the offsets: no block holds more than max_rows rows (moe_layer passes T:
+  // a token picks distinct experts), and under the global average every block
+  // takes the same variant.  An empty list's launch is skipped.
+  if (max_rows < 0 || max_rows > R) max_rows = R;
+  bool any_skinny = true, any_tile = max_rows > m_skinny;
+  if (dispatch == MOE_DISPATCH_GLOBAL_AVG) {
+    const int64_t avg = E_blocks > 0 ? (int64_t)R / E_blocks : R;
+    const bool tile = (avg < 1 ? 1 : avg) > m_skinny;
+    any_skinny = !tile;
+    any_tile = tile;
+  }
   if (fp8)
     return run_tc_all<true>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                            stream);
+                            stream, any_skinny, any_tile);
   return run_tc_all<false>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                           stream);
+                           stream, any_skinny, any_tile);
 }

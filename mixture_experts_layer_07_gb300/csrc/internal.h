@@ -25,7 +25,7 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 const void* w2, const float* s1, const float* s3,
                                 const float* s2, void* hact, void* y, int m_skinny,
                                 int dispatch, int32_t* block_variant, void* scratch,
-                                int32_t* dev_status, cudaStream_t stream);
+                                int32_t* dev_status, cudaStream_t stream, int max_rows = -1);
 
 cudaError_t launch_unpermute(const void* y, const int32_t* flat_to_row, const float* weights,
                              int T, int K, int H, const void* shared_y, const float* shared_gate,

@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta)
 permute_count_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunks,
                      int32_t* __restrict__ counts, int32_t* dev_status) {
   extern __shared__ int32_t hist[];  // [kWarpsPerCta][E]
+  pdl_wait();
+  pdl_trigger();
   const int w = warp_id(), lane = lane_id();
   const int chunk = blockIdx.x * kWarpsPerCta + w;
   int32_t* h = hist + w * E;
@@ -60,6 +62,8 @@ permute_scan_kernel(int32_t* __restrict__ counts, int E, int nchunks,
                     int32_t* __restrict__ offsets) {
   __shared__ int32_t tot[1024];
   __shared__ int32_t warp_tot[32];
+  pdl_wait();
+  pdl_trigger();
   const int lane = lane_id(), warp = warp_id();
   for (int e = warp; e < E; e += 32) {
     int32_t* row = counts + (size_t)e * nchunks;
@@ -110,6 +114,8 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunk
                        const int32_t* __restrict__ bases, const int32_t* __restrict__ offsets,
                        int32_t* __restrict__ row_to_flat, int32_t* __restrict__ flat_to_row) {
   extern __shared__ int32_t cnt_all[];  // [kWarpsPerCta][E]
+  pdl_wait();
+  pdl_trigger();
   const int w = warp_id(), lane = lane_id();
   const int chunk = blockIdx.x * kWarpsPerCta + w;
   if (chunk >= nchunks) return;
@@ -145,11 +151,131 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunk
   }
 }
 
+// Small problems (R <= 32 warps x 2048 replicas): count, scan and stable
+// scatter in ONE CTA of 32 warps, all counters in shared memory -- one launch
+// instead of three, and no global scratch.  Warp w owns the contiguous replica
+// range [w*span, (w+1)*span); per-warp counts cnt[w][e] become per-warp bases by
+// a scan over warps (per expert) and then over experts, and the scatter walks
+// each range again in order, 32 replicas per step, ranking equal experts with
+// __match_any_sync.  Deterministic and stable like the multi-CTA path.
+constexpr int kFusedWarps = 32;
+constexpr int kFusedMaxSpan = 2048;
+
+__global__ void __launch_bounds__(32 * kFusedWarps)
+permute_fused_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ offsets,
+                     int32_t* __restrict__ row_to_flat, int32_t* __restrict__ flat_to_row,
+                     int32_t* dev_status) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;                           // [kFusedWarps][E]
+  int32_t* off = sm + kFusedWarps * E;         // [E]
+  __shared__ int32_t warp_tot[32];
+  pdl_wait();
+  pdl_trigger();
+  const int w = warp_id(), lane = lane_id();
+  const int span = ((R + kFusedWarps - 1) / kFusedWarps + 31) / 32 * 32;
+  const int f0 = w * span, f1 = min(R, f0 + span);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  int32_t* mine = cnt + w * E;
+  for (int e = lane; e < E; e += 32) mine[e] = 0;
+  __syncwarp();
+  // ids of this warp's range are read 8 steps (256 replicas) at a time, all
+  // loads in flight together, then processed step by step
+  constexpr int kBatch = 8;
+  auto load_batch = [&](int fb, int (&v)[kBatch]) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int f = fb + i * 32 + lane;
+      v[i] = f < f1 ? __ldg(ids + f) : -1;
+    }
+  };
+  // 1. per-warp histogram (one leader per distinct expert per step: no atomics)
+  for (int fb = f0; fb < f1; fb += 32 * kBatch) {
+    int v[kBatch];
+    load_batch(fb, v);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      int e = v[i];
+      if (fb + i * 32 + lane < f1 && (e < 0 || e >= E)) {
+        moe_set_status(dev_status, MOE_DEV_BAD_EXPERT_ID);
+        e = -1;
+      }
+      if (e >= E) e = -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && (peers & lt_mask) == 0) mine[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // 2. scan: over warps per expert, then over experts
+  const int e = threadIdx.x;
+  int32_t tot = 0;
+  if (e < E) {
+    for (int q = 0; q < kFusedWarps; ++q) {
+      const int32_t v = cnt[q * E + e];
+      cnt[q * E + e] = tot;
+      tot += v;
+    }
+  }
+  int32_t incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    const int32_t v = warp_tot[lane];
+    int32_t sc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t n = __shfl_up_sync(0xffffffffu, sc, o);
+      if (lane >= o) sc += n;
+    }
+    warp_tot[lane] = sc - v;
+  }
+  __syncthreads();
+  if (e < E) {
+    const int32_t ex = incl - tot + warp_tot[w];
+    off[e] = ex;
+    offsets[e] = ex;
+    if (e == E - 1) offsets[E] = ex + tot;
+  }
+  __syncthreads();
+  // 3. stable scatter
+  for (int fb = f0; fb < f1; fb += 32 * kBatch) {
+    int v[kBatch];
+    load_batch(fb, v);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int f = fb + i * 32 + lane;
+      const int ee = (v[i] >= 0 && v[i] < E) ? v[i] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, ee);
+      int base = 0;
+      if (ee >= 0) base = off[ee] + mine[ee];
+      __syncwarp();
+      if (ee >= 0 && (peers & lt_mask) == 0) mine[ee] += __popc(peers);
+      __syncwarp();
+      if (f < f1) {
+        if (ee >= 0) {
+          const int row = base + __popc(peers & lt_mask);
+          row_to_flat[row] = f;
+          flat_to_row[f] = row;
+        } else {
+          flat_to_row[f] = -1;
+        }
+      }
+    }
+  }
+}
+
 // one warp per row, 16-byte vectors
 __global__ void __launch_bounds__(256)
 permute_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_to_flat,
                       const int32_t* __restrict__ offsets, int E, int K, int H8,
                       uint4* __restrict__ xp) {
+  pdl_wait();
+  pdl_trigger();
   const int nrows = offsets[E];
   const int lane = lane_id();
   for (int row = blockIdx.x * 8 + warp_id(); row < nrows; row += gridDim.x * 8) {
@@ -175,22 +301,39 @@ cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int 
   int32_t* counts = static_cast<int32_t*>(scratch);
   const size_t smem = (size_t)kWarpsPerCta * E * sizeof(int32_t);
   const int ctas = moe_cdiv(nch, kWarpsPerCta);
-  if (R > 0) {
-    permute_count_kernel<<<ctas, 32 * kWarpsPerCta, smem, stream>>>(ids, R, E, nch, counts,
-                                                                     dev_status);
-  }
-  permute_scan_kernel<<<1, 1024, 0, stream>>>(counts, E, nch, offsets);
-  if (R > 0) {
-    permute_scatter_kernel<<<ctas, 32 * kWarpsPerCta, smem, stream>>>(
-        ids, R, E, nch, counts, offsets, row_to_flat, flat_to_row);
-    if (xp) {
-      const int grid = moe_cdiv(R, 8) < 152 * 16 ? moe_cdiv(R, 8) : 152 * 16;
-      permute_gather_kernel<<<grid, 256, 0, stream>>>(
-          static_cast<const uint4*>(x), row_to_flat, offsets, E, K, H / 8,
-          static_cast<uint4*>(xp));
+  const size_t fused_smem = (size_t)(kFusedWarps + 1) * E * sizeof(int32_t);
+  if (R > 0 && R <= kFusedWarps * kFusedMaxSpan && fused_smem <= 200 * 1024) {
+    static bool attr = false;
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(permute_fused_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e != cudaSuccess) return e;
+      attr = true;
     }
+    cudaError_t e = moe_launch(permute_fused_kernel, dim3(1), dim3(32 * kFusedWarps), fused_smem,
+                               stream, 1, ids, R, E, offsets, row_to_flat, flat_to_row, dev_status);
+    if (e != cudaSuccess || !xp) return e;
+    const int grid = moe_cdiv(R, 8) < 152 * 16 ? moe_cdiv(R, 8) : 152 * 16;
+    return moe_launch(permute_gather_kernel, dim3(grid), dim3(256), 0, stream, 1,
+                      static_cast<const uint4*>(x), row_to_flat, offsets, E, K, H / 8,
+                      static_cast<uint4*>(xp));
   }
-  return cudaGetLastError();
+  cudaError_t e = cudaSuccess;
+  if (R > 0) {
+    e = moe_launch(permute_count_kernel, dim3(ctas), dim3(32 * kWarpsPerCta), smem, stream, 1, ids,
+                   R, E, nch, counts, dev_status);
+    if (e != cudaSuccess) return e;
+  }
+  e = moe_launch(permute_scan_kernel, dim3(1), dim3(1024), 0, stream, 1, counts, E, nch, offsets);
+  if (e != cudaSuccess || R == 0) return e;
+  e = moe_launch(permute_scatter_kernel, dim3(ctas), dim3(32 * kWarpsPerCta), smem, stream, 1, ids,
+                 R, E, nch, (const int32_t*)counts, (const int32_t*)offsets, row_to_flat,
+                 flat_to_row);
+  if (e != cudaSuccess || !xp) return e;
+  const int grid = moe_cdiv(R, 8) < 152 * 16 ? moe_cdiv(R, 8) : 152 * 16;
+  return moe_launch(permute_gather_kernel, dim3(grid), dim3(256), 0, stream, 1,
+                    static_cast<const uint4*>(x), row_to_flat, offsets, E, K, H / 8,
+                    static_cast<uint4*>(xp));
 }
 
 // ---------------------------------------------------------------- static scratch

@@ -34,6 +34,8 @@ router_small_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict
                     const float* __restrict__ bias, float* __restrict__ logits, int T, int H,
                     int G) {
   __shared__ float red[kSmallThreads / 32][ROWS * kSmallTok];
+  pdl_wait();
+  pdl_trigger();
   const int g0 = blockIdx.x * ROWS;
   const int tid = threadIdx.x;
   for (int t0 = 0; t0 < T; t0 += kSmallTok) {
@@ -113,6 +115,8 @@ router_cluster_kernel(const __nv_bfloat16* __restrict__ x, const float* __restri
   __shared__ __align__(16) float xs[kBK][kBM + 4];
   __shared__ __align__(16) float ws[kBK][kBN + 4];
   __shared__ __align__(16) float part[kBM][kBN + 4];
+  pdl_wait();
+  pdl_trigger();
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -221,13 +225,14 @@ cudaError_t launch_router_gemm(const void* x, const float* wg, const float* gate
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   if (T <= kSmallMaxT) {
     if (G <= 256) {
-      router_small_kernel<1><<<G, kSmallThreads, 0, stream>>>(xb, wg, gate_bias, logits, T, H, G);
+      return moe_launch(router_small_kernel<1>, dim3(G), dim3(kSmallThreads), 0, stream, 1, xb, wg,
+                        gate_bias, logits, T, H, G);
     } else if (G <= 512) {
-      router_small_kernel<2><<<moe_cdiv(G, 2), kSmallThreads, 0, stream>>>(xb, wg, gate_bias,
-                                                                          logits, T, H, G);
+      return moe_launch(router_small_kernel<2>, dim3(moe_cdiv(G, 2)), dim3(kSmallThreads), 0,
+                        stream, 1, xb, wg, gate_bias, logits, T, H, G);
     } else {
-      router_small_kernel<4><<<moe_cdiv(G, 4), kSmallThreads, 0, stream>>>(xb, wg, gate_bias,
-                                                                          logits, T, H, G);
+      return moe_launch(router_small_kernel<4>, dim3(moe_cdiv(G, 4)), dim3(kSmallThreads), 0,
+                        stream, 1, xb, wg, gate_bias, logits, T, H, G);
     }
   } else {
     // split H over a cluster until there are about two CTAs per SM
@@ -236,21 +241,9 @@ cudaError_t launch_router_gemm(const void* x, const float* wg, const float* gate
     while (splits < 8 && tiles * splits < 2 * num_sms_router() && H / (splits * 2) >= 2 * kBK)
       splits *= 2;
     const int kchunk = moe_cdiv(moe_cdiv(H, splits), kBK) * kBK;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(moe_cdiv(G, kBN), moe_cdiv(T, kBM), splits);
-    cfg.blockDim = dim3(kTiledThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = splits;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, router_cluster_kernel, xb, wg, gate_bias, logits, T,
-                                       H, G, kchunk);
-    if (e != cudaSuccess) return e;
+    return moe_launch(router_cluster_kernel, dim3(moe_cdiv(G, kBN), moe_cdiv(T, kBM), splits),
+                      dim3(kTiledThreads), 0, stream, splits, xb, wg, gate_bias, logits, T, H, G,
+                      kchunk);
   }
   return cudaGetLastError();
 }

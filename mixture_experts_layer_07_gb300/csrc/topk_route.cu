@@ -1,4 +1,5 @@
-// K: top-K expert selection, one warp per token.
+// K: top-K expert selection, one warp per token (one thread per token for
+// large T and E <= 256).
 //
 // "FlashInfer MoE routing optimisation" (flashinfer PR #4152):
 //  * "1. routing_custom.cu" -- instead of warp 0 holding K-sized score arrays
@@ -68,6 +69,8 @@ __global__ void __launch_bounds__(128)
 topk_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ sel_bias, int T,
             int E, int K, int mode, float scale, int32_t* __restrict__ ids,
             float* __restrict__ weights, float* __restrict__ shared_gate) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x * (blockDim.x / 32) + warp_id();
   if (t >= T) return;
   const int lane = lane_id();
@@ -143,6 +146,77 @@ topk_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ 
   if (shared_gate && lane == 0) shared_gate[t] = sigmoid_key(__ldg(row + E));
 }
 
+// Large T, E <= 256: one THREAD per token.  A CTA stages the logits of its
+// 128 tokens in shared memory with coalesced loads (rows padded by one word so
+// the per-thread row walks are conflict free); each thread then scans its
+// token's E keys keeping a sorted top-LK list (most keys fail the first
+// compare against the current K-th), and writes its K ids and weights.  Same
+// keys, order and weights as the warp kernel.
+constexpr int kTokPerCta = 128;
+
+template <int LK>
+__global__ void __launch_bounds__(kTokPerCta)
+topk_thread_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ sel_bias,
+                   int T, int E, int K, int mode, float scale, int32_t* __restrict__ ids,
+                   float* __restrict__ weights, float* __restrict__ shared_gate) {
+  extern __shared__ float tile[];  // [kTokPerCta][E + 1]
+  pdl_wait();
+  pdl_trigger();
+  const int t0 = blockIdx.x * kTokPerCta;
+  const int nt = min(kTokPerCta, T - t0);
+  const int pitch = E + 1;
+  for (int i = threadIdx.x; i < nt * E; i += kTokPerCta) {
+    const int r = i / E, c = i - r * E;
+    tile[r * pitch + c] = __ldg(logits + (size_t)(t0 + r) * ld + c);
+  }
+  __syncthreads();
+  const int r = threadIdx.x;
+  if (r >= nt) return;
+  const int t = t0 + r;
+  const float* row = tile + r * pitch;
+  float lk[LK];
+  int li[LK];
+#pragma unroll
+  for (int s = 0; s < LK; ++s) { lk[s] = -INFINITY; li[s] = 0x7fffffff; }
+  for (int e = 0; e < E; ++e) {
+    float key = row[e];
+    if (mode == MOE_SCORE_SIGMOID_BIAS_SCALED)
+      key = __fadd_rn(sigmoid_key(key), sel_bias ? __ldg(sel_bias + e) : 0.f);
+    if (better(key, e, lk[LK - 1], li[LK - 1])) {
+      float nk = key;
+      int ni = e;
+#pragma unroll
+      for (int s = 0; s < LK; ++s) {
+        const bool b = better(nk, ni, lk[s], li[s]);
+        const float tk = lk[s];
+        const int ti = li[s];
+        lk[s] = b ? nk : tk;
+        li[s] = b ? ni : ti;
+        nk = b ? tk : nk;
+        ni = b ? ti : ni;
+      }
+    }
+  }
+  float v[LK];
+  float sum = 0.f;
+#pragma unroll
+  for (int s = 0; s < LK; ++s) {
+    if (s < K) {
+      v[s] = mode == MOE_SCORE_SOFTMAX_RENORM ? expf(lk[s] - lk[0]) : sigmoid_key(row[li[s]]);
+      sum += v[s];
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < LK; ++s) {
+    if (s < K) {
+      ids[(size_t)t * K + s] = li[s];
+      weights[(size_t)t * K + s] =
+          mode == MOE_SCORE_SOFTMAX_RENORM ? v[s] / sum : scale * v[s] / sum;
+    }
+  }
+  if (shared_gate) shared_gate[t] = sigmoid_key(__ldg(logits + (size_t)t * ld + E));
+}
+
 template <int NPL>
 cudaError_t launch_npl(const float* logits, int ld, const float* sel_bias, int T, int E, int K,
                        int mode, float scale, int32_t* ids, float* weights, float* shared_gate,
@@ -150,16 +224,15 @@ cudaError_t launch_npl(const float* logits, int ld, const float* sel_bias, int T
   constexpr int kWarps = 4;
   dim3 grid(moe_cdiv(T, kWarps)), block(32 * kWarps);
   // list length = min(K tier, experts per lane)
-#define MOE_TOPK_LAUNCH(KT)                                                                \
-  topk_kernel<NPL, (KT < NPL ? KT : NPL)><<<grid, block, 0, stream>>>(                      \
-      logits, ld, sel_bias, T, E, K, mode, scale, ids, weights, shared_gate)
+#define MOE_TOPK_LAUNCH(KT)                                                                 \
+  return moe_launch(topk_kernel<NPL, (KT < NPL ? KT : NPL)>, grid, block, 0, stream, 1, logits, \
+                    ld, sel_bias, T, E, K, mode, scale, ids, weights, shared_gate)
   if (K <= 2) MOE_TOPK_LAUNCH(2);
-  else if (K <= 4) MOE_TOPK_LAUNCH(4);
-  else if (K <= 8) MOE_TOPK_LAUNCH(8);
-  else if (K <= 16) MOE_TOPK_LAUNCH(16);
-  else MOE_TOPK_LAUNCH(32);
+  if (K <= 4) MOE_TOPK_LAUNCH(4);
+  if (K <= 8) MOE_TOPK_LAUNCH(8);
+  if (K <= 16) MOE_TOPK_LAUNCH(16);
+  MOE_TOPK_LAUNCH(32);
 #undef MOE_TOPK_LAUNCH
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -167,6 +240,29 @@ cudaError_t launch_npl(const float* logits, int ld, const float* sel_bias, int T
 cudaError_t launch_topk_route(const float* logits, int ld, const float* sel_bias, int T, int E,
                               int K, int mode, float scale, int32_t* ids, float* weights,
                               float* shared_gate, cudaStream_t stream) {
+  if (T >= 4096 && E <= 256 && K <= 16) {
+    // enough tokens to fill the GPU one thread each
+    const size_t smem = (size_t)kTokPerCta * (E + 1) * sizeof(float);
+    const dim3 grid(moe_cdiv(T, kTokPerCta)), block(kTokPerCta);
+    static bool attr = false;
+    if (!attr) {
+      for (auto fn : {topk_thread_kernel<2>, topk_thread_kernel<4>, topk_thread_kernel<8>,
+                      topk_thread_kernel<16>}) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(kTokPerCta * 257 * sizeof(float)));
+        if (e != cudaSuccess) return e;
+      }
+      attr = true;
+    }
+#define MOE_TOPK_T_LAUNCH(KT)                                                                    \
+  return moe_launch(topk_thread_kernel<KT>, grid, block, smem, stream, 1, logits, ld, sel_bias, T, \
+                    E, K, mode, scale, ids, weights, shared_gate)
+    if (K <= 2) MOE_TOPK_T_LAUNCH(2);
+    if (K <= 4) MOE_TOPK_T_LAUNCH(4);
+    if (K <= 8) MOE_TOPK_T_LAUNCH(8);
+    MOE_TOPK_T_LAUNCH(16);
+#undef MOE_TOPK_T_LAUNCH
+  }
   const int npl = moe_cdiv(E, 32);
   if (npl <= 1) return launch_npl<1>(logits, ld, sel_bias, T, E, K, mode, scale, ids, weights, shared_gate, stream);
   if (npl <= 2) return launch_npl<2>(logits, ld, sel_bias, T, E, K, mode, scale, ids, weights, shared_gate, stream);

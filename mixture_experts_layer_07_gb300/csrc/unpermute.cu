@@ -20,6 +20,8 @@ unpermute_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ flat_t
                  const float* __restrict__ weights, int K, int H8,
                  const uint4* __restrict__ shared_y, const float* __restrict__ shared_gate,
                  uint4* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   const int c = blockIdx.y * kThreads + threadIdx.x;
   if (c >= H8) return;
@@ -57,8 +59,7 @@ cudaError_t launch_unpermute(const void* y, const int32_t* flat_to_row, const fl
                              void* out, cudaStream_t stream) {
   const int H8 = H / 8;
   dim3 grid(T, moe_cdiv(H8, kThreads));
-  unpermute_kernel<<<grid, kThreads, 0, stream>>>(
-      static_cast<const uint4*>(y), flat_to_row, weights, K, H8,
-      static_cast<const uint4*>(shared_y), shared_gate, static_cast<uint4*>(out));
-  return cudaGetLastError();
+  return moe_launch(unpermute_kernel, grid, dim3(kThreads), 0, stream, 1,
+                    static_cast<const uint4*>(y), flat_to_row, weights, K, H8,
+                    static_cast<const uint4*>(shared_y), shared_gate, static_cast<uint4*>(out));
 }

@@ -54,7 +54,10 @@ TOPK_CASES = [  # E, K, mode, T, shared
     (8, 2, 0, 16, False), (128, 8, 0, 1, False), (128, 8, 0, 2048, False),
     (32, 4, 0, 517, False), (512, 10, 0, 64, True), (896, 16, 1, 512, False),
     (512, 9, 1, 512, False), (1024, 16, 1, 512, False), (1024, 9, 1, 37, False),
-    (8, 8, 0, 5, False), (64, 32, 0, 3, False), (33, 3, 1, 70, True), (1, 1, 0, 4, False)]
+    (8, 8, 0, 5, False), (64, 32, 0, 3, False), (33, 3, 1, 70, True), (1, 1, 0, 4, False),
+    # large T: one thread per token
+    (128, 8, 0, 5000, False), (32, 4, 0, 4096, False), (256, 16, 1, 4100, True),
+    (8, 2, 0, 4097, False), (200, 9, 1, 8191, False)]
 
 
 def run_topk(ops, logits, E, K, mode, scale, sel_bias, shared):
@@ -84,10 +87,10 @@ def test_topk_route(ops, E, K, mode, T, shared):
         U.assert_weights_close(gsh, oracle.shared_gate(lg.astype(np.float64), E))
 
 
-@pytest.mark.parametrize("mode", [0, 1])
-def test_topk_heavy_ties(ops, mode):
+@pytest.mark.parametrize("mode,T", [(0, 300), (1, 300), (0, 5000), (1, 5000)])
+def test_topk_heavy_ties(ops, mode, T):
     # logits from a 3-value set: most keys tie, the index rule decides
-    T, E, K = 300, 128, 8
+    E, K = 128, 8
     r = np.random.default_rng(3)
     lg = r.choice(np.float32([-1.0, 0.0, 1.0]), size=(T, E)).astype(np.float32)
     lg[0] = 0.5                                   # one all-equal row
@@ -124,7 +127,7 @@ def test_sigmoid_key_matches_oracle_bits(ops):
 # ---------------------------------------------------------------- P
 PERMUTE_CASES = [(16, 2, 8, 256), (1, 8, 128, 2048), (37, 8, 128, 2048), (2048, 8, 128, 2048),
                  (4096, 4, 32, 2880), (512, 16, 896, 64), (512, 16, 1024, 64), (64, 10, 512, 2048),
-                 (33, 1, 3, 16)]
+                 (33, 1, 3, 16), (20000, 4, 32, 64), (9000, 8, 128, 16), (5000, 16, 1024, 16)]
 
 
 def run_permute(ops, x, ids, E, want_xp=True):
