@@ -151,15 +151,22 @@ def tensors_of(spec, d):
     return t
 
 
-def launches_per_layer(spec, dispatch=0):
+def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=256):
     """Kernel launches inside one moe_layer call (mirrors the library's
-    launch sequence): router 1, top-K 1, permute 4 (count, scan, scatter,
-    gather), grouped GEMM 1 plan + 4 GEMM (skinny/tile x G1/G2) or 2 GEMM on
-    the CUDA-core path, combine 1; a shared expert adds one grouped GEMM."""
-    simt = dispatch == 2
-    gemm = 1 + (2 if simt else 4)
-    shared = (1 + (2 if dispatch == 2 else 4)) if spec.has_shared else 0
-    return 1 + 1 + 4 + gemm + shared + 1
+    launch sequence): router 1, top-K 1, permute 2 (one fused count/scan/
+    scatter CTA + gather) or 4 (count, scan, scatter, gather) above 65536
+    replicas, grouped GEMM 1 plan + one G1 and one G2 launch per variant list
+    that can be non-empty (skinny always; tile when T > m_skinny; wide when also
+    T >= 256) or 2 on the CUDA-core path, combine 1; a shared expert adds one
+    more grouped GEMM."""
+    def gemm(max_rows):
+        if dispatch == 2:
+            return 1 + 2
+        lists = 1 + (max_rows > m_skinny) + (max_rows > m_skinny and max_rows >= wide_min)
+        return 1 + 2 * lists
+    permute = 2 if T * spec.K <= 32 * 2048 else 4
+    shared = gemm(T) if spec.has_shared else 0
+    return 1 + 1 + permute + gemm(T) + shared + 1
 
 
 def stage_bytes_flops(spec, T, ids, e_active):
@@ -473,7 +480,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(),
                 "d2h_bytes_per_step": out.numel() * out.element_size()},
-        "gpu_launches": launches_per_layer(spec) * args.steps,
+        "gpu_launches": launches_per_layer(spec, T) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
     }

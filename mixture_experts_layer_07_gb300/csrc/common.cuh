@@ -19,7 +19,8 @@
 // Variant predicate shared by the host mirror and the plan kernel.
 //   m_size == 0                      -> skip (no work for the block)
 //   dispatch SIMT                    -> CUDA-core kernel
-//   m (per block, or max(1, R/E))    -> skinny if m <= m_skinny else tile
+//   m (per block, or max(1, R/E))    -> skinny if m <= m_skinny, else wide if
+//                                       m >= MOE_WIDE_MIN_ROWS, else tile
 __host__ __device__ __forceinline__ int moe_variant_of(int64_t m_size, int64_t R, int E,
                                                       int m_skinny, int dispatch) {
   if (m_size <= 0) return MOE_VARIANT_SKIP;
@@ -29,7 +30,8 @@ __host__ __device__ __forceinline__ int moe_variant_of(int64_t m_size, int64_t R
     int64_t avg = E > 0 ? R / E : R;
     m = avg < 1 ? 1 : avg;
   }
-  return m <= (int64_t)m_skinny ? MOE_VARIANT_SKINNY : MOE_VARIANT_TILE;
+  if (m <= (int64_t)m_skinny) return MOE_VARIANT_SKINNY;
+  return m >= MOE_WIDE_MIN_ROWS ? MOE_VARIANT_WIDE : MOE_VARIANT_TILE;
 }
 
 // First error wins.

@@ -14,8 +14,11 @@
 // applies that predicate per block and writes two work lists:
 //   skinny -- blocks with m_size <= m_skinny, 16-row token tiles
 //   tile   -- larger blocks, 128-row token tiles
-// Both lists run on the same tensor-core kernel template, instantiated for the
-// two token-tile widths, so small blocks do not pay for a 128-row tile.
+//   wide   -- blocks of at least 256 rows, 256-row token tiles (each weight
+//             tile is reused over twice the tokens: half the operand traffic
+//             per flop where the GEMM turns tensor-bound)
+// All lists run on the same tensor-core kernel template, instantiated for the
+// three token-tile widths, so small blocks do not pay for a wide tile.
 //
 // Tensor-core kernel (sm_100 family: tcgen05 + TMEM + TMA), "swap-AB" form:
 // the MMA's M side is 128 rows of the expert weight (output features), its N
@@ -51,41 +54,48 @@ using namespace moe_ptx;
 
 constexpr int kBnSkinny = 16;
 constexpr int kBnTile = 128;
+constexpr int kBnWide = 256;
+constexpr int kLists = 3;  // skinny, tile, wide
+__host__ __device__ constexpr int list_bn(int l) { return l == 0 ? kBnSkinny : l == 1 ? kBnTile : kBnWide; }
 constexpr int kBM = 128;  // weight rows per MMA (output features)
 constexpr int kBK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-// scratch layout
+// scratch layout: counts[kLists] then one int4 item list per variant
 struct PlanView {
-  int32_t* counts;  // [0] skinny items, [1] tile items
-  int4* items_s;    // {block, first row, rows, 0}
-  int4* items_t;
-  int cap_s, cap_t;
+  int32_t* counts;          // items per list
+  int4* items[kLists];      // {block, first row, rows, 0}
+  int cap[kLists];
 };
 
 inline PlanView plan_view(void* scratch, int R, int E_blocks) {
   PlanView v;
   char* p = static_cast<char*>(scratch);
   v.counts = reinterpret_cast<int32_t*>(p);
-  v.cap_s = moe_cdiv(R, kBnSkinny) + E_blocks;
-  v.cap_t = moe_cdiv(R, kBnTile) + E_blocks;
-  v.items_s = reinterpret_cast<int4*>(p + 256);
-  v.items_t = reinterpret_cast<int4*>(p + 256 + moe_align_up((size_t)v.cap_s * sizeof(int4), 256));
+  size_t off = 256;
+  for (int l = 0; l < kLists; ++l) {
+    v.cap[l] = moe_cdiv(R, list_bn(l)) + E_blocks;
+    v.items[l] = reinterpret_cast<int4*>(p + off);
+    off += moe_align_up((size_t)v.cap[l] * sizeof(int4), 256);
+  }
   return v;
 }
 
 // ---------------------------------------------------------------- plan
+struct PlanOut {
+  int4* items[kLists];
+};
+
 __global__ void __launch_bounds__(1024)
 gemm_plan_kernel(const int32_t* __restrict__ offsets, int E_blocks, int R, int m_skinny,
-                 int dispatch, int32_t* __restrict__ counts, int4* __restrict__ items_s,
-                 int4* __restrict__ items_t, int32_t* __restrict__ block_variant) {
-  __shared__ int ws[32], wt[32];
-  __shared__ int carry_s, carry_t;
+                 int dispatch, int32_t* __restrict__ counts, PlanOut out,
+                 int32_t* __restrict__ block_variant) {
+  __shared__ int wsum[kLists][32];
+  __shared__ int carry[kLists];
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
-  if (tid == 0) { carry_s = 0; carry_t = 0; }
-  const int64_t total_rows = R;  // the global average divides all R replicas by E
+  if (tid < kLists) carry[tid] = 0;
   __syncthreads();
   for (int base = 0; base < E_blocks; base += 1024) {
     const int e = base + tid;
@@ -94,49 +104,59 @@ gemm_plan_kernel(const int32_t* __restrict__ offsets, int E_blocks, int R, int m
       lo = offsets ? offsets[e] : 0;
       m = (offsets ? offsets[e + 1] : R) - lo;
     }
-    const int v = e < E_blocks ? moe_variant_of(m, total_rows, E_blocks, m_skinny, dispatch)
+    const int v = e < E_blocks ? moe_variant_of(m, R, E_blocks, m_skinny, dispatch)
                                : MOE_VARIANT_SKIP;
-    const int ns = (v == MOE_VARIANT_SKINNY || v == MOE_VARIANT_SIMT) ? moe_cdiv(m, kBnSkinny) : 0;
-    const int nt = v == MOE_VARIANT_TILE ? moe_cdiv(m, kBnTile) : 0;
-    // block-wide exclusive scans of ns and nt
-    int is = ns, it = nt;
+    const int list = (v == MOE_VARIANT_SKINNY || v == MOE_VARIANT_SIMT) ? 0
+                   : v == MOE_VARIANT_TILE ? 1 : v == MOE_VARIANT_WIDE ? 2 : -1;
+    int n[kLists], incl[kLists];
+#pragma unroll
+    for (int l = 0; l < kLists; ++l) {
+      n[l] = (l == list) ? moe_cdiv(m, list_bn(l)) : 0;
+      incl[l] = n[l];
+    }
+    // block-wide exclusive scans of the per-list item counts
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, is, o);
-      const int b = __shfl_up_sync(0xffffffffu, it, o);
-      if (lane >= o) { is += a; it += b; }
+#pragma unroll
+      for (int l = 0; l < kLists; ++l) {
+        const int a = __shfl_up_sync(0xffffffffu, incl[l], o);
+        if (lane >= o) incl[l] += a;
+      }
     }
-    if (lane == 31) { ws[warp] = is; wt[warp] = it; }
+    if (lane == 31) {
+#pragma unroll
+      for (int l = 0; l < kLists; ++l) wsum[l][warp] = incl[l];
+    }
     __syncthreads();
     if (warp == 0) {
-      int a = ws[lane], b = wt[lane];
-      int sa = a, sb = b;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xffffffffu, sa, o);
-        const int y = __shfl_up_sync(0xffffffffu, sb, o);
-        if (lane >= o) { sa += x; sb += y; }
+      for (int l = 0; l < kLists; ++l) {
+        const int a = wsum[l][lane];
+        int sc = a;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, sc, o);
+          if (lane >= o) sc += x;
+        }
+        wsum[l][lane] = sc - a;
       }
-      ws[lane] = sa - a;
-      wt[lane] = sb - b;
     }
     __syncthreads();
-    const int ps = carry_s + ws[warp] + is - ns;
-    const int pt = carry_t + wt[warp] + it - nt;
-    for (int i = 0; i < ns; ++i) {
-      const int r0 = i * kBnSkinny;
-      items_s[ps + i] = make_int4(e, lo + r0, min(kBnSkinny, m - r0), 0);
-    }
-    for (int i = 0; i < nt; ++i) {
-      const int r0 = i * kBnTile;
-      items_t[pt + i] = make_int4(e, lo + r0, min(kBnTile, m - r0), 0);
+    if (list >= 0) {
+      const int bn = list_bn(list);
+      const int pos = carry[list] + wsum[list][warp] + incl[list] - n[list];
+      for (int i = 0; i < n[list]; ++i)
+        out.items[list][pos + i] = make_int4(e, lo + i * bn, min(bn, m - i * bn), 0);
     }
     if (block_variant && e < E_blocks) block_variant[e] = v;
     __syncthreads();
-    if (tid == 1023) { carry_s = ps + ns; carry_t = pt + nt; }
+    if (tid == 1023) {
+#pragma unroll
+      for (int l = 0; l < kLists; ++l) carry[l] += wsum[l][31] + incl[l];
+    }
     __syncthreads();
   }
-  if (tid == 0) { counts[0] = carry_s; counts[1] = carry_t; }
+  if (tid < kLists) counts[tid] = carry[tid];
 }
 
 // ---------------------------------------------------------------- tensor cores
@@ -159,7 +179,7 @@ struct TcCfg {
   static constexpr int kConvBytes = kNA * kABytes;
   static constexpr int kEpiBytes = 4 * 16 * 32 * 2;  // per epilogue warp: 16 tokens x 32 features
   static constexpr int kStagesRaw =
-      (200 * 1024 - kEpiBytes - kConvStages * kConvBytes) / kStageBytes;
+      (216 * 1024 - kEpiBytes - kConvStages * kConvBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kAccCols = kNA * BN;                  // columns of one accumulator set
   static constexpr int kAccStages = 2 * kAccCols <= 512 ? 2 : 1;
@@ -178,6 +198,7 @@ struct TcCfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
   static_assert(kTmemNeed <= 512, "TMEM holds 512 columns");
   static_assert(kStages >= 2, "pipeline needs two stages");
+  static_assert(kSmemBytes <= 232448, "227 KB of shared memory per CTA");
 };
 
 MOE_DEVICE float silu_f(float g) { return g / (1.f + __expf(-g)); }
@@ -633,30 +654,36 @@ template <bool WFP8>
 cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const void* w1,
                        const void* w3, const void* w2, const float* s1, const float* s3,
                        const float* s2, void* hact, void* y, const PlanView& pv,
-                       int32_t* dev_status, cudaStream_t stream, bool any_skinny, bool any_tile) {
-  CUtensorMap m_w1, m_w3, m_w2, m_x16, m_x128, m_h16, m_h128;
+                       int32_t* dev_status, cudaStream_t stream, const bool (&any)[kLists]) {
+  CUtensorMap m_w1, m_w3, m_w2, m_x[kLists], m_h[kLists];
   if (!make_weight_map(&m_w1, w1, E_blocks, I, H, WFP8) ||
       !make_weight_map(&m_w3, w3, E_blocks, I, H, WFP8) ||
-      !make_weight_map(&m_w2, w2, E_blocks, H, I, WFP8) ||
-      !make_act_map(&m_x16, xp, R, H, kBnSkinny) || !make_act_map(&m_x128, xp, R, H, kBnTile) ||
-      !make_act_map(&m_h16, hact, R, I, kBnSkinny) || !make_act_map(&m_h128, hact, R, I, kBnTile))
+      !make_weight_map(&m_w2, w2, E_blocks, H, I, WFP8))
     return cudaErrorInvalidValue;
+  for (int l = 0; l < kLists; ++l)
+    if (any[l] && (!make_act_map(&m_x[l], xp, R, H, list_bn(l)) ||
+                   !make_act_map(&m_h[l], hact, R, I, list_bn(l))))
+      return cudaErrorInvalidValue;
   cudaError_t err = cudaSuccess;
-  if (any_skinny)
-    err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x16, s1, s3, pv.counts, 0, pv.items_s,
-                                        pv.cap_s, I, H, hact, dev_status, stream);
-  if (err != cudaSuccess) return err;
-  if (any_tile)
-    err = run_tc<kBnTile, true, WFP8>(m_w1, m_w3, m_x128, s1, s3, pv.counts, 1, pv.items_t,
-                                      pv.cap_t, I, H, hact, dev_status, stream);
-  if (err != cudaSuccess) return err;
-  if (any_skinny)
-    err = run_tc<kBnSkinny, false, WFP8>(m_w2, m_w2, m_h16, s2, s2, pv.counts, 0, pv.items_s,
-                                         pv.cap_s, H, I, y, dev_status, stream);
-  if (err != cudaSuccess) return err;
-  if (any_tile)
-    err = run_tc<kBnTile, false, WFP8>(m_w2, m_w2, m_h128, s2, s2, pv.counts, 1, pv.items_t,
-                                       pv.cap_t, H, I, y, dev_status, stream);
+  // G1 (SwiGLU, N = I, K = H) for every list, then G2 (N = H, K = I)
+  if (any[0] && err == cudaSuccess)
+    err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x[0], s1, s3, pv.counts, 0, pv.items[0],
+                                        pv.cap[0], I, H, hact, dev_status, stream);
+  if (any[1] && err == cudaSuccess)
+    err = run_tc<kBnTile, true, WFP8>(m_w1, m_w3, m_x[1], s1, s3, pv.counts, 1, pv.items[1],
+                                      pv.cap[1], I, H, hact, dev_status, stream);
+  if (any[2] && err == cudaSuccess)
+    err = run_tc<kBnWide, true, WFP8>(m_w1, m_w3, m_x[2], s1, s3, pv.counts, 2, pv.items[2],
+                                      pv.cap[2], I, H, hact, dev_status, stream);
+  if (any[0] && err == cudaSuccess)
+    err = run_tc<kBnSkinny, false, WFP8>(m_w2, m_w2, m_h[0], s2, s2, pv.counts, 0, pv.items[0],
+                                         pv.cap[0], H, I, y, dev_status, stream);
+  if (any[1] && err == cudaSuccess)
+    err = run_tc<kBnTile, false, WFP8>(m_w2, m_w2, m_h[1], s2, s2, pv.counts, 1, pv.items[1],
+                                       pv.cap[1], H, I, y, dev_status, stream);
+  if (any[2] && err == cudaSuccess)
+    err = run_tc<kBnWide, false, WFP8>(m_w2, m_w2, m_h[2], s2, s2, pv.counts, 2, pv.items[2],
+                                       pv.cap[2], H, I, y, dev_status, stream);
   return err;
 }
 
@@ -678,10 +705,10 @@ cudaError_t run_simt(bool fp8, const void* act, const void* wa, const void* wb, 
 }  // namespace
 
 size_t grouped_gemm_scratch_bytes(int R, int E_blocks) {
-  const int cap_s = moe_cdiv(R, kBnSkinny) + E_blocks;
-  const int cap_t = moe_cdiv(R, kBnTile) + E_blocks;
-  return 256 + moe_align_up((size_t)cap_s * sizeof(int4), 256) +
-         moe_align_up((size_t)cap_t * sizeof(int4), 256);
+  size_t b = 256;
+  for (int l = 0; l < kLists; ++l)
+    b += moe_align_up((size_t)(moe_cdiv(R, list_bn(l)) + E_blocks) * sizeof(int4), 256);
+  return b;
 }
 
 int grouped_gemm_check(int H, int I, int wdtype) {
@@ -702,32 +729,38 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
   const bool fp8 = wdtype == MOE_W_FP8E4M3_B128;
   const bool simt = dispatch == MOE_DISPATCH_SIMT;
   PlanView pv = plan_view(scratch, R, E_blocks);
+  PlanOut po;
+  for (int l = 0; l < kLists; ++l) po.items[l] = pv.items[l];
   cudaError_t err = moe_launch(gemm_plan_kernel, dim3(1), dim3(1024), 0, stream, 1, offsets,
-                               E_blocks, R, m_skinny, dispatch, pv.counts, pv.items_s, pv.items_t,
-                               block_variant);
+                               E_blocks, R, m_skinny, dispatch, pv.counts, po, block_variant);
   if (err != cudaSuccess || R == 0) return err;
 
   if (simt) {
-    err = run_simt<true>(fp8, xp, w1, w3, s1, s3, pv.counts, pv.items_s, pv.cap_s, I, H, hact, stream);
+    err = run_simt<true>(fp8, xp, w1, w3, s1, s3, pv.counts, pv.items[0], pv.cap[0], I, H, hact,
+                         stream);
     if (err != cudaSuccess) return err;
-    return run_simt<false>(fp8, hact, w2, nullptr, s2, nullptr, pv.counts, pv.items_s, pv.cap_s, H,
-                           I, y, stream);
+    return run_simt<false>(fp8, hact, w2, nullptr, s2, nullptr, pv.counts, pv.items[0], pv.cap[0],
+                           H, I, y, stream);
   }
   // Which lists can be non-empty, from what the host knows without reading
   // the offsets: no block holds more than max_rows rows (moe_layer passes T:
   // a token picks distinct experts), and under the global average every block
   // takes the same variant.  An empty list's launch is skipped.
   if (max_rows < 0 || max_rows > R) max_rows = R;
-  bool any_skinny = true, any_tile = max_rows > m_skinny;
+  bool any[kLists];
   if (dispatch == MOE_DISPATCH_GLOBAL_AVG) {
-    const int64_t avg = E_blocks > 0 ? (int64_t)R / E_blocks : R;
-    const bool tile = (avg < 1 ? 1 : avg) > m_skinny;
-    any_skinny = !tile;
-    any_tile = tile;
+    const int v = moe_variant_of(1, R, E_blocks, m_skinny, dispatch);
+    any[0] = v == MOE_VARIANT_SKINNY;
+    any[1] = v == MOE_VARIANT_TILE;
+    any[2] = v == MOE_VARIANT_WIDE;
+  } else {
+    any[0] = true;
+    any[1] = max_rows > m_skinny;
+    any[2] = max_rows > m_skinny && max_rows >= MOE_WIDE_MIN_ROWS;
   }
   if (fp8)
     return run_tc_all<true>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                            stream, any_skinny, any_tile);
+                            stream, any);
   return run_tc_all<false>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                           stream, any_skinny, any_tile);
+                           stream, any);
 }

@@ -50,16 +50,26 @@ def test_status_strings(ops):
 def test_block_variant_golden_predicate(ops):
     g = json.load(open(os.path.join(ROOT, "tests", "golden", "dispatch_predicate.json")))
     thr = g["threshold"]
+    # the pages' predicate is two-way (small block / large tile); on the GPU the
+    # large side is split again by size (128- or 256-row token tiles)
+    large = {ops.VARIANT_TILE, ops.VARIANT_WIDE}
+
+    def pages_code(v):
+        return 2 if v in large else v
+
     for m, want in g["per_block"]:
-        assert ops.block_variant(m, 1 << 20, 8, thr, ops.DISPATCH_PER_BLOCK) == want, m
+        assert pages_code(ops.block_variant(m, 1 << 20, 8, thr, ops.DISPATCH_PER_BLOCK)) == want, m
     w = g["worked"]
     off = w["offsets"]
     R, E = off[-1], w["E"]
     sizes = [off[i + 1] - off[i] for i in range(E)]
-    assert [ops.block_variant(m, R, E, thr, ops.DISPATCH_PER_BLOCK) for m in sizes] == \
+    assert [pages_code(ops.block_variant(m, R, E, thr, ops.DISPATCH_PER_BLOCK)) for m in sizes] == \
         w["per_block_variants"]
-    assert [ops.block_variant(m, R, E, thr, ops.DISPATCH_GLOBAL_AVG) for m in sizes] == \
+    assert [pages_code(ops.block_variant(m, R, E, thr, ops.DISPATCH_GLOBAL_AVG)) for m in sizes] == \
         w["global_average_variants"]
+    assert ops.block_variant(255, R, E, thr) == ops.VARIANT_TILE
+    assert ops.block_variant(256, R, E, thr) == ops.VARIANT_WIDE
+    assert ops.block_variant(4096, R, E, thr) == ops.VARIANT_WIDE
     assert ops.block_variant(3, R, E, thr, ops.DISPATCH_SIMT) == ops.VARIANT_SIMT
     assert ops.block_variant(0, R, E, thr, ops.DISPATCH_SIMT) == ops.VARIANT_SKIP
     assert ops.default_m_skinny() > 0

@@ -265,6 +265,10 @@ GEMM_CASES = [  # spec name, overrides, T, concentrated, dispatch, m_skinny, bot
     ("gpt_oss_20b", {}, 40, True, 0, -1, True),
     ("gpt_oss_20b", {"E": 6}, 40, True, 2, -1, False),
     ("gpt_oss_20b", {"E": 4}, 300, True, 0, -1, False),
+    # blocks of >= 256 rows: the wide (256-row token tile) variant
+    ("qwen3_30b_a3b", {}, 1200, True, 0, -1, True),
+    ("tiny", {"H": 2880, "I": 2880, "E": 4}, 700, True, 0, -1, True),
+    ("gpt_oss_20b", {"E": 6}, 700, True, 0, -1, False),
 ]
 
 
@@ -283,8 +287,11 @@ def test_grouped_gemm(ops, name, over, T, conc, dispatch, m_skinny, both):
     m = np.diff(off)
     want_bv = [ops.block_variant(int(mm), R, spec.E, m_skinny, dispatch) for mm in m]
     assert bv.tolist() == want_bv
-    if both:  # skinny and tile blocks in the same call
-        assert {ops.VARIANT_SKINNY, ops.VARIANT_TILE} <= set(bv.tolist())
+    if both:  # small and large blocks in the same call
+        assert ops.VARIANT_SKINNY in bv.tolist()
+        assert {ops.VARIANT_TILE, ops.VARIANT_WIDE} & set(bv.tolist())
+    if T * spec.K >= 4 * 256 and conc and dispatch == 0:
+        assert ops.VARIANT_WIDE in bv.tolist()
 
 
 def test_grouped_gemm_single_block_without_offsets(ops):
