@@ -151,20 +151,20 @@ def tensors_of(spec, d):
     return t
 
 
-def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=256):
+def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129):
     """Kernel launches inside one moe_layer call (mirrors the library's
     launch sequence): router 1, top-K 1, permute 2 (one fused count/scan/
     scatter CTA + gather) or 4 (count, scan, scatter, gather) above 65536
     replicas, grouped GEMM 1 plan + one G1 and one G2 launch per variant list
     that can be non-empty (skinny always; tile when T > m_skinny; wide when also
-    T >= 256) or 2 on the CUDA-core path, combine 1; a shared expert adds one
+    T > 128) or 2 on the CUDA-core path, combine 1; a shared expert adds one
     more grouped GEMM."""
     def gemm(max_rows):
         if dispatch == 2:
             return 1 + 2
         lists = 1 + (max_rows > m_skinny) + (max_rows > m_skinny and max_rows >= wide_min)
         return 1 + 2 * lists
-    permute = 2 if T * spec.K <= 32 * 2048 else 4
+    permute = 2 if T * spec.K <= 4096 else 4
     shared = gemm(T) if spec.has_shared else 0
     return 1 + 1 + permute + gemm(T) + shared + 1
 

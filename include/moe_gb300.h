@@ -88,8 +88,8 @@ typedef enum {
 #define MOE_VARIANT_SKINNY 1  /* small block: narrow token tile */
 #define MOE_VARIANT_TILE 2    /* large block: wide tensor-core tile */
 #define MOE_VARIANT_SIMT 3    /* CUDA-core kernel (MOE_DISPATCH_SIMT) */
-#define MOE_VARIANT_WIDE 4    /* very large block (m_size >= MOE_WIDE_MIN_ROWS): 256-row token tile */
-#define MOE_WIDE_MIN_ROWS 256
+#define MOE_VARIANT_WIDE 4    /* large block (m_size >= MOE_WIDE_MIN_ROWS): 256-row token tiles */
+#define MOE_WIDE_MIN_ROWS 129
 
 typedef struct {
   int T_max;           /* largest T the workspace must hold */
@@ -135,8 +135,8 @@ int moe_default_m_skinny(void);
  * "1. gemm.h": the large-tile kernel is used above a small-M threshold).
  * R = total rows, E = number of blocks (used by MOE_DISPATCH_GLOBAL_AVG, which
  * decides from max(1, R / E) for every non-empty block).  The large-tile side
- * is split once more on the GPU: blocks of at least MOE_WIDE_MIN_ROWS rows take
- * 256-row token tiles (MOE_VARIANT_WIDE), the others 128-row tiles.
+ * is split once more on the GPU: blocks of more than 128 rows take 256-row
+ * token tiles (MOE_VARIANT_WIDE), the others one 128-row tile.
  * Host-callable copy of the device predicate; returns a MOE_VARIANT_* code.
  */
 int moe_block_variant(int64_t m_size, int64_t R, int E, int m_skinny, int dispatch);

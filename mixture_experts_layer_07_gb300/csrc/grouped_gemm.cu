@@ -14,9 +14,10 @@
 // applies that predicate per block and writes two work lists:
 //   skinny -- blocks with m_size <= m_skinny, 16-row token tiles
 //   tile   -- larger blocks, 128-row token tiles
-//   wide   -- blocks of at least 256 rows, 256-row token tiles (each weight
-//             tile is reused over twice the tokens: half the operand traffic
-//             per flop where the GEMM turns tensor-bound)
+//   wide   -- blocks of more than 128 rows, 256-row token tiles (each weight
+//             tile is read once per 256 tokens: a block of 129..256 rows reads
+//             its weights once instead of twice, and where the GEMM turns
+//             tensor-bound the operand traffic per flop halves)
 // All lists run on the same tensor-core kernel template, instantiated for the
 // three token-tile widths, so small blocks do not pay for a wide tile.
 //

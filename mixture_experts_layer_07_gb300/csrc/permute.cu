@@ -151,7 +151,7 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunk
   }
 }
 
-// Small problems (R <= 32 warps x 2048 replicas): count, scan and stable
+// Small problems (R <= kFusedMaxR replicas, the decode regime): count, scan and stable
 // scatter in ONE CTA of 32 warps, all counters in shared memory -- one launch
 // instead of three, and no global scratch.  Warp w owns the contiguous replica
 // range [w*span, (w+1)*span); per-warp counts cnt[w][e] become per-warp bases by
@@ -159,7 +159,9 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunk
 // each range again in order, 32 replicas per step, ranking equal experts with
 // __match_any_sync.  Deterministic and stable like the multi-CTA path.
 constexpr int kFusedWarps = 32;
-constexpr int kFusedMaxSpan = 2048;
+// Above this many replicas the multi-CTA path (count, scan, scatter) wins: one
+// CTA cannot keep enough loads and stores in flight.
+constexpr int kFusedMaxR = 4096;
 
 __global__ void __launch_bounds__(32 * kFusedWarps)
 permute_fused_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ offsets,
@@ -302,7 +304,7 @@ cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int 
   const size_t smem = (size_t)kWarpsPerCta * E * sizeof(int32_t);
   const int ctas = moe_cdiv(nch, kWarpsPerCta);
   const size_t fused_smem = (size_t)(kFusedWarps + 1) * E * sizeof(int32_t);
-  if (R > 0 && R <= kFusedWarps * kFusedMaxSpan && fused_smem <= 200 * 1024) {
+  if (R > 0 && R <= kFusedMaxR && fused_smem <= 200 * 1024) {
     static bool attr = false;
     if (!attr) {
       cudaError_t e = cudaFuncSetAttribute(permute_fused_kernel,

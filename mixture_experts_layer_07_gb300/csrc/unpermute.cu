@@ -28,14 +28,28 @@ unpermute_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ flat_t
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int k = 0; k < K; ++k) {
-    const int row = __ldg(flat_to_row + (size_t)t * K + k);
-    if (row < 0) continue;
-    const float w = __ldg(weights + (size_t)t * K + k);
-    float f[8];
-    bf16x8_to_f32(__ldg(y + (size_t)row * H8 + c), f);
+  // K sources in groups of 8: all row indices, then all 16-byte vectors in
+  // flight together, then the fp32 sums in k order
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    int rows[8];
+    float wk[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, f[i], acc[i]);
+    for (int j = 0; j < 8; ++j) {
+      rows[j] = k0 + j < K ? __ldg(flat_to_row + (size_t)t * K + k0 + j) : -1;
+      wk[j] = k0 + j < K ? __ldg(weights + (size_t)t * K + k0 + j) : 0.f;
+    }
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      v[j] = rows[j] >= 0 ? __ldg(y + (size_t)rows[j] * H8 + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (rows[j] < 0) continue;
+      float f[8];
+      bf16x8_to_f32(v[j], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wk[j], f[i], acc[i]);
+    }
   }
   if (shared_y) {
     const float g = __ldg(shared_gate + t);

@@ -20,7 +20,7 @@ MODE_SOFTMAX, MODE_SIGMOID_BIAS = 0, 1
 W_BF16, W_FP8 = 0, 1
 DISPATCH_PER_BLOCK, DISPATCH_GLOBAL_AVG, DISPATCH_SIMT = 0, 1, 2
 VARIANT_SKIP, VARIANT_SKINNY, VARIANT_TILE, VARIANT_SIMT, VARIANT_WIDE = 0, 1, 2, 3, 4
-WIDE_MIN_ROWS = 256
+WIDE_MIN_ROWS = 129
 DEV_OK, DEV_BAD_EXPERT_ID, DEV_WAIT_TIMEOUT = 0, 1, 2
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",

@@ -290,7 +290,7 @@ def test_grouped_gemm(ops, name, over, T, conc, dispatch, m_skinny, both):
     if both:  # small and large blocks in the same call
         assert ops.VARIANT_SKINNY in bv.tolist()
         assert {ops.VARIANT_TILE, ops.VARIANT_WIDE} & set(bv.tolist())
-    if T * spec.K >= 4 * 256 and conc and dispatch == 0:
+    if dispatch == 0 and (m >= ops.WIDE_MIN_ROWS).any():
         assert ops.VARIANT_WIDE in bv.tolist()
 
 
