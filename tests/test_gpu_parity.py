@@ -267,7 +267,7 @@ GEMM_CASES = [  # spec name, overrides, T, concentrated, dispatch, m_skinny, bot
     ("gpt_oss_20b", {"E": 4}, 300, True, 0, -1, False),
     # blocks of >= 256 rows: the wide (256-row token tile) variant
     ("qwen3_30b_a3b", {}, 1200, True, 0, -1, True),
-    ("tiny", {"H": 2880, "I": 2880, "E": 4}, 700, True, 0, -1, True),
+    ("tiny", {"H": 2880, "I": 2880, "E": 4}, 700, True, 0, -1, False),
     ("gpt_oss_20b", {"E": 6}, 700, True, 0, -1, False),
 ]
 
