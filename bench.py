@@ -156,13 +156,14 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129):
     launch sequence): router 1, top-K 1, permute 2 (one fused count/scan/
     scatter CTA + gather) or 4 (count, scan, scatter, gather) above 65536
     replicas, grouped GEMM 1 plan + one G1 and one G2 launch per variant list
-    that can be non-empty (skinny always; tile when T > m_skinny; wide when also
-    T > 128) or 2 on the CUDA-core path, combine 1; a shared expert adds one
+    that can be non-empty (skinny always; tile when T > m_skinny; wide for FP8
+    weights when also T > 128) or 2 on the CUDA-core path, combine 1; a shared expert adds one
     more grouped GEMM."""
     def gemm(max_rows):
         if dispatch == 2:
             return 1 + 2
-        lists = 1 + (max_rows > m_skinny) + (max_rows > m_skinny and max_rows >= wide_min)
+        lists = 1 + (max_rows > m_skinny) + (spec.wdtype == "fp8" and max_rows > m_skinny
+                                              and max_rows >= wide_min)
         return 1 + 2 * lists
     permute = 2 if T * spec.K <= 4096 else 4
     shared = gemm(T) if spec.has_shared else 0
@@ -552,6 +553,36 @@ def stage_sweep(spec, Ts, peaks, dev):
     return out
 
 
+def probe_stages(spec, T, reps, dev):
+    """R, K, P, U alone at T, `reps` times, no timing: the command the
+    per-stage ncu captures profile."""
+    from mixture_experts_layer_07_gb300 import ops
+
+    H, E, K, G = spec.H, spec.E, spec.K, spec.G
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    x = torch.randn(T, H, device=dev, generator=gen).to(torch.bfloat16)
+    wg = torch.randn(G, H, device=dev, generator=gen) / H ** 0.5
+    logits = torch.empty(T, G, device=dev)
+    ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+    w = torch.empty(T, K, device=dev)
+    R = T * K
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    r2f = torch.empty(R, dtype=torch.int32, device=dev)
+    f2r = torch.empty(R, dtype=torch.int32, device=dev)
+    xp = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+    scr = torch.empty(ops.permute_scratch_bytes(T, E, K), dtype=torch.uint8, device=dev)
+    o = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    sel_bias = torch.zeros(E, device=dev) if spec.mode == 1 else None
+    for _ in range(reps):
+        ops.router_gemm(x, wg, None, logits)
+        ops.topk_route(logits, E, K, spec.mode, spec.routed_scale, ids, w, sel_bias)
+        ops.permute(x, ids, E, off, r2f, f2r, xp, scr)
+        ops.unpermute(xp, f2r, w, T, K, H, o)
+    torch.cuda.synchronize()
+    return {"probe": "stages", "workload": spec.name, "T": T, "reps": reps}
+
+
 def prefill_points(peaks, dev):
     """The grouped GEMM stage on prefill shapes where it is tensor-bound."""
     from mixture_experts_layer_07_gb300 import ops, synth
@@ -671,6 +702,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--probe-stages", type=int, default=0, metavar="T",
+                    help="only run R/K/P/U at this T a few times (for ncu captures)")
     ap.add_argument("--extra", action="store_true",
                     help="also time R/K/P/U at large T and the grouped GEMM on prefill shapes")
     args = ap.parse_args()
@@ -685,6 +718,13 @@ def main():
         if rank != 0:
             return
         print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if args.probe_stages:
+        from mixture_experts_layer_07_gb300 import synth
+        torch.cuda.set_device(local_rank)
+        print(json.dumps(probe_stages(synth.SPECS[args.workload], args.probe_stages, 3,
+                                      f"cuda:{local_rank}")), flush=True)
         return
 
     if world > 1:

@@ -88,7 +88,7 @@ typedef enum {
 #define MOE_VARIANT_SKINNY 1  /* small block: narrow token tile */
 #define MOE_VARIANT_TILE 2    /* large block: wide tensor-core tile */
 #define MOE_VARIANT_SIMT 3    /* CUDA-core kernel (MOE_DISPATCH_SIMT) */
-#define MOE_VARIANT_WIDE 4    /* large block (m_size >= MOE_WIDE_MIN_ROWS): 256-row token tiles */
+#define MOE_VARIANT_WIDE 4    /* FP8, m_size >= MOE_WIDE_MIN_ROWS: 256-row token tiles */
 #define MOE_WIDE_MIN_ROWS 129
 
 typedef struct {
@@ -135,11 +135,12 @@ int moe_default_m_skinny(void);
  * "1. gemm.h": the large-tile kernel is used above a small-M threshold).
  * R = total rows, E = number of blocks (used by MOE_DISPATCH_GLOBAL_AVG, which
  * decides from max(1, R / E) for every non-empty block).  The large-tile side
- * is split once more on the GPU: blocks of more than 128 rows take 256-row
- * token tiles (MOE_VARIANT_WIDE), the others one 128-row tile.
+ * is split once more on the GPU for FP8 weights (wdtype): blocks of more than
+ * 128 rows take 256-row token tiles (MOE_VARIANT_WIDE), so each dequantised
+ * weight tile serves twice the tokens; otherwise 128-row tiles.
  * Host-callable copy of the device predicate; returns a MOE_VARIANT_* code.
  */
-int moe_block_variant(int64_t m_size, int64_t R, int E, int m_skinny, int dispatch);
+int moe_block_variant(int64_t m_size, int64_t R, int E, int m_skinny, int dispatch, int wdtype);
 
 /*
  * R: router (gate) GEMM.   logits[t, g] = sum_h fp32(x[t, h]) * wg[g, h] (+ gate_bias[g])
@@ -243,8 +244,8 @@ moe_status_t moe_grouped_gemm_scratch_bytes(int R, int E_blocks, size_t* bytes);
  * (moe_block_variant), never from a global average unless dispatch asks for
  * it ([dispatch] "2. moe_fp8.cpp").  Every variant runs tcgen05 tensor-core
  * MMAs fed by TMA with TMEM accumulators: the skinny variant uses a 16-row
- * token tile, the tile variant a 128-row one and the wide variant a 256-row
- * one.  FP8 weights need H, I <= 8192.
+ * token tile, the tile variant a 128-row one and the wide variant (FP8) a
+ * 256-row one.  FP8 weights need H, I <= 8192.
  *   xp        [R, H] bf16, 16-byte aligned
  *   offsets   [E_blocks + 1] int32 (device), or NULL for one block [0, R)
  *   w1, w3    [E_blocks, I, H]; w2 [E_blocks, H, I]; bf16 or e4m3 per wdtype

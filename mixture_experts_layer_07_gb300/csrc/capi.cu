@@ -86,9 +86,9 @@ const char* moe_status_string(moe_status_t s) {
 
 int moe_default_m_skinny(void) { return MOE_DEFAULT_M_SKINNY; }
 
-int moe_block_variant(int64_t m_size, int64_t R, int E, int m_skinny, int dispatch) {
+int moe_block_variant(int64_t m_size, int64_t R, int E, int m_skinny, int dispatch, int wdtype) {
   if (m_skinny < 0) m_skinny = MOE_DEFAULT_M_SKINNY;
-  return moe_variant_of(m_size, R, E, m_skinny, dispatch);
+  return moe_variant_of(m_size, R, E, m_skinny, dispatch, wdtype);
 }
 
 moe_status_t moe_router_gemm(const void* x, const float* wg, const float* gate_bias,

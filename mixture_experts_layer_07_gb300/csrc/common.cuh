@@ -20,9 +20,10 @@
 //   m_size == 0                      -> skip (no work for the block)
 //   dispatch SIMT                    -> CUDA-core kernel
 //   m (per block, or max(1, R/E))    -> skinny if m <= m_skinny, else wide if
-//                                       m >= MOE_WIDE_MIN_ROWS, else tile
+//                                       FP8 weights and m >= MOE_WIDE_MIN_ROWS,
+//                                       else tile
 __host__ __device__ __forceinline__ int moe_variant_of(int64_t m_size, int64_t R, int E,
-                                                      int m_skinny, int dispatch) {
+                                                      int m_skinny, int dispatch, int wdtype) {
   if (m_size <= 0) return MOE_VARIANT_SKIP;
   if (dispatch == MOE_DISPATCH_SIMT) return MOE_VARIANT_SIMT;
   int64_t m = m_size;
@@ -31,7 +32,10 @@ __host__ __device__ __forceinline__ int moe_variant_of(int64_t m_size, int64_t R
     m = avg < 1 ? 1 : avg;
   }
   if (m <= (int64_t)m_skinny) return MOE_VARIANT_SKINNY;
-  return m >= MOE_WIDE_MIN_ROWS ? MOE_VARIANT_WIDE : MOE_VARIANT_TILE;
+  // 256-row token tiles pay off where each weight tile is dequantised (FP8):
+  // the conversion is amortised over twice the tokens
+  return (wdtype == MOE_W_FP8E4M3_B128 && m >= MOE_WIDE_MIN_ROWS) ? MOE_VARIANT_WIDE
+                                                                 : MOE_VARIANT_TILE;
 }
 
 // First error wins.

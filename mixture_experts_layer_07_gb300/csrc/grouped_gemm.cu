@@ -14,10 +14,8 @@
 // applies that predicate per block and writes two work lists:
 //   skinny -- blocks with m_size <= m_skinny, 16-row token tiles
 //   tile   -- larger blocks, 128-row token tiles
-//   wide   -- blocks of more than 128 rows, 256-row token tiles (each weight
-//             tile is read once per 256 tokens: a block of 129..256 rows reads
-//             its weights once instead of twice, and where the GEMM turns
-//             tensor-bound the operand traffic per flop halves)
+//   wide   -- FP8 weights only: blocks of more than 128 rows, 256-row token
+//             tiles, so each dequantised weight tile serves twice the tokens
 // All lists run on the same tensor-core kernel template, instantiated for the
 // three token-tile widths, so small blocks do not pay for a wide tile.
 //
@@ -89,7 +87,7 @@ struct PlanOut {
 
 __global__ void __launch_bounds__(1024)
 gemm_plan_kernel(const int32_t* __restrict__ offsets, int E_blocks, int R, int m_skinny,
-                 int dispatch, int32_t* __restrict__ counts, PlanOut out,
+                 int dispatch, int wdtype, int32_t* __restrict__ counts, PlanOut out,
                  int32_t* __restrict__ block_variant) {
   __shared__ int wsum[kLists][32];
   __shared__ int carry[kLists];
@@ -105,7 +103,7 @@ gemm_plan_kernel(const int32_t* __restrict__ offsets, int E_blocks, int R, int m
       lo = offsets ? offsets[e] : 0;
       m = (offsets ? offsets[e + 1] : R) - lo;
     }
-    const int v = e < E_blocks ? moe_variant_of(m, R, E_blocks, m_skinny, dispatch)
+    const int v = e < E_blocks ? moe_variant_of(m, R, E_blocks, m_skinny, dispatch, wdtype)
                                : MOE_VARIANT_SKIP;
     const int list = (v == MOE_VARIANT_SKINNY || v == MOE_VARIANT_SIMT) ? 0
                    : v == MOE_VARIANT_TILE ? 1 : v == MOE_VARIANT_WIDE ? 2 : -1;
@@ -733,7 +731,8 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
   PlanOut po;
   for (int l = 0; l < kLists; ++l) po.items[l] = pv.items[l];
   cudaError_t err = moe_launch(gemm_plan_kernel, dim3(1), dim3(1024), 0, stream, 1, offsets,
-                               E_blocks, R, m_skinny, dispatch, pv.counts, po, block_variant);
+                               E_blocks, R, m_skinny, dispatch, wdtype, pv.counts, po,
+                               block_variant);
   if (err != cudaSuccess || R == 0) return err;
 
   if (simt) {
@@ -750,14 +749,14 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
   if (max_rows < 0 || max_rows > R) max_rows = R;
   bool any[kLists];
   if (dispatch == MOE_DISPATCH_GLOBAL_AVG) {
-    const int v = moe_variant_of(1, R, E_blocks, m_skinny, dispatch);
+    const int v = moe_variant_of(1, R, E_blocks, m_skinny, dispatch, wdtype);
     any[0] = v == MOE_VARIANT_SKINNY;
     any[1] = v == MOE_VARIANT_TILE;
     any[2] = v == MOE_VARIANT_WIDE;
   } else {
     any[0] = true;
     any[1] = max_rows > m_skinny;
-    any[2] = max_rows > m_skinny && max_rows >= MOE_WIDE_MIN_ROWS;
+    any[2] = fp8 && max_rows > m_skinny && max_rows >= MOE_WIDE_MIN_ROWS;
   }
   if (fp8)
     return run_tc_all<true>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,

@@ -16,7 +16,8 @@
 //   3. scatter one warp per chunk, 32 replicas per step in order: lanes with
 //              the same expert find each other with __match_any_sync, the
 //              rank is the running count plus the popcount of lower lanes
-//   4. gather  xp[row] = x[row_to_flat[row] / K], 16-byte vectors
+//   4. copy    xp[flat_to_row[t*K+k]] = x[t]: each row of x is read once and
+//              written to its token's K rows, 16-byte vectors
 #include "common.cuh"
 #include "internal.h"
 
@@ -41,13 +42,17 @@ permute_count_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunks,
   __syncwarp();
   if (chunk < nchunks) {
     const int f0 = chunk * kChunk;
-    for (int i = lane; i < kChunk; i += 32) {
-      const int f = f0 + i;
-      if (f < R) {
-        const int e = ids[f];
-        if (e >= 0 && e < E) atomicAdd(&h[e], 1);
-        else moe_set_status(dev_status, MOE_DEV_BAD_EXPERT_ID);
-      }
+    int v[kChunk / 32];  // all of the chunk's ids in flight at once
+#pragma unroll
+    for (int i = 0; i < kChunk / 32; ++i) {
+      const int f = f0 + i * 32 + lane;
+      v[i] = f < R ? __ldg(ids + f) : E;
+    }
+#pragma unroll
+    for (int i = 0; i < kChunk / 32; ++i) {
+      const int e = v[i];
+      if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+      else if (f0 + i * 32 + lane < R) moe_set_status(dev_status, MOE_DEV_BAD_EXPERT_ID);
     }
     __syncwarp();
     for (int e = lane; e < E; e += 32) counts[(size_t)e * nchunks + chunk] = h[e];
@@ -65,20 +70,29 @@ permute_scan_kernel(int32_t* __restrict__ counts, int E, int nchunks,
   pdl_wait();
   pdl_trigger();
   const int lane = lane_id(), warp = warp_id();
+  constexpr int kB = 8;  // 8 x 32 chunk counts loaded before they are scanned
   for (int e = warp; e < E; e += 32) {
     int32_t* row = counts + (size_t)e * nchunks;
     int32_t run = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-      const int c = c0 + lane;
-      const int32_t v = c < nchunks ? row[c] : 0;
-      int32_t incl = v;
+    for (int c0 = 0; c0 < nchunks; c0 += 32 * kB) {
+      int32_t v[kB];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
+      for (int b = 0; b < kB; ++b) {
+        const int c = c0 + b * 32 + lane;
+        v[b] = c < nchunks ? row[c] : 0;
       }
-      if (c < nchunks) row[c] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        const int c = c0 + b * 32 + lane;
+        int32_t incl = v[b];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        if (c < nchunks) row[c] = run + incl - v[b];
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
     }
     if (lane == 0) tot[e] = run;
   }
@@ -124,13 +138,16 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunk
   __syncwarp();
   const unsigned lt_mask = (1u << lane) - 1u;
   const int f0 = chunk * kChunk;
-  for (int s = 0; s < kChunk; s += 32) {
-    const int f = f0 + s + lane;
-    int e = -1;
-    if (f < R) {
-      e = ids[f];
-      if (e < 0 || e >= E) e = -1;
-    }
+  int v[kChunk / 32];  // all of the chunk's ids in flight at once
+#pragma unroll
+  for (int i = 0; i < kChunk / 32; ++i) {
+    const int f = f0 + i * 32 + lane;
+    v[i] = f < R ? __ldg(ids + f) : -1;
+  }
+#pragma unroll
+  for (int i = 0; i < kChunk / 32; ++i) {
+    const int f = f0 + i * 32 + lane;
+    const int e = (v[i] >= 0 && v[i] < E) ? v[i] : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt_mask);
     const int leader = __ffs(peers) - 1;
@@ -271,21 +288,49 @@ permute_fused_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __r
   }
 }
 
-// one warp per row, 16-byte vectors
+// xp[flat_to_row[t*K+k]] = x[t]: one warp per token reads each 16-byte vector
+// of x[t] once and writes it to the token's K rows (reading x once instead of
+// once per replica), 8 vectors per lane in flight.
 __global__ void __launch_bounds__(256)
-permute_gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_to_flat,
-                      const int32_t* __restrict__ offsets, int E, int K, int H8,
-                      uint4* __restrict__ xp) {
+permute_copy_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ flat_to_row, int T,
+                    int K, int H8, uint4* __restrict__ xp) {
   pdl_wait();
   pdl_trigger();
-  const int nrows = offsets[E];
   const int lane = lane_id();
-  for (int row = blockIdx.x * 8 + warp_id(); row < nrows; row += gridDim.x * 8) {
-    const int t = row_to_flat[row] / K;
+  for (int t = blockIdx.x * 8 + warp_id(); t < T; t += gridDim.x * 8) {
+    const int myrow = lane < K ? __ldg(flat_to_row + (size_t)t * K + lane) : -1;
     const uint4* src = x + (size_t)t * H8;
-    uint4* dst = xp + (size_t)row * H8;
-    for (int c = lane; c < H8; c += 32) dst[c] = __ldg(src + c);
+    for (int c0 = 0; c0 < H8; c0 += 32 * 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = c0 + j * 32 + lane;
+        if (c < H8) v[j] = __ldg(src + c);
+      }
+      for (int k = 0; k < K; ++k) {
+        const int r = __shfl_sync(0xffffffffu, myrow, k);
+        if (r < 0) continue;
+        uint4* dst = xp + (size_t)r * H8;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int c = c0 + j * 32 + lane;
+          if (c < H8) dst[c] = v[j];
+        }
+      }
+    }
   }
+}
+
+}  // namespace
+
+namespace {
+
+cudaError_t launch_copy(const void* x, const int32_t* flat_to_row, int T, int K, int H, void* xp,
+                        cudaStream_t stream) {
+  const int grid = moe_cdiv(T, 8) < 152 * 16 ? moe_cdiv(T, 8) : 152 * 16;
+  return moe_launch(permute_copy_kernel, dim3(grid), dim3(256), 0, stream, 1,
+                    static_cast<const uint4*>(x), flat_to_row, T, K, H / 8,
+                    static_cast<uint4*>(xp));
 }
 
 }  // namespace
@@ -315,10 +360,7 @@ cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int 
     cudaError_t e = moe_launch(permute_fused_kernel, dim3(1), dim3(32 * kFusedWarps), fused_smem,
                                stream, 1, ids, R, E, offsets, row_to_flat, flat_to_row, dev_status);
     if (e != cudaSuccess || !xp) return e;
-    const int grid = moe_cdiv(R, 8) < 152 * 16 ? moe_cdiv(R, 8) : 152 * 16;
-    return moe_launch(permute_gather_kernel, dim3(grid), dim3(256), 0, stream, 1,
-                      static_cast<const uint4*>(x), row_to_flat, offsets, E, K, H / 8,
-                      static_cast<uint4*>(xp));
+    return launch_copy(x, flat_to_row, T, K, H, xp, stream);
   }
   cudaError_t e = cudaSuccess;
   if (R > 0) {
@@ -332,10 +374,7 @@ cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int 
                  R, E, nch, (const int32_t*)counts, (const int32_t*)offsets, row_to_flat,
                  flat_to_row);
   if (e != cudaSuccess || !xp) return e;
-  const int grid = moe_cdiv(R, 8) < 152 * 16 ? moe_cdiv(R, 8) : 152 * 16;
-  return moe_launch(permute_gather_kernel, dim3(grid), dim3(256), 0, stream, 1,
-                    static_cast<const uint4*>(x), row_to_flat, offsets, E, K, H / 8,
-                    static_cast<uint4*>(xp));
+  return launch_copy(x, flat_to_row, T, K, H, xp, stream);
 }
 
 // ---------------------------------------------------------------- static scratch

@@ -12,7 +12,7 @@
 //    gate rows; its 256 threads split H in 8-element chunks, accumulate all
 //    tokens of an 8-token group, and reduce across the block in a fixed tree.
 //  * prefill (T > 32): FP32-FMA bound (2*T*G*H flops).  64x64 output tiles,
-//    the bf16 tile widened while it is staged into shared memory, an 8x8
+//    the bf16 tile widened while it is staged into shared memory, an 8x4
 //    register micro-tile per thread, and H split across the CTAs of a
 //    thread-block cluster (reduced through distributed shared memory) so that
 //    small T x G still fills the GPU.
@@ -100,15 +100,14 @@ router_small_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict
 constexpr int kBM = 64;  // tokens per tile
 constexpr int kBN = 64;  // gate rows per tile
 constexpr int kBK = 32;  // H per stage
-constexpr int kTiledThreads = 64;
+constexpr int kTiledThreads = 128;
 
 // One CTA computes a 64x64 logit tile over its slice of H; the `splits` CTAs
 // of a thread-block cluster take consecutive slices and the partial tiles are
 // summed through distributed shared memory in rank order (deterministic, no
-// global scratch, no atomics).  64 threads, each owning an 8x8 register block
-// (tokens 8ty.., gate rows 8tx..): per k step two 16-byte loads of x and two of
-// wg feed 64 FMAs.  Operands are staged transposed; the next stage's global
-// loads are issued before this stage's math.
+// global scratch, no atomics).  Thread (ty, tx) owns tokens 8ty..8ty+7 and
+// gate rows 4tx..4tx+3; operands are staged transposed so that each k step is
+// two 16-byte loads of x (a broadcast across the warp) and one of wg.
 __global__ void __launch_bounds__(kTiledThreads)
 router_cluster_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wg,
                       const float* __restrict__ bias, float* __restrict__ logits, int T, int H,
@@ -123,22 +122,22 @@ router_cluster_kernel(const __nv_bfloat16* __restrict__ x, const float* __restri
   const int rank = (int)cluster.block_rank();
   const int splits = (int)cluster.num_blocks();
   const int tid = threadIdx.x;
-  const int ty = tid / 8, tx = tid % 8;
+  const int ty = tid / 16, tx = tid % 16;
   const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
   const int k_lo = rank * kchunk;
   const int k_hi = min(H, k_lo + kchunk);
 
-  float acc[8][8];
+  float acc[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 
-  uint4 xr[4];
-  float4 wr[8];
+  uint4 xr[2];
+  float4 wr[4];
   auto load = [&](int k0) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {  // 64 rows x 32 bf16 = 256 vectors
+    for (int q = 0; q < 2; ++q) {  // 64 rows x 32 bf16 = 256 vectors
       const int idx = tid + q * kTiledThreads;
       const int r = idx / 4, c = (idx % 4) * 8;
       xr[q] = (m0 + r < T && k0 + c < k_hi)
@@ -146,7 +145,7 @@ router_cluster_kernel(const __nv_bfloat16* __restrict__ x, const float* __restri
                   : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {  // 64 rows x 32 fp32 = 512 vectors
+    for (int q = 0; q < 4; ++q) {  // 64 rows x 32 fp32 = 512 vectors
       const int idx = tid + q * kTiledThreads;
       const int r = idx / 8, c = (idx % 8) * 4;
       wr[q] = (n0 + r < G && k0 + c < k_hi)
@@ -156,7 +155,7 @@ router_cluster_kernel(const __nv_bfloat16* __restrict__ x, const float* __restri
   };
   auto stage = [&]() {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 2; ++q) {
       const int idx = tid + q * kTiledThreads;
       const int r = idx / 4, c = (idx % 4) * 8;
       float f[8];
@@ -165,7 +164,7 @@ router_cluster_kernel(const __nv_bfloat16* __restrict__ x, const float* __restri
       for (int i = 0; i < 8; ++i) xs[c + i][r] = f[i];
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < 4; ++q) {
       const int idx = tid + q * kTiledThreads;
       const int r = idx / 8, c = (idx % 8) * 4;
       ws[c + 0][r] = wr[q].x; ws[c + 1][r] = wr[q].y; ws[c + 2][r] = wr[q].z; ws[c + 3][r] = wr[q].w;
@@ -176,29 +175,25 @@ router_cluster_kernel(const __nv_bfloat16* __restrict__ x, const float* __restri
   for (int k0 = k_lo; k0 < k_hi; k0 += kBK) {
     stage();
     __syncthreads();
-    if (k0 + kBK < k_hi) load(k0 + kBK);  // next stage's loads overlap this stage's math
-#pragma unroll 4
+    if (k0 + kBK < k_hi) load(k0 + kBK);  // next tile's loads overlap this tile's math
+#pragma unroll 8
     for (int k = 0; k < kBK; ++k) {
       const float4 a0 = *reinterpret_cast<const float4*>(&xs[k][ty * 8]);
       const float4 a1 = *reinterpret_cast<const float4*>(&xs[k][ty * 8 + 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&ws[k][tx * 8]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&ws[k][tx * 8 + 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[k][tx * 4]);
       const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      const float bb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    *reinterpret_cast<float4*>(&part[ty * 8 + i][tx * 8]) =
+  for (int i = 0; i < 8; ++i)
+    *reinterpret_cast<float4*>(&part[ty * 8 + i][tx * 4]) =
         make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-    *reinterpret_cast<float4*>(&part[ty * 8 + i][tx * 8 + 4]) =
-        make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-  }
   cluster.sync();
   // rank r sums rows [r*64/splits, (r+1)*64/splits) of the tile over the cluster
   const int rows = kBM / splits;

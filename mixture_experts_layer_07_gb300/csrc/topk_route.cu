@@ -1,5 +1,4 @@
-// K: top-K expert selection, one warp per token (one thread per token for
-// large T and E <= 256).
+// K: top-K expert selection, one warp per token.
 //
 // "FlashInfer MoE routing optimisation" (flashinfer PR #4152):
 //  * "1. routing_custom.cu" -- instead of warp 0 holding K-sized score arrays
@@ -7,8 +6,8 @@
 //    the register cost is spread over the warp.  Here lane l reads experts
 //    l, l+32, l+64, ... (coalesced), keeps a sorted list of its best
 //    min(K, experts-per-lane) candidates in registers, and the warp then takes
-//    K rounds of a shuffle arg-max over the lanes' list heads; the winning
-//    lane pops its head.
+//    K rounds of an arg-max over the lanes' list heads (two warp reductions,
+//    redux.sync, per round); the winning lane pops its head.
 //  * "2. routing_common.cu" -- E = 896 gets its own tier (28 experts per lane)
 //    rather than running as the 1024 tier.
 //
@@ -59,8 +58,16 @@ MOE_DEVICE float sigmoid_key(float l) {
   return __fdiv_rn(1.f, __fadd_rn(1.f, e));
 }
 
+// Keys are compared as unsigned integers: the map below is monotone on
+// floats (negative below positive, larger magnitude further out) once -0 is
+// folded to +0 (an fp32 add of +0), so equal floats give equal keys.
+MOE_DEVICE uint32_t order_key(float k) {
+  const uint32_t b = __float_as_uint(__fadd_rn(k, 0.f));
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 // strict total order: larger key first, lower index first among equal keys
-MOE_DEVICE bool better(float ka, int ia, float kb, int ib) {
+MOE_DEVICE bool better(uint32_t ka, int ia, uint32_t kb, int ib) {
   return ka > kb || (ka == kb && ia < ib);
 }
 
@@ -76,11 +83,11 @@ topk_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ 
   const int lane = lane_id();
   const float* row = logits + (size_t)t * ld;
 
-  // lane-owned sorted candidate list
-  float lk[LK];
+  // lane-owned sorted candidate list (keys as ordered u32, empty slots lowest)
+  uint32_t lk[LK];
   int li[LK];
 #pragma unroll
-  for (int s = 0; s < LK; ++s) { lk[s] = -INFINITY; li[s] = 0x7fffffff; }
+  for (int s = 0; s < LK; ++s) { lk[s] = 0u; li[s] = 0x7fffffff; }
 
 #pragma unroll
   for (int j = 0; j < NPL; ++j) {
@@ -90,13 +97,14 @@ topk_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ 
       float key = l;
       if (mode == MOE_SCORE_SIGMOID_BIAS_SCALED)
         key = __fadd_rn(sigmoid_key(l), sel_bias ? __ldg(sel_bias + e) : 0.f);
-      if (better(key, e, lk[LK - 1], li[LK - 1])) {
-        float nk = key;
+      const uint32_t ku = order_key(key);
+      if (better(ku, e, lk[LK - 1], li[LK - 1])) {
+        uint32_t nk = ku;
         int ni = e;
 #pragma unroll
         for (int s = 0; s < LK; ++s) {
           const bool b = better(nk, ni, lk[s], li[s]);
-          const float tk = lk[s];
+          const uint32_t tk = lk[s];
           const int ti = li[s];
           lk[s] = b ? nk : tk;
           li[s] = b ? ni : ti;
@@ -107,31 +115,27 @@ topk_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ 
     }
   }
 
-  // K merge rounds over the lanes' heads
+  // K merge rounds over the lanes' heads: the largest head key by one warp
+  // max-reduction, then the lowest expert index among heads with that key by
+  // one min-reduction; the owning lane pops its head.
   int my_id = -1;
-  float my_key = -INFINITY;
   for (int r = 0; r < K; ++r) {
-    float bk = lk[0];
-    int bi = li[0];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (better(ok, oi, bk, bi)) { bk = ok; bi = oi; }
-    }
-    if (li[0] == bi) {  // the owning lane pops its head
+    const uint32_t m = __reduce_max_sync(0xffffffffu, lk[0]);
+    const uint32_t mi = __reduce_min_sync(0xffffffffu, lk[0] == m ? (uint32_t)li[0] : 0xffffffffu);
+    if (li[0] == (int)mi) {
 #pragma unroll
       for (int s = 0; s < LK - 1; ++s) { lk[s] = lk[s + 1]; li[s] = li[s + 1]; }
-      lk[LK - 1] = -INFINITY;
+      lk[LK - 1] = 0u;
       li[LK - 1] = 0x7fffffff;
     }
-    if (lane == r) { my_id = bi; my_key = bk; }
+    if (lane == r) my_id = (int)mi;
   }
 
   float v = 0.f;
   if (mode == MOE_SCORE_SOFTMAX_RENORM) {
-    const float m = __shfl_sync(0xffffffffu, my_key, 0);  // the first pick is the largest
-    v = lane < K ? expf(my_key - m) : 0.f;
+    const float l = lane < K ? __ldg(row + my_id) : 0.f;
+    const float m = __shfl_sync(0xffffffffu, l, 0);  // the first pick is the largest
+    v = lane < K ? expf(l - m) : 0.f;
   } else {
     v = lane < K ? sigmoid_key(__ldg(row + my_id)) : 0.f;
   }
@@ -144,77 +148,6 @@ topk_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ 
     weights[(size_t)t * K + lane] = w;
   }
   if (shared_gate && lane == 0) shared_gate[t] = sigmoid_key(__ldg(row + E));
-}
-
-// Large T, E <= 256: one THREAD per token.  A CTA stages the logits of its
-// 128 tokens in shared memory with coalesced loads (rows padded by one word so
-// the per-thread row walks are conflict free); each thread then scans its
-// token's E keys keeping a sorted top-LK list (most keys fail the first
-// compare against the current K-th), and writes its K ids and weights.  Same
-// keys, order and weights as the warp kernel.
-constexpr int kTokPerCta = 128;
-
-template <int LK>
-__global__ void __launch_bounds__(kTokPerCta)
-topk_thread_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ sel_bias,
-                   int T, int E, int K, int mode, float scale, int32_t* __restrict__ ids,
-                   float* __restrict__ weights, float* __restrict__ shared_gate) {
-  extern __shared__ float tile[];  // [kTokPerCta][E + 1]
-  pdl_wait();
-  pdl_trigger();
-  const int t0 = blockIdx.x * kTokPerCta;
-  const int nt = min(kTokPerCta, T - t0);
-  const int pitch = E + 1;
-  for (int i = threadIdx.x; i < nt * E; i += kTokPerCta) {
-    const int r = i / E, c = i - r * E;
-    tile[r * pitch + c] = __ldg(logits + (size_t)(t0 + r) * ld + c);
-  }
-  __syncthreads();
-  const int r = threadIdx.x;
-  if (r >= nt) return;
-  const int t = t0 + r;
-  const float* row = tile + r * pitch;
-  float lk[LK];
-  int li[LK];
-#pragma unroll
-  for (int s = 0; s < LK; ++s) { lk[s] = -INFINITY; li[s] = 0x7fffffff; }
-  for (int e = 0; e < E; ++e) {
-    float key = row[e];
-    if (mode == MOE_SCORE_SIGMOID_BIAS_SCALED)
-      key = __fadd_rn(sigmoid_key(key), sel_bias ? __ldg(sel_bias + e) : 0.f);
-    if (better(key, e, lk[LK - 1], li[LK - 1])) {
-      float nk = key;
-      int ni = e;
-#pragma unroll
-      for (int s = 0; s < LK; ++s) {
-        const bool b = better(nk, ni, lk[s], li[s]);
-        const float tk = lk[s];
-        const int ti = li[s];
-        lk[s] = b ? nk : tk;
-        li[s] = b ? ni : ti;
-        nk = b ? tk : nk;
-        ni = b ? ti : ni;
-      }
-    }
-  }
-  float v[LK];
-  float sum = 0.f;
-#pragma unroll
-  for (int s = 0; s < LK; ++s) {
-    if (s < K) {
-      v[s] = mode == MOE_SCORE_SOFTMAX_RENORM ? expf(lk[s] - lk[0]) : sigmoid_key(row[li[s]]);
-      sum += v[s];
-    }
-  }
-#pragma unroll
-  for (int s = 0; s < LK; ++s) {
-    if (s < K) {
-      ids[(size_t)t * K + s] = li[s];
-      weights[(size_t)t * K + s] =
-          mode == MOE_SCORE_SOFTMAX_RENORM ? v[s] / sum : scale * v[s] / sum;
-    }
-  }
-  if (shared_gate) shared_gate[t] = sigmoid_key(__ldg(logits + (size_t)t * ld + E));
 }
 
 template <int NPL>
@@ -240,29 +173,6 @@ cudaError_t launch_npl(const float* logits, int ld, const float* sel_bias, int T
 cudaError_t launch_topk_route(const float* logits, int ld, const float* sel_bias, int T, int E,
                               int K, int mode, float scale, int32_t* ids, float* weights,
                               float* shared_gate, cudaStream_t stream) {
-  if (T >= 4096 && E <= 256 && K <= 16) {
-    // enough tokens to fill the GPU one thread each
-    const size_t smem = (size_t)kTokPerCta * (E + 1) * sizeof(float);
-    const dim3 grid(moe_cdiv(T, kTokPerCta)), block(kTokPerCta);
-    static bool attr = false;
-    if (!attr) {
-      for (auto fn : {topk_thread_kernel<2>, topk_thread_kernel<4>, topk_thread_kernel<8>,
-                      topk_thread_kernel<16>}) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(kTokPerCta * 257 * sizeof(float)));
-        if (e != cudaSuccess) return e;
-      }
-      attr = true;
-    }
-#define MOE_TOPK_T_LAUNCH(KT)                                                                    \
-  return moe_launch(topk_thread_kernel<KT>, grid, block, smem, stream, 1, logits, ld, sel_bias, T, \
-                    E, K, mode, scale, ids, weights, shared_gate)
-    if (K <= 2) MOE_TOPK_T_LAUNCH(2);
-    if (K <= 4) MOE_TOPK_T_LAUNCH(4);
-    if (K <= 8) MOE_TOPK_T_LAUNCH(8);
-    MOE_TOPK_T_LAUNCH(16);
-#undef MOE_TOPK_T_LAUNCH
-  }
   const int npl = moe_cdiv(E, 32);
   if (npl <= 1) return launch_npl<1>(logits, ld, sel_bias, T, E, K, mode, scale, ids, weights, shared_gate, stream);
   if (npl <= 2) return launch_npl<2>(logits, ld, sel_bias, T, E, K, mode, scale, ids, weights, shared_gate, stream);

@@ -79,7 +79,7 @@ def _lib():
         lib.moe_default_m_skinny.restype = _I
         lib.moe_default_m_skinny.argtypes = []
         lib.moe_block_variant.restype = _I
-        lib.moe_block_variant.argtypes = [_I64, _I64, _I, _I, _I]
+        lib.moe_block_variant.argtypes = [_I64, _I64, _I, _I, _I, _I]
         sig = {
             "moe_router_gemm": [_P, _P, _P, _P, _I, _I, _I, _P],
             "moe_topk_route": [_P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P],
@@ -141,8 +141,8 @@ def default_m_skinny() -> int:
 
 
 def block_variant(m_size: int, R: int, E: int, m_skinny: int = -1,
-                  dispatch: int = DISPATCH_PER_BLOCK) -> int:
-    return _lib().moe_block_variant(m_size, R, E, m_skinny, dispatch)
+                  dispatch: int = DISPATCH_PER_BLOCK, wdtype: int = W_BF16) -> int:
+    return _lib().moe_block_variant(m_size, R, E, m_skinny, dispatch, wdtype)
 
 
 def permute_scratch_bytes(T: int, E: int, K: int) -> int:

@@ -67,9 +67,10 @@ def test_block_variant_golden_predicate(ops):
         w["per_block_variants"]
     assert [pages_code(ops.block_variant(m, R, E, thr, ops.DISPATCH_GLOBAL_AVG)) for m in sizes] == \
         w["global_average_variants"]
-    assert ops.block_variant(128, R, E, thr) == ops.VARIANT_TILE
-    assert ops.block_variant(129, R, E, thr) == ops.VARIANT_WIDE
-    assert ops.block_variant(4096, R, E, thr) == ops.VARIANT_WIDE
+    assert ops.block_variant(128, R, E, thr, 0, ops.W_FP8) == ops.VARIANT_TILE
+    assert ops.block_variant(129, R, E, thr, 0, ops.W_FP8) == ops.VARIANT_WIDE
+    assert ops.block_variant(4096, R, E, thr, 0, ops.W_FP8) == ops.VARIANT_WIDE
+    assert ops.block_variant(4096, R, E, thr, 0, ops.W_BF16) == ops.VARIANT_TILE
     assert ops.block_variant(3, R, E, thr, ops.DISPATCH_SIMT) == ops.VARIANT_SIMT
     assert ops.block_variant(0, R, E, thr, ops.DISPATCH_SIMT) == ops.VARIANT_SKIP
     assert ops.default_m_skinny() > 0

@@ -285,12 +285,13 @@ def test_grouped_gemm(ops, name, over, T, conc, dispatch, m_skinny, both):
     U.assert_bf16_close(U.f64(y), ry, rel, "y")
     R = T * spec.K
     m = np.diff(off)
-    want_bv = [ops.block_variant(int(mm), R, spec.E, m_skinny, dispatch) for mm in m]
+    wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
+    want_bv = [ops.block_variant(int(mm), R, spec.E, m_skinny, dispatch, wd) for mm in m]
     assert bv.tolist() == want_bv
     if both:  # small and large blocks in the same call
         assert ops.VARIANT_SKINNY in bv.tolist()
         assert {ops.VARIANT_TILE, ops.VARIANT_WIDE} & set(bv.tolist())
-    if dispatch == 0 and (m >= ops.WIDE_MIN_ROWS).any():
+    if dispatch == 0 and spec.wdtype == "fp8" and (m >= ops.WIDE_MIN_ROWS).any():
         assert ops.VARIANT_WIDE in bv.tolist()
 
 
