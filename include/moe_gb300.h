@@ -288,7 +288,13 @@ moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes);
  *   x    [T, H] bf16 input, out [T, H] bf16 output, T <= cfg->T_max
  *   workspace  >= moe_workspace_bytes(cfg), 256-byte aligned; holds every
  *              intermediate (logits, ids, weights, offsets, permuted rows,
- *              expert activations and outputs, plans)
+ *              expert activations and outputs, plans).  Its 256-byte `sync`
+ *              region (moe_workspace_layout) must be zero before the first
+ *              call -- e.g. zero the whole workspace once after allocating
+ *              it; every call leaves it zero again.
+ * For T <= 32 the router, top-K, permute and the GEMM plan run as one fused
+ * launch (the small-batch regime where launch count dominates); the results
+ * are the same as those of the separate steps.
  */
 moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_weights_t* w,
                        void* out, void* workspace, size_t workspace_bytes,
@@ -301,7 +307,7 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
 typedef struct {
   size_t logits, ids, weights, shared_gate, offsets, row_to_flat, flat_to_row,
       xp, hact, y, shared_hact, shared_y, block_variant, permute_scratch, gemm_scratch,
-      shared_gemm_scratch, total;
+      shared_gemm_scratch, sync, total;
 } moe_workspace_layout_t;
 
 moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_workspace_layout_t* layout);

@@ -48,6 +48,7 @@ void layout_of(const moe_config_t* c, moe_workspace_layout_t* L) {
     off = moe_align_up(off + bytes, 256);
     return o;
   };
+  L->sync = take(256);
   L->logits = take(Tm * G * 4);
   L->ids = take(R * 4);
   L->weights = take(R * 4);
@@ -236,18 +237,38 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
   const int G = E + (cfg->has_shared ? 1 : 0);
   const int R = T * K;
 
-  cudaError_t e = launch_router_gemm(x, w->wg, w->gate_bias, logits, T, H, G, stream);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = launch_topk_route(logits, G, w->sel_bias, T, E, K, cfg->mode, cfg->routed_scale, ids, wts,
-                        cfg->has_shared ? gsh : nullptr, stream);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = launch_permute(x, ids, T, H, E, K, offsets, r2f, f2r, xp, ws + L.permute_scratch, dev_status,
-                     stream);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t* bvar = reinterpret_cast<int32_t*>(ws + L.block_variant);
+  const bool decode = T <= kRouteDecodeMaxT;
+  cudaError_t e;
+  if (decode) {
+    // small batch: router + top-K + permute + GEMM plan in one launch
+    RouteDecodeArgs a;
+    a.x = x; a.wg = w->wg; a.gate_bias = w->gate_bias; a.logits = logits;
+    a.T = T; a.H = H; a.G = G; a.sel_bias = w->sel_bias; a.E = E; a.K = K;
+    a.mode = cfg->mode; a.scale = cfg->routed_scale; a.ids = ids; a.weights = wts;
+    a.shared_gate = cfg->has_shared ? gsh : nullptr; a.offsets = offsets;
+    a.row_to_flat = r2f; a.flat_to_row = f2r; a.dev_status = dev_status;
+    a.m_skinny = cfg->m_skinny; a.dispatch = cfg->dispatch; a.wdtype = cfg->wdtype;
+    a.gemm_scratch = ws + L.gemm_scratch; a.block_variant = bvar;
+    a.done_ctr = reinterpret_cast<unsigned int*>(ws + L.sync);
+    e = launch_route_decode(a, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_permute_copy(x, f2r, T, K, H, xp, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    e = launch_router_gemm(x, w->wg, w->gate_bias, logits, T, H, G, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_topk_route(logits, G, w->sel_bias, T, E, K, cfg->mode, cfg->routed_scale, ids, wts,
+                          cfg->has_shared ? gsh : nullptr, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_permute(x, ids, T, H, E, K, offsets, r2f, f2r, xp, ws + L.permute_scratch,
+                       dev_status, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
   e = launch_grouped_gemm(xp, offsets, E, R, H, cfg->I, cfg->wdtype, w->w1, w->w3, w->w2, w->s1,
-                          w->s3, w->s2, hact, y, cfg->m_skinny, cfg->dispatch,
-                          reinterpret_cast<int32_t*>(ws + L.block_variant), ws + L.gemm_scratch,
-                          dev_status, stream, /*max_rows=*/T);
+                          w->s3, w->s2, hact, y, cfg->m_skinny, cfg->dispatch, bvar,
+                          ws + L.gemm_scratch, dev_status, stream, /*max_rows=*/T,
+                          /*plan_ready=*/decode);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   void* sh_y = nullptr;
   if (cfg->has_shared) {

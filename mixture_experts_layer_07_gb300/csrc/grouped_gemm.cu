@@ -45,117 +45,26 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "plan.cuh"
 #include "sm100_ptx.cuh"
 
 namespace {
 
 using namespace moe_ptx;
+using namespace moe_plan;
 
-constexpr int kBnSkinny = 16;
-constexpr int kBnTile = 128;
-constexpr int kBnWide = 256;
-constexpr int kLists = 3;  // skinny, tile, wide
-__host__ __device__ constexpr int list_bn(int l) { return l == 0 ? kBnSkinny : l == 1 ? kBnTile : kBnWide; }
 constexpr int kBM = 128;  // weight rows per MMA (output features)
 constexpr int kBK = 64;   // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-// scratch layout: counts[kLists] then one int4 item list per variant
-struct PlanView {
-  int32_t* counts;          // items per list
-  int4* items[kLists];      // {block, first row, rows, 0}
-  int cap[kLists];
-};
-
-inline PlanView plan_view(void* scratch, int R, int E_blocks) {
-  PlanView v;
-  char* p = static_cast<char*>(scratch);
-  v.counts = reinterpret_cast<int32_t*>(p);
-  size_t off = 256;
-  for (int l = 0; l < kLists; ++l) {
-    v.cap[l] = moe_cdiv(R, list_bn(l)) + E_blocks;
-    v.items[l] = reinterpret_cast<int4*>(p + off);
-    off += moe_align_up((size_t)v.cap[l] * sizeof(int4), 256);
-  }
-  return v;
-}
-
 // ---------------------------------------------------------------- plan
-struct PlanOut {
-  int4* items[kLists];
-};
-
 __global__ void __launch_bounds__(1024)
 gemm_plan_kernel(const int32_t* __restrict__ offsets, int E_blocks, int R, int m_skinny,
                  int dispatch, int wdtype, int32_t* __restrict__ counts, PlanOut out,
                  int32_t* __restrict__ block_variant) {
-  __shared__ int wsum[kLists][32];
-  __shared__ int carry[kLists];
   pdl_wait();
   pdl_trigger();
-  const int tid = threadIdx.x, lane = lane_id(), warp = warp_id();
-  if (tid < kLists) carry[tid] = 0;
-  __syncthreads();
-  for (int base = 0; base < E_blocks; base += 1024) {
-    const int e = base + tid;
-    int lo = 0, m = 0;
-    if (e < E_blocks) {
-      lo = offsets ? offsets[e] : 0;
-      m = (offsets ? offsets[e + 1] : R) - lo;
-    }
-    const int v = e < E_blocks ? moe_variant_of(m, R, E_blocks, m_skinny, dispatch, wdtype)
-                               : MOE_VARIANT_SKIP;
-    const int list = (v == MOE_VARIANT_SKINNY || v == MOE_VARIANT_SIMT) ? 0
-                   : v == MOE_VARIANT_TILE ? 1 : v == MOE_VARIANT_WIDE ? 2 : -1;
-    int n[kLists], incl[kLists];
-#pragma unroll
-    for (int l = 0; l < kLists; ++l) {
-      n[l] = (l == list) ? moe_cdiv(m, list_bn(l)) : 0;
-      incl[l] = n[l];
-    }
-    // block-wide exclusive scans of the per-list item counts
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-      for (int l = 0; l < kLists; ++l) {
-        const int a = __shfl_up_sync(0xffffffffu, incl[l], o);
-        if (lane >= o) incl[l] += a;
-      }
-    }
-    if (lane == 31) {
-#pragma unroll
-      for (int l = 0; l < kLists; ++l) wsum[l][warp] = incl[l];
-    }
-    __syncthreads();
-    if (warp == 0) {
-#pragma unroll
-      for (int l = 0; l < kLists; ++l) {
-        const int a = wsum[l][lane];
-        int sc = a;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int x = __shfl_up_sync(0xffffffffu, sc, o);
-          if (lane >= o) sc += x;
-        }
-        wsum[l][lane] = sc - a;
-      }
-    }
-    __syncthreads();
-    if (list >= 0) {
-      const int bn = list_bn(list);
-      const int pos = carry[list] + wsum[list][warp] + incl[list] - n[list];
-      for (int i = 0; i < n[list]; ++i)
-        out.items[list][pos + i] = make_int4(e, lo + i * bn, min(bn, m - i * bn), 0);
-    }
-    if (block_variant && e < E_blocks) block_variant[e] = v;
-    __syncthreads();
-    if (tid == 1023) {
-#pragma unroll
-      for (int l = 0; l < kLists; ++l) carry[l] += wsum[l][31] + incl[l];
-    }
-    __syncthreads();
-  }
-  if (tid < kLists) counts[tid] = carry[tid];
+  plan_experts<1024>(offsets, E_blocks, R, m_skinny, dispatch, wdtype, counts, out, block_variant);
 }
 
 // ---------------------------------------------------------------- tensor cores
@@ -723,16 +632,18 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 const void* w2, const float* s1, const float* s3,
                                 const float* s2, void* hact, void* y, int m_skinny,
                                 int dispatch, int32_t* block_variant, void* scratch,
-                                int32_t* dev_status, cudaStream_t stream, int max_rows) {
+                                int32_t* dev_status, cudaStream_t stream, int max_rows,
+                                bool plan_ready) {
   if (m_skinny < 0) m_skinny = MOE_DEFAULT_M_SKINNY;
   const bool fp8 = wdtype == MOE_W_FP8E4M3_B128;
   const bool simt = dispatch == MOE_DISPATCH_SIMT;
   PlanView pv = plan_view(scratch, R, E_blocks);
   PlanOut po;
   for (int l = 0; l < kLists; ++l) po.items[l] = pv.items[l];
-  cudaError_t err = moe_launch(gemm_plan_kernel, dim3(1), dim3(1024), 0, stream, 1, offsets,
-                               E_blocks, R, m_skinny, dispatch, wdtype, pv.counts, po,
-                               block_variant);
+  cudaError_t err = cudaSuccess;
+  if (!plan_ready)
+    err = moe_launch(gemm_plan_kernel, dim3(1), dim3(1024), 0, stream, 1, offsets, E_blocks, R,
+                     m_skinny, dispatch, wdtype, pv.counts, po, block_variant);
   if (err != cudaSuccess || R == 0) return err;
 
   if (simt) {

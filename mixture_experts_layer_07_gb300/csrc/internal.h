@@ -20,12 +20,46 @@ cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int 
 
 size_t grouped_gemm_scratch_bytes(int R, int E_blocks);
 int grouped_gemm_check(int H, int I, int wdtype);  // 0 ok, else a moe_status_t
+// plan_ready: the plan in `scratch` was already written (by the fused decode
+// routing kernel); only the GEMM kernels are launched.
 cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_blocks, int R,
                                 int H, int I, int wdtype, const void* w1, const void* w3,
                                 const void* w2, const float* s1, const float* s3,
                                 const float* s2, void* hact, void* y, int m_skinny,
                                 int dispatch, int32_t* block_variant, void* scratch,
-                                int32_t* dev_status, cudaStream_t stream, int max_rows = -1);
+                                int32_t* dev_status, cudaStream_t stream, int max_rows = -1,
+                                bool plan_ready = false);
+
+// xp[flat_to_row[t*K+k]] = x[t] (the permute's copy step alone)
+cudaError_t launch_permute_copy(const void* x, const int32_t* flat_to_row, int T, int K, int H,
+                                void* xp, cudaStream_t stream);
+
+// Fused decode routing (T <= kRouteDecodeMaxT): router + top-K + permute +
+// grouped-GEMM plan in one launch.  done_ctr must be zero before the launch
+// and is zero again after it.
+constexpr int kRouteDecodeMaxT = 32;
+struct RouteDecodeArgs {
+  const void* x;
+  const float* wg;
+  const float* gate_bias;
+  float* logits;
+  int T, H, G;
+  const float* sel_bias;
+  int E, K, mode;
+  float scale;
+  int32_t* ids;
+  float* weights;
+  float* shared_gate;
+  int32_t* offsets;
+  int32_t* row_to_flat;
+  int32_t* flat_to_row;
+  int32_t* dev_status;
+  int m_skinny, dispatch, wdtype;
+  void* gemm_scratch;  // plan written here (grouped-GEMM scratch layout for R = T*K)
+  int32_t* block_variant;
+  unsigned int* done_ctr;
+};
+cudaError_t launch_route_decode(const RouteDecodeArgs& args, cudaStream_t stream);
 
 cudaError_t launch_unpermute(const void* y, const int32_t* flat_to_row, const float* weights,
                              int T, int K, int H, const void* shared_y, const float* shared_gate,

@@ -20,6 +20,7 @@
 //              written to its token's K rows, 16-byte vectors
 #include "common.cuh"
 #include "internal.h"
+#include "permute_block.cuh"
 
 namespace {
 
@@ -168,13 +169,9 @@ permute_scatter_kernel(const int32_t* __restrict__ ids, int R, int E, int nchunk
   }
 }
 
-// Small problems (R <= kFusedMaxR replicas, the decode regime): count, scan and stable
-// scatter in ONE CTA of 32 warps, all counters in shared memory -- one launch
-// instead of three, and no global scratch.  Warp w owns the contiguous replica
-// range [w*span, (w+1)*span); per-warp counts cnt[w][e] become per-warp bases by
-// a scan over warps (per expert) and then over experts, and the scatter walks
-// each range again in order, 32 replicas per step, ranking equal experts with
-// __match_any_sync.  Deterministic and stable like the multi-CTA path.
+// Small problems (R <= kFusedMaxR replicas, the decode regime): count, scan
+// and stable scatter in ONE CTA (permute_block.cuh) -- one launch instead of
+// three, and no global scratch.
 constexpr int kFusedWarps = 32;
 // Above this many replicas the multi-CTA path (count, scan, scatter) wins: one
 // CTA cannot keep enough loads and stores in flight.
@@ -184,108 +181,11 @@ __global__ void __launch_bounds__(32 * kFusedWarps)
 permute_fused_kernel(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ offsets,
                      int32_t* __restrict__ row_to_flat, int32_t* __restrict__ flat_to_row,
                      int32_t* dev_status) {
-  extern __shared__ int32_t sm[];
-  int32_t* cnt = sm;                           // [kFusedWarps][E]
-  int32_t* off = sm + kFusedWarps * E;         // [E]
-  __shared__ int32_t warp_tot[32];
+  extern __shared__ int32_t sm[];  // [kFusedWarps][E] counters, then [E + 1] offsets
   pdl_wait();
   pdl_trigger();
-  const int w = warp_id(), lane = lane_id();
-  const int span = ((R + kFusedWarps - 1) / kFusedWarps + 31) / 32 * 32;
-  const int f0 = w * span, f1 = min(R, f0 + span);
-  const unsigned lt_mask = (1u << lane) - 1u;
-  int32_t* mine = cnt + w * E;
-  for (int e = lane; e < E; e += 32) mine[e] = 0;
-  __syncwarp();
-  // ids of this warp's range are read 8 steps (256 replicas) at a time, all
-  // loads in flight together, then processed step by step
-  constexpr int kBatch = 8;
-  auto load_batch = [&](int fb, int (&v)[kBatch]) {
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int f = fb + i * 32 + lane;
-      v[i] = f < f1 ? __ldg(ids + f) : -1;
-    }
-  };
-  // 1. per-warp histogram (one leader per distinct expert per step: no atomics)
-  for (int fb = f0; fb < f1; fb += 32 * kBatch) {
-    int v[kBatch];
-    load_batch(fb, v);
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      int e = v[i];
-      if (fb + i * 32 + lane < f1 && (e < 0 || e >= E)) {
-        moe_set_status(dev_status, MOE_DEV_BAD_EXPERT_ID);
-        e = -1;
-      }
-      if (e >= E) e = -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      if (e >= 0 && (peers & lt_mask) == 0) mine[e] += __popc(peers);
-      __syncwarp();
-    }
-  }
-  __syncthreads();
-  // 2. scan: over warps per expert, then over experts
-  const int e = threadIdx.x;
-  int32_t tot = 0;
-  if (e < E) {
-    for (int q = 0; q < kFusedWarps; ++q) {
-      const int32_t v = cnt[q * E + e];
-      cnt[q * E + e] = tot;
-      tot += v;
-    }
-  }
-  int32_t incl = tot;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) warp_tot[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    const int32_t v = warp_tot[lane];
-    int32_t sc = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t n = __shfl_up_sync(0xffffffffu, sc, o);
-      if (lane >= o) sc += n;
-    }
-    warp_tot[lane] = sc - v;
-  }
-  __syncthreads();
-  if (e < E) {
-    const int32_t ex = incl - tot + warp_tot[w];
-    off[e] = ex;
-    offsets[e] = ex;
-    if (e == E - 1) offsets[E] = ex + tot;
-  }
-  __syncthreads();
-  // 3. stable scatter
-  for (int fb = f0; fb < f1; fb += 32 * kBatch) {
-    int v[kBatch];
-    load_batch(fb, v);
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int f = fb + i * 32 + lane;
-      const int ee = (v[i] >= 0 && v[i] < E) ? v[i] : -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, ee);
-      int base = 0;
-      if (ee >= 0) base = off[ee] + mine[ee];
-      __syncwarp();
-      if (ee >= 0 && (peers & lt_mask) == 0) mine[ee] += __popc(peers);
-      __syncwarp();
-      if (f < f1) {
-        if (ee >= 0) {
-          const int row = base + __popc(peers & lt_mask);
-          row_to_flat[row] = f;
-          flat_to_row[f] = row;
-        } else {
-          flat_to_row[f] = -1;
-        }
-      }
-    }
-  }
+  moe_permute_block::permute_block<kFusedWarps>(ids, R, E, offsets, sm + kFusedWarps * E,
+                                                 row_to_flat, flat_to_row, dev_status, sm);
 }
 
 // xp[flat_to_row[t*K+k]] = x[t]: one warp per token reads each 16-byte vector
@@ -335,6 +235,11 @@ cudaError_t launch_copy(const void* x, const int32_t* flat_to_row, int T, int K,
 
 }  // namespace
 
+cudaError_t launch_permute_copy(const void* x, const int32_t* flat_to_row, int T, int K, int H,
+                                void* xp, cudaStream_t stream) {
+  return launch_copy(x, flat_to_row, T, K, H, xp, stream);
+}
+
 size_t permute_scratch_bytes(int T, int E, int K) {
   const int R = T * K;
   return moe_align_up((size_t)num_chunks(R) * E * sizeof(int32_t) + 256, 256);
@@ -348,7 +253,7 @@ cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int 
   int32_t* counts = static_cast<int32_t*>(scratch);
   const size_t smem = (size_t)kWarpsPerCta * E * sizeof(int32_t);
   const int ctas = moe_cdiv(nch, kWarpsPerCta);
-  const size_t fused_smem = (size_t)(kFusedWarps + 1) * E * sizeof(int32_t);
+  const size_t fused_smem = ((size_t)(kFusedWarps + 1) * E + 1) * sizeof(int32_t);
   if (R > 0 && R <= kFusedMaxR && fused_smem <= 200 * 1024) {
     static bool attr = false;
     if (!attr) {

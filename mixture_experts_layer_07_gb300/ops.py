@@ -59,7 +59,7 @@ class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("logits", "ids", "weights", "shared_gate", "offsets", "row_to_flat",
                  "flat_to_row", "xp", "hact", "y", "shared_hact", "shared_y", "block_variant",
-                 "permute_scratch", "gemm_scratch", "shared_gemm_scratch", "total")]
+                 "permute_scratch", "gemm_scratch", "shared_gemm_scratch", "sync", "total")]
 
 
 _L = None
@@ -249,6 +249,7 @@ class MoELayer:
                                                      "w2", "s1", "s3", "s2", "sw1", "sw3", "sw2")])
         self.workspace = torch.empty(workspace_bytes(cfg), dtype=torch.uint8, device=device)
         self.layout = workspace_layout(cfg)
+        self.workspace[self.layout.sync:self.layout.sync + 256].zero_()  # see moe_layer
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
 
     def __call__(self, x, out=None, stream=None):

@@ -381,3 +381,25 @@ def test_layer(ops, name, over, T):
     assert np.array_equal(gid[clear], res["ids"][clear])
     rel = 5e-2 if spec.wdtype == "fp8" else 2e-2
     U.assert_bf16_close(U.f64(out)[clear], res["out"][clear], rel, "layer out")
+
+
+def test_layer_decode_path_repeats_and_leaves_sync_zero(ops):
+    # T <= 32 runs the fused routing launch; its completion counter must come
+    # back to zero so that the next call (same workspace) routes again
+    spec = SPECS["tiny"].with_(E=16, K=4)
+    inp = synth.host_inputs(spec, 32, seed=21)
+    t = U.layer_tensors(inp)
+    layer = ops.MoELayer(U.config_for(ops, spec, T_max=32), t)
+    for T, seed in ((8, 31), (32, 32), (3, 33), (32, 34)):
+        x_bits = synth.host_inputs(spec, T, seed=seed, weights=False)["x_bits"]
+        out = layer(U.bf16_dev(x_bits))
+        sync()
+        sw = layer.workspace[layer.layout.sync:layer.layout.sync + 4].view(torch.int32).item()
+        assert sw == 0
+        case = dict(inp)
+        case["x_bits"] = x_bits
+        res = oracle.moe_layer_from_inputs(case)
+        lg = res["logits"][:, :spec.E]
+        srt = -np.sort(-lg, axis=1)
+        clear = (srt[:, spec.K - 1] - srt[:, spec.K]) > 1e-4
+        U.assert_bf16_close(U.f64(out)[clear], res["out"][clear], 2e-2, f"decode T={T}")
