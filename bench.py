@@ -151,23 +151,48 @@ def tensors_of(spec, d):
     return t
 
 
-def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129):
-    """Kernel launches inside one moe_layer call (mirrors the library's
-    launch sequence): router 1, top-K 1, permute 2 (one fused count/scan/
-    scatter CTA + gather) or 4 (count, scan, scatter, gather) above 65536
-    replicas, grouped GEMM 1 plan + one G1 and one G2 launch per variant list
-    that can be non-empty (skinny always; tile when T > m_skinny; wide for FP8
-    weights when also T > 128) or 2 on the CUDA-core path, combine 1; a shared expert adds one
-    more grouped GEMM."""
-    def gemm(max_rows):
+def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=152):
+    """Kernel launches inside one moe_layer call, mirroring the library's
+    launch sequence.
+      T <= 32: one fused routing launch (router, top-K, permute, GEMM plan)
+               + the permute copy
+      T > 32:  router 1, top-K 1, permute 2 (fused count/scan/scatter + copy)
+               up to 4096 replicas else 4, GEMM plan 1
+      GEMM:    one G1 and one G2 launch per variant list that can be
+               non-empty (skinny always; tile when T > m_skinny; wide for FP8
+               when also T > 128), or 2 on the CUDA-core path; when only the
+               skinny list can be non-empty, each of G1/G2 split along K adds
+               a finalize launch
+      combine 1; a shared expert adds a grouped GEMM with its own plan."""
+    R = T * spec.K
+
+    def ksplit(units, kdim):
+        nk = -(-kdim // 64)
+        s = 1
+        while s < 4 and units * 2 * s <= 2 * num_sms and nk // (2 * s) >= 4:
+            s *= 2
+        return s
+
+    def gemm(max_rows, rows, blocks, with_plan, splittable):
+        n = 1 if with_plan else 0
         if dispatch == 2:
-            return 1 + 2
-        lists = 1 + (max_rows > m_skinny) + (spec.wdtype == "fp8" and max_rows > m_skinny
-                                              and max_rows >= wide_min)
-        return 1 + 2 * lists
-    permute = 2 if T * spec.K <= 4096 else 4
-    shared = gemm(T) if spec.has_shared else 0
-    return 1 + 1 + permute + gemm(T) + shared + 1
+            return n + 2
+        tile = max_rows > m_skinny
+        wide = spec.wdtype == "fp8" and tile and max_rows >= wide_min
+        n += 2 * (1 + tile + wide)
+        if splittable and not tile:
+            b = min(rows, blocks)
+            n += (ksplit(b * -(-spec.I // 128), spec.H) > 1) + (ksplit(b * -(-spec.H // 128), spec.I) > 1)
+        return n
+
+    if T <= 32:
+        route = 2
+        g = gemm(T, R, spec.E, with_plan=False, splittable=True)
+    else:
+        route = 2 + (2 if R <= 4096 else 4)
+        g = gemm(T, R, spec.E, with_plan=True, splittable=False)
+    shared = gemm(T, T, 1, with_plan=True, splittable=False) if spec.has_shared else 0
+    return route + g + shared + 1
 
 
 def stage_bytes_flops(spec, T, ids, e_active):

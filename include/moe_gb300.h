@@ -307,7 +307,7 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
 typedef struct {
   size_t logits, ids, weights, shared_gate, offsets, row_to_flat, flat_to_row,
       xp, hact, y, shared_hact, shared_y, block_variant, permute_scratch, gemm_scratch,
-      shared_gemm_scratch, sync, total;
+      shared_gemm_scratch, sync, splitk, total;
 } moe_workspace_layout_t;
 
 moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_workspace_layout_t* layout);

@@ -65,6 +65,10 @@ void layout_of(const moe_config_t* c, moe_workspace_layout_t* L) {
   L->permute_scratch = take(permute_scratch_bytes(c->T_max, c->E, c->K));
   L->gemm_scratch = take(grouped_gemm_scratch_bytes((int)R, c->E));
   L->shared_gemm_scratch = take(c->has_shared ? grouped_gemm_scratch_bytes(c->T_max, 1) : 0);
+  // split-K slices for small batches (all blocks skinny: T <= m_skinny)
+  const int ms = c->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : c->m_skinny;
+  const int t_split = c->T_max < ms ? c->T_max : ms;
+  L->splitk = take(grouped_gemm_splitk_bytes(t_split * c->K, c->H, c->I));
   L->total = off;
 }
 
@@ -268,7 +272,8 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
   e = launch_grouped_gemm(xp, offsets, E, R, H, cfg->I, cfg->wdtype, w->w1, w->w3, w->w2, w->s1,
                           w->s3, w->s2, hact, y, cfg->m_skinny, cfg->dispatch, bvar,
                           ws + L.gemm_scratch, dev_status, stream, /*max_rows=*/T,
-                          /*plan_ready=*/decode);
+                          /*plan_ready=*/decode, reinterpret_cast<float*>(ws + L.splitk),
+                          L.total - L.splitk);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   void* sh_y = nullptr;
   if (cfg->has_shared) {

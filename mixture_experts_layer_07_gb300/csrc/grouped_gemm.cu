@@ -31,8 +31,9 @@
 //   warp 1     allocates TMEM, one thread issues tcgen05.mma (K = 16 per
 //              instruction, 4 per stage) and commits each stage back to the
 //              producer and the finished accumulator to the epilogue
-//   warps 2-5  epilogue: tcgen05.ld the fp32 accumulators (TMEM lanes are
-//              split by warp % 4), SwiGLU, bf16 store masked to the block
+//   warps 2-9  epilogue: tcgen05.ld the fp32 accumulators (TMEM lanes are
+//              split by warp % 4, token columns between the two warps of a
+//              lane quarter), SwiGLU, bf16 store masked to the block
 // Persistent: one CTA per SM walks (item, 128-feature block) work units.
 // Every mbarrier wait is bounded; a wait that runs out sets
 // MOE_DEV_WAIT_TIMEOUT, the CTA drains its own in-flight copies and MMAs
@@ -85,7 +86,8 @@ struct TcCfg {
   static constexpr int kStageBytes = kNA * (WFP8 ? kQBytes : kABytes) + kBBytes;
   static constexpr int kConvStages = WFP8 ? 2 : 0;
   static constexpr int kConvBytes = kNA * kABytes;
-  static constexpr int kEpiBytes = 4 * 16 * 32 * 2;  // per epilogue warp: 16 tokens x 32 features
+  static constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, splitting the token columns
+  static constexpr int kEpiBytes = kEpiWarps * 16 * 32 * 2;  // per warp: 16 tokens x 32 features
   static constexpr int kStagesRaw =
       (216 * 1024 - kEpiBytes - kConvStages * kConvBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
@@ -100,7 +102,8 @@ struct TcCfg {
   static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes +
                                        (size_t)kConvStages * kConvBytes + kEpiBytes + kBarBytes;
   static constexpr int kConvThreads = WFP8 ? 256 : 0;  // eight converter warps
-  static constexpr int kThreads = 192 + kConvThreads;
+  static constexpr int kConvWarp0 = 2 + kEpiWarps;        // first converter warp
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + kConvThreads;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
@@ -129,14 +132,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
                const __grid_constant__ CUtensorMap tm_act, const float* __restrict__ sa,
                const float* __restrict__ sb, const int32_t* __restrict__ counts, int list,
                const int4* __restrict__ items, int N, int Kdim, __nv_bfloat16* __restrict__ out,
-               int32_t* dev_status) {
+               int ksplit, int R, float* __restrict__ part, int32_t* dev_status) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
   pdl_wait();
   pdl_trigger();
   const int nblk = (N + kBM - 1) / kBM;
-  const int total = counts[list] * nblk;
+  const int total = counts[list] * nblk * ksplit;
   if ((int)blockIdx.x >= total) return;
   const int nk = (Kdim + kBK - 1) / kBK;
+  // work unit w -> (item, 128-feature block nb, K slice ks); with ksplit > 1
+  // each slice writes fp32 partial sums to part[ks][row][feature] instead of
+  // the finished output (a finalize kernel reduces the slices in order)
+  const int kbs = (nk + ksplit - 1) / ksplit;
+  struct Unit { int4 it; int nb, kb_lo, kb_hi, ks; };
+  auto unit_of = [&](int w) {
+    Unit u;
+    u.it = items[w / (nblk * ksplit)];
+    u.nb = (w / ksplit) % nblk;
+    u.ks = w % ksplit;
+    u.kb_lo = u.ks * kbs;
+    u.kb_hi = min(nk, u.kb_lo + kbs);
+    return u;
+  };
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -162,7 +179,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
-    for (int a = 0; a < C::kAccStages; ++a) { mbar_init(acc_full(a), 1); mbar_init(acc_empty(a), 128); }
+    for (int a = 0; a < C::kAccStages; ++a) {
+      mbar_init(acc_full(a), 1);
+      mbar_init(acc_empty(a), 32 * C::kEpiWarps);
+    }
     mbar_init(drain_bar, 1);
     for (int c = 0; c < C::kConvStages; ++c) {
       mbar_init(conv_full(c), C::kConvThreads);
@@ -202,9 +222,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-        const int4 it = items[w / nblk];
-        const int nb = w % nblk;
-        for (int kb = 0; kb < nk; ++kb) {
+        const Unit u = unit_of(w);
+        const int4 it = u.it;
+        const int nb = u.nb;
+        for (int kb = u.kb_lo; kb < u.kb_hi; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             fail();
             ok = false;
@@ -239,7 +260,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
         }
         tc_fence_after();
         const uint32_t d = tmem + a * C::kAccCols;
-        for (int kb = 0; kb < nk; ++kb) {
+        const Unit u = unit_of(w);
+        for (int kb = u.kb_lo; kb < u.kb_hi; ++kb) {
           if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, kWaitLimitNs) ||
               (WFP8 && !mbar_wait_bounded(conv_full(cs), cphase, abort_flag, kWaitLimitNs))) {
             fail();
@@ -253,7 +275,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
           const uint32_t sx = st + C::kNA * kWeightBytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint32_t acc = (kb | kk) != 0;
+            const uint32_t acc = (kb > u.kb_lo || kk > 0) ? 1u : 0u;
             const uint64_t bdesc = sdesc_k128_sw128(sx + kk * 32);
             tc_mma_f16(d, sdesc_k128_sw128(wa_s + kk * 32), bdesc, C::kIdesc, acc);
             if (SWIGLU) tc_mma_f16(d + BN, sdesc_k128_sw128(wb_s + kk * 32), bdesc, C::kIdesc, acc);
@@ -275,17 +297,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
         if (!mbar_wait_bounded(drain_bar, 0, nullptr, kWaitLimitNs)) fail();
       }
     }
-  } else if (warp < 6) {
-    // ---------------- epilogue, warps 2..5
-    // TMEM lane quarter = warp % 4 = 32 output features; each 16-token chunk
-    // is staged in shared memory and written back as 16-byte row segments.
+  } else if (warp < C::kConvWarp0) {
+    // ---------------- epilogue, warps 2..9
+    // TMEM lane quarter = warp % 4 = 32 output features; the two warps of a
+    // quarter take alternate 16-token chunks.  Each chunk is staged in shared
+    // memory and written back as 16-byte row segments.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    uint16_t* stg = epi + quarter * (16 * 32);
+    uint16_t* stg = epi + (warp - 2) * (16 * 32);
     uint32_t unit = 0;
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++unit) {
-      const int4 it = items[w / nblk];
-      const int nb = w % nblk;
+      const Unit un = unit_of(w);
+      const int4 it = un.it;
+      const int nb = un.nb;
       const uint32_t a = acc_set(unit);
       if (!mbar_wait_bounded(acc_full(a), acc_par(unit), abort_flag, kWaitLimitNs)) {
         fail();
@@ -294,11 +319,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
       tc_fence_after();
       const uint32_t tacc = t_lane + a * C::kAccCols;
       const int m = it.z;
-      for (int c0 = 0; c0 < BN && c0 < m; c0 += 16) {
+      for (int c0 = 16 * half; c0 < BN && c0 < m; c0 += 32) {
         uint32_t g[16], u[16];
         tc_ld_32x32b_x16(tacc + c0, g);
         if (SWIGLU) tc_ld_32x32b_x16(tacc + BN + c0, u);
         tc_wait_ld();
+        if (ksplit > 1) {
+          // fp32 partials of this K slice: row-major [ks][R][Npart], Npart = N or 2N
+          const int n = nb * kBM + quarter * 32 + lane;
+          const int np = SWIGLU ? 2 * N : N;
+          float* pr = part + ((size_t)un.ks * R + it.y + c0) * np;
+          const bool empty = un.kb_lo >= un.kb_hi;  // no K left for this slice
+          if (n < N) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if (c0 + j < m) {
+                pr[(size_t)j * np + n] = empty ? 0.f : __uint_as_float(g[j]);
+                if (SWIGLU) pr[(size_t)j * np + N + n] = empty ? 0.f : __uint_as_float(u[j]);
+              }
+            }
+          }
+          continue;
+        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float gv = __uint_as_float(g[j]);
@@ -322,20 +364,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
       mbar_arrive(acc_empty(a));
     }
   } else if (WFP8) {
-    // ---------------- e4m3 -> bf16 converters, warps 6..13
+    // ---------------- e4m3 -> bf16 converters, warps 10..17
     // At the start of each work unit the converters stage that unit's row of
     // block scales (one per 128-wide K block) in shared memory, so the
     // per-stage scale is a shared-memory read, not a global load.  Rows rotate
     // through three buffers: a converter can run at most two stages ahead of
     // the slowest one, so a buffer is never rewritten while still being read.
-    const int ct = threadIdx.x - 192;
+    const int ct = threadIdx.x - 32 * C::kConvWarp0;
     const int rb = (N + 127) / 128, cb = (Kdim + 127) / 128;
     int stage = 0, cs = 0;
     uint32_t phase = 0, cphase = 0, unit = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++unit) {
-      const int4 it = items[w / nblk];
-      const int nb = w % nblk;
+      const Unit un = unit_of(w);
+      const int4 it = un.it;
+      const int nb = un.nb;
       const int buf = (int)(unit % 3u);
       float* scale_row = scale_rows + buf * 2 * C::kMaxScaleCols;
       const size_t row = ((size_t)it.x * rb + nb) * cb;
@@ -348,7 +391,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
         fail();
         break;
       }
-      for (int kb = 0; kb < nk; ++kb) {
+      for (int kb = un.kb_lo; kb < un.kb_hi; ++kb) {
         if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, kWaitLimitNs) ||
             !mbar_wait_bounded(conv_empty(cs), cphase ^ 1u, abort_flag, kWaitLimitNs)) {
           fail();
@@ -475,6 +518,43 @@ gemm_simt_kernel(const __nv_bfloat16* __restrict__ act, const void* __restrict__
   }
 }
 
+// ---------------------------------------------------------------- split-K finalize
+// out[r][n] = bf16( silu(sum_ks g) * sum_ks u )  (SwiGLU)  or  bf16( sum_ks p )
+// with the K slices summed in slice order; 4 features per thread.
+template <bool SWIGLU>
+__global__ void __launch_bounds__(256)
+splitk_finalize_kernel(const float* __restrict__ part, int ksplit, int R, int N,
+                       __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int np = SWIGLU ? 2 * N : N;
+  const int n4 = N / 4;
+  const long long total = (long long)R * n4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(i / n4), n = (int)(i % n4) * 4;
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+    for (int ks = 0; ks < ksplit; ++ks) {
+      const float* pr = part + ((size_t)ks * R + r) * np;
+      const float4 a = *reinterpret_cast<const float4*>(pr + n);
+      g.x += a.x; g.y += a.y; g.z += a.z; g.w += a.w;
+      if (SWIGLU) {
+        const float4 b = *reinterpret_cast<const float4*>(pr + N + n);
+        u.x += b.x; u.y += b.y; u.z += b.z; u.w += b.w;
+      }
+    }
+    float4 v = g;
+    if (SWIGLU) {
+      v.x = silu_f(g.x) * u.x; v.y = silu_f(g.y) * u.y;
+      v.z = silu_f(g.z) * u.z; v.w = silu_f(g.w) * u.w;
+    }
+    uint2 o;
+    o.x = pack_bf16x2(v.x, v.y);
+    o.y = pack_bf16x2(v.z, v.w);
+    *reinterpret_cast<uint2*>(out + (size_t)r * N + n) = o;
+  }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -540,7 +620,7 @@ template <int BN, bool SWIGLU, bool WFP8>
 cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorMap& act,
                    const float* sa, const float* sb, const int32_t* counts, int list,
                    const int4* items, int cap, int N, int Kdim, void* out, int32_t* dev_status,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, int ksplit = 1, int R = 0, float* part = nullptr) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
   static bool attr_set = false;  // per process; the attribute is per function, all devices
   if (!attr_set) {
@@ -550,19 +630,46 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long long work = (long long)cap * moe_cdiv(N, kBM);
+  const long long work = (long long)cap * moe_cdiv(N, kBM) * ksplit;
   const int grid = (int)(work < num_sms() ? work : num_sms());
   if (grid <= 0) return cudaSuccess;
-  return moe_launch(gemm_tc_kernel<BN, SWIGLU, WFP8>, dim3(grid), dim3(C::kThreads),
-                    C::kSmemBytes, stream, 1, wa, wb, act, sa, sb, counts, list, items, N, Kdim,
-                    static_cast<__nv_bfloat16*>(out), dev_status);
+  cudaError_t e = moe_launch(gemm_tc_kernel<BN, SWIGLU, WFP8>, dim3(grid), dim3(C::kThreads),
+                             C::kSmemBytes, stream, 1, wa, wb, act, sa, sb, counts, list, items, N,
+                             Kdim, static_cast<__nv_bfloat16*>(out), ksplit, R, part, dev_status);
+  if (e != cudaSuccess || ksplit <= 1) return e;
+  const long long n = (long long)R * (N / 4);
+  const int fgrid = (int)((n + 255) / 256 < 4 * num_sms() ? (n + 255) / 256 : 4 * num_sms());
+  return moe_launch(splitk_finalize_kernel<SWIGLU>, dim3(fgrid), dim3(256), 0, stream, 1,
+                    (const float*)part, ksplit, R, N, static_cast<__nv_bfloat16*>(out));
+}
+
+// K slices for the skinny variant when few units would leave SMs idle: the
+// largest power of two <= 4 that keeps (units x slices) within two waves and
+// every slice non-empty and at least 4 stages long.  1 = no split.
+int pick_ksplit(long long units, int Kdim) {
+  const int nk = (Kdim + kBK - 1) / kBK;
+  int s = 1;
+  while (s < 4 && units * (2 * s) <= 2LL * num_sms() && nk / (2 * s) >= 4) s *= 2;
+  return s;
 }
 
 template <bool WFP8>
 cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const void* w1,
                        const void* w3, const void* w2, const float* s1, const float* s3,
                        const float* s2, void* hact, void* y, const PlanView& pv,
-                       int32_t* dev_status, cudaStream_t stream, const bool (&any)[kLists]) {
+                       int32_t* dev_status, cudaStream_t stream, const bool (&any)[kLists],
+                       float* splitk_buf, size_t splitk_bytes) {
+  // split-K only when every block is skinny (all rows then belong to skinny
+  // items, which the finalize kernel rewrites) and the buffer holds the slices
+  int ks1 = 1, ks2 = 1;
+  if (splitk_buf && any[0] && !any[1] && !any[2]) {
+    const long long blocks = R < E_blocks ? R : E_blocks;
+    ks1 = pick_ksplit(blocks * moe_cdiv(I, kBM), H);
+    ks2 = pick_ksplit(blocks * moe_cdiv(H, kBM), I);
+    if ((size_t)ks1 * R * 2 * I * sizeof(float) > splitk_bytes) ks1 = 1;
+    if ((size_t)ks2 * R * H * sizeof(float) > splitk_bytes) ks2 = 1;
+    if (I % 4 || H % 4) ks1 = ks2 = 1;
+  }
   CUtensorMap m_w1, m_w3, m_w2, m_x[kLists], m_h[kLists];
   if (!make_weight_map(&m_w1, w1, E_blocks, I, H, WFP8) ||
       !make_weight_map(&m_w3, w3, E_blocks, I, H, WFP8) ||
@@ -576,7 +683,8 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
   // G1 (SwiGLU, N = I, K = H) for every list, then G2 (N = H, K = I)
   if (any[0] && err == cudaSuccess)
     err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x[0], s1, s3, pv.counts, 0, pv.items[0],
-                                        pv.cap[0], I, H, hact, dev_status, stream);
+                                        pv.cap[0], I, H, hact, dev_status, stream, ks1, R,
+                                        splitk_buf);
   if (any[1] && err == cudaSuccess)
     err = run_tc<kBnTile, true, WFP8>(m_w1, m_w3, m_x[1], s1, s3, pv.counts, 1, pv.items[1],
                                       pv.cap[1], I, H, hact, dev_status, stream);
@@ -585,7 +693,8 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
                                       pv.cap[2], I, H, hact, dev_status, stream);
   if (any[0] && err == cudaSuccess)
     err = run_tc<kBnSkinny, false, WFP8>(m_w2, m_w2, m_h[0], s2, s2, pv.counts, 0, pv.items[0],
-                                         pv.cap[0], H, I, y, dev_status, stream);
+                                         pv.cap[0], H, I, y, dev_status, stream, ks2, R,
+                                         splitk_buf);
   if (any[1] && err == cudaSuccess)
     err = run_tc<kBnTile, false, WFP8>(m_w2, m_w2, m_h[1], s2, s2, pv.counts, 1, pv.items[1],
                                        pv.cap[1], H, I, y, dev_status, stream);
@@ -619,6 +728,11 @@ size_t grouped_gemm_scratch_bytes(int R, int E_blocks) {
   return b;
 }
 
+size_t grouped_gemm_splitk_bytes(int R, int H, int I) {
+  const size_t w = (size_t)(2 * I > H ? 2 * I : H);
+  return moe_align_up(4 * (size_t)R * w * sizeof(float), 256);
+}
+
 int grouped_gemm_check(int H, int I, int wdtype) {
   if (H % 16 != 0 || I % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (wdtype != MOE_W_BF16 && wdtype != MOE_W_FP8E4M3_B128) return MOE_ERR_UNSUPPORTED;
@@ -633,7 +747,7 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 const float* s2, void* hact, void* y, int m_skinny,
                                 int dispatch, int32_t* block_variant, void* scratch,
                                 int32_t* dev_status, cudaStream_t stream, int max_rows,
-                                bool plan_ready) {
+                                bool plan_ready, float* splitk_buf, size_t splitk_bytes) {
   if (m_skinny < 0) m_skinny = MOE_DEFAULT_M_SKINNY;
   const bool fp8 = wdtype == MOE_W_FP8E4M3_B128;
   const bool simt = dispatch == MOE_DISPATCH_SIMT;
@@ -671,7 +785,7 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
   }
   if (fp8)
     return run_tc_all<true>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                            stream, any);
+                            stream, any, splitk_buf, splitk_bytes);
   return run_tc_all<false>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                           stream, any);
+                           stream, any, splitk_buf, splitk_bytes);
 }

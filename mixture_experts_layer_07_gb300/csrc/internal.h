@@ -28,7 +28,11 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 const float* s2, void* hact, void* y, int m_skinny,
                                 int dispatch, int32_t* block_variant, void* scratch,
                                 int32_t* dev_status, cudaStream_t stream, int max_rows = -1,
-                                bool plan_ready = false);
+                                bool plan_ready = false, float* splitk_buf = nullptr,
+                                size_t splitk_bytes = 0);
+// fp32 bytes for split-K slices of the skinny variant in moe_layer's decode
+// regime (at most 4 slices of R x max(2I, H) partial sums)
+size_t grouped_gemm_splitk_bytes(int R, int H, int I);
 
 // xp[flat_to_row[t*K+k]] = x[t] (the permute's copy step alone)
 cudaError_t launch_permute_copy(const void* x, const int32_t* flat_to_row, int T, int K, int H,

@@ -59,7 +59,8 @@ class WorkspaceLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("logits", "ids", "weights", "shared_gate", "offsets", "row_to_flat",
                  "flat_to_row", "xp", "hact", "y", "shared_hact", "shared_y", "block_variant",
-                 "permute_scratch", "gemm_scratch", "shared_gemm_scratch", "sync", "total")]
+                 "permute_scratch", "gemm_scratch", "shared_gemm_scratch", "sync", "splitk",
+                 "total")]
 
 
 _L = None

@@ -341,7 +341,11 @@ LAYER_CASES = [("tiny", {}, 16), ("tiny", {}, 1), ("qwen3_30b_a3b", {}, 1),
                ("qwen3_30b_a3b", {}, 2), ("qwen3_30b_a3b", {}, 8), ("qwen3_30b_a3b", {}, 32),
                ("qwen3_30b_a3b", {}, 256), ("gpt_oss_20b", {}, 32), ("shared_gate", {}, 4),
                ("shared_gate", {}, 64), ("high_expert", {}, 2),
-               ("high_expert", {"E": 512, "K": 9}, 2), ("high_expert", {"E": 1024}, 1)]
+               ("high_expert", {"E": 512, "K": 9}, 2), ("high_expert", {"E": 1024}, 1),
+               # few experts active: the skinny GEMM splits K (fp32 slices + finalize)
+               ("tiny", {"H": 1024, "I": 512, "E": 8, "wdtype": "fp8"}, 1),
+               ("tiny", {"H": 1024, "I": 512, "E": 8, "wdtype": "fp8"}, 3),
+               ("tiny", {"H": 2880, "I": 1440, "E": 4}, 1)]
 
 
 def oracle_routing(spec, inp):
