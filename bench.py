@@ -156,7 +156,8 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
     launch sequence.
       T <= 32: one fused routing launch (router, top-K, permute, GEMM plan)
                + the permute copy
-      T > 32:  router 1, top-K 1, permute 2 (fused count/scan/scatter + copy)
+      T > 32:  router 1 (2 from T >= 64: weight split + tensor-core GEMM),
+               top-K 1, permute 2 (fused count/scan/scatter + copy)
                up to 4096 replicas else 4, GEMM plan 1
       GEMM:    one G1 and one G2 launch per variant list that can be
                non-empty (skinny always; tile when T > m_skinny; wide for FP8
@@ -189,7 +190,7 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
         route = 2
         g = gemm(T, R, spec.E, with_plan=False, splittable=True)
     else:
-        route = 2 + (2 if R <= 4096 else 4)
+        route = (3 if T >= ROUTER_TC_MIN_T else 2) + (2 if R <= 4096 else 4)
         g = gemm(T, R, spec.E, with_plan=True, splittable=False)
     shared = gemm(T, T, 1, with_plan=True, splittable=False) if spec.has_shared else 0
     return route + g + shared + 1
@@ -228,6 +229,8 @@ def roofline_of(bytes_, flops, seconds, peaks, compute="tensor", sustained=False
         cpk = FP32_ALU_TFLOPS * 1e12
     else:
         cpk = (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]) * 1e12
+        if compute == "bf16x3":  # fp32-accurate GEMM from three bf16 MMAs per product
+            cpk /= 3
     t_mem, t_c = bytes_ / bw, flops / cpk
     if t_mem >= t_c:
         ach = bytes_ / seconds / 1e9
@@ -235,11 +238,16 @@ def roofline_of(bytes_, flops, seconds, peaks, compute="tensor", sustained=False
                 "frac": ach / peaks["hbm_gbs"]}
     ach = flops / seconds / 1e12
     pk = cpk / 1e12
-    return {"bound": compute, "achieved": ach, "peak": pk, "unit": "TFLOP/s", "frac": ach / pk}
+    return {"bound": "tensor" if compute == "bf16x3" else compute, "achieved": ach, "peak": pk, "unit": "TFLOP/s", "frac": ach / pk}
 
 
 STAGE_COMPUTE = {"router": "alu", "topk": "alu", "permute": "alu", "grouped_gemm": "tensor",
                  "unpermute": "alu"}
+ROUTER_TC_MIN_T = 64  # the layer's router runs on the tensor cores from this batch size on
+
+
+def router_compute(T):
+    return "bf16x3" if T >= ROUTER_TC_MIN_T else "alu"
 
 
 def traffic_record(kernel_file):
@@ -362,8 +370,16 @@ def run_ours(args, rank, world, local_rank):
     wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
     names = ["router", "topk", "permute", "grouped_gemm", "unpermute"]
 
+    rscr = ws[L.router_split:L.splitk]
+
+    def router():
+        if T >= ROUTER_TC_MIN_T:
+            ops.router_gemm_tc(x, t["wg"], t["gate_bias"], logits, rscr, layer.dev_status)
+        else:
+            ops.router_gemm(x, t["wg"], t["gate_bias"], logits)
+
     def stages():
-        yield lambda: ops.router_gemm(x, t["wg"], t["gate_bias"], logits)
+        yield router
         yield lambda: ops.topk_route(logits, E, K, spec.mode, spec.routed_scale, ids, wts,
                                      t["sel_bias"], gsh)
         yield lambda: ops.permute(x, ids, E, off, r2f, f2r, xp, pscr, layer.dev_status)
@@ -396,12 +412,13 @@ def run_ours(args, rank, world, local_rank):
     sbf = stage_bytes_flops(spec, T, ids_h, e_active)
     per_stage = {}
     for n in names:
-        r = roofline_of(sbf[n]["bytes"], sbf[n]["flops"], stage_ms[n] / 1e3, peaks, STAGE_COMPUTE[n])
+        kind = router_compute(T) if n == "router" else STAGE_COMPUTE[n]
+        r = roofline_of(sbf[n]["bytes"], sbf[n]["flops"], stage_ms[n] / 1e3, peaks, kind)
         per_stage[n] = {"us": round(stage_ms[n] * 1e3, 2), "bound": r["bound"],
                         "frac": round(r["frac"], 4)}
     dom = max(names, key=lambda n: stage_ms[n])
     roof = roofline_of(sbf[dom]["bytes"], sbf[dom]["flops"], stage_ms[dom] / 1e3, peaks,
-                       STAGE_COMPUTE[dom])
+                       router_compute(T) if dom == "router" else STAGE_COMPUTE[dom])
     roof = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()}
     roof["kernel"] = dom
     roof["peak_source"] = f"of {peaks['source']}"
@@ -559,9 +576,14 @@ def stage_sweep(spec, Ts, peaks, dev):
         sel_bias = torch.zeros(E, device=dev) if spec.mode == 1 else None
         sb = stage_bytes_flops(spec, T, None, 0)
         row = {"T": T}
+        rscr = torch.empty(ops.router_tc_scratch_bytes(H, G), dtype=torch.uint8, device=dev)
+        t = _time(lambda: ops.router_gemm_tc(x, wg, None, logits, rscr, st), 5, stream)
+        r = roofline_of(sb["router"]["bytes"], sb["router"]["flops"], t, peaks, "bf16x3")
+        row["router"] = {"us": round(t * 1e6, 1), "bound": r["bound"], "frac": round(r["frac"], 3)}
         t = _time(lambda: ops.router_gemm(x, wg, None, logits), 5, stream)
         r = roofline_of(sb["router"]["bytes"], sb["router"]["flops"], t, peaks, "alu")
-        row["router"] = {"us": round(t * 1e6, 1), "bound": r["bound"], "frac": round(r["frac"], 3)}
+        row["router_fp32_simt"] = {"us": round(t * 1e6, 1), "bound": r["bound"],
+                                   "frac": round(r["frac"], 3)}
         t = _time(lambda: ops.topk_route(logits, E, K, spec.mode, spec.routed_scale, ids, w,
                                          sel_bias), 10, stream)
         r = roofline_of(sb["topk"]["bytes"], 0, t, peaks, "alu")
@@ -573,7 +595,7 @@ def stage_sweep(spec, Ts, peaks, dev):
         r = roofline_of(sb["unpermute"]["bytes"], 0, t, peaks, "alu")
         row["unpermute"] = {"us": round(t * 1e6, 1), "GB/s": round(r["achieved"], 1), "frac": round(r["frac"], 3)}
         out.append(row)
-        del x, logits, ids, w, off, r2f, f2r, xp, scratch, o
+        del x, logits, ids, w, off, r2f, f2r, xp, scratch, o, rscr
         torch.cuda.empty_cache()
     return out
 
@@ -599,8 +621,12 @@ def probe_stages(spec, T, reps, dev):
     scr = torch.empty(ops.permute_scratch_bytes(T, E, K), dtype=torch.uint8, device=dev)
     o = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     sel_bias = torch.zeros(E, device=dev) if spec.mode == 1 else None
+    rscr = torch.empty(ops.router_tc_scratch_bytes(H, G), dtype=torch.uint8, device=dev)
     for _ in range(reps):
-        ops.router_gemm(x, wg, None, logits)
+        if T >= ROUTER_TC_MIN_T:
+            ops.router_gemm_tc(x, wg, None, logits, rscr)
+        else:
+            ops.router_gemm(x, wg, None, logits)
         ops.topk_route(logits, E, K, spec.mode, spec.routed_scale, ids, w, sel_bias)
         ops.permute(x, ids, E, off, r2f, f2r, xp, scr)
         ops.unpermute(xp, f2r, w, T, K, H, o)

@@ -157,6 +157,30 @@ int moe_block_variant(int64_t m_size, int64_t R, int E, int m_skinny, int dispat
 moe_status_t moe_router_gemm(const void* x, const float* wg, const float* gate_bias,
                              float* logits, int T, int H, int G, moe_stream_t stream);
 
+/* Scratch bytes moe_router_gemm_tc needs for (H, G): 3 * G * H bf16, rounded up. */
+moe_status_t moe_router_tc_scratch_bytes(int H, int G, size_t* bytes);
+
+/*
+ * R on the tensor cores, for prefill-sized batches.  Same operation and
+ * arguments as moe_router_gemm, computed to fp32 accuracy from bf16 MMAs:
+ * [router] "2. CUDA kernel" keeps the gate in fp32 with bf16 activations;
+ * the bf16 activations are exact MMA operands, and the fp32 weight is split
+ * exactly into three bf16 parts (hi = bf16(w), mid = bf16(w - hi),
+ * lo = bf16(w - hi - mid)) whose products with x are exact in fp32 and
+ * accumulate in one fp32 TMEM accumulator.  |error| stays within a few fp32
+ * roundings of sum_h |x_h w_h|.
+ *   scratch    >= moe_router_tc_scratch_bytes(H, G), 256-byte aligned; the
+ *              split weight is written there on every call (two launches:
+ *              split, then the GEMM), so wg may change between calls
+ *   dev_status optional int32 device word: MOE_DEV_WAIT_TIMEOUT when a
+ *              pipeline wait gave up (the logits are then undefined)
+ * Deterministic: the split-K partials are summed in a fixed order.
+ * moe_layer uses this path for T >= 64 and moe_router_gemm below that.
+ */
+moe_status_t moe_router_gemm_tc(const void* x, const float* wg, const float* gate_bias,
+                                float* logits, int T, int H, int G, void* scratch,
+                                size_t scratch_bytes, int32_t* dev_status, moe_stream_t stream);
+
 /*
  * K: top-K routing, one warp per token.  [routing] "1. routing_custom.cu":
  * every lane keeps its own sorted top-K candidates (from the experts it
@@ -307,7 +331,7 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
 typedef struct {
   size_t logits, ids, weights, shared_gate, offsets, row_to_flat, flat_to_row,
       xp, hact, y, shared_hact, shared_y, block_variant, permute_scratch, gemm_scratch,
-      shared_gemm_scratch, sync, splitk, total;
+      shared_gemm_scratch, sync, splitk, router_split, total;
 } moe_workspace_layout_t;
 
 moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_workspace_layout_t* layout);

@@ -68,6 +68,9 @@ void layout_of(const moe_config_t* c, moe_workspace_layout_t* L) {
   // split-K slices for small batches (all blocks skinny: T <= m_skinny)
   const int ms = c->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : c->m_skinny;
   const int t_split = c->T_max < ms ? c->T_max : ms;
+  // the three bf16 parts of the gate weight for the tensor-core router
+  L->router_split = take(c->T_max >= kRouterTcMinT ? router_tc_scratch_bytes(c->H, G) : 0);
+  // split-K slices for small batches (all blocks skinny: T <= m_skinny); last
   L->splitk = take(grouped_gemm_splitk_bytes(t_split * c->K, c->H, c->I));
   L->total = off;
 }
@@ -105,6 +108,26 @@ moe_status_t moe_router_gemm(const void* x, const float* wg, const float* gate_b
       (gate_bias && misaligned(gate_bias, 4)))
     return MOE_ERR_MISALIGNED;
   return cuda_status(launch_router_gemm(x, wg, gate_bias, logits, T, H, G, stream));
+}
+
+moe_status_t moe_router_tc_scratch_bytes(int H, int G, size_t* bytes) {
+  if (!bytes || H <= 0 || G <= 0 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+  *bytes = router_tc_scratch_bytes(H, G);
+  return MOE_OK;
+}
+
+moe_status_t moe_router_gemm_tc(const void* x, const float* wg, const float* gate_bias,
+                                float* logits, int T, int H, int G, void* scratch,
+                                size_t scratch_bytes, int32_t* dev_status, moe_stream_t stream) {
+  if (T < 0 || H <= 0 || G <= 0 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !wg || !logits || !scratch) return MOE_ERR_INVALID_ARG;
+  if (scratch_bytes < router_tc_scratch_bytes(H, G)) return MOE_ERR_WORKSPACE;
+  if (misaligned(x, 16) || misaligned(wg, 16) || misaligned(logits, 4) ||
+      misaligned(scratch, 256) || (gate_bias && misaligned(gate_bias, 4)))
+    return MOE_ERR_MISALIGNED;
+  return cuda_status(
+      launch_router_tc(x, wg, gate_bias, logits, T, H, G, scratch, dev_status, stream));
 }
 
 moe_status_t moe_topk_route(const float* logits, int ld_logits, const float* sel_bias, int T,
@@ -260,7 +283,10 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
     e = launch_permute_copy(x, f2r, T, K, H, xp, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else {
-    e = launch_router_gemm(x, w->wg, w->gate_bias, logits, T, H, G, stream);
+    e = T >= kRouterTcMinT
+            ? launch_router_tc(x, w->wg, w->gate_bias, logits, T, H, G, ws + L.router_split,
+                               dev_status, stream)
+            : launch_router_gemm(x, w->wg, w->gate_bias, logits, T, H, G, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_topk_route(logits, G, w->sel_bias, T, E, K, cfg->mode, cfg->routed_scale, ids, wts,
                           cfg->has_shared ? gsh : nullptr, stream);

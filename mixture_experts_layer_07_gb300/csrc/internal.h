@@ -9,6 +9,14 @@
 cudaError_t launch_router_gemm(const void* x, const float* wg, const float* gate_bias,
                                float* logits, int T, int H, int G, cudaStream_t stream);
 
+// Router on the tensor cores (exact three-way bf16 split of wg, three MMAs per
+// K step into one fp32 accumulator); scratch holds the split parts.
+constexpr int kRouterTcMinT = 64;  // moe_layer uses it from this batch size on
+size_t router_tc_scratch_bytes(int H, int G);
+cudaError_t launch_router_tc(const void* x, const float* wg, const float* gate_bias,
+                             float* logits, int T, int H, int G, void* scratch,
+                             int32_t* dev_status, cudaStream_t stream);
+
 cudaError_t launch_topk_route(const float* logits, int ld, const float* sel_bias, int T, int E,
                               int K, int mode, float scale, int32_t* ids, float* weights,
                               float* shared_gate, cudaStream_t stream);

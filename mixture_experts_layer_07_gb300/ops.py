@@ -30,7 +30,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTS = ["moe_status_string", "moe_default_m_skinny", "moe_block_variant", "moe_router_gemm",
            "moe_topk_route", "moe_permute_scratch_bytes", "moe_permute",
            "moe_grouped_gemm_scratch_bytes", "moe_grouped_gemm", "moe_unpermute",
-           "moe_workspace_bytes", "moe_layer", "moe_workspace_layout", "moe_permute_static"]
+           "moe_workspace_bytes", "moe_layer", "moe_workspace_layout", "moe_permute_static",
+           "moe_router_tc_scratch_bytes", "moe_router_gemm_tc"]
 
 PERMUTE_STATIC_SCRATCH_BYTES = 1 << 20
 
@@ -60,7 +61,7 @@ class WorkspaceLayout(ctypes.Structure):
                 ("logits", "ids", "weights", "shared_gate", "offsets", "row_to_flat",
                  "flat_to_row", "xp", "hact", "y", "shared_hact", "shared_y", "block_variant",
                  "permute_scratch", "gemm_scratch", "shared_gemm_scratch", "sync", "splitk",
-                 "total")]
+                 "router_split", "total")]
 
 
 _L = None
@@ -83,6 +84,8 @@ def _lib():
         lib.moe_block_variant.argtypes = [_I64, _I64, _I, _I, _I, _I]
         sig = {
             "moe_router_gemm": [_P, _P, _P, _P, _I, _I, _I, _P],
+            "moe_router_tc_scratch_bytes": [_I, _I, ctypes.POINTER(_S)],
+            "moe_router_gemm_tc": [_P, _P, _P, _P, _I, _I, _I, _P, _S, _P, _P],
             "moe_topk_route": [_P, _I, _P, _I, _I, _I, _I, _F, _P, _P, _P, _P],
             "moe_permute_scratch_bytes": [_I, _I, _I, ctypes.POINTER(_S)],
             "moe_permute": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P, _P],
@@ -183,6 +186,20 @@ def router_gemm(x, wg, gate_bias, logits, stream=None):
     G = wg.shape[0]
     _check(_lib().moe_router_gemm(_p(x), _p(wg), _p(gate_bias), _p(logits), T, H, G,
                                   _stream(stream)), "moe_router_gemm")
+
+
+def router_tc_scratch_bytes(H: int, G: int) -> int:
+    n = _S()
+    _check(_lib().moe_router_tc_scratch_bytes(H, G, ctypes.byref(n)), "moe_router_tc_scratch_bytes")
+    return n.value
+
+
+def router_gemm_tc(x, wg, gate_bias, logits, scratch, dev_status=None, stream=None):
+    T, H = x.shape
+    G = wg.shape[0]
+    _check(_lib().moe_router_gemm_tc(_p(x), _p(wg), _p(gate_bias), _p(logits), T, H, G,
+                                     _p(scratch), scratch.numel() * scratch.element_size(),
+                                     _p(dev_status), _stream(stream)), "moe_router_gemm_tc")
 
 
 def topk_route(logits, E, K, mode, scale, ids, weights, sel_bias=None, shared_gate=None,

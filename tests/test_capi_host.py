@@ -121,6 +121,25 @@ def test_router_gemm_rejects_bad_arguments(ops):
     assert call(ops, "moe_router_gemm", 0x1000, 0x1000, None, 0x1000, 0, 64, 8, None) == 0
 
 
+def test_router_gemm_tc_rejects_bad_arguments(ops):
+    need = ops.router_tc_scratch_bytes(64, 8)
+    assert need >= 3 * 64 * 8 * 2
+    f = "moe_router_gemm_tc"
+
+    def r(x=0x1000, T=4, H=64, scratch=0x10000, nbytes=need):
+        return call(ops, f, x, 0x1000, None, 0x1000, T, H, 8, scratch, nbytes, None, None)
+
+    assert r(H=60) == 1
+    assert r(scratch=None) == 1
+    assert r(x=None) == 1
+    assert r(nbytes=need - 1) == 3
+    assert r(scratch=0x10010) == 4
+    assert r(x=0x1008) == 4
+    assert r(T=0) == 0
+    with pytest.raises(ops.MoEError):
+        ops.router_tc_scratch_bytes(60, 8)
+
+
 def test_topk_route_rejects_bad_arguments(ops):
     f = "moe_topk_route"
     assert call(ops, f, 0x1000, 8, None, 4, 8, 9, 0, 1.0, 0x1000, 0x1000, None, None) == 1

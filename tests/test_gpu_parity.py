@@ -49,13 +49,66 @@ def test_router_gemm(ops, name, T):
                           inp["gate_bias"])
 
 
+# tensor-core router: the same bound, from the bf16 three-way weight split;
+# cases cover one and two 128-token halves per CTA, split-K clusters, several
+# gate tiles, G = E + 1, a K tail below the 64-wide step and T below one tile
+ROUTER_TC_CASES = [("tiny", 1), ("tiny", 16), ("qwen3_30b_a3b", 64), ("qwen3_30b_a3b", 2125),
+                   ("qwen3_30b_a3b", 9733), ("gpt_oss_20b", 300), ("shared_gate", 131),
+                   ("high_expert", 4100), ("ragged_h", 200)]
+
+
+def router_tc_spec(name):
+    if name == "ragged_h":
+        return SPECS["tiny"].with_(name="ragged_h", H=136, E=40, K=4)
+    return SPECS[name]
+
+
+@pytest.mark.parametrize("name,T", ROUTER_TC_CASES)
+def test_router_gemm_tc(ops, name, T):
+    spec = router_tc_spec(name)
+    inp = synth.host_inputs(spec, T, seed=3, weights=False)
+    x, wg, gb = U.bf16_dev(inp["x_bits"]), U.dev(inp["wg"]), U.dev(inp["gate_bias"])
+    scratch = torch.empty(ops.router_tc_scratch_bytes(spec.H, spec.G), dtype=torch.uint8,
+                          device="cuda")
+    st = i32(1).zero_()
+    logits = torch.full((T, spec.G), float("nan"), device="cuda")
+    ops.router_gemm_tc(x, wg, gb, logits, scratch, st)
+    sync()
+    assert st.item() == 0
+    U.assert_router_close(U.f64(logits), oracle.bf16_to_f64(inp["x_bits"]), inp["wg"],
+                          inp["gate_bias"])
+    # deterministic: the same bits on a second call
+    again = torch.full_like(logits, float("nan"))
+    ops.router_gemm_tc(x, wg, gb, again, scratch, st)
+    sync()
+    assert torch.equal(logits, again)
+
+
+def test_router_gemm_tc_extreme_weights(ops):
+    # weights spanning many binades (the split must carry each one's own 24
+    # bits) and exact zeros
+    spec = SPECS["tiny"]
+    T = 130
+    inp = synth.host_inputs(spec, T, seed=5, weights=False)
+    rng = np.random.default_rng(11)
+    wg = (inp["wg"].astype(np.float64) * 2.0 ** rng.integers(-40, 40, inp["wg"].shape))
+    wg[:, ::7] = 0.0
+    wg = wg.astype(np.float32)
+    logits = torch.empty((T, spec.G), device="cuda")
+    scratch = torch.empty(ops.router_tc_scratch_bytes(spec.H, spec.G), dtype=torch.uint8,
+                          device="cuda")
+    ops.router_gemm_tc(U.bf16_dev(inp["x_bits"]), U.dev(wg), None, logits, scratch)
+    sync()
+    U.assert_router_close(U.f64(logits), oracle.bf16_to_f64(inp["x_bits"]), wg)
+
+
 # ---------------------------------------------------------------- K
 TOPK_CASES = [  # E, K, mode, T, shared
     (8, 2, 0, 16, False), (128, 8, 0, 1, False), (128, 8, 0, 2048, False),
     (32, 4, 0, 517, False), (512, 10, 0, 64, True), (896, 16, 1, 512, False),
     (512, 9, 1, 512, False), (1024, 16, 1, 512, False), (1024, 9, 1, 37, False),
     (8, 8, 0, 5, False), (64, 32, 0, 3, False), (33, 3, 1, 70, True), (1, 1, 0, 4, False),
-    # large T: one thread per token
+    # large T: many CTAs of four token warps
     (128, 8, 0, 5000, False), (32, 4, 0, 4096, False), (256, 16, 1, 4100, True),
     (8, 2, 0, 4097, False), (200, 9, 1, 8191, False)]
 
