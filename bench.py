@@ -169,10 +169,15 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
 
     def ksplit(units, kdim):
         nk = -(-kdim // 64)
-        s = 1
-        while s < 4 and units * 2 * s <= 2 * num_sms and nk // (2 * s) >= 4:
-            s *= 2
-        return s
+        best, best_cost = 1, None
+        for s in range(1, 9):
+            kbs = -(-nk // s)
+            if s > 1 and kbs < 2:
+                break
+            cost = -(-(units * s) // num_sms) * (kbs + 2)
+            if best_cost is None or cost < best_cost:
+                best, best_cost = s, cost
+        return best
 
     def gemm(max_rows, rows, blocks, with_plan, splittable):
         n = 1 if with_plan else 0

@@ -643,14 +643,25 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
                     (const float*)part, ksplit, R, N, static_cast<__nv_bfloat16*>(out));
 }
 
-// K slices for the skinny variant when few units would leave SMs idle: the
-// largest power of two <= 4 that keeps (units x slices) within two waves and
-// every slice non-empty and at least 4 stages long.  1 = no split.
+// K slices for the skinny variant.  The persistent grid walks units x slices
+// in waves of one unit per SM, and a wave lasts as long as its longest slice,
+// so the time is about waves(s) x (K steps per slice + a fixed cost per unit
+// for pipeline fill and epilogue, ~2 K steps).  s = 1..kMaxKSplit minimising
+// that (ties to the smaller s), slices at least 2 K steps long; 1 = no split.
+constexpr int kMaxKSplit = 8;
 int pick_ksplit(long long units, int Kdim) {
   const int nk = (Kdim + kBK - 1) / kBK;
-  int s = 1;
-  while (s < 4 && units * (2 * s) <= 2LL * num_sms() && nk / (2 * s) >= 4) s *= 2;
-  return s;
+  const long long sms = num_sms();
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= kMaxKSplit; ++s) {
+    const int kbs = (nk + s - 1) / s;
+    if (s > 1 && kbs < 2) break;
+    const long long waves = (units * s + sms - 1) / sms;
+    const long long cost = waves * (kbs + 2);
+    if (best_cost < 0 || cost < best_cost) { best = s; best_cost = cost; }
+  }
+  return best;
 }
 
 template <bool WFP8>
@@ -730,7 +741,7 @@ size_t grouped_gemm_scratch_bytes(int R, int E_blocks) {
 
 size_t grouped_gemm_splitk_bytes(int R, int H, int I) {
   const size_t w = (size_t)(2 * I > H ? 2 * I : H);
-  return moe_align_up(4 * (size_t)R * w * sizeof(float), 256);
+  return moe_align_up((size_t)kMaxKSplit * R * w * sizeof(float), 256);
 }
 
 int grouped_gemm_check(int H, int I, int wdtype) {

@@ -245,12 +245,17 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   const int r_lo = rank * per, r_hi = min(rows, r_lo + per);
   for (int e = threadIdx.x; e < (r_hi - r_lo) * (kTile / 4); e += blockDim.x) {
     const int rr = r_lo + e / (kTile / 4), c = (e % (kTile / 4)) * 4;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < splits; ++q) {
-      const float4 v = *reinterpret_cast<const float4*>(
-          cluster.map_shared_rank(part + (size_t)rr * C::kPitch + c, q));
-      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
-    }
+    // all ranks' partials in flight at once, then summed in rank order
+    float4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < splits)
+        v[q] = *reinterpret_cast<const float4*>(
+            cluster.map_shared_rank(part + (size_t)rr * C::kPitch + c, q));
+    float4 s = v[0];
+#pragma unroll
+    for (int q = 1; q < 8; ++q)
+      if (q < splits) { s.x += v[q].x; s.y += v[q].y; s.z += v[q].z; s.w += v[q].w; }
     const int m = m0 + rr, n = n0 + c;
     if (m < T) {
       const float sv[4] = {s.x, s.y, s.z, s.w};
@@ -291,6 +296,33 @@ int sm_count() {
   return n;
 }
 
+// clusters of `splits` CTAs of this kernel that fit on the GPU at once
+// (with one CTA per SM the GPC layout, not the SM count, decides)
+template <int MT>
+int max_active_clusters(int splits) {
+  static int cache[9] = {0};
+  if (!cache[splits]) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, splits);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = RtCfg<MT>::kSmemBytes;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = splits;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, router_tc_kernel<MT>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = sm_count() / (2 * splits);  // conservative
+    }
+    cache[splits] = n > 0 ? n : 1;
+  }
+  return cache[splits];
+}
+
 template <int MT>
 cudaError_t run(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias, float* logits,
                 int T, int H, int G, int32_t* dev_status, cudaStream_t stream) {
@@ -304,8 +336,12 @@ cudaError_t run(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias,
     attr = true;
   }
   const int tiles = moe_cdiv(G, kTile) * moe_cdiv(T, kTile * MT);
+  // split H over a cluster while all clusters still run in one wave and every
+  // rank keeps at least two 64-wide K steps
   int splits = 1;
-  while (splits < 8 && tiles * splits * 2 <= sm_count() && H / (2 * splits) >= 2 * kBK) splits *= 2;
+  while (splits < 8 && tiles <= max_active_clusters<MT>(2 * splits) &&
+         H / (2 * splits) >= 2 * kBK)
+    splits *= 2;
   const int kchunk = moe_cdiv(moe_cdiv(H, splits), kBK) * kBK;
   return moe_launch(router_tc_kernel<MT>, dim3(moe_cdiv(G, kTile), moe_cdiv(T, kTile * MT), splits),
                     dim3(192), C::kSmemBytes, stream, splits, mx, mw, bias, logits, T, H, G,
