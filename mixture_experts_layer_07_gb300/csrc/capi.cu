@@ -62,7 +62,11 @@ void layout_of(const moe_config_t* c, moe_workspace_layout_t* L) {
   L->shared_hact = take(c->has_shared ? Tm * c->I_shared * 2 : 0);
   L->shared_y = take(c->has_shared ? Tm * c->H * 2 : 0);
   L->block_variant = take((size_t)c->E * 4);
-  L->permute_scratch = take(permute_scratch_bytes(c->T_max, c->E, c->K));
+  // the permute's chunk counts: moe_layer's fused routing (T > 32) or the
+  // stand-alone permute, whichever needs more
+  const size_t pb = permute_scratch_bytes(c->T_max, c->E, c->K);
+  const size_t rb = route_prefill_scratch_bytes(c->T_max, c->E);
+  L->permute_scratch = take(pb > rb ? pb : rb);
   L->gemm_scratch = take(grouped_gemm_scratch_bytes((int)R, c->E));
   L->shared_gemm_scratch = take(c->has_shared ? grouped_gemm_scratch_bytes(c->T_max, 1) : 0);
   // split-K slices for small batches (all blocks skinny: T <= m_skinny)
@@ -266,6 +270,7 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
 
   int32_t* bvar = reinterpret_cast<int32_t*>(ws + L.block_variant);
   const bool decode = T <= kRouteDecodeMaxT;
+  bool planned = true;  // the grouped-GEMM plan was written by the routing launch
   cudaError_t e;
   if (decode) {
     // small batch: router + top-K + permute + GEMM plan in one launch
@@ -280,25 +285,44 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
     a.done_ctr = reinterpret_cast<unsigned int*>(ws + L.sync);
     e = launch_route_decode(a, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    e = launch_permute_copy(x, f2r, T, K, H, xp, stream);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else {
     e = T >= kRouterTcMinT
             ? launch_router_tc(x, w->wg, w->gate_bias, logits, T, H, G, ws + L.router_split,
                                dev_status, stream)
             : launch_router_gemm(x, w->wg, w->gate_bias, logits, T, H, G, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    e = launch_topk_route(logits, G, w->sel_bias, T, E, K, cfg->mode, cfg->routed_scale, ids, wts,
-                          cfg->has_shared ? gsh : nullptr, stream);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    e = launch_permute(x, ids, T, H, E, K, offsets, r2f, f2r, xp, ws + L.permute_scratch,
-                       dev_status, stream);
+    if (route_prefill_fits(T, E, K)) {
+      // top-K + chunk histograms + (last CTA) offsets and GEMM plan, then the
+      // stable scatter
+      RoutePrefillArgs a;
+      a.logits = logits; a.ld = G; a.sel_bias = w->sel_bias; a.T = T; a.E = E; a.K = K;
+      a.mode = cfg->mode; a.scale = cfg->routed_scale; a.ids = ids; a.weights = wts;
+      a.shared_gate = cfg->has_shared ? gsh : nullptr;
+      a.counts = reinterpret_cast<int32_t*>(ws + L.permute_scratch); a.offsets = offsets;
+      a.row_to_flat = r2f; a.flat_to_row = f2r;
+      a.m_skinny = cfg->m_skinny; a.dispatch = cfg->dispatch; a.wdtype = cfg->wdtype;
+      a.gemm_scratch = ws + L.gemm_scratch; a.block_variant = bvar;
+      a.done_ctr = reinterpret_cast<unsigned int*>(ws + L.sync + 64);
+      e = launch_route_prefill(a, stream);
+    } else {
+      // very large batches (the fused routing's shared memory would not
+      // fit): top-K, the multi-kernel permute, and the GEMM's own plan
+      e = launch_topk_route(logits, G, w->sel_bias, T, E, K, cfg->mode, cfg->routed_scale, ids,
+                            wts, cfg->has_shared ? gsh : nullptr, stream);
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+      e = launch_permute(x, ids, T, H, E, K, offsets, r2f, f2r, nullptr, ws + L.permute_scratch,
+                         dev_status, stream);
+      planned = false;
+    }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
+  // the permuted activations: each row of x written to its token's K rows
+  e = launch_permute_copy(x, f2r, T, K, H, xp, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = launch_grouped_gemm(xp, offsets, E, R, H, cfg->I, cfg->wdtype, w->w1, w->w3, w->w2, w->s1,
                           w->s3, w->s2, hact, y, cfg->m_skinny, cfg->dispatch, bvar,
                           ws + L.gemm_scratch, dev_status, stream, /*max_rows=*/T,
-                          /*plan_ready=*/decode, reinterpret_cast<float*>(ws + L.splitk),
+                          /*plan_ready=*/planned, reinterpret_cast<float*>(ws + L.splitk),
                           L.total - L.splitk);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   void* sh_y = nullptr;

@@ -97,8 +97,13 @@ struct TcCfg {
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
                                  : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
   static constexpr int kScaleBufs = WFP8 ? 3 : 0;  // per-unit scale rows, reused every 3 units
-  static constexpr int kNumBars = 2 * kStages + 2 * kAccStages + 1 + 2 * kConvStages + kScaleBufs;
-  static constexpr int kBarBytes = kNumBars * 8 + 16 + kScaleBufs * 2 * kMaxScaleCols * 4;
+  // work-unit queue: warp 0 takes units (its first is blockIdx.x, the rest
+  // from the launch's atomic counter) and hands each to the other roles
+  static constexpr int kQ = 8;
+  static constexpr int kQConsumers = 1 + kEpiWarps + (WFP8 ? 8 : 0);  // MMA thread + warps
+  static constexpr int kNumBars =
+      2 * kStages + 2 * kAccStages + 1 + 2 * kConvStages + kScaleBufs + 2 * kQ;
+  static constexpr int kBarBytes = kNumBars * 8 + 16 + kScaleBufs * 2 * kMaxScaleCols * 4 + kQ * 4;
   static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes +
                                        (size_t)kConvStages * kConvBytes + kEpiBytes + kBarBytes;
   static constexpr int kConvThreads = WFP8 ? 256 : 0;  // eight converter warps
@@ -130,7 +135,7 @@ template <int BN, bool SWIGLU, bool WFP8>
 __global__ void __launch_bounds__(TcCfg<BN, SWIGLU, WFP8>::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wb,
                const __grid_constant__ CUtensorMap tm_act, const float* __restrict__ sa,
-               const float* __restrict__ sb, const int32_t* __restrict__ counts, int list,
+               const float* __restrict__ sb, int32_t* __restrict__ counts, int list,
                const int4* __restrict__ items, int N, int Kdim, __nv_bfloat16* __restrict__ out,
                int ksplit, int R, float* __restrict__ part, int32_t* dev_status) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
@@ -172,9 +177,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
   auto conv_full = [&](int c) { return drain_bar + 8u * (1 + c); };
   auto conv_empty = [&](int c) { return drain_bar + 8u * (1 + C::kConvStages + c); };
   auto scale_bar = [&](int b) { return drain_bar + 8u * (1 + 2 * C::kConvStages + b); };
+  auto uq_full = [&](int q) {
+    return drain_bar + 8u * (1 + 2 * C::kConvStages + C::kScaleBufs + q);
+  };
+  auto uq_empty = [&](int q) {
+    return drain_bar + 8u * (1 + 2 * C::kConvStages + C::kScaleBufs + C::kQ + q);
+  };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 8 * C::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* scale_rows = reinterpret_cast<float*>(tmem_slot + 4);  // FP8: [3][2][kMaxScaleCols]
+  volatile int32_t* uq = reinterpret_cast<volatile int32_t*>(scale_rows + C::kScaleBufs * 2 * C::kMaxScaleCols);
+  int32_t* sched = counts + kSchedBase + 2 * list + (SWIGLU ? 0 : 1);
 
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -189,6 +202,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
       mbar_init(conv_empty(c), 1);
     }
     for (int b = 0; b < C::kScaleBufs; ++b) mbar_init(scale_bar(b), C::kConvThreads);
+    for (int q = 0; q < C::kQ; ++q) {
+      mbar_init(uq_full(q), 1);
+      mbar_init(uq_empty(q), C::kQConsumers);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -214,14 +231,34 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
   auto acc_set = [](uint32_t i) { return C::kAccStages == 2 ? (i & 1u) : 0u; };
   auto acc_par = [](uint32_t i) { return (C::kAccStages == 2 ? (i >> 1) : i) & 1u; };
   constexpr int kWeightBytes = WFP8 ? C::kQBytes : C::kABytes;
+  // next work unit from the queue (every consumer sees every unit, in order);
+  // `arrive` frees the entry (one arrival per consuming warp or thread).
+  // total (or more) ends the walk; -1 means the wait gave up.
+  auto pop_unit = [&](uint32_t& q, uint32_t& qph, bool arrive) {
+    int w = -1;
+    if (mbar_wait_bounded(uq_full(q), qph, abort_flag, kWaitLimitNs)) w = uq[q];
+    if (arrive) mbar_arrive(uq_empty(q));
+    if (++q == C::kQ) { q = 0; qph ^= 1u; }
+    return w;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
       int stage = 0;
-      uint32_t phase = 0, armed = 0, armed_parity = 0;
+      uint32_t phase = 0, armed = 0, armed_parity = 0, q = 0, qph = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      int w = blockIdx.x;  // first unit; later ones come from the launch's counter
+      for (;;) {
+        // hand the unit (or the end mark) to the other roles
+        if (!mbar_wait_bounded(uq_empty(q), qph ^ 1u, abort_flag, kWaitLimitNs)) {
+          fail();
+          break;
+        }
+        uq[q] = ok ? w : total;
+        mbar_arrive(uq_full(q));
+        if (++q == C::kQ) { q = 0; qph ^= 1u; }
+        if (!ok || w >= total) break;
         const Unit u = unit_of(w);
         const int4 it = u.it;
         const int nb = u.nb;
@@ -240,6 +277,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
+        // the next unit: taken once this one's loads are issued, so a CTA that
+        // drew short units takes more (the grid's first units are blockIdx.x)
+        if (ok) w = (int)gridDim.x + atomicAdd(sched, 1);
       }
       // every copy this thread started has landed before the CTA moves on
       for (int s = 0; s < C::kStages; ++s)
@@ -250,9 +290,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
     if (lane == 0) {
       // ---------------- MMA issuer
       int stage = 0, cs = 0;
-      uint32_t phase = 0, cphase = 0, unit = 0;
+      uint32_t phase = 0, cphase = 0, unit = 0, q = 0, qph = 0;
       bool ok = true, issued = false;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++unit) {
+      for (;; ++unit) {
+        const int w = pop_unit(q, qph, true);
+        if (w < 0) fail();
+        if (w < 0 || w >= total) break;
         const uint32_t a = acc_set(unit);
         if (!mbar_wait_bounded(acc_empty(a), acc_par(unit) ^ 1u, abort_flag, kWaitLimitNs)) {
           fail();
@@ -306,8 +349,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
     const int half = (warp - 2) >> 2;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     uint16_t* stg = epi + (warp - 2) * (16 * 32);
-    uint32_t unit = 0;
-    for (int w = blockIdx.x; w < total; w += gridDim.x, ++unit) {
+    uint32_t unit = 0, q = 0, qph = 0;
+    for (;; ++unit) {
+      const int w = pop_unit(q, qph, false);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(uq_empty((q + C::kQ - 1) % C::kQ));
+      if (w < 0) fail();
+      if (w < 0 || w >= total) break;
       const Unit un = unit_of(w);
       const int4 it = un.it;
       const int nb = un.nb;
@@ -373,9 +421,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
     const int ct = threadIdx.x - 32 * C::kConvWarp0;
     const int rb = (N + 127) / 128, cb = (Kdim + 127) / 128;
     int stage = 0, cs = 0;
-    uint32_t phase = 0, cphase = 0, unit = 0;
+    uint32_t phase = 0, cphase = 0, unit = 0, q = 0, qph = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++unit) {
+    for (;; ++unit) {
+      const int w = pop_unit(q, qph, false);
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(uq_empty((q + C::kQ - 1) % C::kQ));
+      if (w < 0) fail();
+      if (w < 0 || w >= total || !ok) break;
       const Unit un = unit_of(w);
       const int4 it = un.it;
       const int nb = un.nb;
@@ -618,7 +671,7 @@ int num_sms() {
 
 template <int BN, bool SWIGLU, bool WFP8>
 cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorMap& act,
-                   const float* sa, const float* sb, const int32_t* counts, int list,
+                   const float* sa, const float* sb, int32_t* counts, int list,
                    const int4* items, int cap, int N, int Kdim, void* out, int32_t* dev_status,
                    cudaStream_t stream, int ksplit = 1, int R = 0, float* part = nullptr) {
   using C = TcCfg<BN, SWIGLU, WFP8>;

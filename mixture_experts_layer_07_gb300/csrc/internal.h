@@ -73,6 +73,32 @@ struct RouteDecodeArgs {
 };
 cudaError_t launch_route_decode(const RouteDecodeArgs& args, cudaStream_t stream);
 
+// Fused routing above the decode range: top-K + per-chunk expert histograms +
+// (last CTA) scan to offsets and the grouped-GEMM plan, then the stable
+// scatter -- two launches in all.  done_ctr must be zero before the launch and
+// is zero again after it.  counts: route_prefill_scratch_bytes(T, E) bytes.
+struct RoutePrefillArgs {
+  const float* logits;
+  int ld;
+  const float* sel_bias;
+  int T, E, K, mode;
+  float scale;
+  int32_t* ids;
+  float* weights;
+  float* shared_gate;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* row_to_flat;
+  int32_t* flat_to_row;
+  int m_skinny, dispatch, wdtype;
+  void* gemm_scratch;  // plan written here (grouped-GEMM scratch layout for R = T*K)
+  int32_t* block_variant;
+  unsigned int* done_ctr;
+};
+bool route_prefill_fits(int T, int E, int K);  // shared memory and E limits
+size_t route_prefill_scratch_bytes(int T, int E);
+cudaError_t launch_route_prefill(const RoutePrefillArgs& args, cudaStream_t stream);
+
 cudaError_t launch_unpermute(const void* y, const int32_t* flat_to_row, const float* weights,
                              int T, int K, int H, const void* shared_y, const float* shared_gate,
                              void* out, cudaStream_t stream);

@@ -13,7 +13,10 @@ constexpr int kBnTile = 128;
 constexpr int kBnWide = 256;
 constexpr int kLists = 3;  // skinny, tile, wide
 __host__ __device__ constexpr int list_bn(int l) { return l == 0 ? kBnSkinny : l == 1 ? kBnTile : kBnWide; }
-// scratch layout: counts[kLists] then one int4 item list per variant
+// scratch layout: counts[kLists] and the GEMM launches' work counters
+// (counts[kSchedBase + 2*list + {0: G1, 1: G2}], zeroed by every plan) in a
+// 256-byte head, then one int4 item list per variant
+constexpr int kSchedBase = 8;
 struct PlanView {
   int32_t* counts;          // items per list
   int4* items[kLists];      // {block, first row, rows, 0}
@@ -109,6 +112,7 @@ MOE_DEVICE void plan_experts(const int32_t* offsets, int E_blocks, int R, int m_
     __syncthreads();
   }
   if (tid < kLists) counts[tid] = carry[tid];
+  if (tid < 2 * kLists) counts[kSchedBase + tid] = 0;
 }
 
 }  // namespace moe_plan

@@ -440,6 +440,56 @@ def test_layer(ops, name, over, T):
     U.assert_bf16_close(U.f64(out)[clear], res["out"][clear], rel, "layer out")
 
 
+# T > 32: one fused routing launch (top-K, chunk histograms, and in the last
+# CTA the scan to offsets and the GEMM plan) and the stable scatter.  Its
+# intermediates are checked bit for bit against the oracle's permute of the
+# GPU's own ids and its top-K of the GPU's own logits; its completion counter
+# must come back to zero, call after call, on one workspace.
+PREFILL_CASES = [("tiny", {"E": 16, "K": 4}, (33, 129, 1000, 40000)),
+                 ("tiny", {"E": 40, "K": 3, "mode": 1, "routed_scale": 2.5, "sel_bias_var": 0.1},
+                  (64, 777)),
+                 ("high_expert", {"E": 1024, "H": 256, "I": 128}, (100,)),
+                 ("shared_gate", {"H": 256, "I": 128, "I_shared": 128}, (300,))]
+
+
+@pytest.mark.parametrize("name,over,Ts", PREFILL_CASES)
+def test_layer_prefill_routing_is_exact_and_repeats(ops, name, over, Ts):
+    spec = SPECS[name].with_(**over)
+    inp = synth.host_inputs(spec, max(Ts), seed=41)
+    t = U.layer_tensors(inp)
+    layer = ops.MoELayer(U.config_for(ops, spec, T_max=max(Ts)), t)
+    for T in Ts:
+        x = t["x"][:T].contiguous()
+        layer(x)
+        sync()
+        assert int(layer.dev_status.item()) == 0
+        R, E, K = T * spec.K, spec.E, spec.K
+        lg = layer.view("logits", torch.float32, (T, spec.G)).cpu().numpy()
+        gid = layer.view("ids", torch.int32, (T, K)).cpu().numpy()
+        gw = layer.view("weights", torch.float32, (T, K)).cpu().numpy()
+        if spec.mode == 0:
+            rid, rw = oracle.topk_softmax_renorm(lg.astype(np.float64), E, K)
+        else:
+            rid, rw = oracle.topk_sigmoid_bias(lg, inp["sel_bias"], E, K, spec.routed_scale)
+        assert np.array_equal(gid, rid)
+        assert np.allclose(gw, rw, rtol=1e-5, atol=1e-7)
+        off, r2f, f2r = oracle.permute(gid, E)
+        assert np.array_equal(layer.view("offsets", torch.int32, (E + 1,)).cpu().numpy(), off)
+        assert np.array_equal(layer.view("row_to_flat", torch.int32, (R,)).cpu().numpy(), r2f)
+        assert np.array_equal(layer.view("flat_to_row", torch.int32, (R,)).cpu().numpy(), f2r)
+        wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
+        want = [ops.block_variant(int(m), R, E, -1, 0, wd) for m in np.diff(off)]
+        assert layer.view("block_variant", torch.int32, (E,)).cpu().numpy().tolist() == want
+        sw = layer.workspace[layer.layout.sync:layer.layout.sync + 256].view(torch.int32)
+        assert int(sw.abs().sum().item()) == 0
+        if T <= 1000:
+            case = dict(inp)
+            case["x_bits"] = inp["x_bits"][:T]
+            res = oracle.moe_layer_from_inputs(case, logits_override=lg.astype(np.float64))
+            rel = 5e-2 if spec.wdtype == "fp8" else 2e-2
+            U.assert_bf16_close(U.f64(layer(x)), res["out"], rel, f"prefill T={T}")
+
+
 def test_layer_decode_path_repeats_and_leaves_sync_zero(ops):
     # T <= 32 runs the fused routing launch; its completion counter must come
     # back to zero so that the next call (same workspace) routes again
