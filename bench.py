@@ -159,9 +159,10 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
       T > 32:  router 1 (2 from T >= 64: weight split + tensor-core GEMM),
                fused routing 1 (top-K, chunk histograms, and in its last CTA
                the scan and the GEMM plan), scatter 1, permute copy 1
-      GEMM:    one G1 and one G2 launch per variant list that can be
-               non-empty (skinny always; tile when T > m_skinny; wide for FP8
-               when also T > 128), or 2 on the CUDA-core path; when only the
+      GEMM:    skinny list (always): one G1 and one G2 launch; tile list
+               (T > m_skinny) and wide list (FP8, T > 128): a G1 and a G2
+               launch each, or one launch running both while the mean rows
+               per expert are <= 64 and H <= 3 I; 2 on the CUDA-core path; when only the
                skinny list can be non-empty, each of G1/G2 split along K adds
                a finalize launch
       combine 1; a shared expert adds a grouped GEMM with its own plan."""
@@ -179,25 +180,28 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
                 best, best_cost = s, cost
         return best
 
-    def gemm(max_rows, rows, blocks, with_plan, splittable):
+    def gemm(max_rows, rows, blocks, with_plan, splittable, inter):
         n = 1 if with_plan else 0
         if dispatch == 2:
             return n + 2
         tile = max_rows > m_skinny
         wide = spec.wdtype == "fp8" and tile and max_rows >= wide_min
-        n += 2 * (1 + tile + wide)
+        # tile and wide lists: one G1+G2 launch each (mean rows <= 64, H <= 3 I)
+        fused = rows <= 64 * blocks and spec.H <= 3 * inter
+        n += 2 + (tile + wide) * (1 if fused else 2)
         if splittable and not tile:
             b = min(rows, blocks)
-            n += (ksplit(b * -(-spec.I // 128), spec.H) > 1) + (ksplit(b * -(-spec.H // 128), spec.I) > 1)
+            n += (ksplit(b * -(-inter // 128), spec.H) > 1) + (ksplit(b * -(-spec.H // 128), inter) > 1)
         return n
 
     if T <= 32:
         route = 2
-        g = gemm(T, R, spec.E, with_plan=False, splittable=True)
+        g = gemm(T, R, spec.E, with_plan=False, splittable=True, inter=spec.I)
     else:
         route = (2 if T >= ROUTER_TC_MIN_T else 1) + 3
-        g = gemm(T, R, spec.E, with_plan=False, splittable=False)
-    shared = gemm(T, T, 1, with_plan=True, splittable=False) if spec.has_shared else 0
+        g = gemm(T, R, spec.E, with_plan=False, splittable=False, inter=spec.I)
+    shared = (gemm(T, T, 1, with_plan=True, splittable=False, inter=spec.I_shared)
+              if spec.has_shared else 0)
     return route + g + shared + 1
 
 

@@ -119,6 +119,32 @@ struct TcCfg {
 
 MOE_DEVICE float silu_f(float g) { return g / (1.f + __expf(-g)); }
 
+// generic-proxy global writes (made visible to this thread) -> later TMA reads
+MOE_DEVICE void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// wait until *p >= target (acquire, GPU scope); bounded like the mbarrier waits
+MOE_DEVICE bool wait_count_geq(const int32_t* p, int target, const volatile int* abort,
+                               uint64_t limit_ns) {
+  auto ld = [&]() {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+  };
+  if (ld() >= target) return true;
+  const uint64_t t0 = moe_ptx::globaltimer_ns();
+  for (uint32_t i = 1; i < (1u << 30); ++i) {
+    __nanosleep(64);
+    if (ld() >= target) return true;
+    if ((i & 15) == 0) {
+      if (abort && *abort) return false;
+      if (moe_ptx::globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+  return false;
+}
+
 MOE_DEVICE void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -131,32 +157,60 @@ MOE_DEVICE uint32_t e4m3x2_to_bf16x2(uint32_t two, float sc) {
   return pack_bf16x2(f.x * sc, f.y * sc);
 }
 
-template <int BN, bool SWIGLU, bool WFP8>
+// FUSED (G1 layout, SWIGLU = true): one persistent launch runs the list's G1
+// units and then its G2 units (W2 = tm_w2, activations hact = tm_h, output
+// y = out2, N2 x K2).  A G2 unit of token tile i starts loading only after
+// all G1 units of tile i have stored their hact rows: each G1 epilogue warp
+// fences its stores and bumps done[i]; the G2 producer waits (bounded) for
+// nblk x 8 and fences the generic-proxy writes for its TMA reads.  So the
+// CTAs that finish G1 early start G2 work instead of idling, and the launch
+// boundary between the two disappears.
+template <int BN, bool SWIGLU, bool WFP8, bool FUSED>
 __global__ void __launch_bounds__(TcCfg<BN, SWIGLU, WFP8>::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wb,
                const __grid_constant__ CUtensorMap tm_act, const float* __restrict__ sa,
                const float* __restrict__ sb, int32_t* __restrict__ counts, int list,
                const int4* __restrict__ items, int N, int Kdim, __nv_bfloat16* __restrict__ out,
-               int ksplit, int R, float* __restrict__ part, int32_t* dev_status) {
+               int ksplit, int R, float* __restrict__ part, int32_t* dev_status,
+               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_h,
+               const float* __restrict__ s2, int N2, int K2, __nv_bfloat16* __restrict__ out2,
+               int32_t* __restrict__ done) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
+  static_assert(!FUSED || SWIGLU, "the fused launch uses the G1 layout");
   pdl_wait();
   pdl_trigger();
   const int nblk = (N + kBM - 1) / kBM;
-  const int total = counts[list] * nblk * ksplit;
+  const int total1 = counts[list] * nblk * ksplit;
+  const int nblk2 = FUSED ? (N2 + kBM - 1) / kBM : 1;
+  const int total = FUSED ? total1 + counts[list] * nblk2 : total1;
   if ((int)blockIdx.x >= total) return;
   const int nk = (Kdim + kBK - 1) / kBK;
+  const int nk2 = FUSED ? (K2 + kBK - 1) / kBK : 0;
   // work unit w -> (item, 128-feature block nb, K slice ks); with ksplit > 1
   // each slice writes fp32 partial sums to part[ks][row][feature] instead of
-  // the finished output (a finalize kernel reduces the slices in order)
+  // the finished output (a finalize kernel reduces the slices in order).
+  // FUSED: units total1.. are the G2 units (no K slices).
   const int kbs = (nk + ksplit - 1) / ksplit;
-  struct Unit { int4 it; int nb, kb_lo, kb_hi, ks; };
+  struct Unit { int4 it; int nb, kb_lo, kb_hi, ks, idx; bool g1; };
   auto unit_of = [&](int w) {
     Unit u;
-    u.it = items[w / (nblk * ksplit)];
-    u.nb = (w / ksplit) % nblk;
-    u.ks = w % ksplit;
-    u.kb_lo = u.ks * kbs;
-    u.kb_hi = min(nk, u.kb_lo + kbs);
+    if (FUSED && w >= total1) {
+      const int w2 = w - total1;
+      u.idx = w2 / nblk2;
+      u.nb = w2 % nblk2;
+      u.ks = 0;
+      u.kb_lo = 0;
+      u.kb_hi = nk2;
+      u.g1 = false;
+    } else {
+      u.idx = w / (nblk * ksplit);
+      u.nb = (w / ksplit) % nblk;
+      u.ks = w % ksplit;
+      u.kb_lo = u.ks * kbs;
+      u.kb_hi = min(nk, u.kb_lo + kbs);
+      u.g1 = SWIGLU;
+    }
+    u.it = items[u.idx];
     return u;
   };
 
@@ -213,6 +267,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
     prefetch_tmap(&tm_wa);
     if (SWIGLU) prefetch_tmap(&tm_wb);
     prefetch_tmap(&tm_act);
+    if (FUSED) {
+      prefetch_tmap(&tm_w2);
+      prefetch_tmap(&tm_h);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -262,17 +320,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
         const Unit u = unit_of(w);
         const int4 it = u.it;
         const int nb = u.nb;
-        for (int kb = u.kb_lo; kb < u.kb_hi; ++kb) {
+        if (FUSED && !u.g1) {
+          // this tile's hact rows: every G1 unit of the tile stored and counted
+          if (!wait_count_geq(done + u.idx, nblk * C::kEpiWarps, abort_flag, kWaitLimitNs)) {
+            fail();
+            ok = false;
+          }
+          fence_proxy_async_global();
+        }
+        const CUtensorMap* wmap = (FUSED && !u.g1) ? &tm_w2 : &tm_wa;
+        const CUtensorMap* amap = (FUSED && !u.g1) ? &tm_h : &tm_act;
+        const uint32_t stage_bytes = u.g1 ? C::kStageBytes : kWeightBytes + C::kBBytes;
+        for (int kb = u.kb_lo; kb < u.kb_hi && ok; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             fail();
             ok = false;
             break;
           }
           const uint32_t st = sbase + stage * C::kStageBytes;
-          mbar_arrive_expect_tx(full_bar(stage), C::kStageBytes);
-          tma_load_3d(st, &tm_wa, full_bar(stage), kb * kBK, nb * kBM, it.x);
-          if (SWIGLU) tma_load_3d(st + kWeightBytes, &tm_wb, full_bar(stage), kb * kBK, nb * kBM, it.x);
-          tma_load_2d(st + C::kNA * kWeightBytes, &tm_act, full_bar(stage), kb * kBK, it.y);
+          mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
+          tma_load_3d(st, wmap, full_bar(stage), kb * kBK, nb * kBM, it.x);
+          if (u.g1) tma_load_3d(st + kWeightBytes, &tm_wb, full_bar(stage), kb * kBK, nb * kBM, it.x);
+          tma_load_2d(st + C::kNA * kWeightBytes, amap, full_bar(stage), kb * kBK, it.y);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -321,7 +390,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
             const uint32_t acc = (kb > u.kb_lo || kk > 0) ? 1u : 0u;
             const uint64_t bdesc = sdesc_k128_sw128(sx + kk * 32);
             tc_mma_f16(d, sdesc_k128_sw128(wa_s + kk * 32), bdesc, C::kIdesc, acc);
-            if (SWIGLU) tc_mma_f16(d + BN, sdesc_k128_sw128(wb_s + kk * 32), bdesc, C::kIdesc, acc);
+            if (u.g1) tc_mma_f16(d + BN, sdesc_k128_sw128(wb_s + kk * 32), bdesc, C::kIdesc, acc);
           }
           issued = true;
           tc_commit(empty_bar(stage));
@@ -367,10 +436,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
       tc_fence_after();
       const uint32_t tacc = t_lane + a * C::kAccCols;
       const int m = it.z;
+      const bool sw = un.g1;  // SwiGLU of the gate and up accumulators
+      const int Nu = sw || !FUSED ? N : N2;
+      __nv_bfloat16* outu = sw || !FUSED ? out : out2;
       for (int c0 = 16 * half; c0 < BN && c0 < m; c0 += 32) {
         uint32_t g[16], u[16];
         tc_ld_32x32b_x16(tacc + c0, g);
-        if (SWIGLU) tc_ld_32x32b_x16(tacc + BN + c0, u);
+        if (sw) tc_ld_32x32b_x16(tacc + BN + c0, u);
         tc_wait_ld();
         if (ksplit > 1) {
           // fp32 partials of this K slice: row-major [ks][R][Npart], Npart = N or 2N
@@ -392,7 +464,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float gv = __uint_as_float(g[j]);
-          const float v = SWIGLU ? silu_f(gv) * __uint_as_float(u[j]) : gv;
+          const float v = sw ? silu_f(gv) * __uint_as_float(u[j]) : gv;
           stg[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
         }
         __syncwarp();
@@ -401,15 +473,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
         for (int i = 0; i < 2; ++i) {
           const int r = (lane >> 2) + 8 * i;
           const int n0 = nb * kBM + quarter * 32 + (lane & 3) * 8;
-          if (c0 + r < m && n0 < N) {
+          if (c0 + r < m && n0 < Nu) {
             const uint4 v = *reinterpret_cast<const uint4*>(stg + r * 32 + (lane & 3) * 8);
-            *reinterpret_cast<uint4*>(out + (size_t)(it.y + c0 + r) * N + n0) = v;
+            *reinterpret_cast<uint4*>(outu + (size_t)(it.y + c0 + r) * Nu + n0) = v;
           }
         }
         __syncwarp();
       }
       tc_fence_before();
       mbar_arrive(acc_empty(a));
+      if (FUSED && sw) {
+        // this warp's share of the tile's hact rows is stored: count it
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(done + un.idx, 1);
+      }
     }
   } else if (WFP8) {
     // ---------------- e4m3 -> bf16 converters, warps 10..17
@@ -419,7 +497,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
     // through three buffers: a converter can run at most two stages ahead of
     // the slowest one, so a buffer is never rewritten while still being read.
     const int ct = threadIdx.x - 32 * C::kConvWarp0;
-    const int rb = (N + 127) / 128, cb = (Kdim + 127) / 128;
     int stage = 0, cs = 0;
     uint32_t phase = 0, cphase = 0, unit = 0, q = 0, qph = 0;
     bool ok = true;
@@ -434,10 +511,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
       const int nb = un.nb;
       const int buf = (int)(unit % 3u);
       float* scale_row = scale_rows + buf * 2 * C::kMaxScaleCols;
+      // the unit's matrices: W1 and W3 (G1) or W2 (G2 of a fused launch)
+      const bool g1 = un.g1;
+      const int rb = ((g1 || !FUSED ? N : N2) + 127) / 128;
+      const int cb = ((g1 || !FUSED ? Kdim : K2) + 127) / 128;
+      const float* s_a = g1 || !FUSED ? sa : s2;
       const size_t row = ((size_t)it.x * rb + nb) * cb;
       for (int c = ct; c < cb; c += C::kConvThreads) {
-        scale_row[c] = __ldg(sa + row + c);
-        scale_row[C::kMaxScaleCols + c] = SWIGLU ? __ldg(sb + row + c) : 0.f;
+        scale_row[c] = __ldg(s_a + row + c);
+        scale_row[C::kMaxScaleCols + c] = g1 ? __ldg(sb + row + c) : 0.f;
       }
       mbar_arrive(scale_bar(buf));
       if (!mbar_wait_bounded(scale_bar(buf), (unit / 3u) & 1u, abort_flag, kWaitLimitNs)) {
@@ -454,6 +536,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
         const int sc = (kb * kBK) / 128;
 #pragma unroll
         for (int t = 0; t < C::kNA; ++t) {
+          if (t > 0 && !g1) break;
           const float scl = scale_row[t * C::kMaxScaleCols + sc];
           const uint8_t* src = smem + (size_t)stage * C::kStageBytes + t * C::kQBytes;
           uint8_t* dst = conv + (size_t)cs * C::kConvBytes + t * C::kABytes;
@@ -669,26 +752,35 @@ int num_sms() {
   return n[dev];
 }
 
-template <int BN, bool SWIGLU, bool WFP8>
+// One launch of the tensor-core kernel over a list.  FUSED: the list's G1
+// and G2 units in one persistent launch (w2/h/s2/N2/K2/out2/done describe G2;
+// ksplit must be 1).
+template <int BN, bool SWIGLU, bool WFP8, bool FUSED = false>
 cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorMap& act,
                    const float* sa, const float* sb, int32_t* counts, int list,
                    const int4* items, int cap, int N, int Kdim, void* out, int32_t* dev_status,
-                   cudaStream_t stream, int ksplit = 1, int R = 0, float* part = nullptr) {
+                   cudaStream_t stream, int ksplit = 1, int R = 0, float* part = nullptr,
+                   const CUtensorMap* w2 = nullptr, const CUtensorMap* h = nullptr,
+                   const float* s2 = nullptr, int N2 = 0, int K2 = 0, void* out2 = nullptr,
+                   int32_t* done = nullptr) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
   static bool attr_set = false;  // per process; the attribute is per function, all devices
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, SWIGLU, WFP8>,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, SWIGLU, WFP8, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long long work = (long long)cap * moe_cdiv(N, kBM) * ksplit;
+  const long long work =
+      (long long)cap * (moe_cdiv(N, kBM) * ksplit + (FUSED ? moe_cdiv(N2, kBM) : 0));
   const int grid = (int)(work < num_sms() ? work : num_sms());
   if (grid <= 0) return cudaSuccess;
-  cudaError_t e = moe_launch(gemm_tc_kernel<BN, SWIGLU, WFP8>, dim3(grid), dim3(C::kThreads),
-                             C::kSmemBytes, stream, 1, wa, wb, act, sa, sb, counts, list, items, N,
-                             Kdim, static_cast<__nv_bfloat16*>(out), ksplit, R, part, dev_status);
+  cudaError_t e = moe_launch(gemm_tc_kernel<BN, SWIGLU, WFP8, FUSED>, dim3(grid),
+                             dim3(C::kThreads), C::kSmemBytes, stream, 1, wa, wb, act, sa, sb,
+                             counts, list, items, N, Kdim, static_cast<__nv_bfloat16*>(out),
+                             ksplit, R, part, dev_status, FUSED ? *w2 : wa, FUSED ? *h : act, s2,
+                             N2, K2, static_cast<__nv_bfloat16*>(out2), done);
   if (e != cudaSuccess || ksplit <= 1) return e;
   const long long n = (long long)R * (N / 4);
   const int fgrid = (int)((n + 255) / 256 < 4 * num_sms() ? (n + 255) / 256 : 4 * num_sms());
@@ -734,6 +826,15 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
     if ((size_t)ks2 * R * H * sizeof(float) > splitk_bytes) ks2 = 1;
     if (I % 4 || H % 4) ks1 = ks2 = 1;
   }
+  // One fused G1+G2 launch per list pays off while the G1 units are few (its
+  // last wave is a large share of the G1 time): mean rows per block <= 64, and
+  // G2 not much larger than G1 (H <= 3 I).  Otherwise G2 prefers its own
+  // deeper pipeline: in the fused layout a G2 stage occupies a G1-sized slot,
+  // so its own launch keeps half again as many stages in flight.
+  // (Measured: qwen3-30b-a3b shape T=256 264 -> 254 us and gpt-oss-20b shape
+  // T=512 427 -> 415 us fused; the H = 4 I shared-gate shape at T=1024 went
+  // 630 -> 655 us fused.)
+  const bool fuse = (long long)R <= 64LL * E_blocks && H <= 3 * I;
   CUtensorMap m_w1, m_w3, m_w2, m_x[kLists], m_h[kLists];
   if (!make_weight_map(&m_w1, w1, E_blocks, I, H, WFP8) ||
       !make_weight_map(&m_w3, w3, E_blocks, I, H, WFP8) ||
@@ -749,22 +850,37 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
     err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x[0], s1, s3, pv.counts, 0, pv.items[0],
                                         pv.cap[0], I, H, hact, dev_status, stream, ks1, R,
                                         splitk_buf);
-  if (any[1] && err == cudaSuccess)
-    err = run_tc<kBnTile, true, WFP8>(m_w1, m_w3, m_x[1], s1, s3, pv.counts, 1, pv.items[1],
-                                      pv.cap[1], I, H, hact, dev_status, stream);
-  if (any[2] && err == cudaSuccess)
-    err = run_tc<kBnWide, true, WFP8>(m_w1, m_w3, m_x[2], s1, s3, pv.counts, 2, pv.items[2],
-                                      pv.cap[2], I, H, hact, dev_status, stream);
+  if (fuse) {
+    // tile and wide lists: G1 and G2 in one persistent launch each
+    if (any[1] && err == cudaSuccess)
+      err = run_tc<kBnTile, true, WFP8, true>(m_w1, m_w3, m_x[1], s1, s3, pv.counts, 1,
+                                              pv.items[1], pv.cap[1], I, H, hact, dev_status,
+                                              stream, 1, R, nullptr, &m_w2, &m_h[1], s2, H, I, y,
+                                              pv.done[1]);
+    if (any[2] && err == cudaSuccess)
+      err = run_tc<kBnWide, true, WFP8, true>(m_w1, m_w3, m_x[2], s1, s3, pv.counts, 2,
+                                              pv.items[2], pv.cap[2], I, H, hact, dev_status,
+                                              stream, 1, R, nullptr, &m_w2, &m_h[2], s2, H, I, y,
+                                              pv.done[2]);
+  } else {
+    if (any[1] && err == cudaSuccess)
+      err = run_tc<kBnTile, true, WFP8>(m_w1, m_w3, m_x[1], s1, s3, pv.counts, 1, pv.items[1],
+                                        pv.cap[1], I, H, hact, dev_status, stream);
+    if (any[2] && err == cudaSuccess)
+      err = run_tc<kBnWide, true, WFP8>(m_w1, m_w3, m_x[2], s1, s3, pv.counts, 2, pv.items[2],
+                                        pv.cap[2], I, H, hact, dev_status, stream);
+    if (any[1] && err == cudaSuccess)
+      err = run_tc<kBnTile, false, WFP8>(m_w2, m_w2, m_h[1], s2, s2, pv.counts, 1, pv.items[1],
+                                         pv.cap[1], H, I, y, dev_status, stream);
+    if (any[2] && err == cudaSuccess)
+      err = run_tc<kBnWide, false, WFP8>(m_w2, m_w2, m_h[2], s2, s2, pv.counts, 2, pv.items[2],
+                                         pv.cap[2], H, I, y, dev_status, stream);
+  }
   if (any[0] && err == cudaSuccess)
     err = run_tc<kBnSkinny, false, WFP8>(m_w2, m_w2, m_h[0], s2, s2, pv.counts, 0, pv.items[0],
                                          pv.cap[0], H, I, y, dev_status, stream, ks2, R,
                                          splitk_buf);
-  if (any[1] && err == cudaSuccess)
-    err = run_tc<kBnTile, false, WFP8>(m_w2, m_w2, m_h[1], s2, s2, pv.counts, 1, pv.items[1],
-                                       pv.cap[1], H, I, y, dev_status, stream);
-  if (any[2] && err == cudaSuccess)
-    err = run_tc<kBnWide, false, WFP8>(m_w2, m_w2, m_h[2], s2, s2, pv.counts, 2, pv.items[2],
-                                       pv.cap[2], H, I, y, dev_status, stream);
+
   return err;
 }
 
@@ -785,12 +901,7 @@ cudaError_t run_simt(bool fp8, const void* act, const void* wa, const void* wb, 
 
 }  // namespace
 
-size_t grouped_gemm_scratch_bytes(int R, int E_blocks) {
-  size_t b = 256;
-  for (int l = 0; l < kLists; ++l)
-    b += moe_align_up((size_t)(moe_cdiv(R, list_bn(l)) + E_blocks) * sizeof(int4), 256);
-  return b;
-}
+size_t grouped_gemm_scratch_bytes(int R, int E_blocks) { return plan_bytes(R, E_blocks); }
 
 size_t grouped_gemm_splitk_bytes(int R, int H, int I) {
   const size_t w = (size_t)(2 * I > H ? 2 * I : H);
@@ -816,8 +927,7 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
   const bool fp8 = wdtype == MOE_W_FP8E4M3_B128;
   const bool simt = dispatch == MOE_DISPATCH_SIMT;
   PlanView pv = plan_view(scratch, R, E_blocks);
-  PlanOut po;
-  for (int l = 0; l < kLists; ++l) po.items[l] = pv.items[l];
+  PlanOut po = plan_out(pv);
   cudaError_t err = cudaSuccess;
   if (!plan_ready)
     err = moe_launch(gemm_plan_kernel, dim3(1), dim3(1024), 0, stream, 1, offsets, E_blocks, R,

@@ -20,8 +20,19 @@ constexpr int kSchedBase = 8;
 struct PlanView {
   int32_t* counts;          // items per list
   int4* items[kLists];      // {block, first row, rows, 0}
+  int32_t* done[kLists];    // per item: finished G1 epilogue warps (fused launch)
   int cap[kLists];
 };
+
+// bytes of the plan for R rows in E_blocks blocks (the layout plan_view reads)
+inline size_t plan_bytes(int R, int E_blocks) {
+  size_t b = 256;
+  for (int l = 0; l < kLists; ++l) {
+    const size_t cap = (size_t)moe_cdiv(R, list_bn(l)) + E_blocks;
+    b += moe_align_up(cap * sizeof(int4), 256) + moe_align_up(cap * sizeof(int32_t), 256);
+  }
+  return b;
+}
 
 inline PlanView plan_view(void* scratch, int R, int E_blocks) {
   PlanView v;
@@ -32,13 +43,25 @@ inline PlanView plan_view(void* scratch, int R, int E_blocks) {
     v.cap[l] = moe_cdiv(R, list_bn(l)) + E_blocks;
     v.items[l] = reinterpret_cast<int4*>(p + off);
     off += moe_align_up((size_t)v.cap[l] * sizeof(int4), 256);
+    v.done[l] = reinterpret_cast<int32_t*>(p + off);
+    off += moe_align_up((size_t)v.cap[l] * sizeof(int32_t), 256);
   }
   return v;
 }
 
 struct PlanOut {
   int4* items[kLists];
+  int32_t* done[kLists];
 };
+
+inline PlanOut plan_out(const PlanView& v) {
+  PlanOut o;
+  for (int l = 0; l < kLists; ++l) {
+    o.items[l] = v.items[l];
+    o.done[l] = v.done[l];
+  }
+  return o;
+}
 
 // Plan for E_blocks blocks by one CTA of NT threads (NT a multiple of 32, at
 // most 1024).  offsets == nullptr: a single block [0, R).
@@ -100,8 +123,10 @@ MOE_DEVICE void plan_experts(const int32_t* offsets, int E_blocks, int R, int m_
     if (list >= 0) {
       const int bn = list_bn(list);
       const int pos = carry[list] + wsum[list][warp] + incl[list] - n[list];
-      for (int i = 0; i < n[list]; ++i)
+      for (int i = 0; i < n[list]; ++i) {
         out.items[list][pos + i] = make_int4(e, lo + i * bn, min(bn, m - i * bn), 0);
+        out.done[list][pos + i] = 0;
+      }
     }
     if (block_variant && e < E_blocks) block_variant[e] = v;
     __syncthreads();

@@ -120,9 +120,9 @@ route_decode_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict
 template <int NPL>
 cudaError_t launch_npl(const RouteDecodeArgs& a, cudaStream_t stream) {
   const size_t smem = ((size_t)(kWarps + 1) * a.E + 1 + (size_t)a.T * a.K) * sizeof(int32_t);
-  PlanOut po;
-  for (int l = 0; l < kLists; ++l) po.items[l] = plan_view(a.gemm_scratch, a.T * a.K, a.E).items[l];
-  int32_t* counts = plan_view(a.gemm_scratch, a.T * a.K, a.E).counts;
+  const PlanView pv = plan_view(a.gemm_scratch, a.T * a.K, a.E);
+  PlanOut po = plan_out(pv);
+  int32_t* counts = pv.counts;
   const int m_skinny = a.m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : a.m_skinny;
 #define MOE_RD_LAUNCH(KT)                                                                      \
   return moe_launch(route_decode_kernel<NPL, (KT < NPL ? KT : NPL)>, dim3(a.G), dim3(kThreads), \

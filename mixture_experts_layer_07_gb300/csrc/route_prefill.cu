@@ -94,21 +94,32 @@ route_prefill_kernel(const float* __restrict__ logits, int ld, const float* __re
   // lanes share an expert, each summing a contiguous run of chunks; a shuffle
   // scan over the tpe lanes joins the runs.
   int tpe = 1;
-  while (tpe < 32 && tpe * 2 * E <= kThreads) tpe *= 2;
+  while (tpe < 32 && tpe * E < kThreads) tpe *= 2;
   const int per_pass = kThreads / tpe;
   const int seg = moe_cdiv(nchunks, tpe);
   const int sub = tid % tpe;
+  constexpr int kV = 8;  // chunk counts a thread keeps in registers
   for (int e0 = 0; e0 < E; e0 += per_pass) {
     const int e = e0 + tid / tpe;
     const bool on = e < E;
     const int c_lo = min(nchunks, sub * seg), c_hi = min(nchunks, c_lo + seg);
+    int32_t v[kV];
     int32_t run = 0;
-    for (int cb = c_lo; cb < c_hi; cb += 8) {
-      int32_t v[8];
+    if (seg <= kV) {
+      // one round trip: the thread's whole run of chunks in flight at once
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = (on && cb + j < c_hi) ? __ldcg(counts + (size_t)(cb + j) * E + e) : 0;
+      for (int j = 0; j < kV; ++j)
+        v[j] = (on && c_lo + j < c_hi) ? __ldcg(counts + (size_t)(c_lo + j) * E + e) : 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) run += v[j];
+      for (int j = 0; j < kV; ++j) run += v[j];
+    } else {
+      for (int cb = c_lo; cb < c_hi; cb += kV) {
+#pragma unroll
+        for (int j = 0; j < kV; ++j)
+          v[j] = (on && cb + j < c_hi) ? __ldcg(counts + (size_t)(cb + j) * E + e) : 0;
+#pragma unroll
+        for (int j = 0; j < kV; ++j) run += v[j];
+      }
     }
     // exclusive scan of the runs over the expert's tpe lanes
     int32_t incl = run;
@@ -118,14 +129,22 @@ route_prefill_kernel(const float* __restrict__ logits, int ld, const float* __re
     }
     int32_t base = incl - run;
     if (on && sub == tpe - 1) tot_s[e] = incl;
-    for (int cb = c_lo; cb < c_hi; cb += 8) {
-      int32_t v[8];
+    if (seg <= kV) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = (on && cb + j < c_hi) ? __ldcg(counts + (size_t)(cb + j) * E + e) : 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (on && cb + j < c_hi) counts[(size_t)(cb + j) * E + e] = base;
+      for (int j = 0; j < kV; ++j) {
+        if (on && c_lo + j < c_hi) counts[(size_t)(c_lo + j) * E + e] = base;
         base += v[j];
+      }
+    } else {
+      for (int cb = c_lo; cb < c_hi; cb += kV) {
+#pragma unroll
+        for (int j = 0; j < kV; ++j)
+          v[j] = (on && cb + j < c_hi) ? __ldcg(counts + (size_t)(cb + j) * E + e) : 0;
+#pragma unroll
+        for (int j = 0; j < kV; ++j) {
+          if (on && cb + j < c_hi) counts[(size_t)(cb + j) * E + e] = base;
+          base += v[j];
+        }
       }
     }
   }
@@ -227,8 +246,7 @@ template <int NPL>
 cudaError_t launch_npl(const RoutePrefillArgs& a, int tpc, int nchunks, cudaStream_t stream) {
   const size_t smem = prefill_smem(tpc, a.E, a.K);
   PlanView pv = plan_view(a.gemm_scratch, a.T * a.K, a.E);
-  PlanOut po;
-  for (int l = 0; l < kLists; ++l) po.items[l] = pv.items[l];
+  PlanOut po = plan_out(pv);
   const int m_skinny = a.m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : a.m_skinny;
 #define MOE_RP_LAUNCH(KT)                                                                       \
   do {                                                                                          \
