@@ -165,25 +165,26 @@ MOE_DEVICE uint32_t e4m3x2_to_bf16x2(uint32_t two, float sc) {
 // nblk x 8 and fences the generic-proxy writes for its TMA reads.  So the
 // CTAs that finish G1 early start G2 work instead of idling, and the launch
 // boundary between the two disappears.
+// The kernel body for one work list, run by CTAs cta = 0..ncta-1 of a group
+// (the whole grid, or one of the two groups of the two-list launch below).
 template <int BN, bool SWIGLU, bool WFP8, bool FUSED>
-__global__ void __launch_bounds__(TcCfg<BN, SWIGLU, WFP8>::kThreads, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wb,
-               const __grid_constant__ CUtensorMap tm_act, const float* __restrict__ sa,
-               const float* __restrict__ sb, int32_t* __restrict__ counts, int list,
-               const int4* __restrict__ items, int N, int Kdim, __nv_bfloat16* __restrict__ out,
-               int ksplit, int R, float* __restrict__ part, int32_t* dev_status,
-               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_h,
-               const float* __restrict__ s2, int N2, int K2, __nv_bfloat16* __restrict__ out2,
-               int32_t* __restrict__ done) {
+MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
+                             const CUtensorMap& tm_act, const float* __restrict__ sa,
+                             const float* __restrict__ sb, int32_t* __restrict__ counts, int list,
+                             const int4* __restrict__ items, int N, int Kdim,
+                             __nv_bfloat16* __restrict__ out, int ksplit, int R,
+                             float* __restrict__ part, int32_t* dev_status,
+                             const CUtensorMap& tm_w2, const CUtensorMap& tm_h,
+                             const float* __restrict__ s2, int N2, int K2,
+                             __nv_bfloat16* __restrict__ out2, int32_t* __restrict__ done,
+                             const int cta, const int ncta) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
   static_assert(!FUSED || SWIGLU, "the fused launch uses the G1 layout");
-  pdl_wait();
-  pdl_trigger();
   const int nblk = (N + kBM - 1) / kBM;
   const int total1 = counts[list] * nblk * ksplit;
   const int nblk2 = FUSED ? (N2 + kBM - 1) / kBM : 1;
   const int total = FUSED ? total1 + counts[list] * nblk2 : total1;
-  if ((int)blockIdx.x >= total) return;
+  if (cta >= total) return;
   const int nk = (Kdim + kBK - 1) / kBK;
   const int nk2 = FUSED ? (K2 + kBK - 1) / kBK : 0;
   // work unit w -> (item, 128-feature block nb, K slice ks); with ksplit > 1
@@ -306,7 +307,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0, q = 0, qph = 0;
       bool ok = true;
-      int w = blockIdx.x;  // first unit; later ones come from the launch's counter
+      int w = cta;  // first unit; later ones come from the launch's counter
       for (;;) {
         // hand the unit (or the end mark) to the other roles
         if (!mbar_wait_bounded(uq_empty(q), qph ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -347,8 +348,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
         // the next unit: taken once this one's loads are issued, so a CTA that
-        // drew short units takes more (the grid's first units are blockIdx.x)
-        if (ok) w = (int)gridDim.x + atomicAdd(sched, 1);
+        // drew short units takes more (the group's first units are its CTA ids)
+        if (ok) w = ncta + atomicAdd(sched, 1);
       }
       // every copy this thread started has landed before the CTA moves on
       for (int s = 0; s < C::kStages; ++s)
@@ -576,6 +577,68 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
   }
 }
 
+template <int BN, bool SWIGLU, bool WFP8, bool FUSED>
+__global__ void __launch_bounds__(TcCfg<BN, SWIGLU, WFP8>::kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wb,
+               const __grid_constant__ CUtensorMap tm_act, const float* __restrict__ sa,
+               const float* __restrict__ sb, int32_t* __restrict__ counts, int list,
+               const int4* __restrict__ items, int N, int Kdim, __nv_bfloat16* __restrict__ out,
+               int ksplit, int R, float* __restrict__ part, int32_t* dev_status,
+               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_h,
+               const float* __restrict__ s2, int N2, int K2, __nv_bfloat16* __restrict__ out2,
+               int32_t* __restrict__ done) {
+  pdl_wait();
+  pdl_trigger();
+  gemm_tc_body<BN, SWIGLU, WFP8, FUSED>(tm_wa, tm_wb, tm_act, sa, sb, counts, list, items, N, Kdim,
+                                        out, ksplit, R, part, dev_status, tm_w2, tm_h, s2, N2, K2,
+                                        out2, done, (int)blockIdx.x, (int)gridDim.x);
+}
+
+// The skinny and the tile list in ONE launch: the grid splits into two CTA
+// groups in proportion to each list's work units (read on the device from the
+// plan's counts), each group walking its own list with its
+// own token-tile width and pipeline -- both variants run side by side instead
+// of one launch after the other, each block still on the variant its own
+// m_size chose.
+struct DualMaps {
+  CUtensorMap act[2];  // per list: G1 activations (xp) or, for G2, hact
+  CUtensorMap h[2];    // FUSED: hact per list
+};
+
+template <bool SWIGLU, bool WFP8, bool FUSED>
+__global__ void __launch_bounds__(TcCfg<kBnSkinny, SWIGLU, WFP8>::kThreads, 1)
+gemm_tc_dual_kernel(const __grid_constant__ CUtensorMap tm_wa,
+                    const __grid_constant__ CUtensorMap tm_wb, const __grid_constant__ DualMaps maps,
+                    const float* __restrict__ sa, const float* __restrict__ sb,
+                    int32_t* __restrict__ counts, const int4* __restrict__ items0,
+                    const int4* __restrict__ items1, int N, int Kdim,
+                    __nv_bfloat16* __restrict__ out, int R, int32_t* dev_status,
+                    const __grid_constant__ CUtensorMap tm_w2, const float* __restrict__ s2,
+                    int N2, int K2, __nv_bfloat16* __restrict__ out2,
+                    int32_t* __restrict__ done0, int32_t* __restrict__ done1) {
+  using C0 = TcCfg<kBnSkinny, SWIGLU, WFP8>;
+  using C1 = TcCfg<kBnTile, SWIGLU, WFP8>;
+  static_assert(C0::kThreads == C1::kThreads, "one block size for both groups");
+  pdl_wait();
+  pdl_trigger();
+  // a unit of either list streams the same weight tile, which dominates its
+  // time: split by unit count
+  const long long b0 = counts[0];
+  const long long b1 = counts[1];
+  const int g = (int)gridDim.x;
+  int s0 = b0 + b1 > 0 ? (int)((b0 * g + (b0 + b1) / 2) / (b0 + b1)) : 0;
+  if (b0 > 0 && s0 < 1) s0 = 1;
+  if (b1 > 0 && s0 > g - 1) s0 = g - 1;
+  if ((int)blockIdx.x < s0)
+    gemm_tc_body<kBnSkinny, SWIGLU, WFP8, FUSED>(
+        tm_wa, tm_wb, maps.act[0], sa, sb, counts, 0, items0, N, Kdim, out, 1, R, nullptr,
+        dev_status, tm_w2, maps.h[0], s2, N2, K2, out2, done0, (int)blockIdx.x, s0);
+  else
+    gemm_tc_body<kBnTile, SWIGLU, WFP8, FUSED>(
+        tm_wa, tm_wb, maps.act[1], sa, sb, counts, 1, items1, N, Kdim, out, 1, R, nullptr,
+        dev_status, tm_w2, maps.h[1], s2, N2, K2, out2, done1, (int)blockIdx.x - s0, g - s0);
+}
+
 // ---------------------------------------------------------------- CUDA cores
 // One CTA = one skinny item (<= 16 rows) x 64 output features, 256 threads:
 // thread = feature (tid % 64) x 4 rows (tid / 64).  Weights and activations
@@ -788,6 +851,31 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
                     (const float*)part, ksplit, R, N, static_cast<__nv_bfloat16*>(out));
 }
 
+// Both lists (skinny, tile) in one launch of two CTA groups.  FUSED: each
+// group runs its list's G1 and G2 units (act = xp maps, h = hact maps).
+template <bool SWIGLU, bool WFP8, bool FUSED>
+cudaError_t run_tc_dual(const CUtensorMap& wa, const CUtensorMap& wb, const DualMaps& maps,
+                        const float* sa, const float* sb, const PlanView& pv, int N, int Kdim,
+                        void* out, int R, int32_t* dev_status, cudaStream_t stream,
+                        const CUtensorMap& w2, const float* s2, int N2, int K2, void* out2) {
+  using C0 = TcCfg<kBnSkinny, SWIGLU, WFP8>;
+  using C1 = TcCfg<kBnTile, SWIGLU, WFP8>;
+  const size_t smem = C0::kSmemBytes > C1::kSmemBytes ? C0::kSmemBytes : C1::kSmemBytes;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_dual_kernel<SWIGLU, WFP8, FUSED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = num_sms();
+  return moe_launch(gemm_tc_dual_kernel<SWIGLU, WFP8, FUSED>, dim3(grid), dim3(C0::kThreads), smem,
+                    stream, 1, wa, wb, maps, sa, sb, pv.counts, (const int4*)pv.items[0],
+                    (const int4*)pv.items[1], N, Kdim, static_cast<__nv_bfloat16*>(out), R,
+                    dev_status, w2, s2, N2, K2, static_cast<__nv_bfloat16*>(out2), pv.done[0],
+                    pv.done[1]);
+}
+
 // K slices for the skinny variant.  The persistent grid walks units x slices
 // in waves of one unit per SM, and a wave lasts as long as its longest slice,
 // so the time is about waves(s) x (K steps per slice + a fixed cost per unit
@@ -845,6 +933,25 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
                    !make_act_map(&m_h[l], hact, R, I, list_bn(l))))
       return cudaErrorInvalidValue;
   cudaError_t err = cudaSuccess;
+  if (any[0] && any[1] && !any[2] && ks1 == 1 && ks2 == 1) {
+    // skinny and tile blocks both present: one launch per phase (or one in
+    // all, fused) in which the two lists run side by side
+    DualMaps mx, mh;
+    for (int l = 0; l < 2; ++l) {
+      mx.act[l] = m_x[l];
+      mx.h[l] = m_h[l];
+      mh.act[l] = m_h[l];
+      mh.h[l] = m_h[l];
+    }
+    if (fuse)
+      return run_tc_dual<true, WFP8, true>(m_w1, m_w3, mx, s1, s3, pv, I, H, hact, R, dev_status,
+                                           stream, m_w2, s2, H, I, y);
+    err = run_tc_dual<true, WFP8, false>(m_w1, m_w3, mx, s1, s3, pv, I, H, hact, R, dev_status,
+                                         stream, m_w2, s2, 0, 0, nullptr);
+    if (err != cudaSuccess) return err;
+    return run_tc_dual<false, WFP8, false>(m_w2, m_w2, mh, s2, s2, pv, H, I, y, R, dev_status,
+                                           stream, m_w2, s2, 0, 0, nullptr);
+  }
   // G1 (SwiGLU, N = I, K = H) for every list, then G2 (N = H, K = I)
   if (any[0] && err == cudaSuccess)
     err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x[0], s1, s3, pv.counts, 0, pv.items[0],
