@@ -316,14 +316,19 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
     }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
-  // the permuted activations: each row of x written to its token's K rows
-  e = launch_permute_copy(x, f2r, T, K, H, xp, stream);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // the permuted activations: each row of x written to its token's K rows --
+  // except for small batches on the tensor cores, where G1 copies its few
+  // rows per tile straight from x itself
+  const bool gather = decode && cfg->dispatch != MOE_DISPATCH_SIMT;
+  if (!gather) {
+    e = launch_permute_copy(x, f2r, T, K, H, xp, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
   e = launch_grouped_gemm(xp, offsets, E, R, H, cfg->I, cfg->wdtype, w->w1, w->w3, w->w2, w->s1,
                           w->s3, w->s2, hact, y, cfg->m_skinny, cfg->dispatch, bvar,
                           ws + L.gemm_scratch, dev_status, stream, /*max_rows=*/T,
                           /*plan_ready=*/planned, reinterpret_cast<float*>(ws + L.splitk),
-                          L.total - L.splitk);
+                          L.total - L.splitk, gather ? x : nullptr, gather ? r2f : nullptr, K);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   void* sh_y = nullptr;
   if (cfg->has_shared) {

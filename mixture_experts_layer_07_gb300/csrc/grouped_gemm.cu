@@ -43,6 +43,7 @@
 // FMA, bf16 or e4m3 weights; it is the cross-check of the tensor-core path.
 #include <cuda.h>
 #include <cuda_fp8.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -103,12 +104,16 @@ struct TcCfg {
   static constexpr int kQConsumers = 1 + kEpiWarps + (WFP8 ? 8 : 0);  // MMA thread + warps
   static constexpr int kNumBars =
       2 * kStages + 2 * kAccStages + 1 + 2 * kConvStages + kScaleBufs + 2 * kQ;
-  static constexpr int kBarBytes = kNumBars * 8 + 16 + kScaleBufs * 2 * kMaxScaleCols * 4 + kQ * 4;
+  static constexpr int kBarBytes =
+      kNumBars * 8 + 16 + kScaleBufs * 2 * kMaxScaleCols * 4 + kQ * 4 + BN * 4;
   static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes +
                                        (size_t)kConvStages * kConvBytes + kEpiBytes + kBarBytes;
   static constexpr int kConvThreads = WFP8 ? 256 : 0;  // eight converter warps
   static constexpr int kConvWarp0 = 2 + kEpiWarps;        // first converter warp
-  static constexpr int kThreads = 64 + 32 * kEpiWarps + kConvThreads;
+  // G1 (SwiGLU) only: one more warp that, in gather mode, copies the tile's
+  // rows straight from x (small batches: a few rows per tile)
+  static constexpr int kGatherWarp = kConvWarp0 + kConvThreads / 32;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + kConvThreads + (SWIGLU ? 32 : 0);
   static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
   static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
@@ -118,6 +123,17 @@ struct TcCfg {
 };
 
 MOE_DEVICE float silu_f(float g) { return g / (1.f + __expf(-g)); }
+
+// 16-byte cp.async (L2 only); src_bytes = 0 writes zeros and reads nothing
+MOE_DEVICE void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+MOE_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+MOE_DEVICE void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // generic-proxy global writes (made visible to this thread) -> later TMA reads
 MOE_DEVICE void fence_proxy_async_global() {
@@ -177,9 +193,15 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
                              const CUtensorMap& tm_w2, const CUtensorMap& tm_h,
                              const float* __restrict__ s2, int N2, int K2,
                              __nv_bfloat16* __restrict__ out2, int32_t* __restrict__ done,
-                             const int cta, const int ncta) {
+                             const __nv_bfloat16* __restrict__ gx,
+                             const int32_t* __restrict__ grows, int gk, const int cta,
+                             const int ncta) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
   static_assert(!FUSED || SWIGLU, "the fused launch uses the G1 layout");
+  // gather mode (G1, small batches): the gather warp copies each tile's rows
+  // from x -- row r of the expert-ordered layout is token grows[r] / gk -- so
+  // the permuted copy of the activations is not needed
+  const bool gat = SWIGLU && !FUSED && gx != nullptr;
   const int nblk = (N + kBM - 1) / kBM;
   const int total1 = counts[list] * nblk * ksplit;
   const int nblk2 = FUSED ? (N2 + kBM - 1) / kBM : 1;
@@ -242,11 +264,17 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* scale_rows = reinterpret_cast<float*>(tmem_slot + 4);  // FP8: [3][2][kMaxScaleCols]
   volatile int32_t* uq = reinterpret_cast<volatile int32_t*>(scale_rows + C::kScaleBufs * 2 * C::kMaxScaleCols);
+  int32_t* tok_s = const_cast<int32_t*>(uq + C::kQ);  // gather mode: token of each tile row
   int32_t* sched = counts + kSchedBase + 2 * list + (SWIGLU ? 0 : 1);
 
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    // gather mode: a stage is full after the weight bytes (expect_tx) and the
+    // gather warp's arrival once its row copies have landed
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full_bar(s), gat ? 2 : 1);
+      mbar_init(empty_bar(s), 1);
+    }
     for (int a = 0; a < C::kAccStages; ++a) {
       mbar_init(acc_full(a), 1);
       mbar_init(acc_empty(a), 32 * C::kEpiWarps);
@@ -259,7 +287,7 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
     for (int b = 0; b < C::kScaleBufs; ++b) mbar_init(scale_bar(b), C::kConvThreads);
     for (int q = 0; q < C::kQ; ++q) {
       mbar_init(uq_full(q), 1);
-      mbar_init(uq_empty(q), C::kQConsumers);
+      mbar_init(uq_empty(q), C::kQConsumers + (gat ? 1 : 0));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -267,7 +295,7 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_wa);
     if (SWIGLU) prefetch_tmap(&tm_wb);
-    prefetch_tmap(&tm_act);
+    if (!gat) prefetch_tmap(&tm_act);
     if (FUSED) {
       prefetch_tmap(&tm_w2);
       prefetch_tmap(&tm_h);
@@ -339,10 +367,10 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
             break;
           }
           const uint32_t st = sbase + stage * C::kStageBytes;
-          mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
+          mbar_arrive_expect_tx(full_bar(stage), gat ? C::kNA * kWeightBytes : stage_bytes);
           tma_load_3d(st, wmap, full_bar(stage), kb * kBK, nb * kBM, it.x);
           if (u.g1) tma_load_3d(st + kWeightBytes, &tm_wb, full_bar(stage), kb * kBK, nb * kBM, it.x);
-          tma_load_2d(st + C::kNA * kWeightBytes, amap, full_bar(stage), kb * kBK, it.y);
+          if (!gat) tma_load_2d(st + C::kNA * kWeightBytes, amap, full_bar(stage), kb * kBK, it.y);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -490,7 +518,68 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
         if (lane == 0) atomicAdd(done + un.idx, 1);
       }
     }
-  } else if (WFP8) {
+  } else if (SWIGLU && warp == C::kGatherWarp) {
+    if (gat) {
+      // ---------------- activation rows from x (gather mode)
+      // 16-byte cp.async into the 128-byte-swizzled layout the MMA reads
+      // (chunk c of row r at chunk c ^ (r % 8), as a swizzled TMA box would
+      // land), only the unit's m valid rows (the rest of the tile only feeds
+      // token columns the epilogue never stores).  A stage's copies are known
+      // complete kLag stages later (cp.async.wait_group); then every lane
+      // fences them for the tensor core and lane 0 arrives on the stage.
+      constexpr int kLag = C::kStages - 1;
+      int stage = 0, issued = 0;
+      uint32_t phase = 0, q = 0, qph = 0;
+      bool ok = true;
+      for (;;) {
+        const int w = pop_unit(q, qph, false);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(uq_empty((q + C::kQ - 1) % C::kQ));
+        if (w < 0) fail();
+        if (w < 0 || w >= total || !ok) break;
+        const Unit u = unit_of(w);
+        const int4 it = u.it;
+        const int m = it.z < BN ? it.z : BN;
+        __syncwarp();
+        for (int r = lane; r < m; r += 32) tok_s[r] = __ldg(grows + it.y + r) / gk;
+        __syncwarp();
+        for (int kb = u.kb_lo; kb < u.kb_hi; ++kb) {
+          int good = 1;
+          if (lane == 0)
+            good = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs);
+          if (!__shfl_sync(0xffffffffu, good, 0)) {
+            if (lane == 0) fail();
+            ok = false;
+            break;
+          }
+          const uint32_t sx = sbase + stage * C::kStageBytes + C::kNA * kWeightBytes;
+          for (int i = lane; i < m * 8; i += 32) {
+            const int r = i >> 3, ch = i & 7;
+            const int k0 = kb * kBK + ch * 8;
+            const int nbytes = k0 < Kdim ? 16 : 0;
+            cp_async_16(sx + r * 128 + ((ch ^ (r & 7)) << 4),
+                        gx + (size_t)tok_s[r] * Kdim + (nbytes ? k0 : 0), nbytes);
+          }
+          cp_async_commit();
+          if (++issued > kLag) {
+            cp_async_wait<kLag>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar((stage + C::kStages - kLag) % C::kStages));
+          }
+          if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // the newest stages are still owed their arrival (also after a failure,
+      // so that warp 0 can drain its weight copies)
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0)
+        for (int j = issued < kLag ? issued : kLag; j > 0; --j)
+          mbar_arrive(full_bar((stage + C::kStages - j) % C::kStages));
+    }
+  } else if (WFP8 && warp < C::kConvWarp0 + C::kConvThreads / 32) {
     // ---------------- e4m3 -> bf16 converters, warps 10..17
     // At the start of each work unit the converters stage that unit's row of
     // block scales (one per 128-wide K block) in shared memory, so the
@@ -586,12 +675,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
                int ksplit, int R, float* __restrict__ part, int32_t* dev_status,
                const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_h,
                const float* __restrict__ s2, int N2, int K2, __nv_bfloat16* __restrict__ out2,
-               int32_t* __restrict__ done) {
+               int32_t* __restrict__ done, const __nv_bfloat16* __restrict__ gx,
+               const int32_t* __restrict__ grows, int gk) {
   pdl_wait();
   pdl_trigger();
   gemm_tc_body<BN, SWIGLU, WFP8, FUSED>(tm_wa, tm_wb, tm_act, sa, sb, counts, list, items, N, Kdim,
                                         out, ksplit, R, part, dev_status, tm_w2, tm_h, s2, N2, K2,
-                                        out2, done, (int)blockIdx.x, (int)gridDim.x);
+                                        out2, done, gx, grows, gk, (int)blockIdx.x,
+                                        (int)gridDim.x);
 }
 
 // The skinny and the tile list in ONE launch: the grid splits into two CTA
@@ -615,7 +706,9 @@ gemm_tc_dual_kernel(const __grid_constant__ CUtensorMap tm_wa,
                     __nv_bfloat16* __restrict__ out, int R, int32_t* dev_status,
                     const __grid_constant__ CUtensorMap tm_w2, const float* __restrict__ s2,
                     int N2, int K2, __nv_bfloat16* __restrict__ out2,
-                    int32_t* __restrict__ done0, int32_t* __restrict__ done1) {
+                    int32_t* __restrict__ done0, int32_t* __restrict__ done1,
+                    const __nv_bfloat16* __restrict__ gx, const int32_t* __restrict__ grows,
+                    int gk) {
   using C0 = TcCfg<kBnSkinny, SWIGLU, WFP8>;
   using C1 = TcCfg<kBnTile, SWIGLU, WFP8>;
   static_assert(C0::kThreads == C1::kThreads, "one block size for both groups");
@@ -632,11 +725,13 @@ gemm_tc_dual_kernel(const __grid_constant__ CUtensorMap tm_wa,
   if ((int)blockIdx.x < s0)
     gemm_tc_body<kBnSkinny, SWIGLU, WFP8, FUSED>(
         tm_wa, tm_wb, maps.act[0], sa, sb, counts, 0, items0, N, Kdim, out, 1, R, nullptr,
-        dev_status, tm_w2, maps.h[0], s2, N2, K2, out2, done0, (int)blockIdx.x, s0);
+        dev_status, tm_w2, maps.h[0], s2, N2, K2, out2, done0, gx, grows, gk, (int)blockIdx.x,
+        s0);
   else
     gemm_tc_body<kBnTile, SWIGLU, WFP8, FUSED>(
         tm_wa, tm_wb, maps.act[1], sa, sb, counts, 1, items1, N, Kdim, out, 1, R, nullptr,
-        dev_status, tm_w2, maps.h[1], s2, N2, K2, out2, done1, (int)blockIdx.x - s0, g - s0);
+        dev_status, tm_w2, maps.h[1], s2, N2, K2, out2, done1, gx, grows, gk,
+        (int)blockIdx.x - s0, g - s0);
 }
 
 // ---------------------------------------------------------------- CUDA cores
@@ -825,7 +920,8 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
                    cudaStream_t stream, int ksplit = 1, int R = 0, float* part = nullptr,
                    const CUtensorMap* w2 = nullptr, const CUtensorMap* h = nullptr,
                    const float* s2 = nullptr, int N2 = 0, int K2 = 0, void* out2 = nullptr,
-                   int32_t* done = nullptr) {
+                   int32_t* done = nullptr, const void* gx = nullptr,
+                   const int32_t* grows = nullptr, int gk = 0) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
   static bool attr_set = false;  // per process; the attribute is per function, all devices
   if (!attr_set) {
@@ -843,7 +939,8 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
                              dim3(C::kThreads), C::kSmemBytes, stream, 1, wa, wb, act, sa, sb,
                              counts, list, items, N, Kdim, static_cast<__nv_bfloat16*>(out),
                              ksplit, R, part, dev_status, FUSED ? *w2 : wa, FUSED ? *h : act, s2,
-                             N2, K2, static_cast<__nv_bfloat16*>(out2), done);
+                             N2, K2, static_cast<__nv_bfloat16*>(out2), done,
+                             static_cast<const __nv_bfloat16*>(gx), grows, gk);
   if (e != cudaSuccess || ksplit <= 1) return e;
   const long long n = (long long)R * (N / 4);
   const int fgrid = (int)((n + 255) / 256 < 4 * num_sms() ? (n + 255) / 256 : 4 * num_sms());
@@ -857,7 +954,8 @@ template <bool SWIGLU, bool WFP8, bool FUSED>
 cudaError_t run_tc_dual(const CUtensorMap& wa, const CUtensorMap& wb, const DualMaps& maps,
                         const float* sa, const float* sb, const PlanView& pv, int N, int Kdim,
                         void* out, int R, int32_t* dev_status, cudaStream_t stream,
-                        const CUtensorMap& w2, const float* s2, int N2, int K2, void* out2) {
+                        const CUtensorMap& w2, const float* s2, int N2, int K2, void* out2,
+                        const void* gx = nullptr, const int32_t* grows = nullptr, int gk = 0) {
   using C0 = TcCfg<kBnSkinny, SWIGLU, WFP8>;
   using C1 = TcCfg<kBnTile, SWIGLU, WFP8>;
   const size_t smem = C0::kSmemBytes > C1::kSmemBytes ? C0::kSmemBytes : C1::kSmemBytes;
@@ -873,7 +971,7 @@ cudaError_t run_tc_dual(const CUtensorMap& wa, const CUtensorMap& wb, const Dual
                     stream, 1, wa, wb, maps, sa, sb, pv.counts, (const int4*)pv.items[0],
                     (const int4*)pv.items[1], N, Kdim, static_cast<__nv_bfloat16*>(out), R,
                     dev_status, w2, s2, N2, K2, static_cast<__nv_bfloat16*>(out2), pv.done[0],
-                    pv.done[1]);
+                    pv.done[1], static_cast<const __nv_bfloat16*>(gx), grows, gk);
 }
 
 // K slices for the skinny variant.  The persistent grid walks units x slices
@@ -902,7 +1000,8 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
                        const void* w3, const void* w2, const float* s1, const float* s3,
                        const float* s2, void* hact, void* y, const PlanView& pv,
                        int32_t* dev_status, cudaStream_t stream, const bool (&any)[kLists],
-                       float* splitk_buf, size_t splitk_bytes) {
+                       float* splitk_buf, size_t splitk_bytes, const void* gx,
+                       const int32_t* grows, int gk) {
   // split-K only when every block is skinny (all rows then belong to skinny
   // items, which the finalize kernel rewrites) and the buffer holds the slices
   int ks1 = 1, ks2 = 1;
@@ -922,14 +1021,15 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
   // (Measured: qwen3-30b-a3b shape T=256 264 -> 254 us and gpt-oss-20b shape
   // T=512 427 -> 415 us fused; the H = 4 I shared-gate shape at T=1024 went
   // 630 -> 655 us fused.)
-  const bool fuse = (long long)R <= 64LL * E_blocks && H <= 3 * I;
+  const bool fuse = (long long)R <= 64LL * E_blocks && H <= 3 * I && !gx;
   CUtensorMap m_w1, m_w3, m_w2, m_x[kLists], m_h[kLists];
+  memset(m_x, 0, sizeof(m_x));  // gather mode: G1 reads x rows itself, no activation map
   if (!make_weight_map(&m_w1, w1, E_blocks, I, H, WFP8) ||
       !make_weight_map(&m_w3, w3, E_blocks, I, H, WFP8) ||
       !make_weight_map(&m_w2, w2, E_blocks, H, I, WFP8))
     return cudaErrorInvalidValue;
   for (int l = 0; l < kLists; ++l)
-    if (any[l] && (!make_act_map(&m_x[l], xp, R, H, list_bn(l)) ||
+    if (any[l] && ((!gx && !make_act_map(&m_x[l], xp, R, H, list_bn(l))) ||
                    !make_act_map(&m_h[l], hact, R, I, list_bn(l))))
       return cudaErrorInvalidValue;
   cudaError_t err = cudaSuccess;
@@ -947,7 +1047,7 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
       return run_tc_dual<true, WFP8, true>(m_w1, m_w3, mx, s1, s3, pv, I, H, hact, R, dev_status,
                                            stream, m_w2, s2, H, I, y);
     err = run_tc_dual<true, WFP8, false>(m_w1, m_w3, mx, s1, s3, pv, I, H, hact, R, dev_status,
-                                         stream, m_w2, s2, 0, 0, nullptr);
+                                         stream, m_w2, s2, 0, 0, nullptr, gx, grows, gk);
     if (err != cudaSuccess) return err;
     return run_tc_dual<false, WFP8, false>(m_w2, m_w2, mh, s2, s2, pv, H, I, y, R, dev_status,
                                            stream, m_w2, s2, 0, 0, nullptr);
@@ -956,7 +1056,8 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
   if (any[0] && err == cudaSuccess)
     err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x[0], s1, s3, pv.counts, 0, pv.items[0],
                                         pv.cap[0], I, H, hact, dev_status, stream, ks1, R,
-                                        splitk_buf);
+                                        splitk_buf, nullptr, nullptr, nullptr, 0, 0, nullptr,
+                                        nullptr, gx, grows, gk);
   if (fuse) {
     // tile and wide lists: G1 and G2 in one persistent launch each
     if (any[1] && err == cudaSuccess)
@@ -972,10 +1073,14 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
   } else {
     if (any[1] && err == cudaSuccess)
       err = run_tc<kBnTile, true, WFP8>(m_w1, m_w3, m_x[1], s1, s3, pv.counts, 1, pv.items[1],
-                                        pv.cap[1], I, H, hact, dev_status, stream);
+                                        pv.cap[1], I, H, hact, dev_status, stream, 1, R, nullptr,
+                                        nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, gx,
+                                        grows, gk);
     if (any[2] && err == cudaSuccess)
       err = run_tc<kBnWide, true, WFP8>(m_w1, m_w3, m_x[2], s1, s3, pv.counts, 2, pv.items[2],
-                                        pv.cap[2], I, H, hact, dev_status, stream);
+                                        pv.cap[2], I, H, hact, dev_status, stream, 1, R, nullptr,
+                                        nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, gx,
+                                        grows, gk);
     if (any[1] && err == cudaSuccess)
       err = run_tc<kBnTile, false, WFP8>(m_w2, m_w2, m_h[1], s2, s2, pv.counts, 1, pv.items[1],
                                          pv.cap[1], H, I, y, dev_status, stream);
@@ -1029,7 +1134,8 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 const float* s2, void* hact, void* y, int m_skinny,
                                 int dispatch, int32_t* block_variant, void* scratch,
                                 int32_t* dev_status, cudaStream_t stream, int max_rows,
-                                bool plan_ready, float* splitk_buf, size_t splitk_bytes) {
+                                bool plan_ready, float* splitk_buf, size_t splitk_bytes,
+                                const void* gather_x, const int32_t* gather_rows, int gather_k) {
   if (m_skinny < 0) m_skinny = MOE_DEFAULT_M_SKINNY;
   const bool fp8 = wdtype == MOE_W_FP8E4M3_B128;
   const bool simt = dispatch == MOE_DISPATCH_SIMT;
@@ -1041,6 +1147,7 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                      m_skinny, dispatch, wdtype, pv.counts, po, block_variant);
   if (err != cudaSuccess || R == 0) return err;
 
+  if (simt && gather_x) return cudaErrorInvalidValue;  // the CUDA-core path reads xp only
   if (simt) {
     err = run_simt<true>(fp8, xp, w1, w3, s1, s3, pv.counts, pv.items[0], pv.cap[0], I, H, hact,
                          stream);
@@ -1066,7 +1173,8 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
   }
   if (fp8)
     return run_tc_all<true>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                            stream, any, splitk_buf, splitk_bytes);
+                            stream, any, splitk_buf, splitk_bytes, gather_x, gather_rows,
+                            gather_k);
   return run_tc_all<false>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                           stream, any, splitk_buf, splitk_bytes);
+                           stream, any, splitk_buf, splitk_bytes, gather_x, gather_rows, gather_k);
 }

@@ -37,7 +37,8 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 int dispatch, int32_t* block_variant, void* scratch,
                                 int32_t* dev_status, cudaStream_t stream, int max_rows = -1,
                                 bool plan_ready = false, float* splitk_buf = nullptr,
-                                size_t splitk_bytes = 0);
+                                size_t splitk_bytes = 0, const void* gather_x = nullptr,
+                                const int32_t* gather_rows = nullptr, int gather_k = 0);
 // fp32 bytes for split-K slices of the skinny variant in moe_layer's decode
 // regime (at most 4 slices of R x max(2I, H) partial sums)
 size_t grouped_gemm_splitk_bytes(int R, int H, int I);
