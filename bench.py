@@ -154,7 +154,8 @@ def tensors_of(spec, d):
 def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=152):
     """Kernel launches inside one moe_layer call, mirroring the library's
     launch sequence.
-      T <= 32: one fused routing launch (router, top-K, permute, GEMM plan)
+      T <= 32: one fused routing launch (router, top-K, permute, GEMM plan);
+               G1 copies its rows from x itself
                + the permute copy
       T > 32:  router 1 (2 from T >= 64: weight split + tensor-core GEMM),
                fused routing 1 (top-K, chunk histograms, and in its last CTA
@@ -180,23 +181,24 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
                 best, best_cost = s, cost
         return best
 
-    def gemm(max_rows, rows, blocks, with_plan, splittable, inter):
+    def gemm(max_rows, rows, blocks, with_plan, splittable, inter, gather=False):
         n = 1 if with_plan else 0
         if dispatch == 2:
             return n + 2
         tile = max_rows > m_skinny
         wide = spec.wdtype == "fp8" and tile and max_rows >= wide_min
         # tile and wide lists: one G1+G2 launch each (mean rows <= 64, H <= 3 I)
-        fused = rows <= 64 * blocks and spec.H <= 3 * inter
-        n += 2 + (tile + wide) * (1 if fused else 2)
+        fused = rows <= 64 * blocks and spec.H <= 3 * inter and not gather
         if splittable and not tile:
-            b = min(rows, blocks)
-            n += (ksplit(b * -(-inter // 128), spec.H) > 1) + (ksplit(b * -(-spec.H // 128), inter) > 1)
+            return n + 2  # small batch, all blocks skinny: G1, G2 (K slices reduced in-kernel)
+        if tile and not wide:
+            return n + (1 if fused else 2)  # both lists side by side in each launch
+        n += 2 + (tile + wide) * (1 if fused else 2)
         return n
 
     if T <= 32:
-        route = 2
-        g = gemm(T, R, spec.E, with_plan=False, splittable=True, inter=spec.I)
+        route = 1  # G1 reads its rows from x: no permuted copy
+        g = gemm(T, R, spec.E, with_plan=False, splittable=True, inter=spec.I, gather=True)
     else:
         route = (2 if T >= ROUTER_TC_MIN_T else 1) + 3
         g = gemm(T, R, spec.E, with_plan=False, splittable=False, inter=spec.I)

@@ -312,10 +312,11 @@ moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes);
  *   x    [T, H] bf16 input, out [T, H] bf16 output, T <= cfg->T_max
  *   workspace  >= moe_workspace_bytes(cfg), 256-byte aligned; holds every
  *              intermediate (logits, ids, weights, offsets, permuted rows,
- *              expert activations and outputs, plans).  Its 256-byte `sync`
- *              region (moe_workspace_layout) must be zero before the first
- *              call -- e.g. zero the whole workspace once after allocating
- *              it; every call leaves it zero again.
+ *              expert activations and outputs, plans).  Its `sync` region
+ *              (moe_workspace_layout: from `sync` up to `logits`; completion
+ *              counters) must be zero before the first call -- e.g. zero the
+ *              whole workspace once after allocating it; every call leaves it
+ *              zero again.
  * For T <= 32 the router, top-K, permute and the GEMM plan run as one fused
  * launch (the small-batch regime where launch count dominates); the results
  * are the same as those of the separate steps.

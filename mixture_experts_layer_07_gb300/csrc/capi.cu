@@ -48,7 +48,14 @@ void layout_of(const moe_config_t* c, moe_workspace_layout_t* L) {
     off = moe_align_up(off + bytes, 256);
     return o;
   };
-  L->sync = take(256);
+  // zero before the first call, zero again after every call: completion
+  // counters of the fused routing launches (first 256 bytes) and of the
+  // in-kernel reduction of K slices in the small-batch GEMM launch
+  {
+    const int ms0 = c->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : c->m_skinny;
+    const int tsp = c->T_max < ms0 ? c->T_max : ms0;
+    L->sync = take(256 + grouped_gemm_split_counter_bytes(tsp * c->K, c->E, c->H, c->I));
+  }
   L->logits = take(Tm * G * 4);
   L->ids = take(R * 4);
   L->weights = take(R * 4);
@@ -328,7 +335,8 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
                           w->s3, w->s2, hact, y, cfg->m_skinny, cfg->dispatch, bvar,
                           ws + L.gemm_scratch, dev_status, stream, /*max_rows=*/T,
                           /*plan_ready=*/planned, reinterpret_cast<float*>(ws + L.splitk),
-                          L.total - L.splitk, gather ? x : nullptr, gather ? r2f : nullptr, K);
+                          L.total - L.splitk, gather ? x : nullptr, gather ? r2f : nullptr, K,
+                          reinterpret_cast<int32_t*>(ws + L.sync + 256));
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   void* sh_y = nullptr;
   if (cfg->has_shared) {

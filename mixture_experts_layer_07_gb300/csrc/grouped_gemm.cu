@@ -194,36 +194,40 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
                              const float* __restrict__ s2, int N2, int K2,
                              __nv_bfloat16* __restrict__ out2, int32_t* __restrict__ done,
                              const __nv_bfloat16* __restrict__ gx,
-                             const int32_t* __restrict__ grows, int gk, const int cta,
-                             const int ncta) {
+                             const int32_t* __restrict__ grows, int gk, int ksplit2,
+                             float* __restrict__ part2, int32_t* __restrict__ scnt1,
+                             int32_t* __restrict__ scnt2, const int cta, const int ncta) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
   static_assert(!FUSED || SWIGLU, "the fused launch uses the G1 layout");
   // gather mode (G1, small batches): the gather warp copies each tile's rows
   // from x -- row r of the expert-ordered layout is token grows[r] / gk -- so
   // the permuted copy of the activations is not needed
-  const bool gat = SWIGLU && !FUSED && gx != nullptr;
+  const bool gat = SWIGLU && gx != nullptr;
   const int nblk = (N + kBM - 1) / kBM;
   const int total1 = counts[list] * nblk * ksplit;
   const int nblk2 = FUSED ? (N2 + kBM - 1) / kBM : 1;
-  const int total = FUSED ? total1 + counts[list] * nblk2 : total1;
+  const int ks2 = FUSED ? ksplit2 : 1;
+  const int total = FUSED ? total1 + counts[list] * nblk2 * ks2 : total1;
   if (cta >= total) return;
   const int nk = (Kdim + kBK - 1) / kBK;
   const int nk2 = FUSED ? (K2 + kBK - 1) / kBK : 0;
   // work unit w -> (item, 128-feature block nb, K slice ks); with ksplit > 1
   // each slice writes fp32 partial sums to part[ks][row][feature] instead of
-  // the finished output (a finalize kernel reduces the slices in order).
-  // FUSED: units total1.. are the G2 units (no K slices).
+  // the finished output, and the last slice to finish (counted in scnt)
+  // reduces the slices in order (or, without scnt, a finalize kernel does).
+  // FUSED: units total1.. are the G2 units (ksplit2 slices, partials in part2).
   const int kbs = (nk + ksplit - 1) / ksplit;
+  const int kbs2 = FUSED ? (nk2 + ks2 - 1) / ks2 : 1;
   struct Unit { int4 it; int nb, kb_lo, kb_hi, ks, idx; bool g1; };
   auto unit_of = [&](int w) {
     Unit u;
     if (FUSED && w >= total1) {
       const int w2 = w - total1;
-      u.idx = w2 / nblk2;
-      u.nb = w2 % nblk2;
-      u.ks = 0;
-      u.kb_lo = 0;
-      u.kb_hi = nk2;
+      u.idx = w2 / (nblk2 * ks2);
+      u.nb = (w2 / ks2) % nblk2;
+      u.ks = w2 % ks2;
+      u.kb_lo = u.ks * kbs2;
+      u.kb_hi = min(nk2, u.kb_lo + kbs2);
       u.g1 = false;
     } else {
       u.idx = w / (nblk * ksplit);
@@ -349,28 +353,61 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
         const Unit u = unit_of(w);
         const int4 it = u.it;
         const int nb = u.nb;
+        int kb0 = u.kb_lo;
         if (FUSED && !u.g1) {
-          // this tile's hact rows: every G1 unit of the tile stored and counted
-          if (!wait_count_geq(done + u.idx, nblk * C::kEpiWarps, abort_flag, kWaitLimitNs)) {
+          // The unit's first weight tiles do not depend on G1: start them into
+          // free stages now (transaction bytes only, no arrival, so a stage
+          // cannot complete early), then wait for this tile's hact rows --
+          // every G1 unit of the tile stored and counted -- and add the
+          // activation tiles with the arrival.
+          int npre = 0;
+          uint32_t pre_par = 0;
+          for (int kb = u.kb_lo; kb < u.kb_hi && npre < C::kStages; ++kb, ++npre) {
+            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+              fail();
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(full_bar(stage), kWeightBytes);
+            tma_load_3d(sbase + stage * C::kStageBytes, &tm_w2, full_bar(stage), kb * kBK, nb * kBM,
+                        it.x);
+            pre_par |= phase << npre;
+            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+          }
+          if (ok && !wait_count_geq(done + u.idx, nblk * C::kEpiWarps, abort_flag, kWaitLimitNs)) {
             fail();
             ok = false;
           }
           fence_proxy_async_global();
+          for (int i = 0; i < npre; ++i) {
+            const int s_i = (stage + C::kStages - npre + i) % C::kStages;
+            if (ok) {
+              mbar_arrive_expect_tx(full_bar(s_i), C::kBBytes);
+              tma_load_2d(sbase + s_i * C::kStageBytes + C::kNA * kWeightBytes, &tm_h, full_bar(s_i),
+                          (u.kb_lo + i) * kBK, it.y);
+            } else {
+              mbar_arrive(full_bar(s_i));  // the weight bytes alone complete it: drainable
+            }
+            armed |= 1u << s_i;
+            armed_parity = (armed_parity & ~(1u << s_i)) | (((pre_par >> i) & 1u) << s_i);
+          }
+          kb0 = u.kb_lo + npre;
         }
         const CUtensorMap* wmap = (FUSED && !u.g1) ? &tm_w2 : &tm_wa;
         const CUtensorMap* amap = (FUSED && !u.g1) ? &tm_h : &tm_act;
         const uint32_t stage_bytes = u.g1 ? C::kStageBytes : kWeightBytes + C::kBBytes;
-        for (int kb = u.kb_lo; kb < u.kb_hi && ok; ++kb) {
+        for (int kb = kb0; kb < u.kb_hi && ok; ++kb) {
           if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             fail();
             ok = false;
             break;
           }
           const uint32_t st = sbase + stage * C::kStageBytes;
-          mbar_arrive_expect_tx(full_bar(stage), gat ? C::kNA * kWeightBytes : stage_bytes);
+          mbar_arrive_expect_tx(full_bar(stage), gat && u.g1 ? C::kNA * kWeightBytes : stage_bytes);
           tma_load_3d(st, wmap, full_bar(stage), kb * kBK, nb * kBM, it.x);
           if (u.g1) tma_load_3d(st + kWeightBytes, &tm_wb, full_bar(stage), kb * kBK, nb * kBM, it.x);
-          if (!gat) tma_load_2d(st + C::kNA * kWeightBytes, amap, full_bar(stage), kb * kBK, it.y);
+          if (!(gat && u.g1))
+            tma_load_2d(st + C::kNA * kWeightBytes, amap, full_bar(stage), kb * kBK, it.y);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -468,23 +505,26 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
       const bool sw = un.g1;  // SwiGLU of the gate and up accumulators
       const int Nu = sw || !FUSED ? N : N2;
       __nv_bfloat16* outu = sw || !FUSED ? out : out2;
+      const int ksu = sw || !FUSED ? ksplit : ks2;  // K slices of this unit's GEMM
+      float* partu = sw || !FUSED ? part : part2;
+      int32_t* scntu = sw || !FUSED ? scnt1 : scnt2;
       for (int c0 = 16 * half; c0 < BN && c0 < m; c0 += 32) {
         uint32_t g[16], u[16];
         tc_ld_32x32b_x16(tacc + c0, g);
         if (sw) tc_ld_32x32b_x16(tacc + BN + c0, u);
         tc_wait_ld();
-        if (ksplit > 1) {
+        if (ksu > 1) {
           // fp32 partials of this K slice: row-major [ks][R][Npart], Npart = N or 2N
           const int n = nb * kBM + quarter * 32 + lane;
-          const int np = SWIGLU ? 2 * N : N;
-          float* pr = part + ((size_t)un.ks * R + it.y + c0) * np;
+          const int np = sw ? 2 * Nu : Nu;
+          float* pr = partu + ((size_t)un.ks * R + it.y + c0) * np;
           const bool empty = un.kb_lo >= un.kb_hi;  // no K left for this slice
-          if (n < N) {
+          if (n < Nu) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               if (c0 + j < m) {
                 pr[(size_t)j * np + n] = empty ? 0.f : __uint_as_float(g[j]);
-                if (SWIGLU) pr[(size_t)j * np + N + n] = empty ? 0.f : __uint_as_float(u[j]);
+                if (sw) pr[(size_t)j * np + Nu + n] = empty ? 0.f : __uint_as_float(u[j]);
               }
             }
           }
@@ -511,7 +551,50 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
       }
       tc_fence_before();
       mbar_arrive(acc_empty(a));
-      if (FUSED && sw) {
+      if (ksu > 1 && scntu) {
+        // K slices: every epilogue warp of every slice counts itself once its
+        // partials are stored; the last one reduces the unit's slices in slice
+        // order (deterministic) and stores the bf16 rows
+        __threadfence();
+        __syncwarp();
+        int32_t* cnt = scntu + (size_t)un.idx * (sw || !FUSED ? nblk : nblk2) + nb;
+        int old = 0;
+        if (lane == 0) old = atomicAdd(cnt, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old == ksu * C::kEpiWarps - 1) {
+          __threadfence();
+          const int np = sw ? 2 * Nu : Nu;
+          const int n = nb * kBM + lane * 4;
+          for (int r = 0; r < m && n < Nu; ++r) {
+            float4 gs = make_float4(0.f, 0.f, 0.f, 0.f), us = gs;
+            for (int q = 0; q < ksu; ++q) {
+              const float* pr = partu + ((size_t)q * R + it.y + r) * np + n;
+              const float4 a4 = __ldcg(reinterpret_cast<const float4*>(pr));
+              gs.x += a4.x; gs.y += a4.y; gs.z += a4.z; gs.w += a4.w;
+              if (sw) {
+                const float4 b4 = __ldcg(reinterpret_cast<const float4*>(pr + Nu));
+                us.x += b4.x; us.y += b4.y; us.z += b4.z; us.w += b4.w;
+              }
+            }
+            if (sw) {
+              gs.x = silu_f(gs.x) * us.x; gs.y = silu_f(gs.y) * us.y;
+              gs.z = silu_f(gs.z) * us.z; gs.w = silu_f(gs.w) * us.w;
+            }
+            uint2 o;
+            o.x = pack_bf16x2(gs.x, gs.y);
+            o.y = pack_bf16x2(gs.z, gs.w);
+            *reinterpret_cast<uint2*>(outu + (size_t)(it.y + r) * Nu + n) = o;
+          }
+          __syncwarp();
+          if (lane == 0) *cnt = 0;  // ready for the next call
+          if (FUSED && sw) {
+            // the whole 128-feature block of the tile's hact rows is stored
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) atomicAdd(done + un.idx, C::kEpiWarps);
+          }
+        }
+      } else if (FUSED && sw) {
         // this warp's share of the tile's hact rows is stored: count it
         __threadfence();
         __syncwarp();
@@ -525,8 +608,9 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
       // (chunk c of row r at chunk c ^ (r % 8), as a swizzled TMA box would
       // land), only the unit's m valid rows (the rest of the tile only feeds
       // token columns the epilogue never stores).  A stage's copies are known
-      // complete kLag stages later (cp.async.wait_group); then every lane
-      // fences them for the tensor core and lane 0 arrives on the stage.
+      // complete kLag stages later (cp.async.wait_group), or at the end of the
+      // unit; then every lane fences them for the tensor core and lane 0
+      // arrives on the stage.
       constexpr int kLag = C::kStages - 1;
       int stage = 0, issued = 0;
       uint32_t phase = 0, q = 0, qph = 0;
@@ -539,7 +623,9 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
         if (w < 0 || w >= total || !ok) break;
         const Unit u = unit_of(w);
         const int4 it = u.it;
-        const int m = it.z < BN ? it.z : BN;
+        // G2 units of a fused launch bring their rows by TMA: no copies, but
+        // the warp still arrives on their stages
+        const int m = u.g1 ? (it.z < BN ? it.z : BN) : 0;
         __syncwarp();
         for (int r = lane; r < m; r += 32) tok_s[r] = __ldg(grows + it.y + r) / gk;
         __syncwarp();
@@ -566,18 +652,27 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(full_bar((stage + C::kStages - kLag) % C::kStages));
+            --issued;
           }
           if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
         }
+        // settle the unit before waiting for the next one: the next unit may
+        // only be handed out once this one is done (a fused launch's G2 unit
+        // waits for G1 results), so no arrival may stay owed across the wait
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          for (int j = issued; j > 0; --j) mbar_arrive(full_bar((stage + C::kStages - j) % C::kStages));
+        issued = 0;
       }
-      // the newest stages are still owed their arrival (also after a failure,
-      // so that warp 0 can drain its weight copies)
+      // after a failure: the stages still owed their arrival, so that warp 0
+      // can drain its weight copies
       cp_async_wait<0>();
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0)
-        for (int j = issued < kLag ? issued : kLag; j > 0; --j)
-          mbar_arrive(full_bar((stage + C::kStages - j) % C::kStages));
+        for (int j = issued; j > 0; --j) mbar_arrive(full_bar((stage + C::kStages - j) % C::kStages));
     }
   } else if (WFP8 && warp < C::kConvWarp0 + C::kConvThreads / 32) {
     // ---------------- e4m3 -> bf16 converters, warps 10..17
@@ -676,13 +771,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
                const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_h,
                const float* __restrict__ s2, int N2, int K2, __nv_bfloat16* __restrict__ out2,
                int32_t* __restrict__ done, const __nv_bfloat16* __restrict__ gx,
-               const int32_t* __restrict__ grows, int gk) {
+               const int32_t* __restrict__ grows, int gk, int ksplit2,
+               float* __restrict__ part2, int32_t* __restrict__ scnt1,
+               int32_t* __restrict__ scnt2) {
   pdl_wait();
   pdl_trigger();
   gemm_tc_body<BN, SWIGLU, WFP8, FUSED>(tm_wa, tm_wb, tm_act, sa, sb, counts, list, items, N, Kdim,
                                         out, ksplit, R, part, dev_status, tm_w2, tm_h, s2, N2, K2,
-                                        out2, done, gx, grows, gk, (int)blockIdx.x,
-                                        (int)gridDim.x);
+                                        out2, done, gx, grows, gk, ksplit2, part2, scnt1, scnt2,
+                                        (int)blockIdx.x, (int)gridDim.x);
 }
 
 // The skinny and the tile list in ONE launch: the grid splits into two CTA
@@ -725,13 +822,13 @@ gemm_tc_dual_kernel(const __grid_constant__ CUtensorMap tm_wa,
   if ((int)blockIdx.x < s0)
     gemm_tc_body<kBnSkinny, SWIGLU, WFP8, FUSED>(
         tm_wa, tm_wb, maps.act[0], sa, sb, counts, 0, items0, N, Kdim, out, 1, R, nullptr,
-        dev_status, tm_w2, maps.h[0], s2, N2, K2, out2, done0, gx, grows, gk, (int)blockIdx.x,
-        s0);
+        dev_status, tm_w2, maps.h[0], s2, N2, K2, out2, done0, gx, grows, gk, 1, nullptr, nullptr,
+        nullptr, (int)blockIdx.x, s0);
   else
     gemm_tc_body<kBnTile, SWIGLU, WFP8, FUSED>(
         tm_wa, tm_wb, maps.act[1], sa, sb, counts, 1, items1, N, Kdim, out, 1, R, nullptr,
-        dev_status, tm_w2, maps.h[1], s2, N2, K2, out2, done1, gx, grows, gk,
-        (int)blockIdx.x - s0, g - s0);
+        dev_status, tm_w2, maps.h[1], s2, N2, K2, out2, done1, gx, grows, gk, 1, nullptr, nullptr,
+        nullptr, (int)blockIdx.x - s0, g - s0);
 }
 
 // ---------------------------------------------------------------- CUDA cores
@@ -921,7 +1018,8 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
                    const CUtensorMap* w2 = nullptr, const CUtensorMap* h = nullptr,
                    const float* s2 = nullptr, int N2 = 0, int K2 = 0, void* out2 = nullptr,
                    int32_t* done = nullptr, const void* gx = nullptr,
-                   const int32_t* grows = nullptr, int gk = 0) {
+                   const int32_t* grows = nullptr, int gk = 0, int ksplit2 = 1,
+                   float* part2 = nullptr, int32_t* scnt1 = nullptr, int32_t* scnt2 = nullptr) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
   static bool attr_set = false;  // per process; the attribute is per function, all devices
   if (!attr_set) {
@@ -932,7 +1030,7 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
     attr_set = true;
   }
   const long long work =
-      (long long)cap * (moe_cdiv(N, kBM) * ksplit + (FUSED ? moe_cdiv(N2, kBM) : 0));
+      (long long)cap * (moe_cdiv(N, kBM) * ksplit + (FUSED ? moe_cdiv(N2, kBM) * ksplit2 : 0));
   const int grid = (int)(work < num_sms() ? work : num_sms());
   if (grid <= 0) return cudaSuccess;
   cudaError_t e = moe_launch(gemm_tc_kernel<BN, SWIGLU, WFP8, FUSED>, dim3(grid),
@@ -940,8 +1038,11 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
                              counts, list, items, N, Kdim, static_cast<__nv_bfloat16*>(out),
                              ksplit, R, part, dev_status, FUSED ? *w2 : wa, FUSED ? *h : act, s2,
                              N2, K2, static_cast<__nv_bfloat16*>(out2), done,
-                             static_cast<const __nv_bfloat16*>(gx), grows, gk);
-  if (e != cudaSuccess || ksplit <= 1) return e;
+                             static_cast<const __nv_bfloat16*>(gx), grows, gk, ksplit2, part2,
+                             scnt1, scnt2);
+  // K slices are reduced in the kernel by their last slice when counters are
+  // given, else by a finalize launch
+  if (e != cudaSuccess || ksplit <= 1 || scnt1) return e;
   const long long n = (long long)R * (N / 4);
   const int fgrid = (int)((n + 255) / 256 < 4 * num_sms() ? (n + 255) / 256 : 4 * num_sms());
   return moe_launch(splitk_finalize_kernel<SWIGLU>, dim3(fgrid), dim3(256), 0, stream, 1,
@@ -1001,7 +1102,7 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
                        const float* s2, void* hact, void* y, const PlanView& pv,
                        int32_t* dev_status, cudaStream_t stream, const bool (&any)[kLists],
                        float* splitk_buf, size_t splitk_bytes, const void* gx,
-                       const int32_t* grows, int gk) {
+                       const int32_t* grows, int gk, int32_t* split_cnt) {
   // split-K only when every block is skinny (all rows then belong to skinny
   // items, which the finalize kernel rewrites) and the buffer holds the slices
   int ks1 = 1, ks2 = 1;
@@ -1033,6 +1134,24 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
                    !make_act_map(&m_h[l], hact, R, I, list_bn(l))))
       return cudaErrorInvalidValue;
   cudaError_t err = cudaSuccess;
+  if (split_cnt && splitk_buf && any[0] && !any[1] && !any[2]) {
+    // small batches, every block skinny: the K slices of each unit are
+    // reduced in the kernel by the slice that finishes last (no finalize
+    // launch); G2 reuses the slice buffer once G1 is done with it.  (One
+    // launch for G1 and G2 together measured no faster here: G2 units wait for
+    // G1 results, and in the shared layout a G2 stage occupies a G1-sized slot.)
+    int32_t* c1 = split_cnt;
+    int32_t* c2 = split_cnt + (size_t)pv.cap[0] * moe_cdiv(I, kBM);
+    err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x[0], s1, s3, pv.counts, 0, pv.items[0],
+                                        pv.cap[0], I, H, hact, dev_status, stream, ks1, R,
+                                        splitk_buf, nullptr, nullptr, nullptr, 0, 0, nullptr,
+                                        nullptr, gx, grows, gk, 1, nullptr, c1, nullptr);
+    if (err != cudaSuccess) return err;
+    return run_tc<kBnSkinny, false, WFP8>(m_w2, m_w2, m_h[0], s2, s2, pv.counts, 0, pv.items[0],
+                                          pv.cap[0], H, I, y, dev_status, stream, ks2, R,
+                                          splitk_buf, nullptr, nullptr, nullptr, 0, 0, nullptr,
+                                          nullptr, nullptr, nullptr, 0, 1, nullptr, c2, nullptr);
+  }
   if (any[0] && any[1] && !any[2] && ks1 == 1 && ks2 == 1) {
     // skinny and tile blocks both present: one launch per phase (or one in
     // all, fused) in which the two lists run side by side
@@ -1115,6 +1234,11 @@ cudaError_t run_simt(bool fp8, const void* act, const void* wa, const void* wb, 
 
 size_t grouped_gemm_scratch_bytes(int R, int E_blocks) { return plan_bytes(R, E_blocks); }
 
+size_t grouped_gemm_split_counter_bytes(int R, int E_blocks, int H, int I) {
+  const size_t cap0 = (size_t)moe_cdiv(R, kBnSkinny) + E_blocks;
+  return moe_align_up(cap0 * (moe_cdiv(I, kBM) + moe_cdiv(H, kBM)) * sizeof(int32_t), 256);
+}
+
 size_t grouped_gemm_splitk_bytes(int R, int H, int I) {
   const size_t w = (size_t)(2 * I > H ? 2 * I : H);
   return moe_align_up((size_t)kMaxKSplit * R * w * sizeof(float), 256);
@@ -1135,7 +1259,8 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 int dispatch, int32_t* block_variant, void* scratch,
                                 int32_t* dev_status, cudaStream_t stream, int max_rows,
                                 bool plan_ready, float* splitk_buf, size_t splitk_bytes,
-                                const void* gather_x, const int32_t* gather_rows, int gather_k) {
+                                const void* gather_x, const int32_t* gather_rows, int gather_k,
+                                int32_t* split_cnt) {
   if (m_skinny < 0) m_skinny = MOE_DEFAULT_M_SKINNY;
   const bool fp8 = wdtype == MOE_W_FP8E4M3_B128;
   const bool simt = dispatch == MOE_DISPATCH_SIMT;
@@ -1174,7 +1299,8 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
   if (fp8)
     return run_tc_all<true>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
                             stream, any, splitk_buf, splitk_bytes, gather_x, gather_rows,
-                            gather_k);
+                            gather_k, split_cnt);
   return run_tc_all<false>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                           stream, any, splitk_buf, splitk_bytes, gather_x, gather_rows, gather_k);
+                           stream, any, splitk_buf, splitk_bytes, gather_x, gather_rows, gather_k,
+                           split_cnt);
 }

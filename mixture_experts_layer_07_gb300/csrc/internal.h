@@ -38,7 +38,11 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 int32_t* dev_status, cudaStream_t stream, int max_rows = -1,
                                 bool plan_ready = false, float* splitk_buf = nullptr,
                                 size_t splitk_bytes = 0, const void* gather_x = nullptr,
-                                const int32_t* gather_rows = nullptr, int gather_k = 0);
+                                const int32_t* gather_rows = nullptr, int gather_k = 0,
+                                int32_t* split_cnt = nullptr);
+// zero-initialised counters for the in-kernel reduction of K slices in the
+// small-batch launch (every call leaves them zero again)
+size_t grouped_gemm_split_counter_bytes(int R, int E_blocks, int H, int I);
 // fp32 bytes for split-K slices of the skinny variant in moe_layer's decode
 // regime (at most 4 slices of R x max(2I, H) partial sums)
 size_t grouped_gemm_splitk_bytes(int R, int H, int I);

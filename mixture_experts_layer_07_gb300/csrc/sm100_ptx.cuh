@@ -33,6 +33,12 @@ MOE_DEVICE void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 
+// add `bytes` to the transaction count of the current phase without arriving
+MOE_DEVICE void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
 MOE_DEVICE void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }

@@ -267,7 +267,8 @@ class MoELayer:
                                                      "w2", "s1", "s3", "s2", "sw1", "sw3", "sw2")])
         self.workspace = torch.empty(workspace_bytes(cfg), dtype=torch.uint8, device=device)
         self.layout = workspace_layout(cfg)
-        self.workspace[self.layout.sync:self.layout.sync + 256].zero_()  # see moe_layer
+        # the sync region (up to the logits) starts at zero; see moe_layer
+        self.workspace[self.layout.sync:self.layout.logits].zero_()
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=device)
 
     def __call__(self, x, out=None, stream=None):

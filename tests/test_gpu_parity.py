@@ -480,7 +480,7 @@ def test_layer_prefill_routing_is_exact_and_repeats(ops, name, over, Ts):
         wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
         want = [ops.block_variant(int(m), R, E, -1, 0, wd) for m in np.diff(off)]
         assert layer.view("block_variant", torch.int32, (E,)).cpu().numpy().tolist() == want
-        sw = layer.workspace[layer.layout.sync:layer.layout.sync + 256].view(torch.int32)
+        sw = layer.workspace[layer.layout.sync:layer.layout.logits].view(torch.int32)
         assert int(sw.abs().sum().item()) == 0
         if T <= 1000:
             case = dict(inp)
@@ -501,8 +501,8 @@ def test_layer_decode_path_repeats_and_leaves_sync_zero(ops):
         x_bits = synth.host_inputs(spec, T, seed=seed, weights=False)["x_bits"]
         out = layer(U.bf16_dev(x_bits))
         sync()
-        sw = layer.workspace[layer.layout.sync:layer.layout.sync + 4].view(torch.int32).item()
-        assert sw == 0
+        sw = layer.workspace[layer.layout.sync:layer.layout.logits].view(torch.int32)
+        assert int(sw.abs().sum().item()) == 0
         case = dict(inp)
         case["x_bits"] = x_bits
         res = oracle.moe_layer_from_inputs(case)
