@@ -155,17 +155,18 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
     """Kernel launches inside one moe_layer call, mirroring the library's
     launch sequence.
       T <= 32: one fused routing launch (router, top-K, permute, GEMM plan);
-               G1 copies its rows from x itself
-               + the permute copy
+               with bf16 weights G1 copies its rows from x itself, with FP8
+               weights a permute-copy launch follows
       T > 32:  router 1 (2 from T >= 64: weight split + tensor-core GEMM),
                fused routing 1 (top-K, chunk histograms, and in its last CTA
                the scan and the GEMM plan), scatter 1, permute copy 1
-      GEMM:    skinny list (always): one G1 and one G2 launch; tile list
-               (T > m_skinny) and wide list (FP8, T > 128): a G1 and a G2
-               launch each, or one launch running both while the mean rows
-               per expert are <= 64 and H <= 3 I; 2 on the CUDA-core path; when only the
-               skinny list can be non-empty, each of G1/G2 split along K adds
-               a finalize launch
+      GEMM:    every block skinny (small batch): a G1 and a G2 launch (K
+               slices reduced in the kernel); skinny + tile lists: a G1 and a
+               G2 launch each running both lists side by side, or one launch
+               for everything while the mean rows per expert are <= 64 and
+               H <= 3 I (not with the small-batch row gather); with the FP8
+               wide list, per list a G1 and a G2 launch (or one fused); 2 on
+               the CUDA-core path
       combine 1; a shared expert adds a grouped GEMM with its own plan."""
     R = T * spec.K
 
@@ -197,10 +198,11 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
         return n
 
     if T <= 32:
-        route = 1  # G1 reads its rows from x: no permuted copy
-        g = gemm(T, R, spec.E, with_plan=False, splittable=True, inter=spec.I, gather=True)
+        gather = spec.wdtype != "fp8"  # bf16: G1 reads its rows from x, no permuted copy
+        route = 1 if gather else 2
+        g = gemm(T, R, spec.E, with_plan=False, splittable=True, inter=spec.I, gather=gather)
     else:
-        route = (2 if T >= ROUTER_TC_MIN_T else 1) + 3
+        route = (2 if T >= ROUTER_TC_MIN_T else 1) + 3  # fused routing, scatter, row copy
         g = gemm(T, R, spec.E, with_plan=False, splittable=False, inter=spec.I)
     shared = (gemm(T, T, 1, with_plan=True, splittable=False, inter=spec.I_shared)
               if spec.has_shared else 0)
