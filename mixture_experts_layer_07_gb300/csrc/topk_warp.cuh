@@ -43,12 +43,14 @@ MOE_DEVICE float sigmoid_key(float l) {
   return __fdiv_rn(1.f, __fadd_rn(1.f, e));
 }
 
-// Keys are compared as unsigned integers: the map below is monotone on
-// floats (negative below positive, larger magnitude further out) once -0 is
-// folded to +0 (an fp32 add of +0), so equal floats give equal keys.
+// Keys are compared as unsigned integers: non-negative floats map to
+// bits + 2^31, negative floats to 2^32 - bits (two's complement negation).
+// The map is monotone (larger magnitude further out), -0 and +0 both land on
+// 2^31, and no float (not even a NaN pattern) maps to 0, so 0 can mark an
+// empty slot.
 MOE_DEVICE uint32_t order_key(float k) {
-  const uint32_t b = __float_as_uint(__fadd_rn(k, 0.f));
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  const uint32_t b = __float_as_uint(k);
+  return (b & 0x80000000u) ? 0u - b : (b | 0x80000000u);
 }
 
 // strict total order: larger key first, lower index first among equal keys

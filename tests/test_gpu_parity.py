@@ -110,7 +110,12 @@ TOPK_CASES = [  # E, K, mode, T, shared
     (8, 8, 0, 5, False), (64, 32, 0, 3, False), (33, 3, 1, 70, True), (1, 1, 0, 4, False),
     # large T: many CTAs of four token warps
     (128, 8, 0, 5000, False), (32, 4, 0, 4096, False), (256, 16, 1, 4100, True),
-    (8, 2, 0, 4097, False), (200, 9, 1, 8191, False)]
+    (8, 2, 0, 4097, False), (200, 9, 1, 8191, False),
+    # E <= 128 at T >= 32768: groups of 8 lanes per token (float4 rows and,
+    # with a shared-gate column, scalar rows)
+    (128, 8, 0, 40000, False), (32, 4, 0, 33000, False), (64, 6, 1, 33000, True),
+    (100, 7, 0, 32768, False), (33, 3, 1, 40000, True), (64, 32, 0, 32768, False),
+    (8, 8, 1, 32770, False)]
 
 
 def run_topk(ops, logits, E, K, mode, scale, sel_bias, shared):
@@ -140,7 +145,8 @@ def test_topk_route(ops, E, K, mode, T, shared):
         U.assert_weights_close(gsh, oracle.shared_gate(lg.astype(np.float64), E))
 
 
-@pytest.mark.parametrize("mode,T", [(0, 300), (1, 300), (0, 5000), (1, 5000)])
+@pytest.mark.parametrize("mode,T", [(0, 300), (1, 300), (0, 5000), (1, 5000), (0, 40000),
+                                    (1, 40000)])
 def test_topk_heavy_ties(ops, mode, T):
     # logits from a 3-value set: most keys tie, the index rule decides
     E, K = 128, 8
@@ -157,6 +163,29 @@ def test_topk_heavy_ties(ops, mode, T):
         rid, rw = oracle.topk_sigmoid_bias(lg, bias, E, K, 2.5)
     assert np.array_equal(ids, rid)
     assert ids[0].tolist() == list(range(K)) and ids[1].tolist() == list(range(K))
+    U.assert_weights_close(w, rw)
+
+
+@pytest.mark.parametrize("E,K,G,T", [(128, 8, 128, 40000), (128, 8, 129, 40000),
+                                     (896, 16, 896, 600), (1024, 16, 1024, 300),
+                                     (256, 16, 257, 700)])
+def test_topk_top_experts_on_one_lane(ops, E, K, G, T):
+    # every token's top 2K logits sit on the experts one lane of a routing
+    # group owns, under both lane layouts (float4 rows: lane q of a group of
+    # GS owns e with (e % 4GS) // 4 == q; scalar rows: e % GS == q), so that
+    # lane supplies all K picks and must rebuild its candidate list
+    GS = 8 if E <= 128 else 16 if E <= 256 else 32
+    r = np.random.default_rng(E + G)
+    lg = r.standard_normal((T, G)).astype(np.float32)
+    e = np.arange(E)
+    for t in range(T):
+        q = t % GS
+        own = (e % (4 * GS)) // 4 == q if G % 4 == 0 else e % GS == q
+        sel = e[own][:2 * K]
+        lg[t, sel] = 10.0 + r.standard_normal(len(sel)).astype(np.float32)
+    ids, w, _ = run_topk(ops, lg, E, K, 0, 1.0, None, False)
+    rid, rw = oracle.topk_softmax_renorm(lg.astype(np.float64), E, K)
+    assert np.array_equal(ids, rid)
     U.assert_weights_close(w, rw)
 
 
