@@ -10,7 +10,8 @@
 //      from 16-byte bf16 vectors, fixed-order block reduction) -> logits
 //   2. each CTA, after its stores, fences and bumps a completion counter; the
 //      CTA that sees the last count (no CTA ever waits) then
-//   3. routes every token (warp top-K, logits read through L2),
+//   3. routes every token (warp top-K, logits read through L2; for E > 128
+//      the shorter-list group route of topk_group.cuh),
 //   4. permutes the T*K replicas in one CTA (shared-memory counters),
 //   5. plans the grouped GEMM (per-block variant and work lists),
 //   6. and resets the counter to zero for the next call.
@@ -20,6 +21,7 @@
 #include "internal.h"
 #include "permute_block.cuh"
 #include "plan.cuh"
+#include "topk_group.cuh"
 #include "topk_warp.cuh"
 
 namespace {
@@ -31,7 +33,10 @@ constexpr int kThreads = 256;
 constexpr int kTok = 8;  // tokens accumulated together
 constexpr int kWarps = kThreads / 32;
 
-template <int NPL, int LK>
+// kGroup (E > 128): the token's route is group_route over the whole warp
+// (lists of 4 or 8 with refill instead of K-long lists: a shorter chain per
+// token); kVec: float4 logit rows
+template <int NPL, int LK, bool kGroup, bool kVec>
 __global__ void __launch_bounds__(kThreads)
 route_decode_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ wg,
                     const float* __restrict__ gate_bias, float* __restrict__ logits, int T, int H,
@@ -102,8 +107,16 @@ route_decode_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict
   // 3. top-K, one warp per token
   for (int t = warp; t < T; t += kWarps) {
     const float* row = logits + (size_t)t * G;
-    warp_topk<NPL, LK, true>(row, sel_bias, E, K, mode, scale, ids + (size_t)t * K,
-                             weights + (size_t)t * K, ids_s + t * K);
+    if constexpr (kGroup) {
+      float l[NPL];
+      group_load<32, NPL, kVec, true>(row, true, E, l);
+      group_route<32, NPL, LK, kVec, true>(l, row, true, 1, sel_bias, E, K, mode, scale,
+                                           ids + (size_t)t * K, weights + (size_t)t * K, nullptr,
+                                           ids_s + t * K);
+    } else {
+      warp_topk<NPL, LK, true>(row, sel_bias, E, K, mode, scale, ids + (size_t)t * K,
+                               weights + (size_t)t * K, ids_s + t * K);
+    }
     if (shared_gate && lane == 0) shared_gate[t] = sigmoid_key(__ldcg(row + E));
   }
   __syncthreads();
@@ -117,20 +130,24 @@ route_decode_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict
   if (tid == 0) *done_ctr = 0u;
 }
 
-template <int NPL>
-cudaError_t launch_npl(const RouteDecodeArgs& a, cudaStream_t stream) {
+template <int NPL, int LK, bool kGroup, bool kVec>
+cudaError_t launch_one(const RouteDecodeArgs& a, cudaStream_t stream) {
   const size_t smem = ((size_t)(kWarps + 1) * a.E + 1 + (size_t)a.T * a.K) * sizeof(int32_t);
   const PlanView pv = plan_view(a.gemm_scratch, a.T * a.K, a.E);
   PlanOut po = plan_out(pv);
-  int32_t* counts = pv.counts;
   const int m_skinny = a.m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : a.m_skinny;
-#define MOE_RD_LAUNCH(KT)                                                                      \
-  return moe_launch(route_decode_kernel<NPL, (KT < NPL ? KT : NPL)>, dim3(a.G), dim3(kThreads), \
-                    smem, stream, 1, static_cast<const __nv_bfloat16*>(a.x), a.wg, a.gate_bias,  \
-                    a.logits, a.T, a.H, a.G, a.sel_bias, a.E, a.K, a.mode, a.scale, a.ids,       \
-                    a.weights, a.shared_gate, a.offsets, a.row_to_flat, a.flat_to_row,            \
-                    a.dev_status, m_skinny, a.dispatch, a.wdtype, counts, po, a.block_variant,    \
-                    a.done_ctr)
+  return moe_launch(route_decode_kernel<NPL, LK, kGroup, kVec>, dim3(a.G), dim3(kThreads), smem,
+                    stream, 1, static_cast<const __nv_bfloat16*>(a.x), a.wg, a.gate_bias,
+                    a.logits, a.T, a.H, a.G, a.sel_bias, a.E, a.K, a.mode, a.scale, a.ids,
+                    a.weights, a.shared_gate, a.offsets, a.row_to_flat, a.flat_to_row,
+                    a.dev_status, m_skinny, a.dispatch, a.wdtype, pv.counts, po, a.block_variant,
+                    a.done_ctr);
+}
+
+// E <= 128: one warp per token, lists of min(K tier, experts per lane)
+template <int NPL>
+cudaError_t launch_warp(const RouteDecodeArgs& a, cudaStream_t stream) {
+#define MOE_RD_LAUNCH(KT) return launch_one<NPL, (KT < NPL ? KT : NPL), false, false>(a, stream)
   if (a.K <= 2) MOE_RD_LAUNCH(2);
   if (a.K <= 4) MOE_RD_LAUNCH(4);
   if (a.K <= 8) MOE_RD_LAUNCH(8);
@@ -139,15 +156,34 @@ cudaError_t launch_npl(const RouteDecodeArgs& a, cudaStream_t stream) {
 #undef MOE_RD_LAUNCH
 }
 
+// E > 128: group_route over the warp, lists of 4 (K <= 8) or 8
+template <int NPL, bool kVec>
+cudaError_t launch_group(const RouteDecodeArgs& a, cudaStream_t stream) {
+  if (a.K <= 8) return launch_one<NPL, 4, true, kVec>(a, stream);
+  return launch_one<NPL, 8, true, kVec>(a, stream);
+}
+
+template <bool kVec>
+cudaError_t launch_group_tier(const RouteDecodeArgs& a, cudaStream_t stream) {
+  // experts per lane: whole float4s of 4 * 32 experts per step (kVec) or
+  // one expert per 32 (scalar)
+  const int npl = kVec ? 4 * moe_cdiv(a.E, 128) : moe_cdiv(a.E, 32);
+  if (npl <= 8) return launch_group<8, kVec>(a, stream);
+  if (npl <= 16) return launch_group<16, kVec>(a, stream);
+  if (npl <= 28) return launch_group<28, kVec>(a, stream);
+  return launch_group<32, kVec>(a, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_route_decode(const RouteDecodeArgs& a, cudaStream_t stream) {
+  if (a.E > 128) {
+    const bool vec = a.E % 4 == 0 && a.G % 4 == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0;
+    return vec ? launch_group_tier<true>(a, stream) : launch_group_tier<false>(a, stream);
+  }
   const int npl = moe_cdiv(a.E, 32);
-  if (npl <= 1) return launch_npl<1>(a, stream);
-  if (npl <= 2) return launch_npl<2>(a, stream);
-  if (npl <= 4) return launch_npl<4>(a, stream);
-  if (npl <= 8) return launch_npl<8>(a, stream);
-  if (npl <= 16) return launch_npl<16>(a, stream);
-  if (npl <= 28) return launch_npl<28>(a, stream);
-  return launch_npl<32>(a, stream);
+  if (npl <= 1) return launch_warp<1>(a, stream);
+  if (npl <= 2) return launch_warp<2>(a, stream);
+  return launch_warp<4>(a, stream);
 }

@@ -5,7 +5,8 @@
 //
 // "FlashInfer MoE routing optimisation" (flashinfer PR #4152), "1.
 // routing_custom.cu": one warp per token keeps lane-owned top-K candidates
-// (topk_warp.cuh).  "vLLM MoE permute optimisation: buffer pre-allocation"
+// (topk_warp.cuh; for E > 128 the shorter-list group route of
+// topk_group.cuh).  "vLLM MoE permute optimisation: buffer pre-allocation"
 // (vllm PR #43014), introduction and "1. C++ kernel level": the permute's
 // counts, offsets and rows live in caller-owned scratch; here the expert
 // histogram of each chunk of tokens is taken right where its ids are chosen,
@@ -26,6 +27,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "plan.cuh"
+#include "topk_group.cuh"
 #include "topk_warp.cuh"
 
 namespace {
@@ -42,7 +44,9 @@ inline int tokens_per_cta(int T) {
   return kWarps * (tpw > 0 ? tpw : 1);
 }
 
-template <int NPL, int LK>
+// kGroup (E > 128): each token's route is group_route over the whole warp
+// (lists of 4 or 8 with refill: a shorter chain per token); kVec: float4 rows
+template <int NPL, int LK, bool kGroup, bool kVec>
 __global__ void __launch_bounds__(kThreads)
 route_prefill_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ sel_bias,
                      int T, int E, int K, int mode, float scale, int32_t* __restrict__ ids,
@@ -70,8 +74,16 @@ route_prefill_kernel(const float* __restrict__ logits, int ld, const float* __re
   for (int i = warp; i < ntok; i += kWarps) {
     const int t = t0 + i;
     const float* row = logits + (size_t)t * ld;
-    warp_topk<NPL, LK>(row, sel_bias, E, K, mode, scale, ids + (size_t)t * K,
-                       weights + (size_t)t * K, ids_s + i * K);
+    if constexpr (kGroup) {
+      float l[NPL];
+      group_load<32, NPL, kVec>(row, true, E, l);
+      group_route<32, NPL, LK, kVec>(l, row, true, 1, sel_bias, E, K, mode, scale,
+                                     ids + (size_t)t * K, weights + (size_t)t * K, nullptr,
+                                     ids_s + i * K);
+    } else {
+      warp_topk<NPL, LK>(row, sel_bias, E, K, mode, scale, ids + (size_t)t * K,
+                         weights + (size_t)t * K, ids_s + i * K);
+    }
     if (shared_gate && lane == 0) shared_gate[t] = sigmoid_key(__ldg(row + E));
   }
   __syncthreads();
@@ -242,31 +254,54 @@ size_t prefill_smem(int tpc, int E, int K) {
   return ((size_t)tpc * K + 3 * (size_t)E + 1) * sizeof(int32_t);
 }
 
-template <int NPL>
-cudaError_t launch_npl(const RoutePrefillArgs& a, int tpc, int nchunks, cudaStream_t stream) {
+template <int NPL, int LK, bool kGroup, bool kVec>
+cudaError_t launch_one(const RoutePrefillArgs& a, int tpc, int nchunks, cudaStream_t stream) {
   const size_t smem = prefill_smem(tpc, a.E, a.K);
   PlanView pv = plan_view(a.gemm_scratch, a.T * a.K, a.E);
   PlanOut po = plan_out(pv);
   const int m_skinny = a.m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : a.m_skinny;
-#define MOE_RP_LAUNCH(KT)                                                                       \
-  do {                                                                                          \
-    auto kern = route_prefill_kernel<NPL, (KT < NPL ? KT : NPL)>;                               \
-    if (smem > 48 * 1024) {                                                                     \
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                                           (int)smem);                                          \
-      if (e != cudaSuccess) return e;                                                           \
-    }                                                                                           \
-    return moe_launch(kern, dim3(nchunks), dim3(kThreads), smem, stream, 1, a.logits, a.ld,     \
-                      a.sel_bias, a.T, a.E, a.K, a.mode, a.scale, a.ids, a.weights,             \
-                      a.shared_gate, tpc, a.counts, a.offsets, m_skinny, a.dispatch, a.wdtype,  \
-                      pv.counts, po, a.block_variant, a.done_ctr);                              \
-  } while (0)
+  auto kern = route_prefill_kernel<NPL, LK, kGroup, kVec>;
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return moe_launch(kern, dim3(nchunks), dim3(kThreads), smem, stream, 1, a.logits, a.ld,
+                    a.sel_bias, a.T, a.E, a.K, a.mode, a.scale, a.ids, a.weights, a.shared_gate,
+                    tpc, a.counts, a.offsets, m_skinny, a.dispatch, a.wdtype, pv.counts, po,
+                    a.block_variant, a.done_ctr);
+}
+
+// E <= 128: one warp per token, lists of min(K tier, experts per lane)
+template <int NPL>
+cudaError_t launch_warp(const RoutePrefillArgs& a, int tpc, int nchunks, cudaStream_t stream) {
+#define MOE_RP_LAUNCH(KT) \
+  return launch_one<NPL, (KT < NPL ? KT : NPL), false, false>(a, tpc, nchunks, stream)
   if (a.K <= 2) MOE_RP_LAUNCH(2);
   if (a.K <= 4) MOE_RP_LAUNCH(4);
   if (a.K <= 8) MOE_RP_LAUNCH(8);
   if (a.K <= 16) MOE_RP_LAUNCH(16);
   MOE_RP_LAUNCH(32);
 #undef MOE_RP_LAUNCH
+}
+
+// E > 128: group_route over the warp, lists of 4 (K <= 8) or 8
+template <int NPL, bool kVec>
+cudaError_t launch_group(const RoutePrefillArgs& a, int tpc, int nchunks, cudaStream_t stream) {
+  if (a.K <= 8) return launch_one<NPL, 4, true, kVec>(a, tpc, nchunks, stream);
+  return launch_one<NPL, 8, true, kVec>(a, tpc, nchunks, stream);
+}
+
+template <bool kVec>
+cudaError_t launch_group_tier(const RoutePrefillArgs& a, int tpc, int nchunks,
+                              cudaStream_t stream) {
+  // experts per lane: whole float4s of 4 * 32 experts per step (kVec) or
+  // one expert per 32 (scalar)
+  const int npl = kVec ? 4 * moe_cdiv(a.E, 128) : moe_cdiv(a.E, 32);
+  if (npl <= 8) return launch_group<8, kVec>(a, tpc, nchunks, stream);
+  if (npl <= 16) return launch_group<16, kVec>(a, tpc, nchunks, stream);
+  if (npl <= 28) return launch_group<28, kVec>(a, tpc, nchunks, stream);
+  return launch_group<32, kVec>(a, tpc, nchunks, stream);
 }
 
 }  // namespace
@@ -285,15 +320,18 @@ cudaError_t launch_route_prefill(const RoutePrefillArgs& a, cudaStream_t stream)
   if (a.T <= 0) return cudaSuccess;
   const int tpc = tokens_per_cta(a.T);
   const int nchunks = moe_cdiv(a.T, tpc);
-  const int npl = moe_cdiv(a.E, 32);
   cudaError_t e;
-  if (npl <= 1) e = launch_npl<1>(a, tpc, nchunks, stream);
-  else if (npl <= 2) e = launch_npl<2>(a, tpc, nchunks, stream);
-  else if (npl <= 4) e = launch_npl<4>(a, tpc, nchunks, stream);
-  else if (npl <= 8) e = launch_npl<8>(a, tpc, nchunks, stream);
-  else if (npl <= 16) e = launch_npl<16>(a, tpc, nchunks, stream);
-  else if (npl <= 28) e = launch_npl<28>(a, tpc, nchunks, stream);
-  else e = launch_npl<32>(a, tpc, nchunks, stream);
+  if (a.E > 128) {
+    const bool vec = a.E % 4 == 0 && a.ld % 4 == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0;
+    e = vec ? launch_group_tier<true>(a, tpc, nchunks, stream)
+            : launch_group_tier<false>(a, tpc, nchunks, stream);
+  } else {
+    const int npl = moe_cdiv(a.E, 32);
+    e = npl <= 1   ? launch_warp<1>(a, tpc, nchunks, stream)
+        : npl <= 2 ? launch_warp<2>(a, tpc, nchunks, stream)
+                   : launch_warp<4>(a, tpc, nchunks, stream);
+  }
   if (e != cudaSuccess) return e;
   const int R = a.T * a.K;
   const size_t smem = (size_t)kScatterWarps * a.E * sizeof(int32_t);
