@@ -519,6 +519,40 @@ def test_layer_prefill_routing_is_exact_and_repeats(ops, name, over, Ts):
             U.assert_bf16_close(U.f64(layer(x)), res["out"], rel, f"prefill T={T}")
 
 
+@pytest.mark.parametrize("shared", [False, True])
+def test_fused_routing_one_lane_holds_every_pick(ops, shared):
+    # E = 512 routes by warp-wide groups inside the fused routing launches;
+    # a gate bias of +20 on the 16 experts lane 0 owns (float4 rows: e with
+    # (e % 128) // 4 == 0; 513-float rows with the shared gate: e % 32 == 0)
+    # makes that lane supply all K = 10 picks, past its 8-entry list
+    E, K = 512, 10
+    e = np.arange(E)
+    own = e[e % 32 == 0] if shared else e[(e % 128) // 4 == 0]
+    spec = SPECS["tiny"].with_(E=E, K=K, H=256, I=128, hot_experts=tuple(int(v) for v in own),
+                               hot_bias=20.0)
+    if shared:
+        spec = spec.with_(has_shared=True, I_shared=128)
+    inp = synth.host_inputs(spec, 100, seed=5)
+    t = U.layer_tensors(inp)
+    layer = ops.MoELayer(U.config_for(ops, spec, T_max=100), t)
+    for T in (5, 100):  # the decode launch, then the prefill launch
+        layer(t["x"][:T].contiguous())
+        sync()
+        assert int(layer.dev_status.item()) == 0
+        lg = layer.view("logits", torch.float32, (T, spec.G)).cpu().numpy()
+        gid = layer.view("ids", torch.int32, (T, K)).cpu().numpy()
+        gw = layer.view("weights", torch.float32, (T, K)).cpu().numpy()
+        rid, rw = oracle.topk_softmax_renorm(lg.astype(np.float64), E, K)
+        assert np.array_equal(gid, rid)
+        assert set(np.unique(gid).tolist()) <= set(own.tolist())
+        assert np.allclose(gw, rw, rtol=1e-5, atol=1e-7)
+        off, r2f, f2r = oracle.permute(gid, E)
+        assert np.array_equal(layer.view("offsets", torch.int32, (E + 1,)).cpu().numpy(), off)
+        assert np.array_equal(layer.view("flat_to_row", torch.int32, (T * K,)).cpu().numpy(), f2r)
+        sw = layer.workspace[layer.layout.sync:layer.layout.logits].view(torch.int32)
+        assert int(sw.abs().sum().item()) == 0
+
+
 def test_layer_decode_path_repeats_and_leaves_sync_zero(ops):
     # T <= 32 runs the fused routing launch; its completion counter must come
     # back to zero so that the next call (same workspace) routes again
