@@ -1,0 +1,182 @@
+// Host emulation of the group top-K device code (topk_group.cuh).
+//
+// One warp is 32 std::threads; every warp-collective intrinsic the routing
+// code uses (shuffle, redux, ballot, any, syncwarp) is a write to a shared
+// slot array between two barriers, so the threads run the device source
+// itself, lane by lane, on the CPU.  The selection is checked against a
+// stable sort of the same keys (larger first, lower expert index first among
+// equal keys), for float4 and scalar rows, groups of 8, 16 and 32 lanes,
+// random, tie-heavy and "one lane owns every pick" logits, both score modes.
+// Exit status 0 when every token matches.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <barrier>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <numeric>
+#include <random>
+#include <thread>
+#include <vector>
+
+// device-code keywords become plain host C++
+#undef __device__
+#define __device__
+#undef __constant__
+#define __constant__
+#undef __forceinline__
+#define __forceinline__ inline
+
+static std::barrier<>* g_bar;
+static uint64_t g_slot[32];
+thread_local int t_lane;
+
+template <class T>
+T exchange(T v, int src) {
+  uint64_t u = 0;
+  std::memcpy(&u, &v, sizeof(T));
+  g_slot[t_lane] = u;
+  g_bar->arrive_and_wait();
+  const uint64_t r = g_slot[src];
+  g_bar->arrive_and_wait();
+  T o;
+  std::memcpy(&o, &r, sizeof(T));
+  return o;
+}
+template <class T> T __shfl_xor_sync(unsigned, T v, int d) { return exchange(v, t_lane ^ d); }
+template <class T> T __shfl_sync(unsigned, T v, int s) { return exchange(v, s); }
+template <class F> uint32_t reduce_all(uint32_t v, F f) {
+  g_slot[t_lane] = v;
+  g_bar->arrive_and_wait();
+  uint32_t a = (uint32_t)g_slot[0];
+  for (int i = 1; i < 32; ++i) a = f(a, (uint32_t)g_slot[i]);
+  g_bar->arrive_and_wait();
+  return a;
+}
+inline uint32_t __reduce_max_sync(unsigned, uint32_t v) {
+  return reduce_all(v, [](uint32_t a, uint32_t b) { return a > b ? a : b; });
+}
+inline uint32_t __reduce_min_sync(unsigned, uint32_t v) {
+  return reduce_all(v, [](uint32_t a, uint32_t b) { return a < b ? a : b; });
+}
+inline uint32_t __reduce_add_sync(unsigned, uint32_t v) {
+  return reduce_all(v, [](uint32_t a, uint32_t b) { return a + b; });
+}
+inline unsigned __ballot_sync(unsigned, int p) {
+  g_slot[t_lane] = p ? 1 : 0;
+  g_bar->arrive_and_wait();
+  unsigned m = 0;
+  for (int i = 0; i < 32; ++i)
+    if (g_slot[i]) m |= 1u << i;
+  g_bar->arrive_and_wait();
+  return m;
+}
+inline int __any_sync(unsigned m, int p) { return __ballot_sync(m, p) != 0; }
+inline void __syncwarp(unsigned = 0xffffffffu) { g_bar->arrive_and_wait(); }
+template <class T> T __ldg(const T* p) { return *p; }
+template <class T> T __ldcg(const T* p) { return *p; }
+inline uint32_t __float_as_uint(float f) { uint32_t u; std::memcpy(&u, &f, 4); return u; }
+inline float __uint_as_float(uint32_t u) { float f; std::memcpy(&f, &u, 4); return f; }
+inline float __int_as_float(int u) { float f; std::memcpy(&f, &u, 4); return f; }
+// single IEEE operations, round to nearest (what the _rn intrinsics are)
+inline float __fadd_rn(float a, float b) { volatile float r = a + b; return r; }
+inline float __fsub_rn(float a, float b) { volatile float r = a - b; return r; }
+inline float __fmul_rn(float a, float b) { volatile float r = a * b; return r; }
+inline float __fdiv_rn(float a, float b) { volatile float r = a / b; return r; }
+inline uint32_t max(uint32_t a, uint32_t b) { return a > b ? a : b; }
+inline uint32_t min(uint32_t a, uint32_t b) { return a < b ? a : b; }
+inline int atomicCAS(int* p, int c, int v) { const int o = *p; if (o == c) *p = v; return o; }
+struct EmuDim { unsigned x, y, z; };
+thread_local EmuDim emu_thread_idx;
+#undef threadIdx
+#define threadIdx emu_thread_idx
+
+#include "topk_group.cuh"
+
+using namespace moe_route;
+
+// one warp routes tokens t0 .. t0 + 32/GS - 1
+template <int GS, int NPL, int LK, bool kVec>
+void run_warp(const float* logits, int ld, const float* bias, int T, int E, int K, int mode,
+              int t0, int32_t* ids, float* w) {
+  std::barrier<> bar(32);
+  g_bar = &bar;
+  std::vector<int32_t> slots(32 * K);
+  std::vector<std::thread> th;
+  for (int L = 0; L < 32; ++L)
+    th.emplace_back([&, L]() {
+      t_lane = L;
+      emu_thread_idx = {(unsigned)L, 0, 0};
+      const int g = L / GS;
+      const int t = t0 + g;
+      const bool valid = t < T;
+      const int nvalid = std::min(T - t0, 32 / GS);
+      const float* row = logits + (size_t)(valid ? t : 0) * ld;
+      float l[NPL];
+      group_load<GS, NPL, kVec>(row, valid, E, l);
+      group_route<GS, NPL, LK, kVec>(l, row, valid, nvalid, bias, E, K, mode, 2.5f,
+                                     ids + (size_t)t * K, w + (size_t)t * K, nullptr,
+                                     slots.data() + g * K);
+    });
+  for (auto& x : th) x.join();
+}
+
+// pattern 0: normal logits; 1: values from {-1, 0, 1} (ties decided by index);
+// 2: +20 on the experts lane 0 of each group owns (that lane supplies every
+// pick); 3: as 2 with every other logit 0, so lane 0's experts all tie and
+// its list rebuilds across equal keys
+template <int GS, int NPL, int LK, bool kVec>
+int check(int E, int K, int G, int T, int mode, int pattern, unsigned seed) {
+  std::mt19937 rng(seed);
+  std::normal_distribution<float> nd(0.f, 1.f);
+  std::vector<float> lg((size_t)T * G), bias(E);
+  for (auto& v : lg) v = pattern == 1 ? (float)((int)(rng() % 3) - 1) : pattern == 3 ? 0.f : nd(rng);
+  for (auto& v : bias) v = mode ? 0.3f * nd(rng) : 0.f;
+  if (pattern >= 2)
+    for (int t = 0; t < T; ++t)
+      for (int e = 0; e < E; ++e)
+        if (kVec ? ((e % (4 * GS)) / 4 == 0) : (e % GS == 0)) lg[(size_t)t * G + e] += 20.f;
+  std::vector<int32_t> ids((size_t)T * K, -1);
+  std::vector<float> w((size_t)T * K);
+  for (int t0 = 0; t0 < T; t0 += 32 / GS)
+    run_warp<GS, NPL, LK, kVec>(lg.data(), G, mode ? bias.data() : nullptr, T, E, K, mode, t0,
+                                ids.data(), w.data());
+  int bad = 0;
+  for (int t = 0; t < T; ++t) {
+    const float* r = lg.data() + (size_t)t * G;
+    std::vector<float> key(E);
+    for (int e = 0; e < E; ++e) key[e] = mode ? __fadd_rn(sigmoid_key(r[e]), bias[e]) : r[e];
+    std::vector<int> idx(E);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return key[a] > key[b]; });
+    float wsum = 0.f;
+    for (int k = 0; k < K; ++k) {
+      if (ids[(size_t)t * K + k] != idx[k]) {
+        if (!bad) printf("  token %d pick %d: %d, expected %d\n", t, k, ids[(size_t)t * K + k], idx[k]);
+        ++bad;
+        break;
+      }
+      wsum += w[(size_t)t * K + k];
+    }
+    if (std::fabs(wsum - (mode ? 2.5f : 1.f)) > 1e-5f * K) ++bad;
+  }
+  printf("GS=%d NPL=%d LK=%d vec=%d E=%d K=%d G=%d mode=%d pattern=%d: %d of %d tokens wrong\n",
+         GS, NPL, LK, (int)kVec, E, K, G, mode, pattern, bad, T);
+  return bad;
+}
+
+int main() {
+  int bad = 0;
+  for (int pat = 0; pat < 4; ++pat) {
+    bad += check<8, 16, 4, true>(128, 8, 128, 16, 0, pat, 11 + pat);
+    bad += check<8, 16, 4, false>(128, 8, 129, 16, 1, pat, 21 + pat);
+    bad += check<8, 4, 4, true>(32, 4, 32, 16, 0, pat, 31 + pat);
+    bad += check<16, 16, 8, false>(256, 16, 257, 8, 1, pat, 41 + pat);
+    bad += check<32, 16, 8, false>(512, 10, 513, 8, 0, pat, 51 + pat);
+    bad += check<32, 28, 8, true>(896, 16, 896, 4, 1, pat, 61 + pat);
+  }
+  printf("%s\n", bad ? "FAIL" : "OK");
+  return bad != 0;
+}
