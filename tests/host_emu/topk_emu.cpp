@@ -1,4 +1,4 @@
-// Host emulation of the group top-K device code (topk_group.cuh).
+// Host emulation of the top-K device code (topk_group.cuh, topk_warp.cuh).
 //
 // One warp is 32 std::threads; every warp-collective intrinsic the routing
 // code uses (shuffle, redux, ballot, any, syncwarp) is a write to a shared
@@ -6,7 +6,8 @@
 // itself, lane by lane, on the CPU.  The selection is checked against a
 // stable sort of the same keys (larger first, lower expert index first among
 // equal keys), for float4 and scalar rows, groups of 8, 16 and 32 lanes,
-// random, tie-heavy and "one lane owns every pick" logits, both score modes.
+// random, tie-heavy and "one lane owns every pick" logits, both score modes;
+// and the one-warp-per-token route (warp_topk) on random and tie-heavy rows.
 // Exit status 0 when every token matches.
 #include <cuda_runtime.h>
 
@@ -167,6 +168,45 @@ int check(int E, int K, int G, int T, int mode, int pattern, unsigned seed) {
   return bad;
 }
 
+// the one-warp-per-token route (warp_topk, topk_warp.cuh) on the same inputs
+template <int NPL, int LK>
+int check_warp(int E, int K, int G, int T, int mode, int pattern, unsigned seed) {
+  std::mt19937 rng(seed);
+  std::normal_distribution<float> nd(0.f, 1.f);
+  std::vector<float> lg((size_t)T * G), bias(E);
+  for (auto& v : lg) v = pattern == 1 ? (float)((int)(rng() % 3) - 1) : nd(rng);
+  for (auto& v : bias) v = mode ? 0.3f * nd(rng) : 0.f;
+  std::vector<int32_t> ids((size_t)T * K, -1);
+  std::vector<float> w((size_t)T * K);
+  for (int t = 0; t < T; ++t) {
+    std::barrier<> bar(32);
+    g_bar = &bar;
+    std::vector<std::thread> th;
+    for (int L = 0; L < 32; ++L)
+      th.emplace_back([&, L]() {
+        t_lane = L;
+        emu_thread_idx = {(unsigned)L, 0, 0};
+        warp_topk<NPL, LK>(lg.data() + (size_t)t * G, mode ? bias.data() : nullptr, E, K, mode,
+                           2.5f, ids.data() + (size_t)t * K, w.data() + (size_t)t * K);
+      });
+    for (auto& x : th) x.join();
+  }
+  int bad = 0;
+  for (int t = 0; t < T; ++t) {
+    const float* r = lg.data() + (size_t)t * G;
+    std::vector<float> key(E);
+    for (int e = 0; e < E; ++e) key[e] = mode ? __fadd_rn(sigmoid_key(r[e]), bias[e]) : r[e];
+    std::vector<int> idx(E);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) { return key[a] > key[b]; });
+    for (int k = 0; k < K; ++k)
+      if (ids[(size_t)t * K + k] != idx[k]) { ++bad; break; }
+  }
+  printf("warp NPL=%d LK=%d E=%d K=%d mode=%d pattern=%d: %d of %d tokens wrong\n", NPL, LK, E,
+         K, mode, pattern, bad, T);
+  return bad;
+}
+
 int main() {
   int bad = 0;
   for (int pat = 0; pat < 4; ++pat) {
@@ -176,6 +216,12 @@ int main() {
     bad += check<16, 16, 8, false>(256, 16, 257, 8, 1, pat, 41 + pat);
     bad += check<32, 16, 8, false>(512, 10, 513, 8, 0, pat, 51 + pat);
     bad += check<32, 28, 8, true>(896, 16, 896, 4, 1, pat, 61 + pat);
+  }
+  for (int pat = 0; pat < 2; ++pat) {
+    bad += check_warp<4, 4>(128, 8, 128, 8, 0, pat, 71 + pat);
+    bad += check_warp<1, 1>(8, 2, 8, 8, 1, pat, 81 + pat);
+    bad += check_warp<16, 10>(512, 10, 513, 4, 0, pat, 91 + pat);
+    bad += check_warp<28, 16>(896, 16, 896, 2, 1, pat, 101 + pat);
   }
   printf("%s\n", bad ? "FAIL" : "OK");
   return bad != 0;

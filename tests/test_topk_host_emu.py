@@ -1,6 +1,6 @@
-"""The group top-K device code (csrc/topk_group.cuh) run on the CPU.
+"""The top-K device code (csrc/topk_group.cuh, csrc/topk_warp.cuh) run on the CPU.
 
-tests/host_emu/topk_group_emu.cpp compiles that header with the host C++
+tests/host_emu/topk_emu.cpp compiles that header with the host C++
 compiler, runs one warp as 32 threads whose warp intrinsics meet at barriers,
 and checks the picks against a stable sort of the same keys (random,
 tie-heavy, and one-lane-owns-every-pick logits; float4 and scalar rows; groups
@@ -21,13 +21,13 @@ def _cuda_include():
     return inc if os.path.exists(os.path.join(inc, "cuda_runtime.h")) else None
 
 
-def test_group_topk_logic_on_host(tmp_path):
+def test_topk_logic_on_host(tmp_path):
     cxx = shutil.which("g++")
     inc = _cuda_include()
     if not cxx or not inc:
         pytest.skip("needs g++ and the CUDA headers")
-    exe = tmp_path / "topk_group_emu"
-    src = os.path.join(ROOT, "tests", "host_emu", "topk_group_emu.cpp")
+    exe = tmp_path / "topk_emu"
+    src = os.path.join(ROOT, "tests", "host_emu", "topk_emu.cpp")
     cmd = [cxx, "-std=c++20", "-O1", "-ffp-contract=off", "-I", inc,
            "-I", os.path.join(ROOT, "mixture_experts_layer_07_gb300", "csrc"),
            "-I", os.path.join(ROOT, "include"), src, "-o", str(exe), "-lpthread"]
