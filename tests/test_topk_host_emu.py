@@ -1,11 +1,12 @@
 """The top-K device code (csrc/topk_group.cuh, csrc/topk_warp.cuh) run on the CPU.
 
-tests/host_emu/topk_emu.cpp compiles that header with the host C++
+tests/host_emu/topk_emu.cpp compiles those headers with the host C++
 compiler, runs one warp as 32 threads whose warp intrinsics meet at barriers,
 and checks the picks against a stable sort of the same keys (random,
 tie-heavy, and one-lane-owns-every-pick logits; float4 and scalar rows; groups
-of 8, 16 and 32 lanes; both score modes).  No GPU is involved: this pins the
-routing logic itself, while the GPU parity tests pin the compiled kernels."""
+of 8, 16 and 32 lanes and one warp per token; both score modes).  No GPU is
+involved: this pins the routing logic itself, while the GPU parity tests pin
+the compiled kernels."""
 import os
 import shutil
 import subprocess
