@@ -1,99 +1,19 @@
 // Host emulation of the top-K device code (topk_group.cuh, topk_warp.cuh).
 //
-// One warp is 32 std::threads; every warp-collective intrinsic the routing
-// code uses (shuffle, redux, ballot, any, syncwarp) is a write to a shared
-// slot array between two barriers, so the threads run the device source
-// itself, lane by lane, on the CPU.  The selection is checked against a
+// One warp is 32 host threads (simt_emu.h): every warp-collective intrinsic
+// the routing code uses (shuffle, redux, ballot, any, syncwarp) is a write to
+// a shared slot array between two barriers, so the threads run the device
+// source itself, lane by lane, on the CPU.  The selection is checked against a
 // stable sort of the same keys (larger first, lower expert index first among
 // equal keys), for float4 and scalar rows, groups of 8, 16 and 32 lanes,
 // random, tie-heavy and "one lane owns every pick" logits, both score modes;
 // and the one-warp-per-token route (warp_topk) on random and tie-heavy rows.
 // Exit status 0 when every token matches.
-#include <cuda_runtime.h>
-
-#include <algorithm>
-#include <barrier>
-#include <cmath>
-#include <cstdint>
 #include <cstdio>
-#include <cstring>
 #include <numeric>
 #include <random>
-#include <thread>
-#include <vector>
 
-// device-code keywords become plain host C++
-#undef __device__
-#define __device__
-#undef __constant__
-#define __constant__
-#undef __forceinline__
-#define __forceinline__ inline
-
-static std::barrier<>* g_bar;
-static uint64_t g_slot[32];
-thread_local int t_lane;
-
-template <class T>
-T exchange(T v, int src) {
-  uint64_t u = 0;
-  std::memcpy(&u, &v, sizeof(T));
-  g_slot[t_lane] = u;
-  g_bar->arrive_and_wait();
-  const uint64_t r = g_slot[src];
-  g_bar->arrive_and_wait();
-  T o;
-  std::memcpy(&o, &r, sizeof(T));
-  return o;
-}
-template <class T> T __shfl_xor_sync(unsigned, T v, int d) { return exchange(v, t_lane ^ d); }
-template <class T> T __shfl_sync(unsigned, T v, int s) { return exchange(v, s); }
-template <class F> uint32_t reduce_all(uint32_t v, F f) {
-  g_slot[t_lane] = v;
-  g_bar->arrive_and_wait();
-  uint32_t a = (uint32_t)g_slot[0];
-  for (int i = 1; i < 32; ++i) a = f(a, (uint32_t)g_slot[i]);
-  g_bar->arrive_and_wait();
-  return a;
-}
-inline uint32_t __reduce_max_sync(unsigned, uint32_t v) {
-  return reduce_all(v, [](uint32_t a, uint32_t b) { return a > b ? a : b; });
-}
-inline uint32_t __reduce_min_sync(unsigned, uint32_t v) {
-  return reduce_all(v, [](uint32_t a, uint32_t b) { return a < b ? a : b; });
-}
-inline uint32_t __reduce_add_sync(unsigned, uint32_t v) {
-  return reduce_all(v, [](uint32_t a, uint32_t b) { return a + b; });
-}
-inline unsigned __ballot_sync(unsigned, int p) {
-  g_slot[t_lane] = p ? 1 : 0;
-  g_bar->arrive_and_wait();
-  unsigned m = 0;
-  for (int i = 0; i < 32; ++i)
-    if (g_slot[i]) m |= 1u << i;
-  g_bar->arrive_and_wait();
-  return m;
-}
-inline int __any_sync(unsigned m, int p) { return __ballot_sync(m, p) != 0; }
-inline void __syncwarp(unsigned = 0xffffffffu) { g_bar->arrive_and_wait(); }
-template <class T> T __ldg(const T* p) { return *p; }
-template <class T> T __ldcg(const T* p) { return *p; }
-inline uint32_t __float_as_uint(float f) { uint32_t u; std::memcpy(&u, &f, 4); return u; }
-inline float __uint_as_float(uint32_t u) { float f; std::memcpy(&f, &u, 4); return f; }
-inline float __int_as_float(int u) { float f; std::memcpy(&f, &u, 4); return f; }
-// single IEEE operations, round to nearest (what the _rn intrinsics are)
-inline float __fadd_rn(float a, float b) { volatile float r = a + b; return r; }
-inline float __fsub_rn(float a, float b) { volatile float r = a - b; return r; }
-inline float __fmul_rn(float a, float b) { volatile float r = a * b; return r; }
-inline float __fdiv_rn(float a, float b) { volatile float r = a / b; return r; }
-inline uint32_t max(uint32_t a, uint32_t b) { return a > b ? a : b; }
-inline uint32_t min(uint32_t a, uint32_t b) { return a < b ? a : b; }
-inline int atomicCAS(int* p, int c, int v) { const int o = *p; if (o == c) *p = v; return o; }
-struct EmuDim { unsigned x, y, z; };
-thread_local EmuDim emu_thread_idx;
-#undef threadIdx
-#define threadIdx emu_thread_idx
-
+#include "simt_emu.h"
 #include "topk_group.cuh"
 
 using namespace moe_route;
@@ -102,26 +22,19 @@ using namespace moe_route;
 template <int GS, int NPL, int LK, bool kVec>
 void run_warp(const float* logits, int ld, const float* bias, int T, int E, int K, int mode,
               int t0, int32_t* ids, float* w) {
-  std::barrier<> bar(32);
-  g_bar = &bar;
   std::vector<int32_t> slots(32 * K);
-  std::vector<std::thread> th;
-  for (int L = 0; L < 32; ++L)
-    th.emplace_back([&, L]() {
-      t_lane = L;
-      emu_thread_idx = {(unsigned)L, 0, 0};
-      const int g = L / GS;
-      const int t = t0 + g;
-      const bool valid = t < T;
-      const int nvalid = std::min(T - t0, 32 / GS);
-      const float* row = logits + (size_t)(valid ? t : 0) * ld;
-      float l[NPL];
-      group_load<GS, NPL, kVec>(row, valid, E, l);
-      group_route<GS, NPL, LK, kVec>(l, row, valid, nvalid, bias, E, K, mode, 2.5f,
-                                     ids + (size_t)t * K, w + (size_t)t * K, nullptr,
-                                     slots.data() + g * K);
-    });
-  for (auto& x : th) x.join();
+  emu_run_cta(32, [&]() {
+    const int g = simt_emu::lane / GS;
+    const int t = t0 + g;
+    const bool valid = t < T;
+    const int nvalid = std::min(T - t0, 32 / GS);
+    const float* row = logits + (size_t)(valid ? t : 0) * ld;
+    float l[NPL];
+    group_load<GS, NPL, kVec>(row, valid, E, l);
+    group_route<GS, NPL, LK, kVec>(l, row, valid, nvalid, bias, E, K, mode, 2.5f,
+                                   ids + (size_t)t * K, w + (size_t)t * K, nullptr,
+                                   slots.data() + g * K);
+  });
 }
 
 // pattern 0: normal logits; 1: values from {-1, 0, 1} (ties decided by index);
@@ -178,19 +91,11 @@ int check_warp(int E, int K, int G, int T, int mode, int pattern, unsigned seed)
   for (auto& v : bias) v = mode ? 0.3f * nd(rng) : 0.f;
   std::vector<int32_t> ids((size_t)T * K, -1);
   std::vector<float> w((size_t)T * K);
-  for (int t = 0; t < T; ++t) {
-    std::barrier<> bar(32);
-    g_bar = &bar;
-    std::vector<std::thread> th;
-    for (int L = 0; L < 32; ++L)
-      th.emplace_back([&, L]() {
-        t_lane = L;
-        emu_thread_idx = {(unsigned)L, 0, 0};
-        warp_topk<NPL, LK>(lg.data() + (size_t)t * G, mode ? bias.data() : nullptr, E, K, mode,
-                           2.5f, ids.data() + (size_t)t * K, w.data() + (size_t)t * K);
-      });
-    for (auto& x : th) x.join();
-  }
+  for (int t = 0; t < T; ++t)
+    emu_run_cta(32, [&]() {
+      warp_topk<NPL, LK>(lg.data() + (size_t)t * G, mode ? bias.data() : nullptr, E, K, mode,
+                         2.5f, ids.data() + (size_t)t * K, w.data() + (size_t)t * K);
+    });
   int bad = 0;
   for (int t = 0; t < T; ++t) {
     const float* r = lg.data() + (size_t)t * G;
