@@ -337,6 +337,21 @@ typedef struct {
 
 moe_status_t moe_workspace_layout(const moe_config_t* cfg, moe_workspace_layout_t* layout);
 
+/*
+ * Self-test of the library's bounded cross-CTA wait (the one the grouped
+ * GEMM's single-launch G1+G2 path uses for a G2 tile's dependency on G1): one
+ * thread waits until the device int32 *counter >= target, reading it with GPU
+ * acquire loads, for at most limit_us microseconds; if the wait runs out it
+ * writes MOE_DEV_WAIT_TIMEOUT into *dev_status (first error wins) and
+ * returns, leaving the context usable.  Lets a caller check that a stuck
+ * dependency ends in a status word, not a hang.  counter and dev_status are
+ * device pointers owned by the caller; 0 < limit_us <= 10^7, else
+ * MOE_ERR_INVALID_ARG.  Asynchronous on `stream`, not ordered by programmatic
+ * dependent launch (it waits for the stream's earlier work).
+ */
+moe_status_t moe_bounded_wait_check(const int32_t* counter, int target, int limit_us,
+                                    int32_t* dev_status, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -356,3 +356,10 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
 }
 
 }  // extern "C"
+
+moe_status_t moe_bounded_wait_check(const int32_t* counter, int target, int limit_us,
+                                    int32_t* dev_status, moe_stream_t stream) {
+  if (!counter || !dev_status || limit_us <= 0 || limit_us > 10000000) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_bounded_wait_check(counter, target, (uint64_t)limit_us * 1000,
+                                               dev_status, static_cast<cudaStream_t>(stream)));
+}

@@ -161,6 +161,15 @@ MOE_DEVICE bool wait_count_geq(const int32_t* p, int target, const volatile int*
   return false;
 }
 
+// one thread waits (bounded) until *counter >= target and reports
+// MOE_DEV_WAIT_TIMEOUT if the wait runs out: the wait the fused G1+G2 launch
+// uses for its cross-CTA dependency, on its own
+__global__ void __launch_bounds__(32)
+bounded_wait_kernel(const int32_t* counter, int target, uint64_t limit_ns, int32_t* dev_status) {
+  if (threadIdx.x == 0 && !wait_count_geq(counter, target, nullptr, limit_ns))
+    moe_set_status(dev_status, MOE_DEV_WAIT_TIMEOUT);
+}
+
 MOE_DEVICE void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -1231,6 +1240,13 @@ cudaError_t run_simt(bool fp8, const void* act, const void* wa, const void* wb, 
 }
 
 }  // namespace
+
+cudaError_t launch_bounded_wait_check(const int32_t* counter, int target, uint64_t limit_ns,
+                                      int32_t* dev_status, cudaStream_t stream) {
+  // a plain launch: it reads caller memory that earlier stream work may write
+  bounded_wait_kernel<<<1, 32, 0, stream>>>(counter, target, limit_ns, dev_status);
+  return cudaGetLastError();
+}
 
 size_t grouped_gemm_scratch_bytes(int R, int E_blocks) { return plan_bytes(R, E_blocks); }
 

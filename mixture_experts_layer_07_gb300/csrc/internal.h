@@ -48,6 +48,9 @@ size_t grouped_gemm_split_counter_bytes(int R, int E_blocks, int H, int I);
 size_t grouped_gemm_splitk_bytes(int R, int H, int I);
 
 // xp[flat_to_row[t*K+k]] = x[t] (the permute's copy step alone)
+// one bounded wait (the fused GEMM's cross-CTA wait) on *counter >= target
+cudaError_t launch_bounded_wait_check(const int32_t* counter, int target, uint64_t limit_ns,
+                                      int32_t* dev_status, cudaStream_t stream);
 cudaError_t launch_permute_copy(const void* x, const int32_t* flat_to_row, int T, int K, int H,
                                 void* xp, cudaStream_t stream);
 

@@ -31,7 +31,7 @@ EXPORTS = ["moe_status_string", "moe_default_m_skinny", "moe_block_variant", "mo
            "moe_topk_route", "moe_permute_scratch_bytes", "moe_permute",
            "moe_grouped_gemm_scratch_bytes", "moe_grouped_gemm", "moe_unpermute",
            "moe_workspace_bytes", "moe_layer", "moe_workspace_layout", "moe_permute_static",
-           "moe_router_tc_scratch_bytes", "moe_router_gemm_tc"]
+           "moe_router_tc_scratch_bytes", "moe_router_gemm_tc", "moe_bounded_wait_check"]
 
 PERMUTE_STATIC_SCRATCH_BYTES = 1 << 20
 
@@ -98,6 +98,7 @@ def _lib():
             "moe_workspace_layout": [ctypes.POINTER(Config), ctypes.POINTER(WorkspaceLayout)],
             "moe_layer": [ctypes.POINTER(Config), _I, _P, ctypes.POINTER(Weights), _P, _P, _S,
                           _P, _P],
+            "moe_bounded_wait_check": [_P, _I, _I, _P, _P],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -285,3 +286,8 @@ class MoELayer:
             n *= s
         nbytes = n * torch.empty((), dtype=dtype).element_size()
         return self.workspace[off:off + nbytes].view(dtype).view(*shape)
+
+
+def bounded_wait_check(counter, target, limit_us, dev_status, stream=None):
+    _check(_lib().moe_bounded_wait_check(_p(counter), target, limit_us, _p(dev_status),
+                                         _stream(stream)), "moe_bounded_wait_check")

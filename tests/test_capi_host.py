@@ -206,3 +206,11 @@ def test_layer_rejects_bad_arguments(ops):
     sh = _cfg(ops, has_shared=True, I_shared=64)
     assert lib.moe_layer(by(sh), 8, 0x1000, by(w), 0x1000, 0x10000,
                          ops.workspace_bytes(sh), None, None) == 1
+
+
+def test_bounded_wait_check_rejects_bad_arguments(ops):
+    f = "moe_bounded_wait_check"
+    assert call(ops, f, None, 1, 1000, 0x1000, None) == 1
+    assert call(ops, f, 0x1000, 1, 1000, None, None) == 1
+    assert call(ops, f, 0x1000, 1, 0, 0x1000, None) == 1
+    assert call(ops, f, 0x1000, 1, 10000001, 0x1000, None) == 1

@@ -2,6 +2,8 @@
 element against the CPU oracle on the same seeded inputs (tolerances in
 tests/gpu_util.py).  Sizes span several tiles and a ragged tail; full-size
 workloads are checked on sampled tokens in test_gpu_fullsize.py."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -551,6 +553,30 @@ def test_fused_routing_one_lane_holds_every_pick(ops, shared):
         assert np.array_equal(layer.view("flat_to_row", torch.int32, (T * K,)).cpu().numpy(), f2r)
         sw = layer.workspace[layer.layout.sync:layer.layout.logits].view(torch.int32)
         assert int(sw.abs().sum().item()) == 0
+
+
+def test_bounded_wait_runs_out_into_a_status_word(ops):
+    # the fused GEMM's cross-CTA wait, on a counter nothing increments: it
+    # must give up after its limit, report MOE_DEV_WAIT_TIMEOUT and leave the
+    # context usable; a satisfied wait returns at once with no status
+    counter = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sync()
+    t0 = time.perf_counter()
+    ops.bounded_wait_check(counter, 1, 20000, st)
+    sync()
+    assert time.perf_counter() - t0 >= 0.02
+    assert int(st.item()) == ops.DEV_WAIT_TIMEOUT
+    counter.fill_(7)
+    st.zero_()
+    ops.bounded_wait_check(counter, 7, 20000, st)
+    sync()
+    assert int(st.item()) == 0
+    # and the library still computes on this context
+    lg = synth.random_logits(64, 32, seed=3)
+    ids, w, _ = run_topk(ops, lg, 32, 4, 0, 1.0, None, False)
+    rid, rw = oracle.topk_softmax_renorm(lg.astype(np.float64), 32, 4)
+    assert np.array_equal(ids, rid)
 
 
 def test_layer_decode_path_repeats_and_leaves_sync_zero(ops):
