@@ -14,13 +14,20 @@ the host:
   stable counting sort and the work lists the variants imply, with
   out-of-range ids flagged.
 
+* sigmoid_emu.cpp -- the selection key's float32 sigmoid (sigmoid_key) and the
+  order-preserving key map (order_key) of csrc/topk_warp.cuh, compared bit
+  for bit with the oracle's float32 sigmoid and with float order.
+
 This pins the routing logic itself; the GPU parity tests pin the compiled
 kernels."""
 import os
 import shutil
 import subprocess
 
+import numpy as np
 import pytest
+
+import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 EMU = os.path.join(ROOT, "tests", "host_emu")
@@ -32,8 +39,7 @@ def _cuda_include():
     return inc if os.path.exists(os.path.join(inc, "cuda_runtime.h")) else None
 
 
-@pytest.mark.parametrize("program", ["topk_emu", "permute_plan_emu"])
-def test_routing_device_code_on_host(tmp_path, program):
+def _compile(tmp_path, program):
     cxx = shutil.which("g++")
     inc = _cuda_include()
     if not cxx or not inc:
@@ -45,5 +51,35 @@ def test_routing_device_code_on_host(tmp_path, program):
            "-o", str(exe), "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr[-2000:]
-    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=300)
+    return str(exe)
+
+
+@pytest.mark.parametrize("program", ["topk_emu", "permute_plan_emu"])
+def test_routing_device_code_on_host(tmp_path, program):
+    exe = _compile(tmp_path, program)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and r.stdout.strip().endswith("OK"), r.stdout[-3000:]
+
+
+def test_selection_key_formula_on_host(tmp_path):
+    # both sides evaluate one float32 formula op by op, so the device source's
+    # bits must equal the oracle's on every input, saturation edges included
+    exe = _compile(tmp_path, "sigmoid_emu")
+    x = np.linspace(-95, 95, 100001, dtype=np.float32)
+    x = np.concatenate([x, np.float32([0.0, -0.0, 1e-30, -1e-30, 87.0, -87.0, 88.0, -88.0,
+                                       88.5, -88.5, np.inf, -np.inf])])
+    inp = "\n".join(str(int(b)) for b in x.view(np.uint32)) + "\n"
+    r = subprocess.run([exe], input=inp, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0
+    out = np.array([[int(v) for v in ln.split()] for ln in r.stdout.split("\n") if ln],
+                   dtype=np.uint64)
+    sig = out[:, 0].astype(np.uint32)
+    ref = oracle.sigmoid_f32(x[np.isfinite(x)]).view(np.uint32)
+    assert np.array_equal(sig[np.isfinite(x)], ref)
+    # order_key: monotone in float order, -0 and +0 equal, and never 0
+    key = out[:, 1].astype(np.uint32)
+    order = np.argsort(x, kind="stable")
+    xs, ks = x[order], key[order]
+    assert (np.diff(ks.astype(np.int64)) >= 0).all()
+    assert ((np.diff(ks.astype(np.int64)) == 0) == (np.diff(xs) == 0)).all()
+    assert (key != 0).all()
