@@ -263,37 +263,59 @@ def router_compute(T):
     return "bf16x3" if T >= ROUTER_TC_MIN_T else "alu"
 
 
-def traffic_record(kernel_file):
-    """Per-launch DRAM traffic from a committed ncu summary, only while the
-    kernel source is unchanged since it was captured."""
+def traffic_record(workload, T, kernel_file):
+    """Per-launch DRAM traffic of the grouped-GEMM stage for this workload and
+    batch from a committed ncu summary (profiles/traffic.json), only while the
+    kernel source is unchanged since it was captured; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         rec = json.load(open(p))
+        recs = rec.get("records", [rec])
         src = open(os.path.join(ROOT, "mixture_experts_layer_07_gb300", "csrc", kernel_file), "rb").read()
-        if rec.get("source_sha256") != hashlib.sha256(src).hexdigest():
-            return None
-        return rec.get("traffic_bytes_per_step")
+        sha = hashlib.sha256(src).hexdigest()
+        for r in recs:
+            if (r.get("workload_name") == workload and r.get("T") == T
+                    and r.get("source_sha256") == sha):
+                return r.get("traffic_bytes_per_step")
+        return None
     except Exception:
         return None
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args, rank, world, local_rank):
+# The five workloads, each at the batch its roofline is quoted on: the tiny
+# layer, the Qwen3-30B-A3B-shaped layer (the headline line), the GPT-OSS-20B
+# shape at its prefill batch (the tensor-bound FP8 case), the 512-expert
+# shared-gate layer and the 896-expert routing stress layer.
+DEFAULT_CONFIGS = (("tiny", 16), ("qwen3_30b_a3b", 2048), ("gpt_oss_20b", 4096),
+                   ("shared_gate", 1024), ("high_expert", 512))
+# oracle tokens per CPU-baseline sample (about 5-10 s of host work each)
+CPU_TOKENS = {"tiny": 32768, "qwen3_30b_a3b": 32768, "gpt_oss_20b": 4096,
+              "shared_gate": 16384, "high_expert": 4}
+
+
+def make_layer(spec, T, seed, dev):
     from mixture_experts_layer_07_gb300 import ops, synth
 
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    peaks = load_peaks()
-    spec = synth.SPECS[args.workload]
-    T = args.T
-    d = synth.device_inputs(spec, T, seed=rank, device=f"cuda:{local_rank}")
+    d = synth.device_inputs(spec, T, seed=seed, device=dev)
     t = tensors_of(spec, d)
     cfg = ops.make_config(T, spec.H, spec.E, spec.K, spec.I, has_shared=spec.has_shared,
                           I_shared=spec.I_shared, mode=spec.mode, routed_scale=spec.routed_scale,
                           wdtype=ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16)
-    layer = ops.MoELayer(cfg, t, device=dev)
+    return d, t, ops.MoELayer(cfg, t, device=dev)
+
+
+def measure(spec, T, args, rank, world, dev, peaks, light=False):
+    """Time one workload at batch T: device-resident steps (the number the
+    line reports), the same layer as a CUDA graph, each stage alone against
+    its roofline, end to end through host buffers, and (rank 0) a cold-L2 T
+    sweep and the oracle on the host cores.  ``light``: N > 1 replicas of a
+    secondary workload, steps and stages only."""
+    from mixture_experts_layer_07_gb300 import ops
+
+    d, t, layer = make_layer(spec, T, rank, dev)
     x = d["x"]
     out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
@@ -305,7 +327,7 @@ def run_ours(args, rank, world, local_rank):
     # ---- device-resident timed region.  The clock sampler starts with the
     # warm-up, which runs for at least one second, so its samples cover the GPU
     # under this load right up to and through the timed steps.
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     t_start = time.perf_counter()
     n_w = 0
@@ -327,34 +349,36 @@ def run_ours(args, rank, world, local_rank):
     ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     st = int(layer.dev_status.item())
     if st != 0:
-        raise RuntimeError(f"device status {st}")
+        raise RuntimeError(f"{spec.name} T={T}: device status {st}")
     ms_step = ms / args.steps
+    tokens = T * args.steps * world
 
     # ---- the same layer captured once as a CUDA graph and replayed
     graph_ms = None
-    try:
-        side = torch.cuda.Stream()
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            layer(x, out)
-        stream.wait_stream(side)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            layer(x, out)
-        for _ in range(args.warmup):
-            g.replay()
-        torch.cuda.synchronize()
-        barrier()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(args.steps):
-            g.replay()
-        g1.record(stream)
-        torch.cuda.synchronize()
-        graph_ms = max_over_ranks(g0.elapsed_time(g1), world, dev)
-        del g
-    except Exception as e:  # report, do not hide: the stream number stands
-        log("graph capture failed:", repr(e))
+    if not light:
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                layer(x, out)
+            stream.wait_stream(side)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                layer(x, out)
+            for _ in range(args.warmup):
+                g.replay()
+            torch.cuda.synchronize()
+            barrier()
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            g1.record(stream)
+            torch.cuda.synchronize()
+            graph_ms = max_over_ranks(g0.elapsed_time(g1), world, dev)
+            del g
+        except Exception as e:  # report, do not hide: the stream number stands
+            log("graph capture failed:", repr(e))
 
     # ---- per-stage times (same workspace, stages called one by one)
     L = layer.layout
@@ -382,7 +406,6 @@ def run_ours(args, rank, world, local_rank):
     sh_y = v("shared_y", torch.bfloat16, (T, H)) if spec.has_shared else None
     wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
     names = ["router", "topk", "permute", "grouped_gemm", "unpermute"]
-
     rscr = ws[L.router_split:L.splitk]
 
     def router():
@@ -434,8 +457,29 @@ def run_ours(args, rank, world, local_rank):
                        router_compute(T) if dom == "router" else STAGE_COMPUTE[dom])
     roof = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()}
     roof["kernel"] = dom
+    roof["algorithmic"] = ({"bytes": sbf[dom]["bytes"]} if roof["unit"] == "GB/s"
+                           else {"flops": sbf[dom]["flops"]})
     roof["peak_source"] = f"of {peaks['source']}"
-    roof["traffic"] = traffic_record("grouped_gemm.cu") if dom == "grouped_gemm" else None
+    roof["traffic"] = (traffic_record(spec.name, T, "grouped_gemm.cu")
+                       if dom == "grouped_gemm" else None)
+    hot = (float(np.isin(ids_h, list(spec.hot_experts)).mean()) if spec.hot_experts else None)
+
+    res = {"workload": spec.name, "T": T, "H": spec.H, "E": spec.E, "K": spec.K, "I": spec.I,
+           "dtype": "bf16" if spec.wdtype == "bf16" else "bf16 activations, fp8-e4m3 weights",
+           "us_per_layer": round(ms_step * 1e3, 2),
+           "tokens_per_s": round(job_throughput(T, args.steps, world, ms), 1),
+           "ms_total": ms, "roofline": roof, "per_stage": per_stage, "clocks": clk,
+           "e_active": e_active, "gpu_launches_per_layer": launches_per_layer(spec, T)}
+    if hot is not None:
+        res["hot_expert_share"] = round(hot, 4)
+    if graph_ms is not None:
+        res["graph"] = {"value": round(tokens / (graph_ms / 1e3), 1), "unit": "tokens/s",
+                        "us_per_layer": round(graph_ms / args.steps * 1e3, 2),
+                        "note": "same layer captured once as a CUDA graph, replayed K times"}
+    if light:
+        del layer, d, t
+        torch.cuda.empty_cache()
+        return res
 
     # ---- end to end through the C ABI with host buffers.  Every step copies
     # its input from pinned host memory and its output back to pinned host
@@ -493,11 +537,16 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     # every step's output reached the host
     assert torch.equal(out_host[(args.steps - 1) % 2].to(dev), out_dev[(args.steps - 1) % 2])
+    res["e2e"] = {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                  "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
+                  "note": ("pinned host buffers; copies on their own streams, double-buffered, "
+                           "overlapping neighbouring steps' layers") if pipelined else
+                          "pinned host buffers; copies in order on the layer's stream"}
+    del x_host, out_host, x_dev, out_dev
 
     # ---- T sweep (rank 0 only, short): stream launches and graph replay.
     # Below T ~ 100 the experts a call touches fit in L2, so every timed call
     # is preceded by a 256 MB write (outside its events) that flushes L2.
-    sweep = None
     if rank == 0 and args.sweep:
         sweep = []
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -534,26 +583,40 @@ def run_ours(args, rank, world, local_rank):
                 log("graph capture failed:", repr(e))
             sweep.append(row)
         del flush
+        res["sweep"] = sweep
+        if int(layer.dev_status.item()) != 0:
+            raise RuntimeError(f"{spec.name}: device status {int(layer.dev_status.item())}")
 
-    # ---- CPU baseline (rank 0, N=1 only)
-    cpu = None
+    # ---- CPU baseline (rank 0, N=1 only): the oracle on the host cores
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(spec, T, args.cpu_tokens)
+        res["cpu_baseline"] = cpu_baseline(spec, d, args.cpu_tokens or CPU_TOKENS[spec.name])
+    del layer, d, t
+    torch.cuda.empty_cache()
+    return res
 
-    tokens = T * args.steps * world
+
+def run_ours(args, rank, world, local_rank):
+    from mixture_experts_layer_07_gb300 import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks = load_peaks()
+    head_spec = synth.SPECS[args.workload]
+    head = measure(head_spec, args.T, args, rank, world, dev, peaks)
+    spec, T = head_spec, args.T
     res = {
         "metric": METRIC,
-        "value": round(job_throughput(T, args.steps, world, ms), 1),
+        "value": head["tokens_per_s"],
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 4),
-        "us_per_layer": round(ms_step * 1e3, 2),
+        "ms_per_step": round(head["ms_total"] / args.steps, 4),
+        "us_per_layer": head["us_per_layer"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if spec.wdtype == "bf16" else "bf16 activations, fp8-e4m3 weights",
+        "dtype": head["dtype"],
         "data": "synthetic (seeded; random-init weights of the named layer shape)",
         "config": {"workload": f"{spec.name} MoE layer", "T": T, "H": spec.H, "E": spec.E,
                    "K": spec.K, "I": spec.I, "routing": "softmax top-K renormalised"
@@ -562,26 +625,34 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (expert weights "
                          f"{spec.E * 3 * spec.H * spec.I * (1 if spec.wdtype == 'fp8' else 2) / 1e9:.2f} GB "
                          "per layer), no flush"},
-        "roofline": roof,
-        "per_stage": per_stage,
-        "graph": None if graph_ms is None else {
-            "value": round(tokens / (graph_ms / 1e3), 1), "unit": "tokens/s",
-            "us_per_layer": round(graph_ms / args.steps * 1e3, 2),
-            "note": "same layer captured once as a CUDA graph, replayed K times"},
-        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": x.numel() * x.element_size(),
-                "d2h_bytes_per_step": out.numel() * out.element_size(),
-                "note": ("pinned host buffers; copies on their own streams, double-buffered, "
-                         "overlapping neighbouring steps' layers") if pipelined else
-                        "pinned host buffers; copies in order on the layer's stream"},
-        "gpu_launches": launches_per_layer(spec, T) * args.steps,
-        "clocks": clk,
-        "cpu_baseline": cpu,
+        "roofline": head["roofline"],
+        "per_stage": head["per_stage"],
+        "graph": head.get("graph"),
+        "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches_per_layer"] * args.steps,
+        "clocks": head["clocks"],
+        "cpu_baseline": head.get("cpu_baseline"),
     }
-    if sweep is not None:
-        res["sweep"] = sweep
+    if "sweep" in head:
+        res["sweep"] = head["sweep"]
+    if args.configs:
+        # every workload at its own batch (the headline's entry is the headline
+        # measurement itself); each entry carries its own roofline, per-stage
+        # fractions, CPU baseline and T sweep
+        confs = []
+        for name, Tc in DEFAULT_CONFIGS:
+            if name == head_spec.name and Tc == args.T:
+                r = head
+            else:
+                r = measure(synth.SPECS[name], Tc, args, rank, world, dev, peaks,
+                            light=world > 1)
+            confs.append({k: v for k, v in r.items() if k != "ms_total"})
+        res["configs"] = confs
     if rank == 0 and args.extra:
-        res["stage_sweep_large_T"] = stage_sweep(spec, (16384, 65536, 262144), peaks, dev)
+        res["stage_sweep_large_T"] = stage_sweep(synth.SPECS["qwen3_30b_a3b"],
+                                                 (16384, 65536, 262144), peaks, dev)
+        res["stage_sweep_large_T_high_expert"] = stage_sweep(synth.SPECS["high_expert"],
+                                                             (16384,), peaks, dev)
         res["prefill_grouped_gemm"] = prefill_points(peaks, dev)
     return res
 
@@ -685,6 +756,27 @@ def probe_stages(spec, T, reps, dev):
     return {"probe": "stages", "workload": spec.name, "T": T, "reps": reps}
 
 
+def probe_layer(spec, T, reps, dev):
+    """The whole layer (``moe_layer``) at T, `reps` calls, no timing: the
+    command the per-kernel ncu captures of the layer profile."""
+    from mixture_experts_layer_07_gb300 import ops, synth
+
+    d = synth.device_inputs(spec, T, seed=1, device=dev)
+    t = tensors_of(spec, d)
+    cfg = ops.make_config(T, spec.H, spec.E, spec.K, spec.I, has_shared=spec.has_shared,
+                          I_shared=spec.I_shared, mode=spec.mode, routed_scale=spec.routed_scale,
+                          wdtype=ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16)
+    layer = ops.MoELayer(cfg, t, device=dev)
+    out = torch.empty_like(d["x"])
+    for _ in range(reps):
+        layer(d["x"], out)
+    torch.cuda.synchronize()
+    st = int(layer.dev_status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+    return {"probe": "layer", "workload": spec.name, "T": T, "reps": reps}
+
+
 def prefill_points(peaks, dev):
     """The grouped GEMM stage on prefill shapes where it is tensor-bound."""
     from mixture_experts_layer_07_gb300 import ops, synth
@@ -744,13 +836,70 @@ def oracle_time(inp, t0, n):
     return time.perf_counter() - start
 
 
-def cpu_baseline(spec, T, tokens):
+class HostExperts:
+    """[E, rows, cols] stored expert weights on the host, holding only the
+    experts a sample of tokens routes to (indexing another one is an error)."""
+
+    def __init__(self, shape, parts):
+        self.shape, self.parts = tuple(shape), parts
+
+    def __getitem__(self, e):
+        return self.parts[int(e)]
+
+    def __len__(self):
+        return self.shape[0]
+
+
+def oracle_inputs_from_device(spec, d, tokens, seed=0):
+    """An oracle input dict for `tokens` host-drawn tokens of the workload,
+    with the gate and the expert weights copied from the device draw ``d``:
+    only the experts the oracle's own routing of those tokens picks (found
+    before any timing), so a layer with tens of GB of experts needs only
+    what the sample touches on the host."""
+    import oracle
+    from mixture_experts_layer_07_gb300 import synth
+
+    inp = synth.host_inputs(spec, tokens, seed=seed, weights=False)
+    inp["wg"] = d["wg"].cpu().numpy()
+    inp["gate_bias"] = None if d["gate_bias"] is None else d["gate_bias"].cpu().numpy()
+    inp["sel_bias"] = None if d["sel_bias"] is None else d["sel_bias"].cpu().numpy()
+    x = oracle.bf16_to_f64(inp["x_bits"])
+    lg = oracle.router_logits(x, inp["wg"], inp["gate_bias"])
+    if spec.mode == 0:
+        ids, _ = oracle.topk_softmax_renorm(lg, spec.E, spec.K)
+    else:
+        ids, _ = oracle.topk_sigmoid_bias(lg.astype(np.float32), inp["sel_bias"], spec.E,
+                                          spec.K, spec.routed_scale)
+    used = sorted(set(ids.ravel().tolist()))
+
+    def bits(t):
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+    if spec.wdtype == "fp8":
+        for k, sk in (("w1", "s1"), ("w3", "s3"), ("w2", "s2")):
+            q, s = d[k + "_q"], d[sk]
+            inp[k + "_q"] = HostExperts(q.shape, {e: q[e].cpu().numpy() for e in used})
+            inp[sk] = HostExperts(s.shape, {e: s[e].cpu().numpy() for e in used})
+    else:
+        for k in ("w1", "w3", "w2"):
+            w = d[k]
+            inp[k + "_bits"] = HostExperts(w.shape, {e: bits(w[e]) for e in used})
+    if spec.has_shared:
+        for k in ("sw1", "sw3", "sw2"):
+            inp[k + "_bits"] = bits(d[k])
+    return inp, len(used)
+
+
+def cpu_baseline(spec, d, tokens):
+    """The oracle as it stands, timed on the host cores on a bounded sample of
+    the workload (`tokens` tokens, the experts they route to)."""
     cores = len(os.sched_getaffinity(0))
-    inp = host_workload(spec, tokens, seed=0)
+    inp, n_exp = oracle_inputs_from_device(spec, d, tokens)
     sec = oracle_time(inp, 0, tokens)
-    return {"value": round(tokens / sec, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{tokens} tokens of the {spec.name} workload (same shapes, all {spec.E} "
-                      f"experts, host draw), float64 numpy oracle, one pass, {sec:.1f} s"}
+    return {"value": round(tokens / sec, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{tokens} tokens of the {spec.name} workload (same shapes; gate and the "
+                      f"{n_exp} experts they route to copied from the device draw), float64 "
+                      f"numpy oracle, one pass, {sec:.1f} s"}
 
 
 def run_reference(args):
@@ -792,6 +941,36 @@ def run_reference(args):
     }
 
 
+def _free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def spawn_ranks(n):
+    """Run this script as n ranks on this node and return their exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
+def print_launch_check(rank, world):
+    """Rank start-up and the timing reduction alone, on CPU over gloo: every
+    rank reports a time of its own, the slowest one wins, rank 0 prints it."""
+    if world > 1:
+        torch.distributed.init_process_group("gloo")
+    try:
+        ms = max_over_ranks(10.0 + rank, world)
+        if rank == 0:
+            print(json.dumps({"launch_check": True, "n_gpus": world, "max_ms": ms,
+                              "value": job_throughput(1, 1, world, ms)}), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -800,21 +979,41 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_30b_a3b")
     ap.add_argument("--T", type=int, default=2048)
-    ap.add_argument("--cpu-tokens", type=int, default=32768)
+    ap.add_argument("--cpu-tokens", type=int, default=0,
+                    help="oracle tokens per CPU-baseline sample (0: per-workload default)")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="time only the headline workload, not all five")
+    ap.add_argument("--no-extra", dest="extra", action="store_false",
+                    help="skip the large-T stage sweep and the prefill GEMM points")
+    ap.add_argument("--launch-check", action="store_true",
+                    help="rank start-up and max-over-ranks timing only, on CPU (gloo)")
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--probe-stages", type=int, default=0, metavar="T",
                     help="only run R/K/P/U at this T a few times (for ncu captures)")
-    ap.add_argument("--extra", action="store_true",
-                    help="also time R/K/P/U at large T and the grouped GEMM on prefill shapes")
+    ap.add_argument("--probe-layer", type=int, default=0, metavar="T",
+                    help="only run moe_layer at this T a few times (for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
 
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # asked for N GPUs without a launcher: start one rank per GPU on this
+        # node (torch.distributed.run, rendezvous on 127.0.0.1) and pass rank
+        # 0's line through
+        sys.exit(spawn_ranks(args.gpus))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus and rank == 0:
+        log(f"--gpus {args.gpus} but the launcher started {world} ranks: timing {world}")
+
+    if args.launch_check:
+        print_launch_check(rank, world)
+        return
 
     if args.impl == "reference":
         if rank != 0:
@@ -827,6 +1026,13 @@ def main():
         torch.cuda.set_device(local_rank)
         print(json.dumps(probe_stages(synth.SPECS[args.workload], args.probe_stages, 3,
                                       f"cuda:{local_rank}")), flush=True)
+        return
+
+    if args.probe_layer:
+        from mixture_experts_layer_07_gb300 import synth
+        torch.cuda.set_device(local_rank)
+        print(json.dumps(probe_layer(synth.SPECS[args.workload], args.probe_layer, 3,
+                                     f"cuda:{local_rank}")), flush=True)
         return
 
     if world > 1:

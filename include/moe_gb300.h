@@ -240,12 +240,18 @@ moe_status_t moe_permute(const void* x, const int32_t* ids, int T, int H, int E,
  * results and errors as moe_permute, minus scratch / scratch_bytes.
  *   - The scratch is a fixed array of MOE_PERMUTE_STATIC_SCRATCH_BYTES inside
  *     the library, held on every GPU that loads the library until the process
- *     exits.  Sizes whose moe_permute_scratch_bytes(T, E, K) exceeds it return
- *     MOE_ERR_WORKSPACE before anything is queued (1 MiB covers, e.g.,
- *     T*K up to 32768 at E = 1024, or up to 262144 at E = 128).
+ *     exits.  It holds one int32 count per expert for every chunk of 256
+ *     replicas, so sizes whose moe_permute_scratch_bytes(T, E, K) exceeds it
+ *     return MOE_ERR_WORKSPACE before anything is queued: the largest accepted
+ *     T*K is 255 chunks (65280 replicas) at E = 1024, 292 chunks (74752) at
+ *     E = 896, 511 chunks (130816) at E = 512 and 2047 chunks (524032) at
+ *     E = 128.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.  No cudaMalloc, cudaFree or allocating routine is called.
+ *     that device current) and caches it with the device's current context;
+ *     a call that finds another context (after cudaDeviceReset) looks it up
+ *     again.  Make the first call on a device, and the first after a reset,
+ *     before any stream capture.  No cudaMalloc, cudaFree or allocating
+ *     routine is called.
  *   - Every call shares the array and it keeps the last call's contents
  *     (nothing in it needs to start at zero).  Calls whose kernels may overlap
  *     on the GPU -- on different streams without ordering, or from different

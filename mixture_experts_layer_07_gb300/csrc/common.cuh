@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "moe_gb300.h"
@@ -97,4 +98,22 @@ static inline cudaError_t moe_launch(void (*kernel)(KArgs...), dim3 grid, dim3 b
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to the (function, device) pair, so a process
+// that launches on several GPUs must set it on each: `done` holds one bit per
+// device index already set (devices past 63 set it on every launch).  Setting
+// it twice is harmless, so two host threads racing here only repeat the call.
+template <typename... KArgs>
+static inline cudaError_t moe_raise_smem(void (*kernel)(KArgs...), size_t bytes,
+                                         std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }

@@ -1004,16 +1004,16 @@ bool make_act_map(CUtensorMap* m, const void* a, int R, int Kdim, int bn) {
 }
 
 int num_sms() {
-  static int n[64] = {0};
+  static std::atomic<int> n[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!n[dev]) {
-    int v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  int v = n[dev].load(std::memory_order_relaxed);
+  if (!v) {
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    n[dev] = v > 0 ? v : 148;
+    v = v > 0 ? v : 148;
+    n[dev].store(v, std::memory_order_relaxed);
   }
-  return n[dev];
+  return v;
 }
 
 // One launch of the tensor-core kernel over a list.  FUSED: the list's G1
@@ -1030,13 +1030,10 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
                    const int32_t* grows = nullptr, int gk = 0, int ksplit2 = 1,
                    float* part2 = nullptr, int32_t* scnt1 = nullptr, int32_t* scnt2 = nullptr) {
   using C = TcCfg<BN, SWIGLU, WFP8>;
-  static bool attr_set = false;  // per process; the attribute is per function, all devices
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, SWIGLU, WFP8, FUSED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmemBytes);
+  static std::atomic<unsigned long long> smem_set{0};  // devices whose limit is raised
+  {
+    cudaError_t e = moe_raise_smem(gemm_tc_kernel<BN, SWIGLU, WFP8, FUSED>, C::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const long long work =
       (long long)cap * (moe_cdiv(N, kBM) * ksplit + (FUSED ? moe_cdiv(N2, kBM) * ksplit2 : 0));
@@ -1069,12 +1066,10 @@ cudaError_t run_tc_dual(const CUtensorMap& wa, const CUtensorMap& wb, const Dual
   using C0 = TcCfg<kBnSkinny, SWIGLU, WFP8>;
   using C1 = TcCfg<kBnTile, SWIGLU, WFP8>;
   const size_t smem = C0::kSmemBytes > C1::kSmemBytes ? C0::kSmemBytes : C1::kSmemBytes;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_dual_kernel<SWIGLU, WFP8, FUSED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static std::atomic<unsigned long long> smem_set{0};  // devices whose limit is raised
+  {
+    cudaError_t e = moe_raise_smem(gemm_tc_dual_kernel<SWIGLU, WFP8, FUSED>, smem, smem_set);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const int grid = num_sms();
   return moe_launch(gemm_tc_dual_kernel<SWIGLU, WFP8, FUSED>, dim3(grid), dim3(C0::kThreads), smem,

@@ -255,14 +255,10 @@ cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int 
   const int ctas = moe_cdiv(nch, kWarpsPerCta);
   const size_t fused_smem = ((size_t)(kFusedWarps + 1) * E + 1) * sizeof(int32_t);
   if (R > 0 && R <= kFusedMaxR && fused_smem <= 200 * 1024) {
-    static bool attr = false;
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(permute_fused_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    cudaError_t e = moe_launch(permute_fused_kernel, dim3(1), dim3(32 * kFusedWarps), fused_smem,
+    static std::atomic<unsigned long long> smem_set{0};  // devices whose limit is raised
+    cudaError_t e = moe_raise_smem(permute_fused_kernel, 200 * 1024, smem_set);
+    if (e != cudaSuccess) return e;
+    e = moe_launch(permute_fused_kernel, dim3(1), dim3(32 * kFusedWarps), fused_smem,
                                stream, 1, ids, R, E, offsets, row_to_flat, flat_to_row, dev_status);
     if (e != cudaSuccess || !xp) return e;
     return launch_copy(x, flat_to_row, T, K, H, xp, stream);
@@ -289,17 +285,41 @@ cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int 
 // call on a device and keeps the previous call's contents; the count kernel
 // overwrites every entry it later reads, so nothing needs clearing.  Two calls
 // whose kernels overlap on the GPU (different streams, no ordering) race on it.
+#include <cuda.h>
+
 #include <mutex>
 
 static __device__ __align__(256) unsigned char g_permute_static_scratch[MOE_PERMUTE_STATIC_SCRATCH_BYTES];
 
 namespace {
 
-// Device address of the array, looked up once per device with that device
-// current (in host code the symbol is only a host-side stand-in).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The driver's current context, to tell a cached address from a stale one.
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  CUcontext c = nullptr;
+  if (fn) fn(&c);
+  return c;
+}
+
+// Device address of the array on the current device (in host code the symbol
+// is only a host-side stand-in).  Looked up with that device current and
+// cached per device together with the context it belongs to: after a
+// cudaDeviceReset the device gets a new context, the module is loaded again
+// and the array may sit elsewhere, so a changed context means a new lookup.
 void* static_scratch_address(cudaError_t* err) {
   static std::mutex mu;
   static void* addr[64] = {nullptr};
+  static CUcontext ctx_of[64] = {nullptr};
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return nullptr;
@@ -307,12 +327,14 @@ void* static_scratch_address(cudaError_t* err) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
+  const CUcontext ctx = current_context();  // null before the runtime binds one
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || !ctx || ctx_of[dev] != ctx) {
     void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_permute_static_scratch);
+    *err = cudaGetSymbolAddress(&p, g_permute_static_scratch);  // binds the context
     if (*err != cudaSuccess) return nullptr;
     addr[dev] = p;
+    ctx_of[dev] = current_context();
   }
   return addr[dev];
 }

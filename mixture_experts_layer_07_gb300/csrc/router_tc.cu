@@ -285,23 +285,32 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  return dev;
+}
+
+// per device: SM counts (and cluster occupancies below) differ between GPUs
 int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0, v = 0;
-    cudaGetDevice(&dev);
+  static std::atomic<int> n[64];
+  const int dev = current_device();
+  int v = n[dev].load(std::memory_order_relaxed);
+  if (!v) {
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    n = v > 0 ? v : 148;
+    v = v > 0 ? v : 148;
+    n[dev].store(v, std::memory_order_relaxed);
   }
-  return n;
+  return v;
 }
 
 // clusters of `splits` CTAs of this kernel that fit on the GPU at once
 // (with one CTA per SM the GPC layout, not the SM count, decides)
 template <int MT>
 int max_active_clusters(int splits) {
-  static int cache[9] = {0};
-  if (!cache[splits]) {
+  static std::atomic<int> cache_all[64][9];
+  std::atomic<int>* cache = cache_all[current_device()];
+  if (!cache[splits].load(std::memory_order_relaxed)) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, splits);
     cfg.blockDim = dim3(192);
@@ -318,22 +327,19 @@ int max_active_clusters(int splits) {
       cudaGetLastError();
       n = sm_count() / (2 * splits);  // conservative
     }
-    cache[splits] = n > 0 ? n : 1;
+    cache[splits].store(n > 0 ? n : 1, std::memory_order_relaxed);
   }
-  return cache[splits];
+  return cache[splits].load(std::memory_order_relaxed);
 }
 
 template <int MT>
 cudaError_t run(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias, float* logits,
                 int T, int H, int G, int32_t* dev_status, cudaStream_t stream) {
   using C = RtCfg<MT>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(router_tc_kernel<MT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmemBytes);
+  static std::atomic<unsigned long long> smem_set{0};  // devices whose limit is raised
+  {
+    cudaError_t e = moe_raise_smem(router_tc_kernel<MT>, C::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const int tiles = moe_cdiv(G, kTile) * moe_cdiv(T, kTile * MT);
   // split H over a cluster while all clusters still run in one wave and every

@@ -49,3 +49,23 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.25, 1) == 3.25
     assert bench.job_throughput(16, 10, 1, 2.0) == pytest.approx(16 * 10 / 0.002)
+
+
+def test_bench_gpus_flag_starts_that_many_ranks():
+    # `bench.py --gpus 2` without a launcher starts two ranks itself
+    # (torch.distributed.run on 127.0.0.1); with --launch-check they meet over
+    # gloo on CPU, reduce their times (the slowest wins) and rank 0 prints
+    # n_gpus = 2
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2",
+                        "--launch-check"], capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    rec = json.loads(lines[0])
+    assert rec["n_gpus"] == 2 and rec["max_ms"] == 11.0

@@ -45,18 +45,29 @@ def permute_both(ops, T, K, E, H, seed):
     return outs
 
 
-def test_static_scratch_permute_matches_scratch_permute_twice(ops):
-    # two different problems back to back: the second runs on what the first
-    # left in the built-in array
-    for T, K, E, H, seed in ((2048, 8, 128, 2048, 1), (512, 16, 1024, 64, 2)):
-        a, b = permute_both(ops, T, K, E, H, seed)
+# (T, K, E, H, seed).  Decode sizes (T*K <= 4096) take the one-CTA permute,
+# which keeps its counts in shared memory; larger ones the count / scan /
+# scatter kernels, whose chunk counts live in the built-in array.  4080 x 16
+# replicas at E = 1024 is the largest size the array holds (255 chunks of 256).
+CASES = [(1, 8, 128, 2048, 3), (8, 8, 128, 2048, 4), (2048, 8, 128, 2048, 1),
+         (512, 16, 1024, 64, 2), (4080, 16, 1024, 16, 5)]
+
+
+@pytest.mark.parametrize("T,K,E,H,seed", CASES)
+def test_static_scratch_permute_matches_scratch_permute_twice(ops, T, K, E, H, seed):
+    # the same problem twice in a row, then another one: each later call runs
+    # on what the earlier one left in the built-in array
+    if T * K == 65280:
+        assert ops.permute_scratch_bytes(T, E, K) <= ops.PERMUTE_STATIC_SCRATCH_BYTES
+    for s in (seed, seed, seed + 100):
+        a, b = permute_both(ops, T, K, E, H, s)
         assert a[4] == 0 and b[4] == 0
         for u, v in zip(a[:4], b[:4]):
             assert torch.equal(u, v)   # integer and copied bytes: bit for bit
 
 
 def test_static_scratch_rejects_sizes_beyond_its_maximum(ops):
-    T, K, E = 4096, 16, 1024       # needs 256 chunks x 1024 x 4 B > 1 MiB
+    T, K, E = 4081, 16, 1024       # one replica past 255 chunks: 256 x 1024 x 4 B > 1 MiB
     assert ops.permute_scratch_bytes(T, K=K, E=E) > ops.PERMUTE_STATIC_SCRATCH_BYTES
     rc = ops.lib().moe_permute_static(None, 0x1000, T, 64, E, K, 0x1000, 0x1000, 0x1000, None,
                                       None, None)
