@@ -80,7 +80,9 @@ typedef enum {
 typedef enum {
   MOE_DISPATCH_PER_BLOCK = 0,  /* from the block's own m_size ([dispatch] after) */
   MOE_DISPATCH_GLOBAL_AVG = 1, /* from max(1, R/E) for every block ([dispatch] before) */
-  MOE_DISPATCH_SIMT = 2        /* every block on the CUDA-core kernel (cross-check) */
+  MOE_DISPATCH_SIMT = 2,       /* every block on the CUDA-core kernel (cross-check) */
+  MOE_DISPATCH_ONE_LAUNCH = 3  /* moe_layer only: every batch of T <= 16 as one launch (see
+                                  moe_layer); blocks otherwise as MOE_DISPATCH_PER_BLOCK */
 } moe_dispatch_t;
 
 /* Variant codes reported per expert block. */
@@ -323,9 +325,18 @@ moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes);
  *              counters) must be zero before the first call -- e.g. zero the
  *              whole workspace once after allocating it; every call leaves it
  *              zero again.
- * For T <= 32 the router, top-K, permute and the GEMM plan run as one fused
- * launch (the small-batch regime where launch count dominates); the results
- * are the same as those of the separate steps.
+ * Small batches ([router] "why" 1: at low concurrency launches and round trips
+ * between them set the time; [permute] performance table):
+ *   - the whole layer -- router, top-K, permute, G1/G2, shared expert and the
+ *     combine -- runs as ONE cooperative launch of one CTA per SM (bf16 expert
+ *     weights, T <= 16) when cfg->dispatch is MOE_DISPATCH_ONE_LAUNCH, or,
+ *     under MOE_DISPATCH_PER_BLOCK, where it measured faster than the
+ *     multi-launch path: a shared expert with T <= 4, or E <= 128 with
+ *     4 <= T <= 8;
+ *   - otherwise for T <= 32 the router, top-K, permute and the GEMM plan run
+ *     as one fused launch, followed by the GEMM and combine launches.
+ * The results are those of the separate steps (same routing and permutation
+ * bit for bit, the same arithmetic up to the order of fp32 sums).
  */
 moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_weights_t* w,
                        void* out, void* workspace, size_t workspace_bytes,

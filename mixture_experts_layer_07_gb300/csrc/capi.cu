@@ -31,12 +31,33 @@ moe_status_t check_cfg(const moe_config_t* c) {
   if (c->mode != MOE_SCORE_SOFTMAX_RENORM && c->mode != MOE_SCORE_SIGMOID_BIAS_SCALED)
     return MOE_ERR_INVALID_ARG;
   if (c->wdtype != MOE_W_BF16 && c->wdtype != MOE_W_FP8E4M3_B128) return MOE_ERR_UNSUPPORTED;
-  if (c->dispatch < MOE_DISPATCH_PER_BLOCK || c->dispatch > MOE_DISPATCH_SIMT)
+  if (c->dispatch < MOE_DISPATCH_PER_BLOCK || c->dispatch > MOE_DISPATCH_ONE_LAUNCH)
     return MOE_ERR_INVALID_ARG;
   if (c->m_skinny < -1) return MOE_ERR_INVALID_ARG;
   if (c->has_shared && (c->I_shared <= 0 || c->I_shared % 16 != 0)) return MOE_ERR_INVALID_ARG;
   if ((int64_t)c->T_max * c->K > 0x7fffffff / 2) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
+}
+
+// byte offset of the one-launch small-batch layer's counters inside `sync`
+// (after the fused routing's 256 bytes and the K-slice counters)
+size_t decode_sync_offset(const moe_config_t* c) {
+  const int ms = c->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : c->m_skinny;
+  const int tsp = c->T_max < ms ? c->T_max : ms;
+  return 256 + moe_align_up(grouped_gemm_split_counter_bytes(tsp * c->K, c->E, c->H, c->I), 256);
+}
+
+// Whether moe_layer runs this batch as one launch (decode_layer.cu): always
+// under MOE_DISPATCH_ONE_LAUNCH; under MOE_DISPATCH_PER_BLOCK where it measured
+// faster than the multi-launch path on one GB300 (L2 flushed before each call):
+// with a shared expert up to T = 4 (512 experts, K = 10: T=1 58 vs 82 us), and
+// with E <= 128 from T = 4 to 8 (128 experts, K = 8: about even).  Elsewhere the
+// split-K reductions at the phase boundaries cost more than the launches they
+// save (128 experts at T = 1: 53 vs 44 us).
+bool one_launch(const moe_config_t* c, int T) {
+  if (c->dispatch == MOE_DISPATCH_ONE_LAUNCH) return true;
+  if (c->dispatch != MOE_DISPATCH_PER_BLOCK) return false;
+  return (c->has_shared && T <= 4) || (c->E <= 128 && T >= 4 && T <= 8);
 }
 
 void layout_of(const moe_config_t* c, moe_workspace_layout_t* L) {
@@ -51,10 +72,14 @@ void layout_of(const moe_config_t* c, moe_workspace_layout_t* L) {
   // zero before the first call, zero again after every call: completion
   // counters of the fused routing launches (first 256 bytes) and of the
   // in-kernel reduction of K slices in the small-batch GEMM launch
+  // and of the one-launch small-batch layer (decode_sync_offset on)
   {
     const int ms0 = c->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : c->m_skinny;
     const int tsp = c->T_max < ms0 ? c->T_max : ms0;
-    L->sync = take(256 + grouped_gemm_split_counter_bytes(tsp * c->K, c->E, c->H, c->I));
+    L->sync = take(decode_sync_offset(c) +
+                   4 * decode_layer_sync_words(c->T_max, c->E, c->K, c->H, c->I,
+                                               c->has_shared ? c->I_shared : 0, c->has_shared));
+    (void)tsp;
   }
   L->logits = take(Tm * G * 4);
   L->ids = take(R * 4);
@@ -81,8 +106,11 @@ void layout_of(const moe_config_t* c, moe_workspace_layout_t* L) {
   const int t_split = c->T_max < ms ? c->T_max : ms;
   // the three bf16 parts of the gate weight for the tensor-core router
   L->router_split = take(c->T_max >= kRouterTcMinT ? router_tc_scratch_bytes(c->H, G) : 0);
-  // split-K slices for small batches (all blocks skinny: T <= m_skinny); last
-  L->splitk = take(grouped_gemm_splitk_bytes(t_split * c->K, c->H, c->I));
+  // split-K slices for small batches (all blocks skinny: T <= m_skinny), or
+  // the one-launch layer's partial sums (the two never run in one call); last
+  const size_t sk = grouped_gemm_splitk_bytes(t_split * c->K, c->H, c->I);
+  const size_t dp = decode_layer_part_bytes();
+  L->splitk = take(sk > dp ? sk : dp);
   L->total = off;
 }
 
@@ -276,6 +304,25 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
   const int R = T * K;
 
   int32_t* bvar = reinterpret_cast<int32_t*>(ws + L.block_variant);
+  const int Is = cfg->has_shared ? cfg->I_shared : 0;
+  if (one_launch(cfg, T) &&
+      decode_layer_supported(T, E, K, H, cfg->I, Is, cfg->has_shared, cfg->wdtype, cfg->dispatch,
+                             cfg->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : cfg->m_skinny)) {
+    // small batch: the whole layer in one launch
+    DecodeLayerArgs a;
+    a.x = x; a.wg = w->wg; a.gate_bias = w->gate_bias; a.sel_bias = w->sel_bias;
+    a.T = T; a.T_max = cfg->T_max; a.H = H; a.G = G; a.E = E; a.K = K; a.I = cfg->I; a.Is = Is;
+    a.mode = cfg->mode; a.has_shared = cfg->has_shared; a.scale = cfg->routed_scale;
+    a.w1 = w->w1; a.w3 = w->w3; a.w2 = w->w2; a.sw1 = w->sw1; a.sw3 = w->sw3; a.sw2 = w->sw2;
+    a.logits = logits; a.ids = ids; a.weights = wts; a.shared_gate = gsh;
+    a.offsets = offsets; a.row_to_flat = r2f; a.flat_to_row = f2r; a.block_variant = bvar;
+    a.hact = hact; a.y = y; a.sh_hact = ws + L.shared_hact; a.sh_y = ws + L.shared_y; a.out = out;
+    a.part = reinterpret_cast<float*>(ws + L.splitk);
+    a.sync = reinterpret_cast<uint32_t*>(ws + L.sync + decode_sync_offset(cfg));
+    a.dev_status = dev_status;
+    a.m_skinny = cfg->m_skinny; a.dispatch = cfg->dispatch; a.wdtype = cfg->wdtype;
+    return cuda_status(launch_decode_layer(a, stream));
+  }
   const bool decode = T <= kRouteDecodeMaxT;
   bool planned = true;  // the grouped-GEMM plan was written by the routing launch
   cudaError_t e;

@@ -110,3 +110,45 @@ cudaError_t launch_route_prefill(const RoutePrefillArgs& args, cudaStream_t stre
 cudaError_t launch_unpermute(const void* y, const int32_t* flat_to_row, const float* weights,
                              int T, int K, int H, const void* shared_y, const float* shared_gate,
                              void* out, cudaStream_t stream);
+
+// The whole layer for small batches in one cooperative launch (decode_layer.cu):
+// router, top-K, permute, G1/G2 (+ shared expert) and combine.  The sync
+// words must be zero before the launch and are zero again after it.
+constexpr int kDecodeMaxT = 16;      // tokens the kernel takes
+constexpr int kDecodeMaxGrid = 256;  // SMs it can use (one CTA each)
+struct DecodeLayerArgs {
+  const void* x;
+  const float* wg;
+  const float* gate_bias;
+  const float* sel_bias;
+  int T, T_max, H, G, E, K, I, Is, mode, has_shared;
+  float scale;
+  const void* w1;
+  const void* w3;
+  const void* w2;
+  const void* sw1;
+  const void* sw3;
+  const void* sw2;
+  float* logits;
+  int32_t* ids;
+  float* weights;
+  float* shared_gate;
+  int32_t* offsets;
+  int32_t* row_to_flat;
+  int32_t* flat_to_row;
+  int32_t* block_variant;
+  void* hact;
+  void* y;
+  void* sh_hact;
+  void* sh_y;
+  void* out;
+  float* part;     // decode_layer_part_bytes()
+  uint32_t* sync;  // decode_layer_sync_words(...) words
+  int32_t* dev_status;
+  int m_skinny, dispatch, wdtype;
+};
+size_t decode_layer_sync_words(int T_max, int E, int K, int H, int I, int Is, int has_shared);
+size_t decode_layer_part_bytes();
+bool decode_layer_supported(int T, int E, int K, int H, int I, int Is, int has_shared, int wdtype,
+                            int dispatch, int m_skinny);
+cudaError_t launch_decode_layer(const DecodeLayerArgs& args, cudaStream_t stream);

@@ -22,6 +22,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "topk_group.cuh"
+#include "topk_thread.cuh"
 #include "topk_warp.cuh"
 
 namespace {
@@ -131,6 +132,89 @@ cudaError_t launch_warp(const float* logits, int ld, const float* sel_bias, int 
 #undef MOE_TOPK_LAUNCH
 }
 
+// ---------------------------------------------------------------- thread per token
+// Large batches with E <= 128: one thread routes one token (thread_topk,
+// topk_thread.cuh).  A thread reading its own 512-byte row would make every
+// warp load touch 32 lines, so each warp first copies its 32 rows into shared
+// memory with row-contiguous (coalesced) loads, rows padded by 16 bytes so
+// the threads' own-row reads fall in distinct banks.
+constexpr int kThreadWarps = 2;
+template <int NV, int KT, bool kVec>
+__global__ void __launch_bounds__(32 * kThreadWarps)
+topk_thread_kernel(const float* __restrict__ logits, int ld, const float* __restrict__ sel_bias,
+                   int T, int E, int K, int mode, float scale, int32_t* __restrict__ ids,
+                   float* __restrict__ weights, float* __restrict__ shared_gate) {
+  constexpr int kRow = 4 * NV + 4;  // floats per staged row
+  __shared__ __align__(16) float rows[kThreadWarps][32][kRow];
+  pdl_wait();
+  pdl_trigger();
+  const int warp = warp_id(), lane = lane_id();
+  const int t0 = (blockIdx.x * kThreadWarps + warp) * 32;
+  if (t0 >= T) return;  // the whole warp
+  float (*mine)[kRow] = rows[warp];
+  if constexpr (kVec) {
+    // 32 / NV rows per load instruction, one float4 per lane
+    constexpr int kRowsPer = 32 / NV;
+    const int rr = lane / NV, v = lane % NV;
+#pragma unroll 4
+    for (int r0 = 0; r0 < 32; r0 += kRowsPer) {
+      const int r = r0 + rr;
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t0 + r < T && 4 * v < E)
+        f = __ldg(reinterpret_cast<const float4*>(logits + (size_t)(t0 + r) * ld + 4 * v));
+      *reinterpret_cast<float4*>(&mine[r][4 * v]) = f;
+    }
+  } else {
+    for (int r = 0; r < 32 && t0 + r < T; ++r)
+      for (int e = lane; e < E; e += 32) mine[r][e] = __ldg(logits + (size_t)(t0 + r) * ld + e);
+  }
+  __syncwarp();
+  const int t = t0 + lane;
+  if (t < T) {
+    thread_topk<NV, KT, kVec, true>(mine[lane], sel_bias, E, K, mode, scale, ids + (size_t)t * K,
+                                    weights + (size_t)t * K);
+    if (shared_gate) shared_gate[t] = sigmoid_key(__ldg(logits + (size_t)t * ld + E));
+  }
+}
+
+template <int NV, bool kVec>
+cudaError_t launch_thread_nv(const float* logits, int ld, const float* sel_bias, int T, int E,
+                             int K, int mode, float scale, int32_t* ids, float* weights,
+                             float* shared_gate, cudaStream_t stream) {
+  const dim3 grid(moe_cdiv(T, 32 * kThreadWarps)), block(32 * kThreadWarps);
+#define MOE_TOPK_THREAD(KT)                                                                   \
+  return moe_launch(topk_thread_kernel<NV, KT, kVec>, grid, block, 0, stream, 1, logits, ld, \
+                    sel_bias, T, E, K, mode, scale, ids, weights, shared_gate)
+  if (K <= 2) MOE_TOPK_THREAD(2);
+  if (K <= 4) MOE_TOPK_THREAD(4);
+  if (K <= 8) MOE_TOPK_THREAD(8);
+  if (K <= 16) MOE_TOPK_THREAD(16);
+  MOE_TOPK_THREAD(32);
+#undef MOE_TOPK_THREAD
+}
+
+// list length (K rounded up to a power of two) no larger than E, so that
+// every group of the bound holds an expert
+bool thread_route_fits(int E, int K) {
+  int kt = 2;
+  while (kt < K) kt *= 2;
+  return E <= 128 && kt <= E && K <= 32;
+}
+
+template <bool kVec>
+cudaError_t launch_thread(const float* logits, int ld, const float* sel_bias, int T, int E, int K,
+                          int mode, float scale, int32_t* ids, float* weights, float* shared_gate,
+                          cudaStream_t stream) {
+  if (E <= 32)
+    return launch_thread_nv<8, kVec>(logits, ld, sel_bias, T, E, K, mode, scale, ids, weights,
+                                     shared_gate, stream);
+  if (E <= 64)
+    return launch_thread_nv<16, kVec>(logits, ld, sel_bias, T, E, K, mode, scale, ids, weights,
+                                      shared_gate, stream);
+  return launch_thread_nv<32, kVec>(logits, ld, sel_bias, T, E, K, mode, scale, ids, weights,
+                                    shared_gate, stream);
+}
+
 template <bool kVec>
 cudaError_t launch_vec(const float* logits, int ld, const float* sel_bias, int T, int E, int K,
                        int mode, float scale, int32_t* ids, float* weights, float* shared_gate,
@@ -161,6 +245,13 @@ cudaError_t launch_topk_route(const float* logits, int ld, const float* sel_bias
   }
   // float4 rows when every row starts on a 16-byte boundary and E fills whole vectors
   const bool vec = E % 4 == 0 && ld % 4 == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+  if (thread_route_fits(E, K)) {
+    if (vec)
+      return launch_thread<true>(logits, ld, sel_bias, T, E, K, mode, scale, ids, weights,
+                                 shared_gate, stream);
+    return launch_thread<false>(logits, ld, sel_bias, T, E, K, mode, scale, ids, weights,
+                                shared_gate, stream);
+  }
   if (vec)
     return launch_vec<true>(logits, ld, sel_bias, T, E, K, mode, scale, ids, weights, shared_gate,
                             stream);

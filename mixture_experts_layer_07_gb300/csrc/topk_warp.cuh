@@ -53,6 +53,11 @@ MOE_DEVICE uint32_t order_key(float k) {
   return (b & 0x80000000u) ? 0u - b : (b | 0x80000000u);
 }
 
+// the float whose order_key is k (exact inverse; -0 comes back as +0)
+MOE_DEVICE float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : 0u - k);
+}
+
 // strict total order: larger key first, lower index first among equal keys
 MOE_DEVICE bool better(uint32_t ka, int ia, uint32_t kb, int ib) {
   return ka > kb || (ka == kb && ia < ib);
@@ -105,6 +110,7 @@ MOE_DEVICE void warp_topk(const float* __restrict__ row, const float* __restrict
   // max-reduction, then the lowest expert index among heads with that key by
   // one min-reduction; the owning lane pops its head.
   int my_id = -1;
+  uint32_t my_key = 0u;
   for (int r = 0; r < K; ++r) {
     const uint32_t m = __reduce_max_sync(0xffffffffu, lk[0]);
     const uint32_t mi = __reduce_min_sync(0xffffffffu, lk[0] == m ? (uint32_t)li[0] : 0xffffffffu);
@@ -114,12 +120,16 @@ MOE_DEVICE void warp_topk(const float* __restrict__ row, const float* __restrict
       lk[LK - 1] = 0u;
       li[LK - 1] = 0x7fffffff;
     }
-    if (lane == r) my_id = (int)mi;
+    if (lane == r) {
+      my_id = (int)mi;
+      my_key = m;
+    }
   }
 
   float v = 0.f;
   if (mode == MOE_SCORE_SOFTMAX_RENORM) {
-    const float l = lane < K ? ld(my_id) : 0.f;
+    // a pick's key is its logit (mode 0): no second read of the row
+    const float l = lane < K ? key_float(my_key) : 0.f;
     const float m = __shfl_sync(0xffffffffu, l, 0);  // the first pick is the largest
     v = lane < K ? expf(l - m) : 0.f;
   } else {

@@ -105,6 +105,7 @@ template <class T> unsigned __match_any_sync(unsigned, T v) {
   for (int i = 0; i < 32; ++i) if (a[i] == a[simt_emu::lane]) m |= 1u << i; return m;
 }
 inline int __popc(unsigned v) { return __builtin_popcount(v); }
+inline int __ffs(unsigned v) { return __builtin_ffs((int)v); }
 template <class T> T __ldg(const T* p) { return *p; }
 template <class T> T __ldcg(const T* p) { return *p; }
 inline uint32_t __float_as_uint(float f) { return emu_val<uint32_t>(emu_bits(f)); }

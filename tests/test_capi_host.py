@@ -100,7 +100,7 @@ def test_workspace_sizes_grow_with_t_max(ops):
 
 
 @pytest.mark.parametrize("kw", [dict(H=100), dict(K=0), dict(K=9), dict(E=2048), dict(I=10),
-                                dict(mode=5), dict(wdtype=7), dict(dispatch=9),
+                                dict(mode=5), dict(wdtype=7), dict(dispatch=9), dict(dispatch=4),
                                 dict(m_skinny=-2), dict(has_shared=True, I_shared=0),
                                 dict(K=33, E=64)])
 def test_config_validation(ops, kw):
@@ -214,3 +214,12 @@ def test_bounded_wait_check_rejects_bad_arguments(ops):
     assert call(ops, f, 0x1000, 1, 1000, None, None) == 1
     assert call(ops, f, 0x1000, 1, 0, 0x1000, None) == 1
     assert call(ops, f, 0x1000, 1, 10000001, 0x1000, None) == 1
+
+
+def test_one_launch_dispatch_is_a_layer_option(ops):
+    # MOE_DISPATCH_ONE_LAUNCH is accepted by the layer's config (same
+    # workspace as per-block dispatch) and refused by the stand-alone grouped
+    # GEMM (checked in test_grouped_gemm_rejects_bad_arguments)
+    a = ops.workspace_bytes(_cfg(ops, dispatch=ops.DISPATCH_ONE_LAUNCH))
+    b = ops.workspace_bytes(_cfg(ops))
+    assert a == b > 0

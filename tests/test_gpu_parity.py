@@ -606,3 +606,64 @@ def test_layer_decode_path_repeats_and_leaves_sync_zero(ops):
         assert np.array_equal(layer.view("ids", torch.int32, (T, spec.K)).cpu().numpy(),
                               res["ids"])
         U.assert_bf16_close(U.f64(out), res["out"], 2e-2, f"decode T={T}")
+
+
+# The whole layer as ONE launch (MOE_DISPATCH_ONE_LAUNCH forces it wherever it
+# applies: bf16 experts, T <= 16), at every shape it takes: shared expert,
+# E up to 1024 (the partitioned route for E > 128 at T <= 4), both score
+# modes, H not a multiple of 128, tokens sharing experts.  Routing is compared
+# bit for bit on the GPU's own logits, every output element against the
+# oracle; a second call on the same workspace must give the same bits and
+# leave the counters at zero.
+ONE_LAUNCH_CASES = [("qwen3_30b_a3b", {}, 1), ("qwen3_30b_a3b", {}, 2), ("qwen3_30b_a3b", {}, 3),
+                    ("qwen3_30b_a3b", {}, 8), ("qwen3_30b_a3b", {}, 16),
+                    ("shared_gate", {}, 1), ("shared_gate", {}, 4), ("shared_gate", {}, 13),
+                    ("high_expert", {}, 1), ("high_expert", {"E": 512, "K": 9}, 3),
+                    ("high_expert", {"E": 1024, "K": 16, "H": 1024, "I": 512}, 4),
+                    ("high_expert", {"E": 1024, "K": 9, "H": 1024, "I": 512}, 11),
+                    ("tiny", {}, 16), ("tiny", {"H": 2880, "I": 1440, "E": 4}, 5),
+                    ("tiny", {"E": 40, "K": 3, "mode": 1, "routed_scale": 2.5,
+                              "sel_bias_var": 0.1}, 7)]
+
+
+@pytest.mark.parametrize("name,over,T", ONE_LAUNCH_CASES)
+def test_one_launch_layer(ops, name, over, T):
+    spec = SPECS[name].with_(**over)
+    base = synth.host_inputs(spec, T, seed=17, weights=False)
+    _, ids, _ = oracle_routing(spec, base)
+    inp = synth.host_inputs(spec, T, seed=17, experts=sorted(set(ids.ravel().tolist())))
+    t = U.layer_tensors(inp, inp["experts"])
+    layer = ops.MoELayer(U.config_for(ops, spec, T_max=max(T, 4),
+                                      dispatch=ops.DISPATCH_ONE_LAUNCH), t)
+    out = layer(t["x"])
+    sync()
+    assert int(layer.dev_status.item()) == 0
+    E, K, R = spec.E, spec.K, T * spec.K
+    lg = layer.view("logits", torch.float32, (T, spec.G)).cpu().numpy()
+    U.assert_router_close(lg.astype(np.float64), oracle.bf16_to_f64(inp["x_bits"]), inp["wg"],
+                          inp["gate_bias"])
+    gid = layer.view("ids", torch.int32, (T, K)).cpu().numpy()
+    gw = layer.view("weights", torch.float32, (T, K)).cpu().numpy()
+    if spec.mode == 0:
+        rid, rw = oracle.topk_softmax_renorm(lg.astype(np.float64), E, K)
+    else:
+        rid, rw = oracle.topk_sigmoid_bias(lg, inp["sel_bias"], E, K, spec.routed_scale)
+    assert np.array_equal(gid, rid)
+    U.assert_weights_close(gw, rw)
+    off, r2f, f2r = oracle.permute(gid, E)
+    assert np.array_equal(layer.view("offsets", torch.int32, (E + 1,)).cpu().numpy(), off)
+    assert np.array_equal(layer.view("row_to_flat", torch.int32, (R,)).cpu().numpy(), r2f)
+    assert np.array_equal(layer.view("flat_to_row", torch.int32, (R,)).cpu().numpy(), f2r)
+    want = [ops.block_variant(int(m), R, E, -1, 0, ops.W_BF16) for m in np.diff(off)]
+    assert layer.view("block_variant", torch.int32, (E,)).cpu().numpy().tolist() == want
+    res = oracle.moe_layer_from_inputs(inp, logits_override=lg.astype(np.float64))
+    U.assert_bf16_close(U.f64(layer.view("hact", torch.bfloat16, (R, spec.I))), res["hact"],
+                        2e-2, "one-launch hact")
+    U.assert_bf16_close(U.f64(layer.view("y", torch.bfloat16, (R, spec.H))), res["y"], 2e-2,
+                        "one-launch y")
+    U.assert_bf16_close(U.f64(out), res["out"], 2e-2, "one-launch out")
+    again = layer(t["x"])
+    sync()
+    assert torch.equal(again.view(torch.int16), out.view(torch.int16))
+    sw = layer.workspace[layer.layout.sync:layer.layout.logits].view(torch.int32)
+    assert int(sw.abs().sum().item()) == 0

@@ -9,14 +9,20 @@ the host:
   sort of the same keys (random, tie-heavy, one-lane-owns-every-pick and
   all-tied-in-one-lane logits; float4 and scalar rows; groups of 8, 16 and 32
   lanes and one warp per token; both score modes);
+* topk_thread_emu.cpp -- csrc/topk_thread.cuh (the thread-per-token route
+  of large batches with E <= 128: a bound from group maxima, then only the
+  experts above it inserted) against a stable sort of the same keys, for
+  every list length, float4 and scalar rows, both score modes and random,
+  tie-heavy, all-equal and every-pick-in-one-group logits;
 * permute_plan_emu.cpp -- csrc/permute_block.cuh and csrc/plan.cuh (the
   one-CTA permute and GEMM plan of the fused routing launches) against a
   stable counting sort and the work lists the variants imply, with
   out-of-range ids flagged.
 
-* sigmoid_emu.cpp -- the selection key's float32 sigmoid (sigmoid_key) and the
-  order-preserving key map (order_key) of csrc/topk_warp.cuh, compared bit
-  for bit with the oracle's float32 sigmoid and with float order.
+* sigmoid_emu.cpp -- the selection key's float32 sigmoid (sigmoid_key), the
+  order-preserving key map (order_key) and its inverse (key_float) of
+  csrc/topk_warp.cuh, compared bit for bit with the oracle's float32 sigmoid,
+  with float order and with the inputs.
 
 This pins the routing logic itself; the GPU parity tests pin the compiled
 kernels."""
@@ -54,7 +60,7 @@ def _compile(tmp_path, program):
     return str(exe)
 
 
-@pytest.mark.parametrize("program", ["topk_emu", "permute_plan_emu"])
+@pytest.mark.parametrize("program", ["topk_emu", "topk_thread_emu", "permute_plan_emu"])
 def test_routing_device_code_on_host(tmp_path, program):
     exe = _compile(tmp_path, program)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
@@ -83,3 +89,7 @@ def test_selection_key_formula_on_host(tmp_path):
     assert (np.diff(ks.astype(np.int64)) >= 0).all()
     assert ((np.diff(ks.astype(np.int64)) == 0) == (np.diff(xs) == 0)).all()
     assert (key != 0).all()
+    # key_float inverts order_key exactly (-0 comes back as +0)
+    back = out[:, 2].astype(np.uint32).view(np.float32)
+    want = np.where(x == 0, np.float32(0.0), x)
+    assert np.array_equal(back.view(np.uint32), want.view(np.uint32))
