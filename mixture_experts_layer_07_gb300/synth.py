@@ -18,6 +18,10 @@ every tensor is random:
 * selection bias           N(0, 0.1) (variance 0.1) for sigmoid+bias routing
 * FP8 weights              e4m3 codes with one fp32 scale per 128x128 block,
                            scale = amax(block)/448, code = RNE(w/scale)
+* MXFP4 weights            e2m1 codes, two per byte (element 2i in the low
+                           nibble), one UE8M0 scale byte per 32 elements of a
+                           row: scale 2^(floor(log2 amax) - 2), code =
+                           RNE(w/scale) clamped to +-6 (OCP Microscaling)
 
 Two back ends draw the same distributions:
 
@@ -38,6 +42,10 @@ TID_X, TID_WG, TID_W1, TID_W3, TID_W2, TID_SW1, TID_SW3, TID_SW2, TID_SELB = ran
 
 FP8_BLOCK = 128
 FP8_MAX = 448.0  # largest finite e4m3 magnitude
+MX_BLOCK = 32    # elements per MXFP4 scale
+# e2m1 magnitudes by code 0..7 and the midpoints between neighbours
+E2M1_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+E2M1_MID = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
 
 MODE_SOFTMAX = 0
 MODE_SIGMOID_BIAS = 1
@@ -54,7 +62,8 @@ class LayerSpec:
     I: int
     mode: int = MODE_SOFTMAX
     routed_scale: float = 1.0
-    wdtype: str = "bf16"          # "bf16" or "fp8" (e4m3, 128x128 block scales)
+    wdtype: str = "bf16"          # "bf16", "fp8" (e4m3, 128x128 block scales) or
+                                  # "mxfp4" (e2m1, a power-of-two scale per 32)
     has_shared: bool = False
     I_shared: int = 0
     hot_experts: tuple = ()       # experts whose gate logit gets ``hot_bias``
@@ -135,6 +144,54 @@ def quantize_fp8_block(w: np.ndarray):
     return codes.numpy(), scales
 
 
+def _e2m1_codes(mag: np.ndarray) -> np.ndarray:
+    """Nearest e2m1 code (0..7) of magnitudes, ties to the even code, clamped
+    to 6."""
+    mid = np.asarray(E2M1_MID, dtype=np.float32)
+    pos = np.searchsorted(mid, mag, side="left")
+    tie = (pos < len(mid)) & (mid[np.minimum(pos, len(mid) - 1)] == mag) & (pos % 2 == 1)
+    return (pos + tie).astype(np.uint8)
+
+
+def quantize_mxfp4(w: np.ndarray):
+    """Quantise one [rows, cols] float32 matrix (cols % 32 == 0) to MXFP4.
+
+    Per 32 consecutive elements of a row: shared exponent
+    e = floor(log2(amax)) - 2 (amax = 0: e = -127), scale byte e + 127 clamped
+    to [0, 254]; code = sign | e2m1(|w| / 2^e) (round to nearest even, clamped
+    to 6).  Returns (packed uint8 [rows, cols/2], scales uint8 [rows, cols/32])."""
+    rows, cols = w.shape
+    blk = np.ascontiguousarray(w, dtype=np.float32).reshape(rows, cols // MX_BLOCK, MX_BLOCK)
+    amax = np.abs(blk).max(axis=2)
+    _, ex = np.frexp(amax)              # amax = m * 2^ex, m in [0.5, 1)
+    e = np.where(amax > 0, ex - 1 - 2, -127).astype(np.int32)
+    sbyte = np.clip(e + 127, 0, 254).astype(np.uint8)
+    e = sbyte.astype(np.int32) - 127
+    scaled = np.abs(blk) * np.exp2(-e.astype(np.float32))[:, :, None].astype(np.float32)
+    code = _e2m1_codes(scaled.astype(np.float32)) | (np.signbit(blk).astype(np.uint8) << 3)
+    code = code.reshape(rows, cols)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    return packed, sbyte
+
+
+def quantize_mxfp4_torch(w):
+    """quantize_mxfp4 with torch ops (same rule, same bits), for device draws."""
+    import torch
+
+    rows, cols = w.shape
+    mid = torch.tensor(E2M1_MID, dtype=torch.float32, device=w.device)
+    blk = w.to(torch.float32).reshape(rows, cols // MX_BLOCK, MX_BLOCK)
+    amax = blk.abs().amax(dim=2)
+    _, ex = torch.frexp(amax)
+    e = torch.where(amax > 0, ex - 3, torch.full_like(ex, -127)).clamp(-127, 127)
+    mag = (blk.abs() * torch.exp2(-e.to(torch.float32))[:, :, None]).contiguous()
+    pos = torch.searchsorted(mid, mag, right=False)
+    hit = mid[pos.clamp(max=len(E2M1_MID) - 1)] == mag
+    code = pos + (hit & (pos < len(E2M1_MID)) & (pos % 2 == 1)).to(pos.dtype)
+    code = (code.to(torch.uint8) | (torch.signbit(blk).to(torch.uint8) << 3)).reshape(rows, cols)
+    return code[:, 0::2] | (code[:, 1::2] << 4), (e + 127).to(torch.uint8)
+
+
 # ----------------------------------------------------------------------------
 # host back end (numpy Philox)
 # ----------------------------------------------------------------------------
@@ -191,6 +248,15 @@ def host_inputs(spec: LayerSpec, T: int, seed: int = 0, experts=None, weights: b
                         dtype=np.float32)
             for e in ex:
                 q[e], s[e] = quantize_fp8_block(_normal(seed, tid, e, shp, std))
+            out[qk], out[sk] = q, s
+    elif spec.wdtype == "mxfp4":
+        for qk, sk, tid, shp, std in (("w1_q4", "s1", TID_W1, (I, H), std1),
+                                      ("w3_q4", "s3", TID_W3, (I, H), std1),
+                                      ("w2_q4", "s2", TID_W2, (H, I), std2)):
+            q = np.zeros((E, shp[0], shp[1] // 2), dtype=np.uint8)
+            s = np.full((E, shp[0], shp[1] // MX_BLOCK), 127, dtype=np.uint8)
+            for e in ex:
+                q[e], s[e] = quantize_mxfp4(_normal(seed, tid, e, shp, std))
             out[qk], out[sk] = q, s
     else:
         raise ValueError(spec.wdtype)
@@ -259,6 +325,15 @@ def device_inputs(spec: LayerSpec, T: int, seed: int = 0, device: str = "cuda") 
             for e in range(E):
                 w[e] = normal(tid, shp, std, sub=e)
             out[key] = w
+    elif spec.wdtype == "mxfp4":
+        for qk, sk, tid, shp, std in (("w1_q4", "s1", TID_W1, (I, H), std1),
+                                      ("w3_q4", "s3", TID_W3, (I, H), std1),
+                                      ("w2_q4", "s2", TID_W2, (H, I), std2)):
+            q = torch.empty((E, shp[0], shp[1] // 2), dtype=torch.uint8, device=device)
+            s = torch.empty((E, shp[0], shp[1] // MX_BLOCK), dtype=torch.uint8, device=device)
+            for e in range(E):
+                q[e], s[e] = quantize_mxfp4_torch(normal(tid, shp, std, sub=e, dtype=torch.float32))
+            out[qk], out[sk] = q, s
     else:
         for qk, sk, tid, shp, std in (("w1_q", "s1", TID_W1, (I, H), std1),
                                       ("w3_q", "s3", TID_W3, (I, H), std1),

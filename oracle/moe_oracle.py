@@ -79,6 +79,38 @@ def dequant_fp8_block(codes, scales, block: int = 128) -> np.ndarray:
     return q * s_full
 
 
+def _e2m1_value(code: int) -> float:
+    """Value of one OCP FP4 E2M1 code: 1 sign bit, 2 exponent bits with bias
+    1, 1 mantissa bit; exponent field 0 holds the subnormal m * 0.5 (so the
+    magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6); no infinities or NaN."""
+    s = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return s * m * 0.5
+    return s * (1.0 + m / 2.0) * 2.0 ** (e - 1)
+
+
+_E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def dequant_mxfp4(packed, scales, block: int = 32) -> np.ndarray:
+    """Dequantise MXFP4 rows ([dispatch] introduction: the CPU MoE path serves
+    FP8 and MXFP4 experts): ``packed`` [..., rows, cols / 2] bytes hold two
+    E2M1 codes each, element 2i in the low nibble and 2i + 1 in the high one;
+    ``scales`` [..., rows, cols / 32] are UE8M0 bytes, scale 2^(s - 127), one
+    per 32 consecutive elements of a row (OCP Microscaling):
+    w[r, c] = e2m1(code[r, c]) * 2^(scales[r, c // 32] - 127)."""
+    b = np.asarray(packed, dtype=np.uint8)
+    codes = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.uint8)
+    codes[..., 0::2] = b & 0xF
+    codes[..., 1::2] = b >> 4
+    q = _E2M1_TABLE[codes]
+    e = np.asarray(scales, dtype=np.float64)
+    s = np.repeat(np.exp2(e - 127.0), block, axis=-1)[..., :q.shape[-1]]
+    return q * s
+
+
 # ----------------------------------------------------------------------------
 # R: router (gate) GEMM
 # ----------------------------------------------------------------------------
@@ -306,12 +338,17 @@ class ExpertBank:
     dequantised by block), so a layer with many large experts never holds all
     of them in float64 at once."""
 
-    def __init__(self, codes, scales=None):
+    def __init__(self, codes, scales=None, fmt="bf16"):
         self.codes = codes
         self.scales = scales
-        self.shape = tuple(codes.shape)
+        self.fmt = fmt
+        shape = tuple(codes.shape)
+        # MXFP4 rows hold two elements per byte
+        self.shape = shape[:-1] + (2 * shape[-1],) if fmt == "mxfp4" else shape
 
     def __getitem__(self, e):
+        if self.fmt == "mxfp4":
+            return dequant_mxfp4(self.codes[e], self.scales[e])
         if self.scales is None:
             return bf16_to_f64(self.codes[e])
         return dequant_fp8_block(self.codes[e], self.scales[e])
@@ -322,10 +359,15 @@ class ExpertBank:
 
 def layer_weights_f64(inp: dict):
     """Expert weights of an input dict (see the package's ``synth`` module) as
-    three ``ExpertBank``s: W1 [E, I, H], W3 [E, I, H], W2 [E, H, I]."""
+    three ``ExpertBank``s: W1 [E, I, H], W3 [E, I, H], W2 [E, H, I] (bf16, FP8
+    or MXFP4 storage)."""
     if "w1_bits" in inp:
         return (ExpertBank(inp["w1_bits"]), ExpertBank(inp["w3_bits"]),
                 ExpertBank(inp["w2_bits"]))
+    if "w1_q4" in inp:
+        return (ExpertBank(inp["w1_q4"], inp["s1"], "mxfp4"),
+                ExpertBank(inp["w3_q4"], inp["s3"], "mxfp4"),
+                ExpertBank(inp["w2_q4"], inp["s2"], "mxfp4"))
     return (ExpertBank(inp["w1_q"], inp["s1"]), ExpertBank(inp["w3_q"], inp["s3"]),
             ExpertBank(inp["w2_q"], inp["s2"]))
 

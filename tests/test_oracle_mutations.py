@@ -143,3 +143,21 @@ def test_wrong_e4m3_bias_is_caught(monkeypatch):
     patch(monkeypatch, "_E4M3_TABLE", table)
     assert fails(P.test_e4m3_known_codes)
     assert fails(P.test_e4m3_all_codes_match_torch)
+
+
+def test_swapped_mxfp4_nibbles_are_caught(monkeypatch):
+    real = M.dequant_mxfp4
+
+    def swapped(packed, scales, block=32):
+        b = np.asarray(packed, np.uint8)
+        return real(((b & 0xF) << 4) | (b >> 4), scales, block)
+    patch(monkeypatch, "dequant_mxfp4", swapped)
+    assert fails(P.test_mxfp4_golden_worked_example)
+
+
+def test_mxfp4_scale_off_by_one_is_caught(monkeypatch):
+    real = M.dequant_mxfp4
+    patch(monkeypatch, "dequant_mxfp4",
+          lambda packed, scales, block=32: real(packed, np.asarray(scales, np.uint8) + 1, block))
+    assert fails(P.test_mxfp4_golden_worked_example)
+    assert fails(P.test_mxfp4_scale_is_a_power_of_two_per_32_elements)

@@ -365,3 +365,75 @@ def test_layer_fp8_equals_bf16_path_on_dequantised_weights():
     # the dequantised weights are the e4m3 values times the block scale
     assert w1[0, 0, 0] == oracle.e4m3_to_f64(inp["w1_q"][0, 0, 0]) * inp["s1"][0, 0, 0]
     assert w1[2, 135, 159] == oracle.e4m3_to_f64(inp["w1_q"][2, 135, 159]) * inp["s1"][2, 1, 1]
+
+
+# ---------------------------------------------------------------- MXFP4 storage
+def test_e2m1_all_codes_closed_form():
+    # E2M1 (OCP Microscaling): sign, 2 exponent bits with bias 1, 1 mantissa
+    # bit, exponent field 0 = subnormal m * 0.5
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    packed = np.array([[c | (c << 4) for c in range(16)]], np.uint8)  # each code twice
+    d = oracle.dequant_mxfp4(packed, np.array([[127]], np.uint8))[0]
+    want = np.array(mags + [-m for m in mags])
+    assert np.array_equal(d[0::2], want) and np.array_equal(d[1::2], want)
+    assert np.signbit(d[16])  # code 8 is -0
+
+
+def test_mxfp4_golden_worked_example():
+    g = json.load(open(os.path.join(GOLD, "mxfp4_worked.json")))
+    d = oracle.dequant_mxfp4(np.array([g["packed"]], np.uint8), np.array([g["scales"]], np.uint8))
+    assert np.array_equal(d[0], np.array(g["values"]))
+
+
+def test_mxfp4_scale_is_a_power_of_two_per_32_elements():
+    # every scale byte s multiplies its 32 elements by 2^(s - 127), exactly
+    packed = np.full((2, 48), 0x22, np.uint8)     # all elements code 2 = 1.0
+    scales = np.array([[0, 1, 254], [127, 130, 100]], np.uint8)
+    d = oracle.dequant_mxfp4(packed, scales)
+    for r in range(2):
+        for b in range(3):
+            assert (d[r, 32 * b:32 * b + 32] == 2.0 ** (int(scales[r, b]) - 127)).all()
+
+
+def test_mxfp4_quantisation_round_trip_bound():
+    # synth's quantiser then the oracle's decode: every element within one
+    # spacing of the e2m1 grid at its block's scale (half a spacing, or the
+    # clamp of values in (6, 8) x scale to 6 x scale), zeros exact, values on
+    # the grid exact
+    rng = np.random.default_rng(3)
+    w = (rng.standard_normal((8, 256)) * 0.03).astype(np.float32)
+    w[0, :32] = 0.0
+    q, s = synth.quantize_mxfp4(w)
+    d = oracle.dequant_mxfp4(q, s)
+    scale = np.repeat(np.exp2(s.astype(np.float64) - 127.0), 32, axis=1)
+    assert (np.abs(d - w) <= 2.0 * scale).all()
+    assert (d[0, :32] == 0).all()
+    # amax / scale lies in [4, 8): the block's largest element reads 4 or 6
+    blk = np.abs(d).reshape(8, 8, 32).max(axis=2) / scale.reshape(8, 8, 32)[:, :, 0]
+    assert np.isin(blk[1:], [4.0, 6.0]).all()
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6, -0.5, -6] + [0] * 22, np.float32)[None] * 2.0 ** -7
+    q, s = synth.quantize_mxfp4(grid.astype(np.float32))
+    assert np.array_equal(oracle.dequant_mxfp4(q, s), grid)
+
+
+def test_mxfp4_device_quantiser_matches_host():
+    # the torch rule (device draws) gives the host rule's bits
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(4)
+    w = (rng.standard_normal((16, 128)) * 0.05).astype(np.float32)
+    w[3, 40] = 0.0
+    w[5, :32] = 0.0
+    q, s = synth.quantize_mxfp4(w)
+    qt, st = synth.quantize_mxfp4_torch(torch.from_numpy(w))
+    assert np.array_equal(q, qt.numpy()) and np.array_equal(s, st.numpy())
+
+
+def test_layer_mxfp4_equals_bf16_path_on_dequantised_weights():
+    spec = synth.LayerSpec("pin4", H=160, E=3, K=2, I=96, wdtype="mxfp4")
+    inp = synth.host_inputs(spec, T=5, seed=15)
+    res = oracle.moe_layer_from_inputs(inp)
+    w1, w3, w2 = (np.stack([b[e] for e in range(3)]) for b in oracle.layer_weights_f64(inp))
+    assert w1.shape == (3, 96, 160) and w2.shape == (3, 160, 96)
+    res2 = oracle.moe_layer(oracle.bf16_to_f64(inp["x_bits"]), inp["wg"], None, None, w1, w3, w2,
+                            E=3, K=2, mode=0)
+    assert np.array_equal(res["out"], res2["out"])
