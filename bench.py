@@ -140,10 +140,26 @@ def job_throughput(tokens_per_rank_step, steps, world, max_ms):
 
 
 # ------------------------------------------------------------------ workload
+def wd_of(ops, spec):
+    return {"bf16": ops.W_BF16, "fp8": ops.W_FP8, "mxfp4": ops.W_MXFP4}[spec.wdtype]
+
+
+def weight_bytes(spec, n):
+    """Stored bytes of n expert-weight elements (MXFP4: half a byte each plus
+    one scale byte per 32)."""
+    return {"bf16": 2 * n, "fp8": n, "mxfp4": n // 2 + n // 32}[spec.wdtype]
+
+
+DTYPE_NAME = {"bf16": "bf16", "fp8": "bf16 activations, fp8-e4m3 weights",
+              "mxfp4": "bf16 activations, mxfp4 (e2m1 + ue8m0/32) weights"}
+
+
 def tensors_of(spec, d):
     t = {"x": d["x"], "wg": d["wg"], "gate_bias": d["gate_bias"], "sel_bias": d["sel_bias"]}
-    if spec.wdtype == "fp8":
-        t.update(w1=d["w1_q"], w3=d["w3_q"], w2=d["w2_q"], s1=d["s1"], s3=d["s3"], s2=d["s2"])
+    if spec.wdtype in ("fp8", "mxfp4"):
+        q = "_q" if spec.wdtype == "fp8" else "_q4"
+        t.update(w1=d["w1" + q], w3=d["w3" + q], w2=d["w2" + q], s1=d["s1"], s3=d["s3"],
+                 s2=d["s2"])
     else:
         t.update(w1=d["w1"], w3=d["w3"], w2=d["w2"])
     if spec.has_shared:
@@ -187,7 +203,7 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
         if dispatch == 2:
             return n + 2
         tile = max_rows > m_skinny
-        wide = spec.wdtype == "fp8" and tile and max_rows >= wide_min
+        wide = spec.wdtype != "bf16" and tile and max_rows >= wide_min
         # tile and wide lists: one G1+G2 launch each (mean rows <= 64, H <= 3 I)
         fused = rows <= 64 * blocks and spec.H <= 3 * inter and not gather
         if splittable and not tile:
@@ -198,7 +214,7 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
         return n
 
     if T <= 32:
-        gather = spec.wdtype != "fp8"  # bf16: G1 reads its rows from x, no permuted copy
+        gather = spec.wdtype == "bf16"  # bf16: G1 reads its rows from x, no permuted copy
         route = 1 if gather else 2
         g = gemm(T, R, spec.E, with_plan=False, splittable=True, inter=spec.I, gather=gather)
     else:
@@ -213,7 +229,6 @@ def stage_bytes_flops(spec, T, ids, e_active):
     """Algorithmic bytes / flops per stage (each tensor read or written once)."""
     H, E, K, I, G = spec.H, spec.E, spec.K, spec.I, spec.G
     R = T * K
-    wb = 1 if spec.wdtype == "fp8" else 2
     sb = 0
     if spec.wdtype == "fp8":
         sb = e_active * 4 * 3 * (-(-I // 128)) * (-(-H // 128))
@@ -221,7 +236,7 @@ def stage_bytes_flops(spec, T, ids, e_active):
         "router": {"bytes": 2 * T * H + 4 * G * H + 4 * T * G, "flops": 2 * T * G * H},
         "topk": {"bytes": 4 * T * G + 8 * T * K + (4 * E if spec.mode == 1 else 0), "flops": 0},
         "permute": {"bytes": 2 * T * H + 2 * R * H + 12 * R + 4 * (E + 1), "flops": 0},
-        "grouped_gemm": {"bytes": e_active * 3 * H * I * wb + sb + 4 * R * H + 4 * R * I,
+        "grouped_gemm": {"bytes": e_active * weight_bytes(spec, 3 * H * I) + sb + 4 * R * H + 4 * R * I,
                          "flops": 6 * R * H * I},
         "unpermute": {"bytes": 2 * R * H + 2 * T * H + 8 * R + (2 * T * H + 4 * T if spec.has_shared else 0),
                       "flops": 0},
@@ -303,7 +318,7 @@ def make_layer(spec, T, seed, dev):
     t = tensors_of(spec, d)
     cfg = ops.make_config(T, spec.H, spec.E, spec.K, spec.I, has_shared=spec.has_shared,
                           I_shared=spec.I_shared, mode=spec.mode, routed_scale=spec.routed_scale,
-                          wdtype=ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16)
+                          wdtype=wd_of(ops, spec))
     return d, t, ops.MoELayer(cfg, t, device=dev)
 
 
@@ -404,7 +419,7 @@ def measure(spec, T, args, rank, world, dev, peaks, light=False):
     sh_scr = ws[L.shared_gemm_scratch:L.total]
     sh_h = v("shared_hact", torch.bfloat16, (T, spec.I_shared)) if spec.has_shared else None
     sh_y = v("shared_y", torch.bfloat16, (T, H)) if spec.has_shared else None
-    wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
+    wd = wd_of(ops, spec)
     names = ["router", "topk", "permute", "grouped_gemm", "unpermute"]
     rscr = ws[L.router_split:L.splitk]
 
@@ -465,7 +480,7 @@ def measure(spec, T, args, rank, world, dev, peaks, light=False):
     hot = (float(np.isin(ids_h, list(spec.hot_experts)).mean()) if spec.hot_experts else None)
 
     res = {"workload": spec.name, "T": T, "H": spec.H, "E": spec.E, "K": spec.K, "I": spec.I,
-           "dtype": "bf16" if spec.wdtype == "bf16" else "bf16 activations, fp8-e4m3 weights",
+           "dtype": DTYPE_NAME[spec.wdtype],
            "us_per_layer": round(ms_step * 1e3, 2),
            "tokens_per_s": round(job_throughput(T, args.steps, world, ms), 1),
            "ms_total": ms, "roofline": roof, "per_stage": per_stage, "clocks": clk,
@@ -623,7 +638,7 @@ def run_ours(args, rank, world, local_rank):
                    if spec.mode == 0 else "sigmoid+bias top-K, scaled-sum", "tokens_per_gpu": T,
                    "parallelism": f"token-dp replicas x{world}",
                    "l2": "inputs larger than L2 (expert weights "
-                         f"{spec.E * 3 * spec.H * spec.I * (1 if spec.wdtype == 'fp8' else 2) / 1e9:.2f} GB "
+                         f"{weight_bytes(spec, spec.E * 3 * spec.H * spec.I) / 1e9:.2f} GB "
                          "per layer), no flush"},
         "roofline": head["roofline"],
         "per_stage": head["per_stage"],
@@ -654,6 +669,7 @@ def run_ours(args, rank, world, local_rank):
         res["stage_sweep_large_T_high_expert"] = stage_sweep(synth.SPECS["high_expert"],
                                                              (16384,), peaks, dev)
         res["prefill_grouped_gemm"] = prefill_points(peaks, dev)
+        res["weight_formats_gpt_oss_20b"] = format_sweep(peaks, dev)
     return res
 
 
@@ -765,7 +781,7 @@ def probe_layer(spec, T, reps, dev):
     t = tensors_of(spec, d)
     cfg = ops.make_config(T, spec.H, spec.E, spec.K, spec.I, has_shared=spec.has_shared,
                           I_shared=spec.I_shared, mode=spec.mode, routed_scale=spec.routed_scale,
-                          wdtype=ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16)
+                          wdtype=wd_of(ops, spec))
     layer = ops.MoELayer(cfg, t, device=dev)
     out = torch.empty_like(d["x"])
     for _ in range(reps):
@@ -788,7 +804,7 @@ def prefill_points(peaks, dev):
         d = synth.device_inputs(spec, T, seed=3, device=dev)
         t = tensors_of(spec, d)
         cfg = ops.make_config(T, spec.H, spec.E, spec.K, spec.I,
-                              wdtype=ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16)
+                              wdtype=wd_of(ops, spec))
         layer = ops.MoELayer(cfg, t, device=dev)
         layer(d["x"])
         torch.cuda.synchronize()
@@ -800,7 +816,7 @@ def prefill_points(peaks, dev):
         y = layer.view("y", torch.bfloat16, (R, H))
         L = layer.layout
         gscr = layer.workspace[L.gemm_scratch:L.shared_gemm_scratch]
-        wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
+        wd = wd_of(ops, spec)
         sec = _time(lambda: ops.grouped_gemm(xp, off, E, H, I, t["w1"], t["w3"], t["w2"], hact, y,
                                              gscr, wdtype=wd, s1=t.get("s1"), s3=t.get("s3"),
                                              s2=t.get("s2")), 10, stream)
@@ -813,6 +829,36 @@ def prefill_points(peaks, dev):
                     "achieved": round(r["achieved"], 1), "unit": r["unit"],
                     "frac": round(r["frac"], 3), "tflops": round(sb["flops"] / sec / 1e12, 1),
                     "hot_expert_share": hot})
+        del layer, d, t
+        torch.cuda.empty_cache()
+    return res
+
+
+def format_sweep(peaks, dev, Ts=(1, 32, 512, 4096)):
+    """The GPT-OSS-20B-shaped layer with its expert weights stored three ways
+    (bf16, FP8 e4m3 + 128x128 scales, MXFP4): device-resident moe_layer time
+    and the grouped GEMM's share of the HBM roofline (weight bytes of the
+    active experts over the layer time, the bound of small batches)."""
+    from mixture_experts_layer_07_gb300 import synth
+
+    stream = torch.cuda.current_stream()
+    res = []
+    for wdt in ("bf16", "fp8", "mxfp4"):
+        spec = synth.SPECS["gpt_oss_20b"].with_(wdtype=wdt)
+        d, t, layer = make_layer(spec, max(Ts), 3, dev)
+        for T in Ts:
+            x = d["x"][:T].contiguous()
+            out = torch.empty_like(x)
+            sec = _time(lambda: layer(x, out), 20, stream)
+            if int(layer.dev_status.item()) != 0:
+                raise RuntimeError(f"device status {int(layer.dev_status.item())}")
+            ids = layer.view("ids", torch.int32, (T, spec.K)).cpu().numpy()
+            e_act = int(len(np.unique(ids)))
+            wbytes = e_act * weight_bytes(spec, 3 * spec.H * spec.I)
+            res.append({"weights": wdt, "T": T, "us_per_layer": round(sec * 1e6, 2),
+                        "tokens_per_s": round(T / sec, 1), "e_active": e_act,
+                        "weight_GB_per_s": round(wbytes / sec / 1e9, 1),
+                        "weight_frac_of_hbm": round(wbytes / sec / 1e9 / peaks["hbm_gbs"], 3)})
         del layer, d, t
         torch.cuda.empty_cache()
     return res
@@ -875,10 +921,11 @@ def oracle_inputs_from_device(spec, d, tokens, seed=0):
     def bits(t):
         return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
-    if spec.wdtype == "fp8":
+    if spec.wdtype in ("fp8", "mxfp4"):
+        sfx = "_q" if spec.wdtype == "fp8" else "_q4"
         for k, sk in (("w1", "s1"), ("w3", "s3"), ("w2", "s2")):
-            q, s = d[k + "_q"], d[sk]
-            inp[k + "_q"] = HostExperts(q.shape, {e: q[e].cpu().numpy() for e in used})
+            q, s = d[k + sfx], d[sk]
+            inp[k + sfx] = HostExperts(q.shape, {e: q[e].cpu().numpy() for e in used})
             inp[sk] = HostExperts(s.shape, {e: s[e].cpu().numpy() for e in used})
     else:
         for k in ("w1", "w3", "w2"):

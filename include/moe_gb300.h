@@ -27,6 +27,12 @@
  *   - bf16 tensors are IEEE bfloat16; FP8 weights are OCP e4m3 ("fn") codes
  *     with one fp32 scale per 128 x 128 block (the last block of a dimension
  *     may be narrower); scales are laid out [E][ceil(rows/128)][ceil(cols/128)].
+ *     MXFP4 weights ([dispatch] introduction: FP8 and MXFP4 experts) follow
+ *     OCP Microscaling: [E][rows][cols/2] bytes, each two E2M1 codes (sign, 2
+ *     exponent bits with bias 1, 1 mantissa bit), element 2i in the low
+ *     nibble; one UE8M0 scale byte s (value 2^(s-127), s < 255) per 32
+ *     consecutive elements of a row, laid out [E][rows][cols/32] (uint8, passed
+ *     through the scale pointers); rows must hold whole 32-element blocks.
  *   - Errors found on the host (null pointer, bad size, misalignment, short
  *     scratch) return a status != MOE_OK before anything is queued.  A failed
  *     launch returns MOE_ERR_CUDA.  Errors found by a kernel (an expert id out
@@ -72,8 +78,9 @@ typedef enum {
 } moe_score_mode_t;
 
 typedef enum {
-  MOE_W_BF16 = 0,         /* expert weights bf16 */
-  MOE_W_FP8E4M3_B128 = 1  /* expert weights e4m3 + fp32 128x128 block scales */
+  MOE_W_BF16 = 0,          /* expert weights bf16 */
+  MOE_W_FP8E4M3_B128 = 1,  /* expert weights e4m3 + fp32 128x128 block scales */
+  MOE_W_MXFP4 = 2          /* expert weights MXFP4: e2m1 pairs + a UE8M0 scale per 32 */
 } moe_wdtype_t;
 
 /* How the grouped GEMM picks a kernel variant for each expert block. */
@@ -116,7 +123,8 @@ typedef struct {
   const void* w1;          /* [E, I, H] gate projection (bf16 or e4m3) */
   const void* w3;          /* [E, I, H] up projection */
   const void* w2;          /* [E, H, I] down projection */
-  const float* s1;         /* FP8 block scales of w1 / w3 / w2, else NULL */
+  const float* s1;         /* FP8 block scales (fp32) or MXFP4 scale bytes (uint8,
+                              cast) of w1 / w3 / w2, else NULL */
   const float* s3;
   const float* s2;
   const void* sw1;         /* shared expert bf16 [I_shared, H], or NULL */

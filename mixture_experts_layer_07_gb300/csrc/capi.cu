@@ -30,7 +30,9 @@ moe_status_t check_cfg(const moe_config_t* c) {
   if (c->I <= 0 || c->I % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (c->mode != MOE_SCORE_SOFTMAX_RENORM && c->mode != MOE_SCORE_SIGMOID_BIAS_SCALED)
     return MOE_ERR_INVALID_ARG;
-  if (c->wdtype != MOE_W_BF16 && c->wdtype != MOE_W_FP8E4M3_B128) return MOE_ERR_UNSUPPORTED;
+  if (c->wdtype != MOE_W_BF16 && c->wdtype != MOE_W_FP8E4M3_B128 && c->wdtype != MOE_W_MXFP4)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->wdtype == MOE_W_MXFP4 && (c->H % 32 != 0 || c->I % 32 != 0)) return MOE_ERR_INVALID_ARG;
   if (c->dispatch < MOE_DISPATCH_PER_BLOCK || c->dispatch > MOE_DISPATCH_ONE_LAUNCH)
     return MOE_ERR_INVALID_ARG;
   if (c->m_skinny < -1) return MOE_ERR_INVALID_ARG;
@@ -226,7 +228,7 @@ moe_status_t moe_grouped_gemm(const void* xp, const int32_t* offsets, int E_bloc
   if (chk != MOE_OK) return (moe_status_t)chk;
   if (!w1 || !w3 || !w2 || !scratch) return MOE_ERR_INVALID_ARG;
   if (R > 0 && (!xp || !hact || !y)) return MOE_ERR_INVALID_ARG;
-  if (wdtype == MOE_W_FP8E4M3_B128 && (!s1 || !s3 || !s2)) return MOE_ERR_INVALID_ARG;
+  if (wdtype != MOE_W_BF16 && (!s1 || !s3 || !s2)) return MOE_ERR_INVALID_ARG;
   if (scratch_bytes < grouped_gemm_scratch_bytes(R, E_blocks)) return MOE_ERR_WORKSPACE;
   if (misaligned(scratch, 256) || misaligned(w1, 16) || misaligned(w3, 16) || misaligned(w2, 16) ||
       (xp && misaligned(xp, 16)) || (hact && misaligned(hact, 16)) || (y && misaligned(y, 16)) ||
@@ -277,7 +279,7 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
   if (T == 0) return MOE_OK;
   if (!x || !w || !out || !workspace || !w->wg || !w->w1 || !w->w3 || !w->w2)
     return MOE_ERR_INVALID_ARG;
-  if (cfg->wdtype == MOE_W_FP8E4M3_B128 && (!w->s1 || !w->s3 || !w->s2)) return MOE_ERR_INVALID_ARG;
+  if (cfg->wdtype != MOE_W_BF16 && (!w->s1 || !w->s3 || !w->s2)) return MOE_ERR_INVALID_ARG;
   if (cfg->has_shared && (!w->sw1 || !w->sw3 || !w->sw2)) return MOE_ERR_INVALID_ARG;
   moe_workspace_layout_t L;
   layout_of(cfg, &L);

@@ -33,10 +33,9 @@ __host__ __device__ __forceinline__ int moe_variant_of(int64_t m_size, int64_t R
     m = avg < 1 ? 1 : avg;
   }
   if (m <= (int64_t)m_skinny) return MOE_VARIANT_SKINNY;
-  // 256-row token tiles pay off where each weight tile is dequantised (FP8):
-  // the conversion is amortised over twice the tokens
-  return (wdtype == MOE_W_FP8E4M3_B128 && m >= MOE_WIDE_MIN_ROWS) ? MOE_VARIANT_WIDE
-                                                                 : MOE_VARIANT_TILE;
+  // 256-row token tiles pay off where each weight tile is dequantised (FP8,
+  // MXFP4): the conversion is amortised over twice the tokens
+  return (wdtype != MOE_W_BF16 && m >= MOE_WIDE_MIN_ROWS) ? MOE_VARIANT_WIDE : MOE_VARIANT_TILE;
 }
 
 // First error wins.

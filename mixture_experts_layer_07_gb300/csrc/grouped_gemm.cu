@@ -70,22 +70,27 @@ gemm_plan_kernel(const int32_t* __restrict__ offsets, int E_blocks, int R, int m
 }
 
 // ---------------------------------------------------------------- tensor cores
-// WFP8: expert weights are e4m3 with one fp32 scale per 128 x 128 block.  TMA
-// brings the e4m3 tile [128 rows x 64 K] in unswizzled; a converter warpgroup
-// turns it into bf16 (e4m3 -> f16 is exact, times the block's scale, rounded
-// once to bf16) written straight into the 128-byte-swizzled K-major layout the
-// MMA reads, in a small ring of its own.  The 128-row weight tile is exactly
-// one scale row block and a 64-wide K stage lies inside one scale column
-// block, so each converted tile needs a single scale.
-template <int BN, bool SWIGLU, bool WFP8>
+// WQ: the expert weights' storage (a MOE_W_* code).  0: bf16, read by the MMA
+// as TMA lands it.  1 (FP8): e4m3 with one fp32 scale per 128 x 128 block.
+// TMA brings the e4m3 tile [128 rows x 64 K] in unswizzled; a converter
+// warpgroup turns it into bf16 (e4m3 -> f16 is exact, times the block's scale,
+// rounded once to bf16) written straight into the 128-byte-swizzled K-major
+// layout the MMA reads, in a small ring of its own.  The 128-row weight tile
+// is exactly one scale row block and a 64-wide K stage lies inside one scale
+// column block, so each converted tile needs a single scale.  2 (MXFP4): the
+// tile is [128 rows x 32 bytes] of e2m1 pairs and each 32 elements of a row
+// carry their own power-of-two scale; the converters turn every element into
+// bf16 exactly (an e2m1 value times a power of two has at most two significant
+// bits), so the MMA sees the stored weights themselves.
+template <int BN, bool SWIGLU, int WQ>
 struct TcCfg {
   static constexpr int kMaxScaleCols = 64;  // FP8: K up to 8192 (64 scale columns of 128)
   static constexpr int kNA = SWIGLU ? 2 : 1;
   static constexpr int kABytes = kBM * kBK * 2;             // bf16 weight tile
-  static constexpr int kQBytes = kBM * kBK;                 // e4m3 weight tile
+  static constexpr int kQBytes = WQ == 2 ? kBM * kBK / 2 : kBM * kBK;  // e4m3 / e2m1-pair tile
   static constexpr int kBBytes = BN * kBK * 2;              // bf16 activation tile
-  static constexpr int kStageBytes = kNA * (WFP8 ? kQBytes : kABytes) + kBBytes;
-  static constexpr int kConvStages = WFP8 ? 2 : 0;
+  static constexpr int kStageBytes = kNA * (WQ ? kQBytes : kABytes) + kBBytes;
+  static constexpr int kConvStages = WQ ? 2 : 0;
   static constexpr int kConvBytes = kNA * kABytes;
   static constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, splitting the token columns
   static constexpr int kEpiBytes = kEpiWarps * 16 * 32 * 2;  // per warp: 16 tokens x 32 features
@@ -97,18 +102,18 @@ struct TcCfg {
   static constexpr int kTmemNeed = kAccStages * kAccCols;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64
                                  : kTmemNeed <= 128 ? 128 : kTmemNeed <= 256 ? 256 : 512;
-  static constexpr int kScaleBufs = WFP8 ? 3 : 0;  // per-unit scale rows, reused every 3 units
+  static constexpr int kScaleBufs = WQ ? 3 : 0;  // per-unit scale rows, reused every 3 units
   // work-unit queue: warp 0 takes units (its first is blockIdx.x, the rest
   // from the launch's atomic counter) and hands each to the other roles
   static constexpr int kQ = 8;
-  static constexpr int kQConsumers = 1 + kEpiWarps + (WFP8 ? 8 : 0);  // MMA thread + warps
+  static constexpr int kQConsumers = 1 + kEpiWarps + (WQ ? 8 : 0);  // MMA thread + warps
   static constexpr int kNumBars =
       2 * kStages + 2 * kAccStages + 1 + 2 * kConvStages + kScaleBufs + 2 * kQ;
   static constexpr int kBarBytes =
       kNumBars * 8 + 16 + kScaleBufs * 2 * kMaxScaleCols * 4 + kQ * 4 + BN * 4;
   static constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes +
                                        (size_t)kConvStages * kConvBytes + kEpiBytes + kBarBytes;
-  static constexpr int kConvThreads = WFP8 ? 256 : 0;  // eight converter warps
+  static constexpr int kConvThreads = WQ ? 256 : 0;  // eight converter warps
   static constexpr int kConvWarp0 = 2 + kEpiWarps;        // first converter warp
   // G1 (SwiGLU) only: one more warp that, in gather mode, copies the tile's
   // rows straight from x (small batches: a few rows per tile)
@@ -182,6 +187,49 @@ MOE_DEVICE uint32_t e4m3x2_to_bf16x2(uint32_t two, float sc) {
   return pack_bf16x2(f.x * sc, f.y * sc);
 }
 
+MOE_DEVICE uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+MOE_DEVICE uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Multipliers that turn an e2m1 code placed in bf16 bits (below) into the
+// weight code * 2^(s - 127) for the UE8M0 scale byte s: mul[0] = 2^(s - 1)
+// and, where that exceeds the bf16 range (s > 128), 2^127 followed by
+// mul[1] = 2^(s - 128).  Both replicated into the two bf16 lanes.
+MOE_DEVICE void mx_multipliers(uint32_t s, uint32_t& m1, uint32_t& m2) {
+  const uint32_t e1 = s <= 128u ? s + 126u : 254u;  // bf16 exponent field of mul[0]
+  const uint32_t e2 = s <= 128u ? 127u : s - 1u;   // 1.0, or 2^(s - 128)
+  m1 = (e1 << 7) * 0x10001u;
+  m2 = (e2 << 7) * 0x10001u;
+}
+
+// Eight e2m1 codes of a word (element 2i in the low nibble of byte i) ->
+// eight bf16 weights in element order.  A code (sign s, exponent e, mantissa
+// m) written as the bf16 bits s<<15 | e<<7 | m<<6 is exactly the bf16 number
+// code * 2^-126 (e = 0 is the bf16 subnormal 2^-127 = 0.5 * 2^-126), so one
+// correctly rounded bf16 multiply by a power of two gives the weight exactly.
+// Per pair: one byte permute spreads the two codes of byte i into the two
+// 16-bit lanes (selector 8 copies the clear top bit of a nibble byte: a zero
+// byte), one multiply by 2^6 + 2^12 puts the magnitude bits at 6..8 and the
+// sign bit at 15 of each lane (the two shifted copies do not overlap), one
+// mask keeps exactly those bits.
+MOE_DEVICE void e2m1x8_to_bf16(uint32_t w, uint32_t m1, uint32_t m2, bool big, uint32_t* out) {
+  const uint32_t lo = w & 0x0F0F0F0Fu, hi = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t x = prmt(lo, hi, 0x8080u | (uint32_t)i | ((uint32_t)(4 + i) << 8));
+    const uint32_t v = bf16x2_mul((x * 0x1040u) & 0x81C081C0u, m1);
+    out[i] = big ? bf16x2_mul(v, m2) : v;
+  }
+}
+
 // FUSED (G1 layout, SWIGLU = true): one persistent launch runs the list's G1
 // units and then its G2 units (W2 = tm_w2, activations hact = tm_h, output
 // y = out2, N2 x K2).  A G2 unit of token tile i starts loading only after
@@ -192,7 +240,7 @@ MOE_DEVICE uint32_t e4m3x2_to_bf16x2(uint32_t two, float sc) {
 // boundary between the two disappears.
 // The kernel body for one work list, run by CTAs cta = 0..ncta-1 of a group
 // (the whole grid, or one of the two groups of the two-list launch below).
-template <int BN, bool SWIGLU, bool WFP8, bool FUSED>
+template <int BN, bool SWIGLU, int WQ, bool FUSED>
 MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
                              const CUtensorMap& tm_act, const float* __restrict__ sa,
                              const float* __restrict__ sb, int32_t* __restrict__ counts, int list,
@@ -206,7 +254,7 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
                              const int32_t* __restrict__ grows, int gk, int ksplit2,
                              float* __restrict__ part2, int32_t* __restrict__ scnt1,
                              int32_t* __restrict__ scnt2, const int cta, const int ncta) {
-  using C = TcCfg<BN, SWIGLU, WFP8>;
+  using C = TcCfg<BN, SWIGLU, WQ>;
   static_assert(!FUSED || SWIGLU, "the fused launch uses the G1 layout");
   // gather mode (G1, small batches): the gather warp copies each tile's rows
   // from x -- row r of the expert-ordered layout is token grows[r] / gk -- so
@@ -330,7 +378,8 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
   // accumulator set and the parity of its barriers for the i-th unit of this CTA
   auto acc_set = [](uint32_t i) { return C::kAccStages == 2 ? (i & 1u) : 0u; };
   auto acc_par = [](uint32_t i) { return (C::kAccStages == 2 ? (i >> 1) : i) & 1u; };
-  constexpr int kWeightBytes = WFP8 ? C::kQBytes : C::kABytes;
+  constexpr int kWeightBytes = WQ ? C::kQBytes : C::kABytes;
+  constexpr int kWx = WQ == 2 ? kBK / 2 : kBK;  // a stage's K step in the weight map's units
   // next work unit from the queue (every consumer sees every unit, in order);
   // `arrive` frees the entry (one arrival per consuming warp or thread).
   // total (or more) ends the walk; -1 means the wait gave up.
@@ -378,7 +427,7 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
               break;
             }
             mbar_expect_tx(full_bar(stage), kWeightBytes);
-            tma_load_3d(sbase + stage * C::kStageBytes, &tm_w2, full_bar(stage), kb * kBK, nb * kBM,
+            tma_load_3d(sbase + stage * C::kStageBytes, &tm_w2, full_bar(stage), kb * kWx, nb * kBM,
                         it.x);
             pre_par |= phase << npre;
             if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -413,8 +462,8 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
           }
           const uint32_t st = sbase + stage * C::kStageBytes;
           mbar_arrive_expect_tx(full_bar(stage), gat && u.g1 ? C::kNA * kWeightBytes : stage_bytes);
-          tma_load_3d(st, wmap, full_bar(stage), kb * kBK, nb * kBM, it.x);
-          if (u.g1) tma_load_3d(st + kWeightBytes, &tm_wb, full_bar(stage), kb * kBK, nb * kBM, it.x);
+          tma_load_3d(st, wmap, full_bar(stage), kb * kWx, nb * kBM, it.x);
+          if (u.g1) tma_load_3d(st + kWeightBytes, &tm_wb, full_bar(stage), kb * kWx, nb * kBM, it.x);
           if (!(gat && u.g1))
             tma_load_2d(st + C::kNA * kWeightBytes, amap, full_bar(stage), kb * kBK, it.y);
           armed |= 1u << stage;
@@ -450,14 +499,14 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
         const Unit u = unit_of(w);
         for (int kb = u.kb_lo; kb < u.kb_hi; ++kb) {
           if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, kWaitLimitNs) ||
-              (WFP8 && !mbar_wait_bounded(conv_full(cs), cphase, abort_flag, kWaitLimitNs))) {
+              (WQ && !mbar_wait_bounded(conv_full(cs), cphase, abort_flag, kWaitLimitNs))) {
             fail();
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t st = sbase + stage * C::kStageBytes;
-          const uint32_t wa_s = WFP8 ? cbase + cs * C::kConvBytes : st;
+          const uint32_t wa_s = WQ ? cbase + cs * C::kConvBytes : st;
           const uint32_t wb_s = wa_s + C::kABytes;
           const uint32_t sx = st + C::kNA * kWeightBytes;
 #pragma unroll
@@ -469,7 +518,7 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
           }
           issued = true;
           tc_commit(empty_bar(stage));
-          if (WFP8) {
+          if (WQ) {
             tc_commit(conv_empty(cs));
             if (++cs == C::kConvStages) { cs = 0; cphase ^= 1u; }
           }
@@ -683,13 +732,16 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
       if (lane == 0)
         for (int j = issued; j > 0; --j) mbar_arrive(full_bar((stage + C::kStages - j) % C::kStages));
     }
-  } else if (WFP8 && warp < C::kConvWarp0 + C::kConvThreads / 32) {
-    // ---------------- e4m3 -> bf16 converters, warps 10..17
-    // At the start of each work unit the converters stage that unit's row of
-    // block scales (one per 128-wide K block) in shared memory, so the
+  } else if (WQ && warp < C::kConvWarp0 + C::kConvThreads / 32) {
+    // ---------------- e4m3 / e2m1 -> bf16 converters, warps 10..17
+    // FP8: at the start of each work unit the converters stage that unit's row
+    // of block scales (one per 128-wide K block) in shared memory, so the
     // per-stage scale is a shared-memory read, not a global load.  Rows rotate
     // through three buffers: a converter can run at most two stages ahead of
     // the slowest one, so a buffer is never rewritten while still being read.
+    // MXFP4: a converter owns one row and 32 K elements of each stage (one
+    // scale byte per matrix) and decodes the e2m1 codes with integer bit
+    // placement and one bf16 multiply (e2m1x8_to_bf16).
     const int ct = threadIdx.x - 32 * C::kConvWarp0;
     int stage = 0, cs = 0;
     uint32_t phase = 0, cphase = 0, unit = 0, q = 0, qph = 0;
@@ -707,19 +759,44 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
       float* scale_row = scale_rows + buf * 2 * C::kMaxScaleCols;
       // the unit's matrices: W1 and W3 (G1) or W2 (G2 of a fused launch)
       const bool g1 = un.g1;
-      const int rb = ((g1 || !FUSED ? N : N2) + 127) / 128;
-      const int cb = ((g1 || !FUSED ? Kdim : K2) + 127) / 128;
-      const float* s_a = g1 || !FUSED ? sa : s2;
-      const size_t row = ((size_t)it.x * rb + nb) * cb;
-      for (int c = ct; c < cb; c += C::kConvThreads) {
-        scale_row[c] = __ldg(s_a + row + c);
-        scale_row[C::kMaxScaleCols + c] = g1 ? __ldg(sb + row + c) : 0.f;
+      const int Nm = g1 || !FUSED ? N : N2, Km = g1 || !FUSED ? Kdim : K2;
+      if (WQ == 1) {
+        const int rb = (Nm + 127) / 128;
+        const int cb = (Km + 127) / 128;
+        const float* s_a = g1 || !FUSED ? sa : s2;
+        const size_t row = ((size_t)it.x * rb + nb) * cb;
+        for (int c = ct; c < cb; c += C::kConvThreads) {
+          scale_row[c] = __ldg(s_a + row + c);
+          scale_row[C::kMaxScaleCols + c] = g1 ? __ldg(sb + row + c) : 0.f;
+        }
+        mbar_arrive(scale_bar(buf));
+        if (!mbar_wait_bounded(scale_bar(buf), (unit / 3u) & 1u, abort_flag, kWaitLimitNs)) {
+          fail();
+          break;
+        }
       }
-      mbar_arrive(scale_bar(buf));
-      if (!mbar_wait_bounded(scale_bar(buf), (unit / 3u) & 1u, abort_flag, kWaitLimitNs)) {
-        fail();
-        break;
-      }
+      // MXFP4: this thread's row of the tile and its 32-element half of each
+      // stage.  Its scale bytes (one per stage and matrix) are fetched eight
+      // stages ahead into registers: the rows of a tile span more cache lines
+      // than L1 keeps next to the pipeline's shared memory, so a load issued
+      // at the stage that needs it would wait on L2 every stage.
+      const int r4 = ct >> 1, j4 = ct & 1;
+      const int n4 = nb * kBM + r4, kcb = Km / 32;
+      const uint8_t* srow[2] = {
+          reinterpret_cast<const uint8_t*>(g1 || !FUSED ? sa : s2) + ((size_t)it.x * Nm + n4) * kcb,
+          reinterpret_cast<const uint8_t*>(sb) + ((size_t)it.x * Nm + n4) * kcb};
+      uint32_t pend[2][8], win[2][2];
+      auto fetch = [&](int kb0) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int kblk = 2 * (kb0 + i) + j4;
+            pend[t][i] = (WQ == 2 && (t == 0 || g1) && n4 < Nm && kb0 + i < un.kb_hi && kblk < kcb)
+                             ? (uint32_t)__ldg(srow[t] + kblk) : 0u;
+          }
+      };
+      if (WQ == 2) fetch(un.kb_lo);
       for (int kb = un.kb_lo; kb < un.kb_hi; ++kb) {
         if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, kWaitLimitNs) ||
             !mbar_wait_bounded(conv_empty(cs), cphase ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -728,9 +805,41 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
           break;
         }
         const int sc = (kb * kBK) / 128;
+        const int wi = (kb - un.kb_lo) & 7;
+        if (WQ == 2 && wi == 0) {
+          // the window's scale bytes (loaded a window ago) -> packed words;
+          // then the next window's loads
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            win[t][0] = pend[t][0] | pend[t][1] << 8 | pend[t][2] << 16 | pend[t][3] << 24;
+            win[t][1] = pend[t][4] | pend[t][5] << 8 | pend[t][6] << 16 | pend[t][7] << 24;
+          }
+          fetch(kb + 8);
+        }
 #pragma unroll
         for (int t = 0; t < C::kNA; ++t) {
           if (t > 0 && !g1) break;
+          if (WQ == 2) {
+            // 16 bytes = 32 e2m1 codes of row r4, K kb*64 + 32*j4 .. +31, times
+            // their block's power of two (rows and blocks past the matrix: TMA
+            // reads zero codes; a zero scale byte keeps them zero)
+            const uint32_t sbyte = ((wi < 4 ? win[t][0] : win[t][1]) >> (8 * (wi & 3))) & 0xFFu;
+            uint32_t m1, m2;
+            mx_multipliers(sbyte, m1, m2);
+            const bool big = sbyte > 128u;
+            const uint8_t* src = smem + (size_t)stage * C::kStageBytes + t * C::kQBytes;
+            uint8_t* dst = conv + (size_t)cs * C::kConvBytes + t * C::kABytes;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + r4 * (kBK / 2) + j4 * 16);
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint4 o;
+              e2m1x8_to_bf16(wv[c], m1, m2, big, &o.x);
+              // 8 bf16 = 16-byte chunk 4*j4 + c of row r4, 128-byte swizzled
+              *reinterpret_cast<uint4*>(dst + r4 * 128 + (((4 * j4 + c) ^ (r4 & 7)) << 4)) = o;
+            }
+            continue;
+          }
           const float scl = scale_row[t * C::kMaxScaleCols + sc];
           const uint8_t* src = smem + (size_t)stage * C::kStageBytes + t * C::kQBytes;
           uint8_t* dst = conv + (size_t)cs * C::kConvBytes + t * C::kABytes;
@@ -770,8 +879,8 @@ MOE_DEVICE void gemm_tc_body(const CUtensorMap& tm_wa, const CUtensorMap& tm_wb,
   }
 }
 
-template <int BN, bool SWIGLU, bool WFP8, bool FUSED>
-__global__ void __launch_bounds__(TcCfg<BN, SWIGLU, WFP8>::kThreads, 1)
+template <int BN, bool SWIGLU, int WQ, bool FUSED>
+__global__ void __launch_bounds__(TcCfg<BN, SWIGLU, WQ>::kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant__ CUtensorMap tm_wb,
                const __grid_constant__ CUtensorMap tm_act, const float* __restrict__ sa,
                const float* __restrict__ sb, int32_t* __restrict__ counts, int list,
@@ -785,7 +894,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_wa, const __grid_constant_
                int32_t* __restrict__ scnt2) {
   pdl_wait();
   pdl_trigger();
-  gemm_tc_body<BN, SWIGLU, WFP8, FUSED>(tm_wa, tm_wb, tm_act, sa, sb, counts, list, items, N, Kdim,
+  gemm_tc_body<BN, SWIGLU, WQ, FUSED>(tm_wa, tm_wb, tm_act, sa, sb, counts, list, items, N, Kdim,
                                         out, ksplit, R, part, dev_status, tm_w2, tm_h, s2, N2, K2,
                                         out2, done, gx, grows, gk, ksplit2, part2, scnt1, scnt2,
                                         (int)blockIdx.x, (int)gridDim.x);
@@ -802,8 +911,8 @@ struct DualMaps {
   CUtensorMap h[2];    // FUSED: hact per list
 };
 
-template <bool SWIGLU, bool WFP8, bool FUSED>
-__global__ void __launch_bounds__(TcCfg<kBnSkinny, SWIGLU, WFP8>::kThreads, 1)
+template <bool SWIGLU, int WQ, bool FUSED>
+__global__ void __launch_bounds__(TcCfg<kBnSkinny, SWIGLU, WQ>::kThreads, 1)
 gemm_tc_dual_kernel(const __grid_constant__ CUtensorMap tm_wa,
                     const __grid_constant__ CUtensorMap tm_wb, const __grid_constant__ DualMaps maps,
                     const float* __restrict__ sa, const float* __restrict__ sb,
@@ -815,8 +924,8 @@ gemm_tc_dual_kernel(const __grid_constant__ CUtensorMap tm_wa,
                     int32_t* __restrict__ done0, int32_t* __restrict__ done1,
                     const __nv_bfloat16* __restrict__ gx, const int32_t* __restrict__ grows,
                     int gk) {
-  using C0 = TcCfg<kBnSkinny, SWIGLU, WFP8>;
-  using C1 = TcCfg<kBnTile, SWIGLU, WFP8>;
+  using C0 = TcCfg<kBnSkinny, SWIGLU, WQ>;
+  using C1 = TcCfg<kBnTile, SWIGLU, WQ>;
   static_assert(C0::kThreads == C1::kThreads, "one block size for both groups");
   pdl_wait();
   pdl_trigger();
@@ -829,12 +938,12 @@ gemm_tc_dual_kernel(const __grid_constant__ CUtensorMap tm_wa,
   if (b0 > 0 && s0 < 1) s0 = 1;
   if (b1 > 0 && s0 > g - 1) s0 = g - 1;
   if ((int)blockIdx.x < s0)
-    gemm_tc_body<kBnSkinny, SWIGLU, WFP8, FUSED>(
+    gemm_tc_body<kBnSkinny, SWIGLU, WQ, FUSED>(
         tm_wa, tm_wb, maps.act[0], sa, sb, counts, 0, items0, N, Kdim, out, 1, R, nullptr,
         dev_status, tm_w2, maps.h[0], s2, N2, K2, out2, done0, gx, grows, gk, 1, nullptr, nullptr,
         nullptr, (int)blockIdx.x, s0);
   else
-    gemm_tc_body<kBnTile, SWIGLU, WFP8, FUSED>(
+    gemm_tc_body<kBnTile, SWIGLU, WQ, FUSED>(
         tm_wa, tm_wb, maps.act[1], sa, sb, counts, 1, items1, N, Kdim, out, 1, R, nullptr,
         dev_status, tm_w2, maps.h[1], s2, N2, K2, out2, done1, gx, grows, gk, 1, nullptr, nullptr,
         nullptr, (int)blockIdx.x - s0, g - s0);
@@ -847,10 +956,19 @@ gemm_tc_dual_kernel(const __grid_constant__ CUtensorMap tm_wa,
 constexpr int kSimtN = 64;
 constexpr int kSimtK = 64;
 
-template <bool FP8>
+template <int WQ>
 MOE_DEVICE float load_w(const void* w, const float* s, int e, int n, int k, int N, int Kdim) {
   const size_t idx = ((size_t)e * N + n) * Kdim + k;
-  if (FP8) {
+  if (WQ == MOE_W_MXFP4) {
+    // element k of the row: byte k/2, low nibble for even k; scale k/32
+    const uint8_t byte = static_cast<const uint8_t*>(w)[idx / 2];
+    const int c = (k & 1) ? byte >> 4 : byte & 15, ex = (c >> 1) & 3, m = c & 1;
+    const float mag = ex == 0 ? 0.5f * m : (1.f + 0.5f * m) * (float)(1 << (ex - 1));
+    const uint32_t sb = reinterpret_cast<const uint8_t*>(s)[((size_t)e * N + n) * (Kdim / 32) + k / 32];
+    const float sc = sb ? __uint_as_float(sb << 23) : __uint_as_float(0x00400000u);
+    return ((c & 8) ? -mag : mag) * sc;
+  }
+  if (WQ == MOE_W_FP8E4M3_B128) {
     const uint8_t code = static_cast<const uint8_t*>(w)[idx];
     const __half_raw hr = __nv_cvt_fp8_to_halfraw(code, __NV_E4M3);
     const int rb = (N + 127) / 128, cb = (Kdim + 127) / 128;
@@ -861,7 +979,7 @@ MOE_DEVICE float load_w(const void* w, const float* s, int e, int n, int k, int 
   }
 }
 
-template <bool SWIGLU, bool FP8>
+template <bool SWIGLU, int WQ>
 __global__ void __launch_bounds__(256)
 gemm_simt_kernel(const __nv_bfloat16* __restrict__ act, const void* __restrict__ wa,
                  const void* __restrict__ wb, const float* __restrict__ sa,
@@ -887,8 +1005,8 @@ gemm_simt_kernel(const __nv_bfloat16* __restrict__ act, const void* __restrict__
     for (int i = tid; i < kSimtN * kSimtK; i += 256) {
       const int r = i / kSimtK, k = k0 + i % kSimtK, n = n0 + r;
       const bool in = n < N && k < Kdim;
-      Wa[r][i % kSimtK] = in ? load_w<FP8>(wa, sa, e, n, k, N, Kdim) : 0.f;
-      if (SWIGLU) Wb[r][i % kSimtK] = in ? load_w<FP8>(wb, sb, e, n, k, N, Kdim) : 0.f;
+      Wa[r][i % kSimtK] = in ? load_w<WQ>(wa, sa, e, n, k, N, Kdim) : 0.f;
+      if (SWIGLU) Wb[r][i % kSimtK] = in ? load_w<WQ>(wb, sb, e, n, k, N, Kdim) : 0.f;
     }
     __syncthreads();
 #pragma unroll 4
@@ -974,19 +1092,22 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [E][N][Kdim] weights, box 64 (K) x 128 (N) x 1: bf16 in the 128-byte swizzle
-// the MMA reads, or e4m3 bytes unswizzled (the converters re-lay them out)
-bool make_weight_map(CUtensorMap* m, const void* w, int E, int N, int Kdim, bool fp8 = false) {
+// [E][N][Kdim] weights, a box of 64 K elements x 128 rows (N) x 1: bf16 in the
+// 128-byte swizzle the MMA reads, or e4m3 bytes / e2m1 byte pairs (32 bytes a
+// row) unswizzled (the converters re-lay them out).  wq: a MOE_W_* code.
+bool make_weight_map(CUtensorMap* m, const void* w, int E, int N, int Kdim, int wq) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const int eb = fp8 ? 1 : 2;
-  cuuint64_t dims[3] = {(cuuint64_t)Kdim, (cuuint64_t)N, (cuuint64_t)E};
-  cuuint64_t strides[2] = {(cuuint64_t)Kdim * eb, (cuuint64_t)N * Kdim * eb};
-  cuuint32_t box[3] = {kBK, kBM, 1};
+  const bool bytes = wq != MOE_W_BF16;
+  const cuuint64_t row = wq == MOE_W_MXFP4 ? (cuuint64_t)Kdim / 2
+                       : (cuuint64_t)Kdim * (wq == MOE_W_BF16 ? 2 : 1);  // bytes per row
+  cuuint64_t dims[3] = {bytes ? row : (cuuint64_t)Kdim, (cuuint64_t)N, (cuuint64_t)E};
+  cuuint64_t strides[2] = {row, (cuuint64_t)N * row};
+  cuuint32_t box[3] = {wq == MOE_W_MXFP4 ? (cuuint32_t)kBK / 2 : (cuuint32_t)kBK, kBM, 1};
   cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+  return enc(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
              const_cast<void*>(w), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+             bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1019,7 +1140,7 @@ int num_sms() {
 // One launch of the tensor-core kernel over a list.  FUSED: the list's G1
 // and G2 units in one persistent launch (w2/h/s2/N2/K2/out2/done describe G2;
 // ksplit must be 1).
-template <int BN, bool SWIGLU, bool WFP8, bool FUSED = false>
+template <int BN, bool SWIGLU, int WQ, bool FUSED = false>
 cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorMap& act,
                    const float* sa, const float* sb, int32_t* counts, int list,
                    const int4* items, int cap, int N, int Kdim, void* out, int32_t* dev_status,
@@ -1029,17 +1150,17 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
                    int32_t* done = nullptr, const void* gx = nullptr,
                    const int32_t* grows = nullptr, int gk = 0, int ksplit2 = 1,
                    float* part2 = nullptr, int32_t* scnt1 = nullptr, int32_t* scnt2 = nullptr) {
-  using C = TcCfg<BN, SWIGLU, WFP8>;
+  using C = TcCfg<BN, SWIGLU, WQ>;
   static std::atomic<unsigned long long> smem_set{0};  // devices whose limit is raised
   {
-    cudaError_t e = moe_raise_smem(gemm_tc_kernel<BN, SWIGLU, WFP8, FUSED>, C::kSmemBytes, smem_set);
+    cudaError_t e = moe_raise_smem(gemm_tc_kernel<BN, SWIGLU, WQ, FUSED>, C::kSmemBytes, smem_set);
     if (e != cudaSuccess) return e;
   }
   const long long work =
       (long long)cap * (moe_cdiv(N, kBM) * ksplit + (FUSED ? moe_cdiv(N2, kBM) * ksplit2 : 0));
   const int grid = (int)(work < num_sms() ? work : num_sms());
   if (grid <= 0) return cudaSuccess;
-  cudaError_t e = moe_launch(gemm_tc_kernel<BN, SWIGLU, WFP8, FUSED>, dim3(grid),
+  cudaError_t e = moe_launch(gemm_tc_kernel<BN, SWIGLU, WQ, FUSED>, dim3(grid),
                              dim3(C::kThreads), C::kSmemBytes, stream, 1, wa, wb, act, sa, sb,
                              counts, list, items, N, Kdim, static_cast<__nv_bfloat16*>(out),
                              ksplit, R, part, dev_status, FUSED ? *w2 : wa, FUSED ? *h : act, s2,
@@ -1057,22 +1178,22 @@ cudaError_t run_tc(const CUtensorMap& wa, const CUtensorMap& wb, const CUtensorM
 
 // Both lists (skinny, tile) in one launch of two CTA groups.  FUSED: each
 // group runs its list's G1 and G2 units (act = xp maps, h = hact maps).
-template <bool SWIGLU, bool WFP8, bool FUSED>
+template <bool SWIGLU, int WQ, bool FUSED>
 cudaError_t run_tc_dual(const CUtensorMap& wa, const CUtensorMap& wb, const DualMaps& maps,
                         const float* sa, const float* sb, const PlanView& pv, int N, int Kdim,
                         void* out, int R, int32_t* dev_status, cudaStream_t stream,
                         const CUtensorMap& w2, const float* s2, int N2, int K2, void* out2,
                         const void* gx = nullptr, const int32_t* grows = nullptr, int gk = 0) {
-  using C0 = TcCfg<kBnSkinny, SWIGLU, WFP8>;
-  using C1 = TcCfg<kBnTile, SWIGLU, WFP8>;
+  using C0 = TcCfg<kBnSkinny, SWIGLU, WQ>;
+  using C1 = TcCfg<kBnTile, SWIGLU, WQ>;
   const size_t smem = C0::kSmemBytes > C1::kSmemBytes ? C0::kSmemBytes : C1::kSmemBytes;
   static std::atomic<unsigned long long> smem_set{0};  // devices whose limit is raised
   {
-    cudaError_t e = moe_raise_smem(gemm_tc_dual_kernel<SWIGLU, WFP8, FUSED>, smem, smem_set);
+    cudaError_t e = moe_raise_smem(gemm_tc_dual_kernel<SWIGLU, WQ, FUSED>, smem, smem_set);
     if (e != cudaSuccess) return e;
   }
   const int grid = num_sms();
-  return moe_launch(gemm_tc_dual_kernel<SWIGLU, WFP8, FUSED>, dim3(grid), dim3(C0::kThreads), smem,
+  return moe_launch(gemm_tc_dual_kernel<SWIGLU, WQ, FUSED>, dim3(grid), dim3(C0::kThreads), smem,
                     stream, 1, wa, wb, maps, sa, sb, pv.counts, (const int4*)pv.items[0],
                     (const int4*)pv.items[1], N, Kdim, static_cast<__nv_bfloat16*>(out), R,
                     dev_status, w2, s2, N2, K2, static_cast<__nv_bfloat16*>(out2), pv.done[0],
@@ -1100,7 +1221,7 @@ int pick_ksplit(long long units, int Kdim) {
   return best;
 }
 
-template <bool WFP8>
+template <int WQ>
 cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const void* w1,
                        const void* w3, const void* w2, const float* s1, const float* s3,
                        const float* s2, void* hact, void* y, const PlanView& pv,
@@ -1129,9 +1250,9 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
   const bool fuse = (long long)R <= 64LL * E_blocks && H <= 3 * I && !gx;
   CUtensorMap m_w1, m_w3, m_w2, m_x[kLists], m_h[kLists];
   memset(m_x, 0, sizeof(m_x));  // gather mode: G1 reads x rows itself, no activation map
-  if (!make_weight_map(&m_w1, w1, E_blocks, I, H, WFP8) ||
-      !make_weight_map(&m_w3, w3, E_blocks, I, H, WFP8) ||
-      !make_weight_map(&m_w2, w2, E_blocks, H, I, WFP8))
+  if (!make_weight_map(&m_w1, w1, E_blocks, I, H, WQ) ||
+      !make_weight_map(&m_w3, w3, E_blocks, I, H, WQ) ||
+      !make_weight_map(&m_w2, w2, E_blocks, H, I, WQ))
     return cudaErrorInvalidValue;
   for (int l = 0; l < kLists; ++l)
     if (any[l] && ((!gx && !make_act_map(&m_x[l], xp, R, H, list_bn(l))) ||
@@ -1146,12 +1267,12 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
     // G1 results, and in the shared layout a G2 stage occupies a G1-sized slot.)
     int32_t* c1 = split_cnt;
     int32_t* c2 = split_cnt + (size_t)pv.cap[0] * moe_cdiv(I, kBM);
-    err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x[0], s1, s3, pv.counts, 0, pv.items[0],
+    err = run_tc<kBnSkinny, true, WQ>(m_w1, m_w3, m_x[0], s1, s3, pv.counts, 0, pv.items[0],
                                         pv.cap[0], I, H, hact, dev_status, stream, ks1, R,
                                         splitk_buf, nullptr, nullptr, nullptr, 0, 0, nullptr,
                                         nullptr, gx, grows, gk, 1, nullptr, c1, nullptr);
     if (err != cudaSuccess) return err;
-    return run_tc<kBnSkinny, false, WFP8>(m_w2, m_w2, m_h[0], s2, s2, pv.counts, 0, pv.items[0],
+    return run_tc<kBnSkinny, false, WQ>(m_w2, m_w2, m_h[0], s2, s2, pv.counts, 0, pv.items[0],
                                           pv.cap[0], H, I, y, dev_status, stream, ks2, R,
                                           splitk_buf, nullptr, nullptr, nullptr, 0, 0, nullptr,
                                           nullptr, nullptr, nullptr, 0, 1, nullptr, c2, nullptr);
@@ -1167,52 +1288,52 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
       mh.h[l] = m_h[l];
     }
     if (fuse)
-      return run_tc_dual<true, WFP8, true>(m_w1, m_w3, mx, s1, s3, pv, I, H, hact, R, dev_status,
+      return run_tc_dual<true, WQ, true>(m_w1, m_w3, mx, s1, s3, pv, I, H, hact, R, dev_status,
                                            stream, m_w2, s2, H, I, y);
-    err = run_tc_dual<true, WFP8, false>(m_w1, m_w3, mx, s1, s3, pv, I, H, hact, R, dev_status,
+    err = run_tc_dual<true, WQ, false>(m_w1, m_w3, mx, s1, s3, pv, I, H, hact, R, dev_status,
                                          stream, m_w2, s2, 0, 0, nullptr, gx, grows, gk);
     if (err != cudaSuccess) return err;
-    return run_tc_dual<false, WFP8, false>(m_w2, m_w2, mh, s2, s2, pv, H, I, y, R, dev_status,
+    return run_tc_dual<false, WQ, false>(m_w2, m_w2, mh, s2, s2, pv, H, I, y, R, dev_status,
                                            stream, m_w2, s2, 0, 0, nullptr);
   }
   // G1 (SwiGLU, N = I, K = H) for every list, then G2 (N = H, K = I)
   if (any[0] && err == cudaSuccess)
-    err = run_tc<kBnSkinny, true, WFP8>(m_w1, m_w3, m_x[0], s1, s3, pv.counts, 0, pv.items[0],
+    err = run_tc<kBnSkinny, true, WQ>(m_w1, m_w3, m_x[0], s1, s3, pv.counts, 0, pv.items[0],
                                         pv.cap[0], I, H, hact, dev_status, stream, ks1, R,
                                         splitk_buf, nullptr, nullptr, nullptr, 0, 0, nullptr,
                                         nullptr, gx, grows, gk);
   if (fuse) {
     // tile and wide lists: G1 and G2 in one persistent launch each
     if (any[1] && err == cudaSuccess)
-      err = run_tc<kBnTile, true, WFP8, true>(m_w1, m_w3, m_x[1], s1, s3, pv.counts, 1,
+      err = run_tc<kBnTile, true, WQ, true>(m_w1, m_w3, m_x[1], s1, s3, pv.counts, 1,
                                               pv.items[1], pv.cap[1], I, H, hact, dev_status,
                                               stream, 1, R, nullptr, &m_w2, &m_h[1], s2, H, I, y,
                                               pv.done[1]);
     if (any[2] && err == cudaSuccess)
-      err = run_tc<kBnWide, true, WFP8, true>(m_w1, m_w3, m_x[2], s1, s3, pv.counts, 2,
+      err = run_tc<kBnWide, true, WQ, true>(m_w1, m_w3, m_x[2], s1, s3, pv.counts, 2,
                                               pv.items[2], pv.cap[2], I, H, hact, dev_status,
                                               stream, 1, R, nullptr, &m_w2, &m_h[2], s2, H, I, y,
                                               pv.done[2]);
   } else {
     if (any[1] && err == cudaSuccess)
-      err = run_tc<kBnTile, true, WFP8>(m_w1, m_w3, m_x[1], s1, s3, pv.counts, 1, pv.items[1],
+      err = run_tc<kBnTile, true, WQ>(m_w1, m_w3, m_x[1], s1, s3, pv.counts, 1, pv.items[1],
                                         pv.cap[1], I, H, hact, dev_status, stream, 1, R, nullptr,
                                         nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, gx,
                                         grows, gk);
     if (any[2] && err == cudaSuccess)
-      err = run_tc<kBnWide, true, WFP8>(m_w1, m_w3, m_x[2], s1, s3, pv.counts, 2, pv.items[2],
+      err = run_tc<kBnWide, true, WQ>(m_w1, m_w3, m_x[2], s1, s3, pv.counts, 2, pv.items[2],
                                         pv.cap[2], I, H, hact, dev_status, stream, 1, R, nullptr,
                                         nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, gx,
                                         grows, gk);
     if (any[1] && err == cudaSuccess)
-      err = run_tc<kBnTile, false, WFP8>(m_w2, m_w2, m_h[1], s2, s2, pv.counts, 1, pv.items[1],
+      err = run_tc<kBnTile, false, WQ>(m_w2, m_w2, m_h[1], s2, s2, pv.counts, 1, pv.items[1],
                                          pv.cap[1], H, I, y, dev_status, stream);
     if (any[2] && err == cudaSuccess)
-      err = run_tc<kBnWide, false, WFP8>(m_w2, m_w2, m_h[2], s2, s2, pv.counts, 2, pv.items[2],
+      err = run_tc<kBnWide, false, WQ>(m_w2, m_w2, m_h[2], s2, s2, pv.counts, 2, pv.items[2],
                                          pv.cap[2], H, I, y, dev_status, stream);
   }
   if (any[0] && err == cudaSuccess)
-    err = run_tc<kBnSkinny, false, WFP8>(m_w2, m_w2, m_h[0], s2, s2, pv.counts, 0, pv.items[0],
+    err = run_tc<kBnSkinny, false, WQ>(m_w2, m_w2, m_h[0], s2, s2, pv.counts, 0, pv.items[0],
                                          pv.cap[0], H, I, y, dev_status, stream, ks2, R,
                                          splitk_buf);
 
@@ -1220,18 +1341,21 @@ cudaError_t run_tc_all(const void* xp, int R, int E_blocks, int H, int I, const 
 }
 
 template <bool SWIGLU>
-cudaError_t run_simt(bool fp8, const void* act, const void* wa, const void* wb, const float* sa,
+cudaError_t run_simt(int wq, const void* act, const void* wa, const void* wb, const float* sa,
                      const float* sb, const int32_t* counts, const int4* items, int cap, int N,
                      int Kdim, void* out, cudaStream_t stream) {
   if (cap <= 0) return cudaSuccess;
   dim3 grid(moe_cdiv(N, kSimtN), cap < 32768 ? cap : 32768);
   const __nv_bfloat16* a = static_cast<const __nv_bfloat16*>(act);
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-  if (fp8)
-    return moe_launch(gemm_simt_kernel<SWIGLU, true>, grid, dim3(256), 0, stream, 1, a, wa, wb, sa,
-                      sb, counts, 0, items, N, Kdim, o);
-  return moe_launch(gemm_simt_kernel<SWIGLU, false>, grid, dim3(256), 0, stream, 1, a, wa, wb, sa,
-                    sb, counts, 0, items, N, Kdim, o);
+  if (wq == MOE_W_MXFP4)
+    return moe_launch(gemm_simt_kernel<SWIGLU, MOE_W_MXFP4>, grid, dim3(256), 0, stream, 1, a, wa,
+                      wb, sa, sb, counts, 0, items, N, Kdim, o);
+  if (wq == MOE_W_FP8E4M3_B128)
+    return moe_launch(gemm_simt_kernel<SWIGLU, MOE_W_FP8E4M3_B128>, grid, dim3(256), 0, stream, 1,
+                      a, wa, wb, sa, sb, counts, 0, items, N, Kdim, o);
+  return moe_launch(gemm_simt_kernel<SWIGLU, MOE_W_BF16>, grid, dim3(256), 0, stream, 1, a, wa, wb,
+                    sa, sb, counts, 0, items, N, Kdim, o);
 }
 
 }  // namespace
@@ -1257,7 +1381,10 @@ size_t grouped_gemm_splitk_bytes(int R, int H, int I) {
 
 int grouped_gemm_check(int H, int I, int wdtype) {
   if (H % 16 != 0 || I % 16 != 0) return MOE_ERR_INVALID_ARG;
-  if (wdtype != MOE_W_BF16 && wdtype != MOE_W_FP8E4M3_B128) return MOE_ERR_UNSUPPORTED;
+  if (wdtype != MOE_W_BF16 && wdtype != MOE_W_FP8E4M3_B128 && wdtype != MOE_W_MXFP4)
+    return MOE_ERR_UNSUPPORTED;
+  // MXFP4: whole 32-element scale blocks along every row
+  if (wdtype == MOE_W_MXFP4 && (H % 32 != 0 || I % 32 != 0)) return MOE_ERR_INVALID_ARG;
   // FP8: each work unit stages its row of 128-wide K-block scales (<= 64)
   if (wdtype == MOE_W_FP8E4M3_B128 && (H > 8192 || I > 8192)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -1273,7 +1400,7 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                                 const void* gather_x, const int32_t* gather_rows, int gather_k,
                                 int32_t* split_cnt) {
   if (m_skinny < 0) m_skinny = MOE_DEFAULT_M_SKINNY;
-  const bool fp8 = wdtype == MOE_W_FP8E4M3_B128;
+  const bool conv = wdtype != MOE_W_BF16;  // weights converted in the kernel (FP8, MXFP4)
   const bool simt = dispatch == MOE_DISPATCH_SIMT;
   PlanView pv = plan_view(scratch, R, E_blocks);
   PlanOut po = plan_out(pv);
@@ -1285,11 +1412,11 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
 
   if (simt && gather_x) return cudaErrorInvalidValue;  // the CUDA-core path reads xp only
   if (simt) {
-    err = run_simt<true>(fp8, xp, w1, w3, s1, s3, pv.counts, pv.items[0], pv.cap[0], I, H, hact,
-                         stream);
+    err = run_simt<true>(wdtype, xp, w1, w3, s1, s3, pv.counts, pv.items[0], pv.cap[0], I, H,
+                         hact, stream);
     if (err != cudaSuccess) return err;
-    return run_simt<false>(fp8, hact, w2, nullptr, s2, nullptr, pv.counts, pv.items[0], pv.cap[0],
-                           H, I, y, stream);
+    return run_simt<false>(wdtype, hact, w2, nullptr, s2, nullptr, pv.counts, pv.items[0],
+                           pv.cap[0], H, I, y, stream);
   }
   // Which lists can be non-empty, from what the host knows without reading
   // the offsets: no block holds more than max_rows rows (moe_layer passes T:
@@ -1305,13 +1432,17 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
   } else {
     any[0] = true;
     any[1] = max_rows > m_skinny;
-    any[2] = fp8 && max_rows > m_skinny && max_rows >= MOE_WIDE_MIN_ROWS;
+    any[2] = conv && max_rows > m_skinny && max_rows >= MOE_WIDE_MIN_ROWS;
   }
-  if (fp8)
-    return run_tc_all<true>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                            stream, any, splitk_buf, splitk_bytes, gather_x, gather_rows,
-                            gather_k, split_cnt);
-  return run_tc_all<false>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv, dev_status,
-                           stream, any, splitk_buf, splitk_bytes, gather_x, gather_rows, gather_k,
-                           split_cnt);
+  if (wdtype == MOE_W_MXFP4)
+    return run_tc_all<MOE_W_MXFP4>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv,
+                                   dev_status, stream, any, splitk_buf, splitk_bytes, gather_x,
+                                   gather_rows, gather_k, split_cnt);
+  if (wdtype == MOE_W_FP8E4M3_B128)
+    return run_tc_all<MOE_W_FP8E4M3_B128>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y,
+                                          pv, dev_status, stream, any, splitk_buf, splitk_bytes,
+                                          gather_x, gather_rows, gather_k, split_cnt);
+  return run_tc_all<MOE_W_BF16>(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv,
+                                dev_status, stream, any, splitk_buf, splitk_bytes, gather_x,
+                                gather_rows, gather_k, split_cnt);
 }

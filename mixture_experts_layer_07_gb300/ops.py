@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 
 MODE_SOFTMAX, MODE_SIGMOID_BIAS = 0, 1
-W_BF16, W_FP8 = 0, 1
+W_BF16, W_FP8, W_MXFP4 = 0, 1, 2
 DISPATCH_PER_BLOCK, DISPATCH_GLOBAL_AVG, DISPATCH_SIMT, DISPATCH_ONE_LAUNCH = 0, 1, 2, 3
 VARIANT_SKIP, VARIANT_SKINNY, VARIANT_TILE, VARIANT_SIMT, VARIANT_WIDE = 0, 1, 2, 3, 4
 WIDE_MIN_ROWS = 129

@@ -9,7 +9,8 @@ oracle):
 * routing weights and the shared gate: 1e-5 relative + 1e-7 absolute;
 * bf16 outputs (expert activations, expert outputs, the layer output):
   |gpu - oracle| <= 2e-2 * |oracle| + 2e-2 * rms(oracle) per tensor (5e-2 when
-  the expert weights are FP8).  Each bf16 rounding is 2^-9 relative; the GPU
+  the expert weights are FP8).  With MXFP4 weights the oracle dequantises the
+  same codes exactly, so the bf16 bound of unquantised weights applies.  Each bf16 rounding is 2^-9 relative; the GPU
   path rounds h, y and out once each and accumulates in fp32.
 Integer outputs (ids, offsets, permutations) are compared bit for bit.
 """
@@ -60,9 +61,10 @@ def layer_tensors(inp: dict, experts=None) -> dict:
     if "w1_bits" in inp:
         for k in ("w1", "w3", "w2"):
             d[k] = _bf16_experts_dev(inp[k + "_bits"], experts)
-    elif "w1_q" in inp:
+    elif "w1_q" in inp or "w1_q4" in inp:
+        sfx = "_q" if "w1_q" in inp else "_q4"
         for k, s in (("w1", "s1"), ("w3", "s3"), ("w2", "s2")):
-            d[k] = _experts_dev(inp[k + "_q"], experts)
+            d[k] = _experts_dev(inp[k + sfx], experts)
             d[s] = dev(inp[s])
     if "sw1_bits" in inp:
         for k in ("sw1", "sw3", "sw2"):
@@ -73,7 +75,11 @@ def layer_tensors(inp: dict, experts=None) -> dict:
 def config_for(ops, spec, T_max, **kw):
     return ops.make_config(T_max, spec.H, spec.E, spec.K, spec.I, has_shared=spec.has_shared,
                            I_shared=spec.I_shared, mode=spec.mode, routed_scale=spec.routed_scale,
-                           wdtype=ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16, **kw)
+                           wdtype=wdtype_of(ops, spec), **kw)
+
+
+def wdtype_of(ops, spec):
+    return {"bf16": ops.W_BF16, "fp8": ops.W_FP8, "mxfp4": ops.W_MXFP4}[spec.wdtype]
 
 
 def assert_router_close(gpu, x, wg, bias=None):

@@ -175,6 +175,9 @@ def test_grouped_gemm_rejects_bad_arguments(ops):
     assert g(I=72) == 1
     assert g(wdtype=4) == 2
     assert g(wdtype=1) == 1          # FP8 without scales
+    assert g(wdtype=2) == 1          # MXFP4 without scales
+    assert g(wdtype=2, H=240, s=0x1000) == 1  # MXFP4 rows hold whole 32-element blocks
+    assert g(wdtype=2, I=144, s=0x1000) == 1
     assert g(nbytes=need - 16) == 3
     assert g(scratch=0x10040) == 4
     assert g(w=0x1002) == 4
@@ -203,6 +206,9 @@ def test_layer_rejects_bad_arguments(ops):
     fp8 = _cfg(ops, wdtype=1)
     assert lib.moe_layer(by(fp8), 8, 0x1000, by(w), 0x1000, 0x10000,
                          ops.workspace_bytes(fp8), None, None) == 1
+    mx = _cfg(ops, wdtype=2)
+    assert lib.moe_layer(by(mx), 8, 0x1000, by(w), 0x1000, 0x10000,
+                         ops.workspace_bytes(mx), None, None) == 1
     sh = _cfg(ops, has_shared=True, I_shared=64)
     assert lib.moe_layer(by(sh), 8, 0x1000, by(w), 0x1000, 0x10000,
                          ops.workspace_bytes(sh), None, None) == 1

@@ -39,15 +39,18 @@ def ops():
 
 class DeviceBank:
     """[E, rows, cols] expert weights on the device, fetched per expert and
-    widened to float64 exactly (bf16 on the device; e4m3 codes dequantised
-    by the oracle on the host)."""
+    widened to float64 exactly (bf16 on the device; e4m3 and e2m1 codes
+    dequantised by the oracle on the host)."""
 
-    def __init__(self, t, s=None):
-        self.t, self.s, self.shape = t, s, tuple(t.shape)
+    def __init__(self, t, s=None, fmt="bf16"):
+        self.t, self.s, self.fmt = t, s, fmt
+        self.shape = tuple(t.shape[:2]) + (t.shape[2] * (2 if fmt == "mxfp4" else 1),)
 
     def __getitem__(self, e):
         if self.s is None:
             return self.t[e].double().cpu().numpy()
+        if self.fmt == "mxfp4":
+            return oracle.dequant_mxfp4(self.t[e].cpu().numpy(), self.s[e].cpu().numpy())
         return oracle.dequant_fp8_block(self.t[e].cpu().numpy(), self.s[e].cpu().numpy())
 
     def __len__(self):
@@ -58,6 +61,7 @@ class DeviceBank:
 FULL = [("qwen3_30b_a3b", {}, 2048, 64), ("qwen3_30b_a3b", {}, 1, 1),
         ("qwen3_30b_a3b", {}, 8, 8),
         ("gpt_oss_20b", {}, 4096, 64), ("gpt_oss_20b", {}, 512, 64), ("gpt_oss_20b", {}, 32, 32),
+        ("gpt_oss_20b", {"wdtype": "mxfp4"}, 4096, 64), ("gpt_oss_20b", {"wdtype": "mxfp4"}, 1, 1),
         ("shared_gate", {}, 1024, 64), ("shared_gate", {}, 1, 1),
         ("high_expert", {}, 512, 16), ("high_expert", {"E": 512, "K": 16}, 512, 16),
         ("high_expert", {"E": 1024, "K": 9}, 512, 16)]
@@ -70,15 +74,19 @@ def sample_tokens(T, n, seed):
     return sorted(set([0, T - 1] + rng.choice(T, size=n - 2, replace=False).tolist()))
 
 
-@pytest.mark.parametrize("name,over,T,n_out", FULL)
+@pytest.mark.parametrize("name,over,T,n_out", FULL,
+                         ids=lambda v: ",".join(f"{k}={x}" for k, x in v.items()) or "base"
+                         if isinstance(v, dict) else None)
 def test_layer_full_size(ops, name, over, T, n_out):
     torch.cuda.empty_cache()
     spec = synth.SPECS[name].with_(**over)
     d = synth.device_inputs(spec, T, seed=5)
     t = {"x": d["x"], "wg": d["wg"], "gate_bias": d["gate_bias"], "sel_bias": d["sel_bias"]}
     fp8 = spec.wdtype == "fp8"
-    if fp8:
-        t.update(w1=d["w1_q"], w3=d["w3_q"], w2=d["w2_q"], s1=d["s1"], s3=d["s3"], s2=d["s2"])
+    sfx = {"fp8": "_q", "mxfp4": "_q4"}.get(spec.wdtype)
+    if sfx:
+        t.update(w1=d["w1" + sfx], w3=d["w3" + sfx], w2=d["w2" + sfx], s1=d["s1"], s3=d["s3"],
+                 s2=d["s2"])
     else:
         t.update(w1=d["w1"], w3=d["w3"], w2=d["w2"])
     if spec.has_shared:
@@ -115,7 +123,7 @@ def test_layer_full_size(ops, name, over, T, n_out):
     o_off, o_r2f, o_f2r = oracle.permute(ids, E)
     assert np.array_equal(off, o_off)
     assert np.array_equal(r2f, o_r2f) and np.array_equal(f2r, o_f2r)
-    wd = ops.W_FP8 if fp8 else ops.W_BF16
+    wd = U.wdtype_of(ops, spec)
     want = [ops.block_variant(int(m), R, E, -1, 0, wd) for m in np.diff(off)]
     assert layer.view("block_variant", torch.int32, (E,)).cpu().numpy().tolist() == want
 
@@ -123,9 +131,9 @@ def test_layer_full_size(ops, name, over, T, n_out):
     rs = sample_tokens(T, 64, T + 1)
     U.assert_router_close(lg[rs].astype(np.float64), x64[rs], wg, gb)
 
-    if fp8:
-        banks = (DeviceBank(d["w1_q"], d["s1"]), DeviceBank(d["w3_q"], d["s3"]),
-                 DeviceBank(d["w2_q"], d["s2"]))
+    if sfx:
+        banks = tuple(DeviceBank(d[k + sfx], d[s], spec.wdtype)
+                      for k, s in (("w1", "s1"), ("w3", "s3"), ("w2", "s2")))
     else:
         banks = (DeviceBank(d["w1"]), DeviceBank(d["w3"]), DeviceBank(d["w2"]))
     rel = 5e-2 if fp8 else 2e-2

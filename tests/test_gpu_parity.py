@@ -297,6 +297,13 @@ def test_permute_then_unpermute_is_identity(ops):
 
 
 # ---------------------------------------------------------------- G
+def case_id(v):
+    """Readable test ids: a spec's overrides as k=v pairs."""
+    if isinstance(v, dict):
+        return ",".join(f"{k}={x}" for k, x in v.items()) or "base"
+    return None
+
+
 def concentrated_ids(T, K, E, seed):
     """Most tokens pick from a few hot experts (big blocks); the rest spread
     over all experts (small blocks); unpicked experts stay empty."""
@@ -328,7 +335,7 @@ def run_gemm(ops, spec, inp, off, r2f, K, dispatch=0, m_skinny=-1):
     bv = i32(E)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ops.grouped_gemm(U.bf16_dev(xp_bits), torch.from_numpy(off).cuda(), E, H, I, t["w1"], t["w3"],
-                     t["w2"], hact, y, scratch, wdtype=ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16,
+                     t["w2"], hact, y, scratch, wdtype=U.wdtype_of(ops, spec),
                      s1=t.get("s1"), s3=t.get("s3"), s2=t.get("s2"), m_skinny=m_skinny,
                      dispatch=dispatch, block_variant=bv, dev_status=st)
     sync()
@@ -349,6 +356,13 @@ GEMM_CASES = [  # spec name, overrides, T, concentrated, dispatch, m_skinny, bot
     ("tiny", {"H": 320, "I": 192, "E": 6}, 200, True, 0, -1, False),
     ("tiny", {"H": 160, "I": 144, "E": 5, "wdtype": "fp8"}, 50, True, 0, -1, False),
     ("tiny", {"H": 160, "I": 144, "E": 5, "wdtype": "fp8"}, 50, True, 2, -1, False),
+    # MXFP4 weights (e2m1 pairs + a UE8M0 scale per 32 along each row)
+    ("tiny", {"H": 160, "I": 96, "E": 5, "wdtype": "mxfp4"}, 50, True, 0, -1, False),
+    ("tiny", {"H": 160, "I": 96, "E": 5, "wdtype": "mxfp4"}, 50, True, 2, -1, False),
+    ("gpt_oss_20b", {"wdtype": "mxfp4"}, 40, True, 0, -1, True),
+    ("gpt_oss_20b", {"E": 4, "wdtype": "mxfp4"}, 300, True, 0, -1, False),
+    ("gpt_oss_20b", {"E": 6, "wdtype": "mxfp4"}, 700, True, 0, -1, False),
+    ("tiny", {"H": 2880, "I": 2880, "E": 4, "wdtype": "mxfp4"}, 40, False, 0, 8, False),
     ("gpt_oss_20b", {}, 40, True, 0, -1, True),
     ("gpt_oss_20b", {"E": 6}, 40, True, 2, -1, False),
     ("gpt_oss_20b", {"E": 4}, 300, True, 0, -1, False),
@@ -359,7 +373,7 @@ GEMM_CASES = [  # spec name, overrides, T, concentrated, dispatch, m_skinny, bot
 ]
 
 
-@pytest.mark.parametrize("name,over,T,conc,dispatch,m_skinny,both", GEMM_CASES)
+@pytest.mark.parametrize("name,over,T,conc,dispatch,m_skinny,both", GEMM_CASES, ids=case_id)
 def test_grouped_gemm(ops, name, over, T, conc, dispatch, m_skinny, both):
     spec = SPECS[name].with_(**over)
     inp, ids, off, r2f, f2r = gemm_case(spec, T, seed=T + spec.E, concentrated=conc)
@@ -372,14 +386,90 @@ def test_grouped_gemm(ops, name, over, T, conc, dispatch, m_skinny, both):
     U.assert_bf16_close(U.f64(y), ry, rel, "y")
     R = T * spec.K
     m = np.diff(off)
-    wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
+    wd = U.wdtype_of(ops, spec)
     want_bv = [ops.block_variant(int(mm), R, spec.E, m_skinny, dispatch, wd) for mm in m]
     assert bv.tolist() == want_bv
     if both:  # small and large blocks in the same call
         assert ops.VARIANT_SKINNY in bv.tolist()
         assert {ops.VARIANT_TILE, ops.VARIANT_WIDE} & set(bv.tolist())
-    if dispatch == 0 and spec.wdtype == "fp8" and (m >= ops.WIDE_MIN_ROWS).any():
+    if dispatch == 0 and spec.wdtype != "bf16" and (m >= ops.WIDE_MIN_ROWS).any():
         assert ops.VARIANT_WIDE in bv.tolist()
+
+
+def _mx_pack(codes):
+    """[rows, cols] e2m1 codes -> [rows, cols / 2] bytes, element 2i low nibble."""
+    c = np.asarray(codes, np.uint8)
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+
+
+def _mx_test_matrix(rows, cols, s_max, seed):
+    """Every e2m1 code in every scale block; scale bytes 0..s_max with the
+    corners (0, 1, 126..130, s_max) present."""
+    r = np.random.default_rng(seed)
+    codes = r.integers(0, 16, size=(rows, cols)).astype(np.uint8)
+    codes[:, :16] = np.arange(16, dtype=np.uint8)  # each row: all 16 codes
+    sc = r.integers(0, s_max + 1, size=(rows, cols // 32)).astype(np.uint8)
+    corners = np.array([0, 1, 126, 127, 128, 129, 130, s_max], np.uint8)
+    sc.flat[:len(corners)] = corners
+    return _mx_pack(codes), sc
+
+
+def _mx_const(rows, cols, code, s):
+    return (_mx_pack(np.full((rows, cols), code, np.uint8)),
+            np.full((rows, cols // 32), s, np.uint8))
+
+
+@pytest.mark.parametrize("T,m_skinny,dispatch", [(256, -1, 0), (128, -1, 0), (256, 1024, 0),
+                                                 (256, -1, 2)])
+def test_grouped_gemm_mxfp4_reads_every_code_exactly(ops, T, m_skinny, dispatch):
+    # one expert, token t = the one-hot row e_t, so G1 reads single weights:
+    # hact[t, i] = silu(w1[i, t]) * w3[i, t] and y[t, h] = sum_i hact[t, i] w2[h, i].
+    # (a) w1 = 24 (code 6.0 at scale byte 129: the two-step multiply) and w3 the
+    #     codes under test: hact = 24 * w3 exactly (silu(24) is 24 in fp32)
+    # (b) w3 = identity: hact = 24 * one-hot, so y = 24 * w2 exactly
+    # (c) w3 = 1: hact = bf16(silu(w1)) for the codes under test in w1
+    H = I = 256
+    x = np.zeros((T, H), np.float32)
+    x[np.arange(T), np.arange(T)] = 1.0
+    xp = U.bf16_dev(synth.f32_to_bf16_bits(x))
+    off = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    scratch = torch.empty(ops.grouped_gemm_scratch_bytes(T, 1), dtype=torch.uint8, device="cuda")
+
+    def run(w1, w3, w2):
+        t = {}
+        for k, (q, sc) in (("1", w1), ("3", w3), ("2", w2)):
+            t["w" + k] = U.dev(q[None])
+            t["s" + k] = U.dev(sc[None])
+        hact = torch.full((T, I), float("nan"), device="cuda").to(torch.bfloat16)
+        y = torch.full((T, H), float("nan"), device="cuda").to(torch.bfloat16)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ops.grouped_gemm(xp, off, 1, H, I, t["w1"], t["w3"], t["w2"], hact, y, scratch,
+                         wdtype=ops.W_MXFP4, s1=t["s1"], s3=t["s3"], s2=t["s2"],
+                         m_skinny=m_skinny, dispatch=dispatch, dev_status=st)
+        sync()
+        assert int(st.item()) == 0
+        return U.f64(hact), U.f64(y)
+
+    w24 = _mx_const(I, H, 7, 129)
+    assert oracle.dequant_mxfp4(*w24)[0, 0] == 24.0
+    # (a)
+    q3, s3 = _mx_test_matrix(I, H, 240, seed=T + 1)
+    w3 = oracle.dequant_mxfp4(q3, s3)
+    hact, _ = run(w24, (q3, s3), _mx_const(H, I, 2, 127))
+    assert np.array_equal(hact, 24.0 * w3[:, :T].T)
+    # (b)
+    eye = np.where(np.eye(I, H, dtype=bool), 2, 0).astype(np.uint8)
+    q2, s2 = _mx_test_matrix(H, I, 240, seed=T + 2)
+    w2 = oracle.dequant_mxfp4(q2, s2)
+    hact, y = run(w24, (_mx_pack(eye), np.full((I, H // 32), 127, np.uint8)), (q2, s2))
+    assert np.array_equal(hact, 24.0 * np.eye(T, I))
+    assert np.array_equal(y, 24.0 * w2[:, :T].T)
+    # (c)
+    q1, s1 = _mx_test_matrix(I, H, 130, seed=T + 3)
+    w1 = oracle.dequant_mxfp4(q1, s1)[:, :T].T
+    hact, _ = run((q1, s1), _mx_const(I, H, 2, 127), _mx_const(H, I, 2, 127))
+    ref = w1 / (1.0 + np.exp(-w1))
+    assert (np.abs(hact - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-37).all()
 
 
 def test_grouped_gemm_single_block_without_offsets(ops):
@@ -432,7 +522,10 @@ LAYER_CASES = [("tiny", {}, 16), ("tiny", {}, 1), ("qwen3_30b_a3b", {}, 1),
                # few experts active: the skinny GEMM splits K (fp32 slices + finalize)
                ("tiny", {"H": 1024, "I": 512, "E": 8, "wdtype": "fp8"}, 1),
                ("tiny", {"H": 1024, "I": 512, "E": 8, "wdtype": "fp8"}, 3),
-               ("tiny", {"H": 2880, "I": 1440, "E": 4}, 1)]
+               ("tiny", {"H": 2880, "I": 1440, "E": 4}, 1),
+               ("tiny", {"H": 1024, "I": 512, "E": 8, "wdtype": "mxfp4"}, 1),
+               ("gpt_oss_20b", {"wdtype": "mxfp4"}, 1), ("gpt_oss_20b", {"wdtype": "mxfp4"}, 8),
+               ("gpt_oss_20b", {"wdtype": "mxfp4"}, 64)]
 
 
 def oracle_routing(spec, inp):
@@ -451,7 +544,7 @@ def oracle_routing(spec, inp):
     return logits, ids, margin
 
 
-@pytest.mark.parametrize("name,over,T", LAYER_CASES)
+@pytest.mark.parametrize("name,over,T", LAYER_CASES, ids=case_id)
 def test_layer(ops, name, over, T):
     spec = SPECS[name].with_(**over)
     base = synth.host_inputs(spec, T, seed=11, weights=False)
@@ -490,7 +583,7 @@ PREFILL_CASES = [("tiny", {"E": 16, "K": 4}, (33, 129, 1000, 40000)),
                  ("shared_gate", {"H": 256, "I": 128, "I_shared": 128}, (300,))]
 
 
-@pytest.mark.parametrize("name,over,Ts", PREFILL_CASES)
+@pytest.mark.parametrize("name,over,Ts", PREFILL_CASES, ids=case_id)
 def test_layer_prefill_routing_is_exact_and_repeats(ops, name, over, Ts):
     spec = SPECS[name].with_(**over)
     inp = synth.host_inputs(spec, max(Ts), seed=41)
@@ -515,7 +608,7 @@ def test_layer_prefill_routing_is_exact_and_repeats(ops, name, over, Ts):
         assert np.array_equal(layer.view("offsets", torch.int32, (E + 1,)).cpu().numpy(), off)
         assert np.array_equal(layer.view("row_to_flat", torch.int32, (R,)).cpu().numpy(), r2f)
         assert np.array_equal(layer.view("flat_to_row", torch.int32, (R,)).cpu().numpy(), f2r)
-        wd = ops.W_FP8 if spec.wdtype == "fp8" else ops.W_BF16
+        wd = U.wdtype_of(ops, spec)
         want = [ops.block_variant(int(m), R, E, -1, 0, wd) for m in np.diff(off)]
         assert layer.view("block_variant", torch.int32, (E,)).cpu().numpy().tolist() == want
         sw = layer.workspace[layer.layout.sync:layer.layout.logits].view(torch.int32)
@@ -626,7 +719,7 @@ ONE_LAUNCH_CASES = [("qwen3_30b_a3b", {}, 1), ("qwen3_30b_a3b", {}, 2), ("qwen3_
                               "sel_bias_var": 0.1}, 7)]
 
 
-@pytest.mark.parametrize("name,over,T", ONE_LAUNCH_CASES)
+@pytest.mark.parametrize("name,over,T", ONE_LAUNCH_CASES, ids=case_id)
 def test_one_launch_layer(ops, name, over, T):
     spec = SPECS[name].with_(**over)
     base = synth.host_inputs(spec, T, seed=17, weights=False)
