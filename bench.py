@@ -772,6 +772,24 @@ def probe_stages(spec, T, reps, dev):
     return {"probe": "stages", "workload": spec.name, "T": T, "reps": reps}
 
 
+def probe_topk(spec, T, reps, dev):
+    """moe_topk_route alone at T on seeded random logits of the workload's
+    E, K and score mode, `reps` calls, no timing (for ncu captures)."""
+    from mixture_experts_layer_07_gb300 import ops
+
+    E, K = spec.E, spec.K
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2)
+    logits = torch.randn(T, E, device=dev, generator=gen)
+    ids = torch.empty(T, K, dtype=torch.int32, device=dev)
+    w = torch.empty(T, K, device=dev)
+    sel_bias = (torch.randn(E, device=dev, generator=gen) * 0.3) if spec.mode == 1 else None
+    for _ in range(reps):
+        ops.topk_route(logits, E, K, spec.mode, spec.routed_scale, ids, w, sel_bias)
+    torch.cuda.synchronize()
+    return {"probe": "topk", "workload": spec.name, "T": T, "reps": reps}
+
+
 def probe_layer(spec, T, reps, dev):
     """The whole layer (``moe_layer``) at T, `reps` calls, no timing: the
     command the per-kernel ncu captures of the layer profile."""
@@ -1039,6 +1057,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--probe-stages", type=int, default=0, metavar="T",
                     help="only run R/K/P/U at this T a few times (for ncu captures)")
+    ap.add_argument("--probe-topk", type=int, default=0, metavar="T",
+                    help="only run moe_topk_route at this T a few times (for ncu captures)")
     ap.add_argument("--probe-layer", type=int, default=0, metavar="T",
                     help="only run moe_layer at this T a few times (for ncu captures)")
     args = ap.parse_args()
@@ -1068,6 +1088,12 @@ def main():
         print(json.dumps(run_reference(args)), flush=True)
         return
 
+    if args.probe_topk:
+        from mixture_experts_layer_07_gb300 import synth
+        torch.cuda.set_device(local_rank)
+        print(json.dumps(probe_topk(synth.SPECS[args.workload], args.probe_topk, 3,
+                                    f"cuda:{local_rank}")), flush=True)
+        return
     if args.probe_stages:
         from mixture_experts_layer_07_gb300 import synth
         torch.cuda.set_device(local_rank)

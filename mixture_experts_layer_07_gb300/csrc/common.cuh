@@ -38,6 +38,20 @@ __host__ __device__ __forceinline__ int moe_variant_of(int64_t m_size, int64_t R
   return (wdtype != MOE_W_BF16 && m >= MOE_WIDE_MIN_ROWS) ? MOE_VARIANT_WIDE : MOE_VARIANT_TILE;
 }
 
+// SM count of the current device, cached per device (148 if the query fails)
+inline int moe_num_sms() {
+  static std::atomic<int> n[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  int v = n[dev].load(std::memory_order_relaxed);
+  if (!v) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 148;
+    n[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 // First error wins.
 MOE_DEVICE void moe_set_status(int32_t* dev_status, int32_t code) {
   if (dev_status) atomicCAS(dev_status, 0, code);

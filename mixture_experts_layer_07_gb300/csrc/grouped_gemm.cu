@@ -129,17 +129,6 @@ struct TcCfg {
 
 MOE_DEVICE float silu_f(float g) { return g / (1.f + __expf(-g)); }
 
-// 16-byte cp.async (L2 only); src_bytes = 0 writes zeros and reads nothing
-MOE_DEVICE void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-MOE_DEVICE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-MOE_DEVICE void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // generic-proxy global writes (made visible to this thread) -> later TMA reads
 MOE_DEVICE void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
@@ -1124,18 +1113,7 @@ bool make_act_map(CUtensorMap* m, const void* a, int R, int Kdim, int bn) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int num_sms() {
-  static std::atomic<int> n[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  int v = n[dev].load(std::memory_order_relaxed);
-  if (!v) {
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    v = v > 0 ? v : 148;
-    n[dev].store(v, std::memory_order_relaxed);
-  }
-  return v;
-}
+int num_sms() { return moe_num_sms(); }
 
 // One launch of the tensor-core kernel over a list.  FUSED: the list's G1
 // and G2 units in one persistent launch (w2/h/s2/N2/K2/out2/done describe G2;

@@ -207,16 +207,7 @@ router_cluster_kernel(const __nv_bfloat16* __restrict__ x, const float* __restri
   cluster.sync();  // keep this CTA's partial tile alive until every rank has read it
 }
 
-int num_sms_router() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0, v = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    n = v > 0 ? v : 148;
-  }
-  return n;
-}
+int num_sms_router() { return moe_num_sms(); }
 
 }  // namespace
 

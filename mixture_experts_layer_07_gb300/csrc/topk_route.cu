@@ -31,16 +31,7 @@ using namespace moe_route;
 
 constexpr int kThreads = 256;
 
-int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0, v = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    n = v > 0 ? v : 148;
-  }
-  return n;
-}
+int sm_count() { return moe_num_sms(); }
 
 // GS lanes per token, 32/GS tokens per warp (group_load + group_route in
 // topk_group.cuh)

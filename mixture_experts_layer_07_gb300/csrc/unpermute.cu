@@ -76,13 +76,7 @@ unpermute_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ flat_t
 cudaError_t launch_unpermute(const void* y, const int32_t* flat_to_row, const float* weights,
                              int T, int K, int H, const void* shared_y, const float* shared_gate,
                              void* out, cudaStream_t stream) {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
+  const int sms = moe_num_sms();
   const int H8 = H / 8;
   const long long n = (long long)T * H8;
   const long long need = (n + kThreads - 1) / kThreads;
