@@ -64,6 +64,8 @@ class LayerSpec:
     routed_scale: float = 1.0
     wdtype: str = "bf16"          # "bf16", "fp8" (e4m3, 128x128 block scales) or
                                   # "mxfp4" (e2m1, a power-of-two scale per 32)
+    act: str = "bf16"             # expert-GEMM activations: "bf16", or "fp8" with
+                                  # fp8 weights (W8A8: e4m3 per row and 128 columns)
     has_shared: bool = False
     I_shared: int = 0
     hot_experts: tuple = ()       # experts whose gate logit gets ``hot_bias``

@@ -111,6 +111,67 @@ def dequant_mxfp4(packed, scales, block: int = 32) -> np.ndarray:
     return q * s
 
 
+# W8A8: activations quantised to e4m3, one fp32 scale per (row, 128 columns).
+# The pages name FP8 expert weights ([dispatch] introduction) but fix no
+# activation format; the W8A8 option's definition is this one (the scale and
+# the scaled value are float32 operations, as the kernels compute them, so the
+# codes are a function of the inputs that both sides evaluate identically).
+_E4M3_POS = np.array([_e4m3_value(c) for c in range(0x7F)], dtype=np.float64)  # 0 .. 448
+
+
+def e4m3_round(v) -> np.ndarray:
+    """e4m3 code of the value nearest v, ties to the even code (round to
+    nearest even), magnitudes above 448 (the largest finite e4m3) saturating
+    to 448; the sign bit is kept (so -0 and negatives that round to zero give
+    0x80)."""
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 1, 0x7E)  # POS[hi] >= a
+    lo = hi - 1
+    d_lo = a - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - a
+    code = np.where((d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0)), hi, lo)
+    return (code.astype(np.uint8) | (np.signbit(v).astype(np.uint8) << 7)).astype(np.uint8)
+
+
+def quantize_act_fp8(a, block: int = 128):
+    """Quantise activations [R, C] per row and per `block` consecutive columns
+    (the last block may be narrower): s = float32(amax) / 448 in float32 (0
+    for an all-zero block), code = e4m3_round(float32(a) / s) in float32 (0
+    where s = 0).  Returns (codes uint8 [R, C], s float32 [R, ceil(C/block)])."""
+    a32 = np.asarray(a, np.float32)
+    R, C = a32.shape
+    nb = -(-C // block)
+    codes = np.zeros((R, C), np.uint8)
+    sc = np.zeros((R, nb), np.float32)
+    for b in range(nb):
+        blk = a32[:, b * block:(b + 1) * block]
+        amax = np.abs(blk).max(axis=1)
+        sb = (amax / np.float32(448.0)).astype(np.float32)
+        safe = np.where(sb > 0, sb, np.float32(1.0)).astype(np.float32)
+        scaled = (blk / safe[:, None]).astype(np.float32)
+        c = e4m3_round(scaled)
+        c[sb == 0] = 0
+        codes[:, b * block:(b + 1) * block] = c
+        sc[:, b] = sb
+    return codes, sc
+
+
+def dequant_act_fp8(codes, scales, block: int = 128) -> np.ndarray:
+    """w[r, c] = e4m3(codes[r, c]) * scales[r, c // block] (float64, exact)."""
+    q = e4m3_to_f64(codes)
+    s = np.repeat(np.asarray(scales, np.float64), block, axis=1)[:, :q.shape[1]]
+    return q * s
+
+
+def round_bf16(v) -> np.ndarray:
+    """float64 -> float32 (nearest) -> bf16 (nearest even), back as float64:
+    the rounding of a float32 result stored as bf16."""
+    b = np.asarray(v, np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 # ----------------------------------------------------------------------------
 # R: router (gate) GEMM
 # ----------------------------------------------------------------------------
@@ -308,6 +369,33 @@ def grouped_gemm(xp, offsets, w1, w3, w2):
     return hact, y
 
 
+def grouped_gemm_w8a8(xp, offsets, w1, w3, w2):
+    """``grouped_gemm`` with both GEMMs' activations quantised (W8A8): the
+    expert input xp -> quantize_act_fp8 -> dequantised x~; h = silu(x~ W1^T) *
+    (x~ W3^T); hact = h stored as bf16 (round_bf16); hact -> quantize_act_fp8
+    -> h~; y = h~ W2^T.  Weights as given (the dequantised FP8 experts).
+    Returns hact (the bf16 values, float64) and y float64."""
+    xp = np.asarray(xp, np.float64)
+    R = xp.shape[0]
+    E = len(offsets) - 1
+    I, H = w1.shape[1], w1.shape[2]
+    xd = dequant_act_fp8(*quantize_act_fp8(xp)) if R else xp
+    hact = np.zeros((R, I))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            a = xd[lo:hi]
+            hact[lo:hi] = round_bf16(silu(a @ np.asarray(w1[e], np.float64).T) *
+                                     (a @ np.asarray(w3[e], np.float64).T))
+    hd = dequant_act_fp8(*quantize_act_fp8(hact)) if R else hact
+    y = np.zeros((R, H))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            y[lo:hi] = hd[lo:hi] @ np.asarray(w2[e], np.float64).T
+    return hact, y
+
+
 # ----------------------------------------------------------------------------
 # U: weighted unpermute / combine
 # ----------------------------------------------------------------------------
@@ -373,12 +461,14 @@ def layer_weights_f64(inp: dict):
 
 
 def moe_layer(x, wg, gate_bias, sel_bias, w1, w3, w2, *, E: int, K: int, mode: int,
-              routed_scale: float = 1.0, shared=None, logits_override=None):
+              routed_scale: float = 1.0, shared=None, logits_override=None, w8a8=False):
     """The whole hot path: R -> K -> P -> G1/G2 -> U, float64.
 
     ``shared`` = (sw1, sw3, sw2) adds g_sh[t] * SwiGLU_shared(x[t]).
     ``logits_override`` (float32 [T, G]) replaces the router output for the
     routing step only (used to study near-tied selections).
+    ``w8a8``: the routed experts' GEMMs quantise their activations
+    (``grouped_gemm_w8a8``); the shared expert stays bf16.
     Returns a dict with every intermediate."""
     x = np.asarray(x, np.float64)
     T = x.shape[0]
@@ -390,7 +480,7 @@ def moe_layer(x, wg, gate_bias, sel_bias, w1, w3, w2, *, E: int, K: int, mode: i
         ids, w = topk_sigmoid_bias(np.asarray(lsel, np.float32), sel_bias, E, K, routed_scale)
     offsets, row_to_flat, flat_to_row = permute(ids, E)
     xp = gather_rows(x, row_to_flat, K)
-    hact, y = grouped_gemm(xp, offsets, w1, w3, w2)
+    hact, y = (grouped_gemm_w8a8 if w8a8 else grouped_gemm)(xp, offsets, w1, w3, w2)
     sh, g = None, None
     if shared is not None:
         g = shared_gate(logits, E)
@@ -412,4 +502,5 @@ def moe_layer_from_inputs(inp: dict, logits_override=None):
                   bf16_to_f64(inp["sw2_bits"]))
     return moe_layer(x, inp["wg"], inp["gate_bias"], inp["sel_bias"], w1, w3, w2,
                      E=spec.E, K=spec.K, mode=spec.mode, routed_scale=spec.routed_scale,
-                     shared=shared, logits_override=logits_override)
+                     shared=shared, logits_override=logits_override,
+                     w8a8=getattr(spec, "act", "bf16") == "fp8")

@@ -161,3 +161,65 @@ def test_mxfp4_scale_off_by_one_is_caught(monkeypatch):
           lambda packed, scales, block=32: real(packed, np.asarray(scales, np.uint8) + 1, block))
     assert fails(P.test_mxfp4_golden_worked_example)
     assert fails(P.test_mxfp4_scale_is_a_power_of_two_per_32_elements)
+
+
+def test_w8a8_ties_away_from_zero_are_caught(monkeypatch):
+    orig = M.e4m3_round
+
+    def away(v):
+        v = np.asarray(v, np.float64)
+        c = orig(v)
+        # at an exact midpoint take the larger magnitude instead of the even code
+        up = orig(np.nextafter(np.abs(v), np.inf) * np.sign(v))
+        mid = (orig(np.nextafter(np.abs(v), 0) * np.sign(v)) != up) & (c != up)
+        return np.where(mid, up, c).astype(np.uint8)
+    patch(monkeypatch, "e4m3_round", away)
+    assert fails(P.test_e4m3_round_matches_torch_cast)
+
+
+def test_w8a8_scale_block_of_64_is_caught(monkeypatch):
+    orig = M.quantize_act_fp8
+    patch(monkeypatch, "quantize_act_fp8", lambda a, block=128: orig(a, 64))
+    assert fails(P.test_quantize_act_fp8_closed_forms)
+    assert fails(P.test_quantize_act_fp8_matches_brute_force)
+
+
+def test_w8a8_scale_over_240_is_caught(monkeypatch):
+    # a wrong largest code (240, the e4m3 maximum of another convention)
+    def q240(a, block=128):
+        a32 = np.asarray(a, np.float32)
+        nb = -(-a32.shape[1] // block)
+        codes = np.zeros(a32.shape, np.uint8)
+        sc = np.zeros((a32.shape[0], nb), np.float32)
+        for j in range(nb):
+            blk = a32[:, j * block:(j + 1) * block]
+            sb = (np.abs(blk).max(axis=1) / np.float32(240.0)).astype(np.float32)
+            safe = np.where(sb > 0, sb, np.float32(1.0)).astype(np.float32)
+            c = M.e4m3_round((blk / safe[:, None]).astype(np.float32))
+            c[sb == 0] = 0
+            codes[:, j * block:(j + 1) * block] = c
+            sc[:, j] = sb
+        return codes, sc
+    patch(monkeypatch, "quantize_act_fp8", q240)
+    assert fails(P.test_quantize_act_fp8_closed_forms)
+    assert fails(P.test_quantize_act_fp8_matches_brute_force)
+
+
+def test_w8a8_unrounded_hact_is_caught(monkeypatch):
+    patch(monkeypatch, "round_bf16", lambda v: np.asarray(v, np.float64))
+    assert fails(P.test_round_bf16_matches_torch)
+    assert fails(P.test_grouped_gemm_w8a8_matches_brute_force)
+
+
+def test_w8a8_unquantised_second_gemm_is_caught(monkeypatch):
+    orig_gg = M.grouped_gemm_w8a8
+
+    def no_second(xp, offsets, w1, w3, w2):
+        hact, _ = orig_gg(xp, offsets, w1, w3, w2)
+        y = np.zeros((hact.shape[0], w2.shape[1]))
+        for e in range(len(offsets) - 1):
+            lo, hi = int(offsets[e]), int(offsets[e + 1])
+            y[lo:hi] = hact[lo:hi] @ np.asarray(w2[e], np.float64).T
+        return hact, y
+    patch(monkeypatch, "grouped_gemm_w8a8", no_second)
+    assert fails(P.test_grouped_gemm_w8a8_matches_brute_force)

@@ -437,3 +437,102 @@ def test_layer_mxfp4_equals_bf16_path_on_dequantised_weights():
     res2 = oracle.moe_layer(oracle.bf16_to_f64(inp["x_bits"]), inp["wg"], None, None, w1, w3, w2,
                             E=3, K=2, mode=0)
     assert np.array_equal(res["out"], res2["out"])
+
+
+# ---------------------------------------------------------------- W8A8 activations
+def test_e4m3_round_matches_torch_cast():
+    # library routine: torch's float32 -> float8_e4m3fn cast rounds to nearest
+    # even; compared inside the finite range on every code, every midpoint,
+    # the float32 neighbours of every midpoint and random values
+    vals = oracle.e4m3_to_f64(np.arange(0x7F, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2
+    m32 = mids.astype(np.float32)
+    v = np.concatenate([vals, mids, np.nextafter(m32, np.float32(0)).astype(np.float64),
+                        np.nextafter(m32, np.float32(1e9)).astype(np.float64),
+                        rng(21).uniform(-448, 448, 4000), rng(22).normal(0, 0.01, 2000)])
+    v = np.concatenate([v, -v]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_round(v.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_round_saturates_and_keeps_sign():
+    got = oracle.e4m3_round(np.array([448.0, 449.0, 464.0, 1e6, 3e38, -500.0, -0.0, -1e-9]))
+    assert got.tolist() == [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x80, 0x80]
+
+
+def test_quantize_act_fp8_closed_forms():
+    a = np.zeros((3, 200), np.float32)
+    a[0, :128] = oracle.e4m3_to_f64(np.arange(128, dtype=np.uint8) % 0x7F)  # amax 448: s = 1
+    a[0, 128:] = -7.0                                                      # narrow last block
+    a[1, 5] = 3.0                                                          # one non-zero
+    codes, s = oracle.quantize_act_fp8(a)
+    assert s.shape == (3, 2) and s.dtype == np.float32
+    assert s[0, 0] == 1.0 and np.array_equal(codes[0, :128], np.arange(128) % 0x7F)
+    assert s[0, 1] == np.float32(7.0) / np.float32(448.0) and (codes[0, 128:] == 0xFE).all()
+    assert s[1, 0] == np.float32(3.0) / np.float32(448.0) and codes[1, 5] == 0x7E
+    assert (codes[1, :5] == 0).all() and s[1, 1] == 0 and s[2, 0] == 0 and (codes[2] == 0).all()
+
+
+def test_quantize_act_fp8_round_trip_bound():
+    # each value within half an e4m3 spacing of its block's grid: 2^-4
+    # relative for normal codes, 2^-10 * s below the smallest normal
+    a = rng(23).normal(0, 1, (6, 300)).astype(np.float32) * rng(24).uniform(0.01, 50, (6, 1))
+    codes, s = oracle.quantize_act_fp8(a)
+    d = oracle.dequant_act_fp8(codes, s)
+    sf = np.repeat(s.astype(np.float64), 128, axis=1)[:, :300]
+    assert (np.abs(d - a) <= 2.0 ** -4 * np.abs(a) * (1 + 1e-6) + 2.0 ** -10 * sf).all()
+    # the block maximum is always the largest code
+    for r in range(6):
+        for b in range(3):
+            blk = a[r, 128 * b:128 * (b + 1)]
+            j = 128 * b + int(np.argmax(np.abs(blk)))
+            assert codes[r, j] & 0x7F == 0x7E
+
+
+def test_quantize_act_fp8_matches_brute_force():
+    a = rng(25).normal(0, 2, (3, 150)).astype(np.float32)
+    a[1, :20] = 0.0
+    codes, s = oracle.quantize_act_fp8(a)
+    bc, bs = brute.quant_rows(a.astype(np.float64).tolist())
+    assert np.array_equal(codes, np.array(bc, np.uint8))
+    assert np.array_equal(s, np.array(bs, np.float32))
+
+
+def test_round_bf16_matches_torch():
+    v = np.concatenate([rng(26).normal(0, 3, 3000), [0.0, -0.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8]])
+    ref = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(oracle.round_bf16(v), ref)
+
+
+def test_grouped_gemm_w8a8_matches_brute_force():
+    r = rng(27)
+    E, H, I = 3, 144, 136  # two scale blocks in each GEMM's K, the second narrow
+    offsets = np.array([0, 2, 2, 5])
+    xp = oracle.bf16_to_f64(synth.f32_to_bf16_bits(r.normal(0, 1, (5, H)).astype(np.float32)))
+    w1 = r.normal(0, H ** -0.5, (E, I, H))
+    w3 = r.normal(0, H ** -0.5, (E, I, H))
+    w2 = r.normal(0, I ** -0.5, (E, H, I))
+    h, y = oracle.grouped_gemm_w8a8(xp, offsets, w1, w3, w2)
+    bh, by = brute.grouped_gemm_w8a8(xp.tolist(), offsets.tolist(), w1.tolist(), w3.tolist(),
+                                      w2.tolist())
+    # the two sum the dot products in different orders: a bf16 rounding of
+    # hact may land one step apart
+    assert (np.abs(h - np.array(bh)) <= 2.0 ** -8 * np.abs(h)).all()
+    assert np.allclose(y, np.array(by), rtol=1e-9, atol=1e-12)
+    # the quantised path is near the unquantised one (e4m3 keeps 3 mantissa
+    # bits), not equal to it
+    h0, y0 = oracle.grouped_gemm(xp, offsets, w1, w3, w2)
+    err = np.sqrt(np.mean((y - y0) ** 2)) / np.sqrt(np.mean(y0 ** 2))
+    assert 1e-3 < err < 0.1
+
+
+def test_layer_w8a8_uses_the_quantised_experts():
+    spec = synth.LayerSpec("pin8a8", H=160, E=3, K=2, I=136, wdtype="fp8", act="fp8")
+    inp = synth.host_inputs(spec, T=5, seed=16)
+    res = oracle.moe_layer_from_inputs(inp)
+    w1, w3, w2 = (np.stack([b[e] for e in range(3)]) for b in oracle.layer_weights_f64(inp))
+    h, y = oracle.grouped_gemm_w8a8(res["xp"], res["offsets"], w1, w3, w2)
+    assert np.array_equal(res["y"], y) and np.array_equal(res["hact"], h)
+    out = oracle.unpermute(y, res["flat_to_row"], res["weights"], 5, 2)
+    assert np.array_equal(res["out"], out)
