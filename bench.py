@@ -141,6 +141,8 @@ def job_throughput(tokens_per_rank_step, steps, world, max_ms):
 
 # ------------------------------------------------------------------ workload
 def wd_of(ops, spec):
+    if spec.act == "fp8":
+        return ops.W8A8_FP8
     return {"bf16": ops.W_BF16, "fp8": ops.W_FP8, "mxfp4": ops.W_MXFP4}[spec.wdtype]
 
 
@@ -152,6 +154,12 @@ def weight_bytes(spec, n):
 
 DTYPE_NAME = {"bf16": "bf16", "fp8": "bf16 activations, fp8-e4m3 weights",
               "mxfp4": "bf16 activations, mxfp4 (e2m1 + ue8m0/32) weights"}
+
+
+def dtype_name(spec):
+    if spec.act == "fp8":
+        return "fp8-e4m3 weights and expert-GEMM activations (W8A8), bf16 in and out"
+    return DTYPE_NAME[spec.wdtype]
 
 
 def tensors_of(spec, d):
@@ -259,6 +267,8 @@ def roofline_of(bytes_, flops, seconds, peaks, compute="tensor", sustained=False
         cpk = (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]) * 1e12
         if compute == "bf16x3":  # fp32-accurate GEMM from three bf16 MMAs per product
             cpk /= 3
+        if compute == "tensor_fp8":  # e4m3 MMAs: the nominal fp8/bf16 ratio (4.5 / 2.25) x bf16
+            cpk *= 2
     t_mem, t_c = bytes_ / bw, flops / cpk
     if t_mem >= t_c:
         ach = bytes_ / seconds / 1e9
@@ -266,12 +276,22 @@ def roofline_of(bytes_, flops, seconds, peaks, compute="tensor", sustained=False
                 "frac": ach / peaks["hbm_gbs"]}
     ach = flops / seconds / 1e12
     pk = cpk / 1e12
-    return {"bound": "tensor" if compute == "bf16x3" else compute, "achieved": ach, "peak": pk, "unit": "TFLOP/s", "frac": ach / pk}
+    bound = "tensor" if compute in ("bf16x3", "tensor") else compute
+    return {"bound": bound, "achieved": ach, "peak": pk, "unit": "TFLOP/s", "frac": ach / pk}
 
 
 STAGE_COMPUTE = {"router": "alu", "topk": "alu", "permute": "alu", "grouped_gemm": "tensor",
                  "unpermute": "alu"}
 ROUTER_TC_MIN_T = 64  # the layer's router runs on the tensor cores from this batch size on
+
+
+def stage_compute(spec, T, n):
+    """The compute ceiling a stage is held against."""
+    if n == "router":
+        return router_compute(T)
+    if n == "grouped_gemm" and spec.act == "fp8":
+        return "tensor_fp8"
+    return STAGE_COMPUTE[n]
 
 
 def router_compute(T):
@@ -463,13 +483,13 @@ def measure(spec, T, args, rank, world, dev, peaks, light=False):
     sbf = stage_bytes_flops(spec, T, ids_h, e_active)
     per_stage = {}
     for n in names:
-        kind = router_compute(T) if n == "router" else STAGE_COMPUTE[n]
+        kind = stage_compute(spec, T, n)
         r = roofline_of(sbf[n]["bytes"], sbf[n]["flops"], stage_ms[n] / 1e3, peaks, kind)
         per_stage[n] = {"us": round(stage_ms[n] * 1e3, 2), "bound": r["bound"],
                         "frac": round(r["frac"], 4)}
     dom = max(names, key=lambda n: stage_ms[n])
     roof = roofline_of(sbf[dom]["bytes"], sbf[dom]["flops"], stage_ms[dom] / 1e3, peaks,
-                       router_compute(T) if dom == "router" else STAGE_COMPUTE[dom])
+                       stage_compute(spec, T, dom))
     roof = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()}
     roof["kernel"] = dom
     roof["algorithmic"] = ({"bytes": sbf[dom]["bytes"]} if roof["unit"] == "GB/s"
@@ -480,7 +500,7 @@ def measure(spec, T, args, rank, world, dev, peaks, light=False):
     hot = (float(np.isin(ids_h, list(spec.hot_experts)).mean()) if spec.hot_experts else None)
 
     res = {"workload": spec.name, "T": T, "H": spec.H, "E": spec.E, "K": spec.K, "I": spec.I,
-           "dtype": DTYPE_NAME[spec.wdtype],
+           "dtype": dtype_name(spec),
            "us_per_layer": round(ms_step * 1e3, 2),
            "tokens_per_s": round(job_throughput(T, args.steps, world, ms), 1),
            "ms_total": ms, "roofline": roof, "per_stage": per_stage, "clocks": clk,
@@ -616,7 +636,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     peaks = load_peaks()
-    head_spec = synth.SPECS[args.workload]
+    head_spec = workload_spec(args)
     head = measure(head_spec, args.T, args, rank, world, dev, peaks)
     spec, T = head_spec, args.T
     res = {
@@ -817,8 +837,9 @@ def prefill_points(peaks, dev):
 
     stream = torch.cuda.current_stream()
     res = []
-    for name, T in (("qwen3_30b_a3b", 16384), ("gpt_oss_20b", 4096)):
-        spec = synth.SPECS[name]
+    for name, T, over in (("qwen3_30b_a3b", 16384, {}), ("gpt_oss_20b", 4096, {}),
+                          ("gpt_oss_20b", 4096, {"act": "fp8"})):
+        spec = synth.SPECS[name].with_(**over)
         d = synth.device_inputs(spec, T, seed=3, device=dev)
         t = tensors_of(spec, d)
         cfg = ops.make_config(T, spec.H, spec.E, spec.K, spec.I,
@@ -841,9 +862,11 @@ def prefill_points(peaks, dev):
         ids = layer.view("ids", torch.int32, (T, K)).cpu().numpy()
         e_act = int(len(np.unique(ids)))
         sb = stage_bytes_flops(spec, T, ids, e_act)["grouped_gemm"]
-        r = roofline_of(sb["bytes"], sb["flops"], sec, peaks, "tensor")
+        kind = "tensor_fp8" if spec.act == "fp8" else "tensor"
+        r = roofline_of(sb["bytes"], sb["flops"], sec, peaks, kind)
         hot = float(np.isin(ids, list(spec.hot_experts)).mean()) if spec.hot_experts else None
-        res.append({"workload": name, "T": T, "us": round(sec * 1e6, 1), "bound": r["bound"],
+        res.append({"workload": name + (" W8A8" if spec.act == "fp8" else ""), "T": T,
+                    "us": round(sec * 1e6, 1), "bound": r["bound"], "peak": round(r["peak"], 1),
                     "achieved": round(r["achieved"], 1), "unit": r["unit"],
                     "frac": round(r["frac"], 3), "tflops": round(sb["flops"] / sec / 1e12, 1),
                     "hot_expert_share": hot})
@@ -861,8 +884,9 @@ def format_sweep(peaks, dev, Ts=(1, 32, 512, 4096)):
 
     stream = torch.cuda.current_stream()
     res = []
-    for wdt in ("bf16", "fp8", "mxfp4"):
-        spec = synth.SPECS["gpt_oss_20b"].with_(wdtype=wdt)
+    for wdt in ("bf16", "fp8", "mxfp4", "w8a8"):
+        spec = synth.SPECS["gpt_oss_20b"].with_(wdtype="fp8" if wdt == "w8a8" else wdt,
+                                                act="fp8" if wdt == "w8a8" else "bf16")
         d, t, layer = make_layer(spec, max(Ts), 3, dev)
         for T in Ts:
             x = d["x"][:T].contiguous()
@@ -968,9 +992,7 @@ def cpu_baseline(spec, d, tokens):
 
 
 def run_reference(args):
-    from mixture_experts_layer_07_gb300 import synth
-
-    spec = synth.SPECS[args.workload]
+    spec = workload_spec(args)
     cores = len(os.sched_getaffinity(0))
     n = max(1, args.ref_tokens)
     inp = host_workload(spec, n * (args.steps + args.warmup), seed=1)
@@ -1036,6 +1058,18 @@ def print_launch_check(rank, world):
             torch.distributed.destroy_process_group()
 
 
+def workload_spec(args):
+    """The named workload, with --act applied (fp8: W8A8 on fp8 weights)."""
+    from mixture_experts_layer_07_gb300 import synth
+
+    spec = synth.SPECS[args.workload]
+    if args.act == "fp8":
+        spec = spec.with_(wdtype="fp8", act="fp8")
+    elif args.act == "bf16":
+        spec = spec.with_(act="bf16")
+    return spec
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1043,6 +1077,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_30b_a3b")
+    ap.add_argument("--act", default=None, choices=["bf16", "fp8"],
+                    help="expert-GEMM activations of the probed workload (fp8: W8A8, fp8 weights)")
     ap.add_argument("--T", type=int, default=2048)
     ap.add_argument("--cpu-tokens", type=int, default=0,
                     help="oracle tokens per CPU-baseline sample (0: per-workload default)")
@@ -1104,7 +1140,7 @@ def main():
     if args.probe_layer:
         from mixture_experts_layer_07_gb300 import synth
         torch.cuda.set_device(local_rank)
-        print(json.dumps(probe_layer(synth.SPECS[args.workload], args.probe_layer, 3,
+        print(json.dumps(probe_layer(workload_spec(args), args.probe_layer, 3,
                                      f"cuda:{local_rank}")), flush=True)
         return
 

@@ -80,7 +80,8 @@ typedef enum {
 typedef enum {
   MOE_W_BF16 = 0,          /* expert weights bf16 */
   MOE_W_FP8E4M3_B128 = 1,  /* expert weights e4m3 + fp32 128x128 block scales */
-  MOE_W_MXFP4 = 2          /* expert weights MXFP4: e2m1 pairs + a UE8M0 scale per 32 */
+  MOE_W_MXFP4 = 2,         /* expert weights MXFP4: e2m1 pairs + a UE8M0 scale per 32 */
+  MOE_W8A8_FP8E4M3_B128 = 3 /* weights as MOE_W_FP8E4M3_B128; activations quantised (W8A8) */
 } moe_wdtype_t;
 
 /* How the grouped GEMM picks a kernel variant for each expert block. */
@@ -272,8 +273,13 @@ moe_status_t moe_permute_static(const void* x, const int32_t* ids, int T, int H,
                                 int32_t* offsets, int32_t* row_to_flat, int32_t* flat_to_row,
                                 void* xp, int32_t* dev_status, moe_stream_t stream);
 
-/* Scratch bytes moe_grouped_gemm needs for R rows in E_blocks blocks. */
+/* Scratch bytes moe_grouped_gemm needs for R rows in E_blocks blocks (every
+ * weight format but MOE_W8A8_FP8E4M3_B128). */
 moe_status_t moe_grouped_gemm_scratch_bytes(int R, int E_blocks, size_t* bytes);
+/* Scratch bytes for any weight format: as above, plus for
+ * MOE_W8A8_FP8E4M3_B128 the e4m3 copies of xp and hact with their scales. */
+moe_status_t moe_grouped_gemm_scratch_bytes_ex(int R, int E_blocks, int H, int I, int wdtype,
+                                               size_t* bytes);
 
 /*
  * G1 + G2: grouped SwiGLU expert GEMM over expert-contiguous row blocks.
@@ -285,16 +291,29 @@ moe_status_t moe_grouped_gemm_scratch_bytes(int R, int E_blocks, size_t* bytes);
  * it ([dispatch] "2. moe_fp8.cpp").  Every variant runs tcgen05 tensor-core
  * MMAs fed by TMA with TMEM accumulators: the skinny variant uses a 16-row
  * token tile, the tile variant a 128-row one and the wide variant (FP8) a
- * 256-row one.  FP8 weights need H, I <= 8192.
+ * 256-row one.  W8A16 FP8 weights need H, I <= 8192.
  *   xp        [R, H] bf16, 16-byte aligned
  *   offsets   [E_blocks + 1] int32 (device), or NULL for one block [0, R)
  *   w1, w3    [E_blocks, I, H]; w2 [E_blocks, H, I]; bf16 or e4m3 per wdtype
  *   s1, s3    [E_blocks, ceil(I/128), ceil(H/128)] fp32; s2 [E_blocks, ceil(H/128), ceil(I/128)]
- *             (wdtype MOE_W_FP8E4M3_B128 only, else NULL)
+ *             (FP8 weights, W8A16 or W8A8); MXFP4: uint8 scale bytes
+ *             [E_blocks, rows, cols/32] cast to these pointers; bf16: NULL
  *   hact      [R, I] bf16 output;  y [R, H] bf16 output (rows outside every
  *             block are left untouched)
  *   block_variant  [E_blocks] int32 output of MOE_VARIANT_* codes, or NULL
- *   scratch   >= moe_grouped_gemm_scratch_bytes(R, E_blocks), 256-byte aligned
+ *   scratch   >= moe_grouped_gemm_scratch_bytes_ex(R, E_blocks, H, I, wdtype),
+ *             256-byte aligned
+ * W8A8 (wdtype MOE_W8A8_FP8E4M3_B128; the pages fix FP8 weights, not the
+ * activations): both GEMMs' activations are quantised to e4m3 with one fp32
+ * scale per row and 128 columns -- s = amax / 448 (IEEE fp32 division, 0 for
+ * an all-zero block), code = e4m3(v / s) rounded to nearest even, saturated
+ * at 448 -- xp before G1, and the bf16 hact (as stored) before G2; the
+ * products run as kind::f8f6f4 MMAs, each 128-wide K block scaled by the
+ * weight block scale times the row's activation scale and summed in fp32.
+ * Every non-empty block takes one kernel with 128-row token tiles (variant
+ * MOE_VARIANT_TILE; a prefill option: no skinny variant), dispatch
+ * MOE_DISPATCH_PER_BLOCK or MOE_DISPATCH_GLOBAL_AVG (MOE_DISPATCH_SIMT:
+ * MOE_ERR_UNSUPPORTED).
  */
 moe_status_t moe_grouped_gemm(const void* xp, const int32_t* offsets, int E_blocks, int R,
                               int H, int I, int wdtype,

@@ -30,7 +30,11 @@ moe_status_t check_cfg(const moe_config_t* c) {
   if (c->I <= 0 || c->I % 16 != 0) return MOE_ERR_INVALID_ARG;
   if (c->mode != MOE_SCORE_SOFTMAX_RENORM && c->mode != MOE_SCORE_SIGMOID_BIAS_SCALED)
     return MOE_ERR_INVALID_ARG;
-  if (c->wdtype != MOE_W_BF16 && c->wdtype != MOE_W_FP8E4M3_B128 && c->wdtype != MOE_W_MXFP4)
+  if (c->wdtype != MOE_W_BF16 && c->wdtype != MOE_W_FP8E4M3_B128 && c->wdtype != MOE_W_MXFP4 &&
+      c->wdtype != MOE_W8A8_FP8E4M3_B128)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->wdtype == MOE_W8A8_FP8E4M3_B128 &&
+      (c->dispatch == MOE_DISPATCH_SIMT || c->dispatch == MOE_DISPATCH_ONE_LAUNCH))
     return MOE_ERR_UNSUPPORTED;
   if (c->wdtype == MOE_W_MXFP4 && (c->H % 32 != 0 || c->I % 32 != 0)) return MOE_ERR_INVALID_ARG;
   if (c->dispatch < MOE_DISPATCH_PER_BLOCK || c->dispatch > MOE_DISPATCH_ONE_LAUNCH)
@@ -101,7 +105,7 @@ void layout_of(const moe_config_t* c, moe_workspace_layout_t* L) {
   const size_t pb = permute_scratch_bytes(c->T_max, c->E, c->K);
   const size_t rb = route_prefill_scratch_bytes(c->T_max, c->E);
   L->permute_scratch = take(pb > rb ? pb : rb);
-  L->gemm_scratch = take(grouped_gemm_scratch_bytes((int)R, c->E));
+  L->gemm_scratch = take(grouped_gemm_scratch_bytes_ex((int)R, c->E, c->H, c->I, c->wdtype));
   L->shared_gemm_scratch = take(c->has_shared ? grouped_gemm_scratch_bytes(c->T_max, 1) : 0);
   // split-K slices for small batches (all blocks skinny: T <= m_skinny)
   const int ms = c->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : c->m_skinny;
@@ -216,6 +220,13 @@ moe_status_t moe_grouped_gemm_scratch_bytes(int R, int E_blocks, size_t* bytes) 
   return MOE_OK;
 }
 
+moe_status_t moe_grouped_gemm_scratch_bytes_ex(int R, int E_blocks, int H, int I, int wdtype,
+                                               size_t* bytes) {
+  if (!bytes || R < 0 || E_blocks <= 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+  *bytes = grouped_gemm_scratch_bytes_ex(R, E_blocks, H, I, wdtype);
+  return MOE_OK;
+}
+
 moe_status_t moe_grouped_gemm(const void* xp, const int32_t* offsets, int E_blocks, int R, int H,
                               int I, int wdtype, const void* w1, const void* w3, const void* w2,
                               const float* s1, const float* s3, const float* s2, void* hact,
@@ -229,7 +240,9 @@ moe_status_t moe_grouped_gemm(const void* xp, const int32_t* offsets, int E_bloc
   if (!w1 || !w3 || !w2 || !scratch) return MOE_ERR_INVALID_ARG;
   if (R > 0 && (!xp || !hact || !y)) return MOE_ERR_INVALID_ARG;
   if (wdtype != MOE_W_BF16 && (!s1 || !s3 || !s2)) return MOE_ERR_INVALID_ARG;
-  if (scratch_bytes < grouped_gemm_scratch_bytes(R, E_blocks)) return MOE_ERR_WORKSPACE;
+  if (wdtype == MOE_W8A8_FP8E4M3_B128 && dispatch == MOE_DISPATCH_SIMT) return MOE_ERR_UNSUPPORTED;
+  if (scratch_bytes < grouped_gemm_scratch_bytes_ex(R, E_blocks, H, I, wdtype))
+    return MOE_ERR_WORKSPACE;
   if (misaligned(scratch, 256) || misaligned(w1, 16) || misaligned(w3, 16) || misaligned(w2, 16) ||
       (xp && misaligned(xp, 16)) || (hact && misaligned(hact, 16)) || (y && misaligned(y, 16)) ||
       (offsets && misaligned(offsets, 4)) || (block_variant && misaligned(block_variant, 4)))

@@ -26,6 +26,8 @@
 __host__ __device__ __forceinline__ int moe_variant_of(int64_t m_size, int64_t R, int E,
                                                       int m_skinny, int dispatch, int wdtype) {
   if (m_size <= 0) return MOE_VARIANT_SKIP;
+  // W8A8: one kernel takes every block, in 128-row token tiles
+  if (wdtype == MOE_W8A8_FP8E4M3_B128) return MOE_VARIANT_TILE;
   if (dispatch == MOE_DISPATCH_SIMT) return MOE_VARIANT_SIMT;
   int64_t m = m_size;
   if (dispatch == MOE_DISPATCH_GLOBAL_AVG) {

@@ -1347,6 +1347,11 @@ cudaError_t launch_bounded_wait_check(const int32_t* counter, int target, uint64
 
 size_t grouped_gemm_scratch_bytes(int R, int E_blocks) { return plan_bytes(R, E_blocks); }
 
+size_t grouped_gemm_scratch_bytes_ex(int R, int E_blocks, int H, int I, int wdtype) {
+  return plan_bytes(R, E_blocks) +
+         (wdtype == MOE_W8A8_FP8E4M3_B128 ? w8a8_act_bytes(R, H, I) : 0);
+}
+
 size_t grouped_gemm_split_counter_bytes(int R, int E_blocks, int H, int I) {
   const size_t cap0 = (size_t)moe_cdiv(R, kBnSkinny) + E_blocks;
   return moe_align_up(cap0 * (moe_cdiv(I, kBM) + moe_cdiv(H, kBM)) * sizeof(int32_t), 256);
@@ -1359,7 +1364,8 @@ size_t grouped_gemm_splitk_bytes(int R, int H, int I) {
 
 int grouped_gemm_check(int H, int I, int wdtype) {
   if (H % 16 != 0 || I % 16 != 0) return MOE_ERR_INVALID_ARG;
-  if (wdtype != MOE_W_BF16 && wdtype != MOE_W_FP8E4M3_B128 && wdtype != MOE_W_MXFP4)
+  if (wdtype != MOE_W_BF16 && wdtype != MOE_W_FP8E4M3_B128 && wdtype != MOE_W_MXFP4 &&
+      wdtype != MOE_W8A8_FP8E4M3_B128)
     return MOE_ERR_UNSUPPORTED;
   // MXFP4: whole 32-element scale blocks along every row
   if (wdtype == MOE_W_MXFP4 && (H % 32 != 0 || I % 32 != 0)) return MOE_ERR_INVALID_ARG;
@@ -1388,6 +1394,12 @@ cudaError_t launch_grouped_gemm(const void* xp, const int32_t* offsets, int E_bl
                      m_skinny, dispatch, wdtype, pv.counts, po, block_variant);
   if (err != cudaSuccess || R == 0) return err;
 
+  if (wdtype == MOE_W8A8_FP8E4M3_B128) {
+    if (simt || gather_x) return cudaErrorInvalidValue;  // W8A8 reads xp, tensor cores only
+    return launch_w8a8(xp, R, E_blocks, H, I, w1, w3, w2, s1, s3, s2, hact, y, pv.counts,
+                       pv.items[1], static_cast<char*>(scratch) + plan_bytes(R, E_blocks),
+                       dev_status, stream);
+  }
   if (simt && gather_x) return cudaErrorInvalidValue;  // the CUDA-core path reads xp only
   if (simt) {
     err = run_simt<true>(wdtype, xp, w1, w3, s1, s3, pv.counts, pv.items[0], pv.cap[0], I, H,

@@ -27,6 +27,18 @@ cudaError_t launch_permute(const void* x, const int32_t* ids, int T, int H, int 
                            void* xp, void* scratch, int32_t* dev_status, cudaStream_t stream);
 
 size_t grouped_gemm_scratch_bytes(int R, int E_blocks);
+// scratch of a grouped-GEMM call: the plan, plus for W8A8 the quantised
+// activations (w8a8_act_bytes) right after it
+size_t grouped_gemm_scratch_bytes_ex(int R, int E_blocks, int H, int I, int wdtype);
+// W8A8 expert GEMMs (gemm_w8a8.cu): e4m3 copies of xp and hact with their
+// per-(row, 128 columns) scales live in act_scratch (w8a8_act_bytes of it);
+// the plan's tile list (every non-empty block, 128-row items) drives both GEMMs
+size_t w8a8_act_bytes(int R, int H, int I);
+cudaError_t launch_w8a8(const void* xp, int R, int E_blocks, int H, int I, const void* w1,
+                        const void* w3, const void* w2, const float* s1, const float* s3,
+                        const float* s2, void* hact, void* y, const int32_t* counts,
+                        const int4* tile_items, void* act_scratch, int32_t* dev_status,
+                        cudaStream_t stream);
 int grouped_gemm_check(int H, int I, int wdtype);  // 0 ok, else a moe_status_t
 // plan_ready: the plan in `scratch` was already written (by the fused decode
 // routing kernel); only the GEMM kernels are launched.

@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 
 MODE_SOFTMAX, MODE_SIGMOID_BIAS = 0, 1
-W_BF16, W_FP8, W_MXFP4 = 0, 1, 2
+W_BF16, W_FP8, W_MXFP4, W8A8_FP8 = 0, 1, 2, 3
 DISPATCH_PER_BLOCK, DISPATCH_GLOBAL_AVG, DISPATCH_SIMT, DISPATCH_ONE_LAUNCH = 0, 1, 2, 3
 VARIANT_SKIP, VARIANT_SKINNY, VARIANT_TILE, VARIANT_SIMT, VARIANT_WIDE = 0, 1, 2, 3, 4
 WIDE_MIN_ROWS = 129
@@ -29,7 +29,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 EXPORTS = ["moe_status_string", "moe_default_m_skinny", "moe_block_variant", "moe_router_gemm",
            "moe_topk_route", "moe_permute_scratch_bytes", "moe_permute",
-           "moe_grouped_gemm_scratch_bytes", "moe_grouped_gemm", "moe_unpermute",
+           "moe_grouped_gemm_scratch_bytes", "moe_grouped_gemm_scratch_bytes_ex",
+           "moe_grouped_gemm", "moe_unpermute",
            "moe_workspace_bytes", "moe_layer", "moe_workspace_layout", "moe_permute_static",
            "moe_router_tc_scratch_bytes", "moe_router_gemm_tc", "moe_bounded_wait_check"]
 
@@ -91,6 +92,7 @@ def _lib():
             "moe_permute": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P, _P],
             "moe_permute_static": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P],
             "moe_grouped_gemm_scratch_bytes": [_I, _I, ctypes.POINTER(_S)],
+            "moe_grouped_gemm_scratch_bytes_ex": [_I, _I, _I, _I, _I, ctypes.POINTER(_S)],
             "moe_grouped_gemm": [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I,
                                  _I, _P, _P, _S, _P, _P],
             "moe_unpermute": [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P],
@@ -156,10 +158,16 @@ def permute_scratch_bytes(T: int, E: int, K: int) -> int:
     return n.value
 
 
-def grouped_gemm_scratch_bytes(R: int, E_blocks: int) -> int:
+def grouped_gemm_scratch_bytes(R: int, E_blocks: int, H: int = 0, I: int = 0,
+                               wdtype: int = W_BF16) -> int:
     n = _S()
-    _check(_lib().moe_grouped_gemm_scratch_bytes(R, E_blocks, ctypes.byref(n)),
-           "moe_grouped_gemm_scratch_bytes")
+    if wdtype == W8A8_FP8:
+        _check(_lib().moe_grouped_gemm_scratch_bytes_ex(R, E_blocks, H, I, wdtype,
+                                                        ctypes.byref(n)),
+               "moe_grouped_gemm_scratch_bytes_ex")
+    else:
+        _check(_lib().moe_grouped_gemm_scratch_bytes(R, E_blocks, ctypes.byref(n)),
+               "moe_grouped_gemm_scratch_bytes")
     return n.value
 
 

@@ -79,6 +79,9 @@ def config_for(ops, spec, T_max, **kw):
 
 
 def wdtype_of(ops, spec):
+    if spec.act == "fp8":
+        assert spec.wdtype == "fp8", "W8A8 takes FP8 weights"
+        return ops.W8A8_FP8
     return {"bf16": ops.W_BF16, "fp8": ops.W_FP8, "mxfp4": ops.W_MXFP4}[spec.wdtype]
 
 

@@ -62,6 +62,7 @@ FULL = [("qwen3_30b_a3b", {}, 2048, 64), ("qwen3_30b_a3b", {}, 1, 1),
         ("qwen3_30b_a3b", {}, 8, 8),
         ("gpt_oss_20b", {}, 4096, 64), ("gpt_oss_20b", {}, 512, 64), ("gpt_oss_20b", {}, 32, 32),
         ("gpt_oss_20b", {"wdtype": "mxfp4"}, 4096, 64), ("gpt_oss_20b", {"wdtype": "mxfp4"}, 1, 1),
+        ("gpt_oss_20b", {"act": "fp8"}, 4096, 64),
         ("shared_gate", {}, 1024, 64), ("shared_gate", {}, 1, 1),
         ("high_expert", {}, 512, 16), ("high_expert", {"E": 512, "K": 16}, 512, 16),
         ("high_expert", {"E": 1024, "K": 9}, 512, 16)]
@@ -148,7 +149,11 @@ def test_layer_full_size(ops, name, over, T, n_out):
     for e in pick:
         lo, hi = int(off[e]), int(off[e + 1])
         a = x64[r2f[lo:hi] // K]
-        h_ref, y_ref = oracle.expert_swiglu(a, banks[0][e], banks[1][e], banks[2][e])
+        if spec.act == "fp8":  # W8A8: the rows are quantised one by one
+            h_ref, y_ref = oracle.grouped_gemm_w8a8(a, np.array([0, hi - lo]), banks[0][e][None],
+                                                    banks[1][e][None], banks[2][e][None])
+        else:
+            h_ref, y_ref = oracle.expert_swiglu(a, banks[0][e], banks[1][e], banks[2][e])
         U.assert_bf16_close(U.f64(hact[lo:hi]), h_ref, rel, f"{name} T={T} expert {e} hact")
         U.assert_bf16_close(U.f64(y[lo:hi]), y_ref, rel, f"{name} T={T} expert {e} y")
 
@@ -159,7 +164,8 @@ def test_layer_full_size(ops, name, over, T, n_out):
         shared = tuple(d[k].double().cpu().numpy() for k in ("sw1", "sw3", "sw2"))
     res = oracle.moe_layer(x64[sample], wg, gb, sb, *banks, E=E, K=K, mode=spec.mode,
                            routed_scale=spec.routed_scale, shared=shared,
-                           logits_override=lg[sample].astype(np.float64))
+                           logits_override=lg[sample].astype(np.float64),
+                           w8a8=spec.act == "fp8")
     assert np.array_equal(ids[sample], res["ids"])
     o64 = U.f64(out)
     assert np.isfinite(o64).all()

@@ -472,6 +472,76 @@ def test_grouped_gemm_mxfp4_reads_every_code_exactly(ops, T, m_skinny, dispatch)
     assert (np.abs(hact - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-37).all()
 
 
+W8A8_CASES = [  # spec name, overrides, T, concentrated
+    ("tiny", {"H": 160, "I": 144, "E": 5, "wdtype": "fp8", "act": "fp8"}, 50, True),
+    ("tiny", {"H": 256, "I": 384, "E": 3, "wdtype": "fp8", "act": "fp8"}, 7, False),
+    ("gpt_oss_20b", {"E": 4, "act": "fp8"}, 300, True),
+    ("gpt_oss_20b", {"E": 6, "act": "fp8"}, 700, True),
+    ("qwen3_30b_a3b", {"wdtype": "fp8", "act": "fp8"}, 256, False),
+]
+
+
+@pytest.mark.parametrize("name,over,T,conc", W8A8_CASES, ids=case_id)
+def test_grouped_gemm_w8a8(ops, name, over, T, conc):
+    # W8A8: the quantised activations the kernels wrote (read back from the
+    # scratch) equal the oracle's quantisation of the same bf16 rows bit for
+    # bit -- xp before G1, the GPU's own hact before G2; each GEMM matches the
+    # oracle applied to the GPU's own quantised input; and the whole call
+    # matches the oracle's W8A8 grouped GEMM end to end
+    spec = SPECS[name].with_(**over)
+    E, H, I, K = spec.E, spec.H, spec.I, spec.K
+    inp, ids, off, r2f, f2r = gemm_case(spec, T, seed=T + E + 1, concentrated=conc)
+    R = T * K
+    xp_bits = inp["x_bits"][r2f // K]
+    t = U.layer_tensors(inp, inp["experts"])
+    wd = ops.W8A8_FP8
+    hact = torch.full((R, I), float("nan"), device="cuda").to(torch.bfloat16)
+    y = torch.full((R, H), float("nan"), device="cuda").to(torch.bfloat16)
+    plan = ops.grouped_gemm_scratch_bytes(R, E)
+    scratch = torch.zeros(ops.grouped_gemm_scratch_bytes(R, E, H, I, wd), dtype=torch.uint8,
+                          device="cuda")
+    bv = i32(E)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ops.grouped_gemm(U.bf16_dev(xp_bits), torch.from_numpy(off).cuda(), E, H, I, t["w1"],
+                     t["w3"], t["w2"], hact, y, scratch, wdtype=wd, s1=t["s1"], s3=t["s3"],
+                     s2=t["s2"], block_variant=bv, dev_status=st)
+    sync()
+    assert int(st.item()) == 0
+    assert bv.cpu().numpy().tolist() == [ops.VARIANT_TILE if m else ops.VARIANT_SKIP
+                                         for m in np.diff(off)]
+    # the scratch after the plan: xq [R,H], sx [R,KB1], hq [R,I], sh [R,KB2]
+    a256 = lambda n: -(-n // 256) * 256  # noqa: E731
+    kb1, kb2 = -(-H // 128), -(-I // 128)
+    sc = scratch.cpu().numpy()[plan:]
+    o = 0
+    xq = sc[o:o + R * H].reshape(R, H); o += a256(R * H)
+    sx = sc[o:o + R * kb1 * 4].view(np.float32).reshape(R, kb1); o += a256(R * kb1 * 4)
+    hq = sc[o:o + R * I].reshape(R, I); o += a256(R * I)
+    sh = sc[o:o + R * kb2 * 4].view(np.float32).reshape(R, kb2)
+    x64 = oracle.bf16_to_f64(xp_bits)
+    rq, rs = oracle.quantize_act_fp8(x64)
+    assert np.array_equal(sx, rs) and np.array_equal(xq, rq)
+    h_gpu = U.f64(hact)
+    hq_ref, sh_ref = oracle.quantize_act_fp8(h_gpu)
+    assert np.array_equal(sh, sh_ref) and np.array_equal(hq, hq_ref)
+    # each GEMM on the GPU's own quantised input: fp32 sums and one bf16 rounding
+    w1, w3, w2 = oracle.layer_weights_f64(inp)
+    xd = oracle.dequant_act_fp8(xq, sx)
+    hd = oracle.dequant_act_fp8(hq, sh)
+    h_ref, _ = oracle.grouped_gemm(xd, off, w1, w3, w2)
+    U.assert_bf16_close(h_gpu, h_ref, 2e-2, "hact from the GPU's xq")
+    y_ref = np.zeros((R, H))
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi > lo:
+            y_ref[lo:hi] = hd[lo:hi] @ np.asarray(w2[e], np.float64).T
+    U.assert_bf16_close(U.f64(y), y_ref, 2e-2, "y from the GPU's hq")
+    # end to end against the oracle's W8A8 definition
+    rh, ry = oracle.grouped_gemm_w8a8(x64, off, w1, w3, w2)
+    U.assert_bf16_close(h_gpu, rh, 5e-2, "hact")
+    U.assert_bf16_close(U.f64(y), ry, 5e-2, "y")
+
+
 def test_grouped_gemm_single_block_without_offsets(ops):
     # offsets == NULL runs one block [0, R) -- the shared-expert form
     spec = SPECS["tiny"].with_(E=1, H=512, I=256)
@@ -525,7 +595,9 @@ LAYER_CASES = [("tiny", {}, 16), ("tiny", {}, 1), ("qwen3_30b_a3b", {}, 1),
                ("tiny", {"H": 2880, "I": 1440, "E": 4}, 1),
                ("tiny", {"H": 1024, "I": 512, "E": 8, "wdtype": "mxfp4"}, 1),
                ("gpt_oss_20b", {"wdtype": "mxfp4"}, 1), ("gpt_oss_20b", {"wdtype": "mxfp4"}, 8),
-               ("gpt_oss_20b", {"wdtype": "mxfp4"}, 64)]
+               ("gpt_oss_20b", {"wdtype": "mxfp4"}, 64),
+               ("gpt_oss_20b", {"act": "fp8"}, 3), ("gpt_oss_20b", {"act": "fp8"}, 64),
+               ("tiny", {"H": 1024, "I": 512, "E": 8, "wdtype": "fp8", "act": "fp8"}, 40)]
 
 
 def oracle_routing(spec, inp):
