@@ -191,8 +191,22 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
                H <= 3 I (not with the small-batch row gather); with the FP8
                wide list, per list a G1 and a G2 launch (or one fused); 2 on
                the CUDA-core path
-      combine 1; a shared expert adds a grouped GEMM with its own plan."""
+      combine 1; a shared expert adds a grouped GEMM with its own plan.
+      Small batches under per-block dispatch: T <= 2 (bf16 or W8A16 FP8): the
+      routing launch, G1 and G2 as CUDA-core matrix-vector products (the
+      shared expert inside them) and the combine; bf16 with a shared expert at
+      T = 3, 4, or E <= 128 at T = 4..8: the one-launch layer.
+      W8A8: quantise xp, G1, quantise hact, G2 (every block one kernel)."""
     R = T * spec.K
+    if dispatch == 0 and T <= 2 and spec.act == "bf16" and spec.wdtype in ("bf16", "fp8"):
+        return 4
+    if (dispatch == 0 and spec.wdtype == "bf16" and spec.act == "bf16" and
+            ((spec.has_shared and T <= 4) or (spec.E <= 128 and 4 <= T <= 8))):
+        return 1
+    if spec.act == "fp8":
+        route = 2 if T <= 32 else (2 if T >= ROUTER_TC_MIN_T else 1) + 3
+        shared = 3 if spec.has_shared else 0  # its plan, G1, G2 (bf16 shared expert)
+        return route + 4 + shared + 1
 
     def ksplit(units, kdim):
         nk = -(-kdim // 64)

@@ -89,8 +89,11 @@ typedef enum {
   MOE_DISPATCH_PER_BLOCK = 0,  /* from the block's own m_size ([dispatch] after) */
   MOE_DISPATCH_GLOBAL_AVG = 1, /* from max(1, R/E) for every block ([dispatch] before) */
   MOE_DISPATCH_SIMT = 2,       /* every block on the CUDA-core kernel (cross-check) */
-  MOE_DISPATCH_ONE_LAUNCH = 3  /* moe_layer only: every batch of T <= 16 as one launch (see
+  MOE_DISPATCH_ONE_LAUNCH = 3, /* moe_layer only: every batch of T <= 16 as one launch (see
                                   moe_layer); blocks otherwise as MOE_DISPATCH_PER_BLOCK */
+  MOE_DISPATCH_GEMV = 4        /* moe_layer only: batches of T <= 4 with the expert GEMMs as
+                                  CUDA-core matrix-vector products (see moe_layer);
+                                  otherwise as MOE_DISPATCH_PER_BLOCK */
 } moe_dispatch_t;
 
 /* Variant codes reported per expert block. */
@@ -354,11 +357,18 @@ moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes);
  *              zero again.
  * Small batches ([router] "why" 1: at low concurrency launches and round trips
  * between them set the time; [permute] performance table):
+ *   - T <= 4 with bf16 or W8A16 FP8 experts, cfg->dispatch MOE_DISPATCH_GEMV,
+ *     or MOE_DISPATCH_PER_BLOCK with T <= 2 (where it measured fastest): the
+ *     fused routing launch, then G1 and G2 as CUDA-core matrix-vector
+ *     products (a warp streams whole weight rows, no K split; the shared
+ *     expert in the same two launches; [dispatch] "1. gemm.h": tiny blocks
+ *     skip the tiled GEMM), then the combine; blocks report the skinny
+ *     variant;
  *   - the whole layer -- router, top-K, permute, G1/G2, shared expert and the
  *     combine -- runs as ONE cooperative launch of one CTA per SM (bf16 expert
  *     weights, T <= 16) when cfg->dispatch is MOE_DISPATCH_ONE_LAUNCH, or,
  *     under MOE_DISPATCH_PER_BLOCK, where it measured faster than the
- *     multi-launch path: a shared expert with T <= 4, or E <= 128 with
+ *     multi-launch path: a shared expert with 3 <= T <= 4, or E <= 128 with
  *     4 <= T <= 8;
  *   - otherwise for T <= 32 the router, top-K, permute and the GEMM plan run
  *     as one fused launch, followed by the GEMM and combine launches.

@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "plan.cuh"
 
 namespace {
 
@@ -34,10 +35,11 @@ moe_status_t check_cfg(const moe_config_t* c) {
       c->wdtype != MOE_W8A8_FP8E4M3_B128)
     return MOE_ERR_UNSUPPORTED;
   if (c->wdtype == MOE_W8A8_FP8E4M3_B128 &&
-      (c->dispatch == MOE_DISPATCH_SIMT || c->dispatch == MOE_DISPATCH_ONE_LAUNCH))
+      (c->dispatch == MOE_DISPATCH_SIMT || c->dispatch == MOE_DISPATCH_ONE_LAUNCH ||
+       c->dispatch == MOE_DISPATCH_GEMV))
     return MOE_ERR_UNSUPPORTED;
   if (c->wdtype == MOE_W_MXFP4 && (c->H % 32 != 0 || c->I % 32 != 0)) return MOE_ERR_INVALID_ARG;
-  if (c->dispatch < MOE_DISPATCH_PER_BLOCK || c->dispatch > MOE_DISPATCH_ONE_LAUNCH)
+  if (c->dispatch < MOE_DISPATCH_PER_BLOCK || c->dispatch > MOE_DISPATCH_GEMV)
     return MOE_ERR_INVALID_ARG;
   if (c->m_skinny < -1) return MOE_ERR_INVALID_ARG;
   if (c->has_shared && (c->I_shared <= 0 || c->I_shared % 16 != 0)) return MOE_ERR_INVALID_ARG;
@@ -60,6 +62,20 @@ size_t decode_sync_offset(const moe_config_t* c) {
 // with E <= 128 from T = 4 to 8 (128 experts, K = 8: about even).  Elsewhere the
 // split-K reductions at the phase boundaries cost more than the launches they
 // save (128 experts at T = 1: 53 vs 44 us).
+// The CUDA-core matrix-vector decode path (gemv_decode.cu): forced by
+// MOE_DISPATCH_GEMV, taken under MOE_DISPATCH_PER_BLOCK where it measured
+// faster than the tensor-core paths (L2 flushed): T <= 2, every workload and
+// weight format (T = 1: Qwen3-30B-A3B shape 38.5 vs 42.7 us, GPT-OSS-20B FP8
+// 57.0 vs 66.2, shared-gate 48.8 vs 86.7, 896 experts 265.9 vs 278.2); at
+// T = 3, 4 the tensor-core paths were faster (e.g. 71.3 vs 79.5 us).
+bool use_gemv(const moe_config_t* c, int T) {
+  const int ms = c->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : c->m_skinny;
+  if (!gemv_supported(T, c->H, c->I, c->has_shared ? c->I_shared : 0, c->wdtype, ms))
+    return false;
+  if (c->dispatch == MOE_DISPATCH_GEMV) return true;
+  return c->dispatch == MOE_DISPATCH_PER_BLOCK && T <= 2;
+}
+
 bool one_launch(const moe_config_t* c, int T) {
   if (c->dispatch == MOE_DISPATCH_ONE_LAUNCH) return true;
   if (c->dispatch != MOE_DISPATCH_PER_BLOCK) return false;
@@ -320,7 +336,8 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
 
   int32_t* bvar = reinterpret_cast<int32_t*>(ws + L.block_variant);
   const int Is = cfg->has_shared ? cfg->I_shared : 0;
-  if (one_launch(cfg, T) &&
+  const bool gemv = use_gemv(cfg, T);
+  if (one_launch(cfg, T) && !gemv &&
       decode_layer_supported(T, E, K, H, cfg->I, Is, cfg->has_shared, cfg->wdtype, cfg->dispatch,
                              cfg->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : cfg->m_skinny)) {
     // small batch: the whole layer in one launch
@@ -354,6 +371,19 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
     a.done_ctr = reinterpret_cast<unsigned int*>(ws + L.sync);
     e = launch_route_decode(a, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (gemv) {
+      // the expert GEMMs as matrix-vector products, then the combine
+      const moe_plan::PlanView pv = moe_plan::plan_view(ws + L.gemm_scratch, R, E);
+      GemvArgs g;
+      g.x = x; g.T = T; g.H = H; g.I = cfg->I; g.K = K; g.Is = Is; g.wdtype = cfg->wdtype;
+      g.counts = pv.counts; g.items = pv.items[0];
+      g.row_to_flat = r2f; g.flat_to_row = f2r; g.ids = ids; g.weights = wts;
+      g.w1 = w->w1; g.w3 = w->w3; g.w2 = w->w2; g.s1 = w->s1; g.s3 = w->s3; g.s2 = w->s2;
+      g.hact = hact; g.y = y; g.sw1 = w->sw1; g.sw3 = w->sw3; g.sw2 = w->sw2;
+      g.shared_hact = ws + L.shared_hact; g.shared_y = ws + L.shared_y;
+      g.shared_gate = cfg->has_shared ? gsh : nullptr; g.out = out;
+      return cuda_status(launch_gemv_layer(g, stream));
+    }
   } else {
     e = T >= kRouterTcMinT
             ? launch_router_tc(x, w->wg, w->gate_bias, logits, T, H, G, ws + L.router_split,

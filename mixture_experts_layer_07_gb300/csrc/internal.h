@@ -70,6 +70,28 @@ cudaError_t launch_permute_copy(const void* x, const int32_t* flat_to_row, int T
 // grouped-GEMM plan in one launch.  done_ctr must be zero before the launch
 // and is zero again after it.
 constexpr int kRouteDecodeMaxT = 32;
+// Decode batches on the CUDA cores (gemv_decode.cu): G1 and G2 as
+// matrix-vector products over the plan's skinny list (x rows gathered through
+// row_to_flat), the shared expert riding in both launches, then the combine.
+constexpr int kGemvMaxT = 4;
+struct GemvArgs {
+  const void* x;
+  int T, H, I, K, Is, wdtype;
+  const int32_t* counts;  // the plan's list counts; items: its skinny list
+  const int4* items;
+  const int32_t *row_to_flat, *flat_to_row, *ids;
+  const float* weights;
+  const void *w1, *w3, *w2;
+  const float *s1, *s3, *s2;
+  void *hact, *y;
+  const void *sw1, *sw3, *sw2;
+  void *shared_hact, *shared_y;
+  const float* shared_gate;
+  void* out;
+};
+bool gemv_supported(int T, int H, int I, int Is, int wdtype, int m_skinny);
+cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t stream);
+
 struct RouteDecodeArgs {
   const void* x;
   const float* wg;

@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 
 MODE_SOFTMAX, MODE_SIGMOID_BIAS = 0, 1
 W_BF16, W_FP8, W_MXFP4, W8A8_FP8 = 0, 1, 2, 3
-DISPATCH_PER_BLOCK, DISPATCH_GLOBAL_AVG, DISPATCH_SIMT, DISPATCH_ONE_LAUNCH = 0, 1, 2, 3
+DISPATCH_PER_BLOCK, DISPATCH_GLOBAL_AVG, DISPATCH_SIMT, DISPATCH_ONE_LAUNCH, DISPATCH_GEMV = \
+    0, 1, 2, 3, 4
 VARIANT_SKIP, VARIANT_SKINNY, VARIANT_TILE, VARIANT_SIMT, VARIANT_WIDE = 0, 1, 2, 3, 4
 WIDE_MIN_ROWS = 129
 DEV_OK, DEV_BAD_EXPERT_ID, DEV_WAIT_TIMEOUT = 0, 1, 2

@@ -100,7 +100,7 @@ def test_workspace_sizes_grow_with_t_max(ops):
 
 
 @pytest.mark.parametrize("kw", [dict(H=100), dict(K=0), dict(K=9), dict(E=2048), dict(I=10),
-                                dict(mode=5), dict(wdtype=7), dict(dispatch=9), dict(dispatch=4),
+                                dict(mode=5), dict(wdtype=7), dict(dispatch=9), dict(dispatch=5),
                                 dict(m_skinny=-2), dict(has_shared=True, I_shared=0),
                                 dict(K=33, E=64)])
 def test_config_validation(ops, kw):
@@ -183,6 +183,7 @@ def test_grouped_gemm_rejects_bad_arguments(ops):
     assert g(w=0x1002) == 4
     assert g(m_skinny=-3) == 1
     assert g(dispatch=3) == 1
+    assert g(dispatch=4) == 1          # the GEMV decode path is a moe_layer option
 
 
 def test_unpermute_rejects_bad_arguments(ops):
@@ -229,3 +230,7 @@ def test_one_launch_dispatch_is_a_layer_option(ops):
     a = ops.workspace_bytes(_cfg(ops, dispatch=ops.DISPATCH_ONE_LAUNCH))
     b = ops.workspace_bytes(_cfg(ops))
     assert a == b > 0
+    # so is MOE_DISPATCH_GEMV, except with W8A8 (tensor cores only)
+    assert ops.workspace_bytes(_cfg(ops, dispatch=ops.DISPATCH_GEMV)) == b
+    with pytest.raises(ops.MoEError):
+        ops.workspace_bytes(_cfg(ops, dispatch=ops.DISPATCH_GEMV, wdtype=ops.W8A8_FP8))

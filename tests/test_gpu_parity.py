@@ -793,13 +793,33 @@ ONE_LAUNCH_CASES = [("qwen3_30b_a3b", {}, 1), ("qwen3_30b_a3b", {}, 2), ("qwen3_
 
 @pytest.mark.parametrize("name,over,T", ONE_LAUNCH_CASES, ids=case_id)
 def test_one_launch_layer(ops, name, over, T):
+    check_small_batch_layer(ops, name, over, T, ops.DISPATCH_ONE_LAUNCH, "one-launch")
+
+
+# The decode batches as CUDA-core matrix-vector products (moe_layer under
+# MOE_DISPATCH_GEMV): bf16 and FP8 experts, with and without the shared
+# expert, T = 1..4, the largest H (the token rows staged in shared memory)
+GEMV_CASES = [("qwen3_30b_a3b", {}, 1), ("qwen3_30b_a3b", {}, 2), ("qwen3_30b_a3b", {}, 3),
+              ("qwen3_30b_a3b", {}, 4), ("shared_gate", {}, 1), ("shared_gate", {}, 4),
+              ("gpt_oss_20b", {}, 1), ("gpt_oss_20b", {}, 4),
+              ("high_expert", {}, 1), ("high_expert", {"E": 512, "K": 9}, 4),
+              ("tiny", {}, 3), ("tiny", {"H": 2880, "I": 1440, "E": 4, "wdtype": "fp8"}, 2),
+              ("tiny", {"E": 40, "K": 3, "mode": 1, "routed_scale": 2.5,
+                        "sel_bias_var": 0.1}, 4)]
+
+
+@pytest.mark.parametrize("name,over,T", GEMV_CASES, ids=case_id)
+def test_gemv_decode_layer(ops, name, over, T):
+    check_small_batch_layer(ops, name, over, T, ops.DISPATCH_GEMV, "gemv")
+
+
+def check_small_batch_layer(ops, name, over, T, dispatch, tag):
     spec = SPECS[name].with_(**over)
     base = synth.host_inputs(spec, T, seed=17, weights=False)
     _, ids, _ = oracle_routing(spec, base)
     inp = synth.host_inputs(spec, T, seed=17, experts=sorted(set(ids.ravel().tolist())))
     t = U.layer_tensors(inp, inp["experts"])
-    layer = ops.MoELayer(U.config_for(ops, spec, T_max=max(T, 4),
-                                      dispatch=ops.DISPATCH_ONE_LAUNCH), t)
+    layer = ops.MoELayer(U.config_for(ops, spec, T_max=max(T, 4), dispatch=dispatch), t)
     out = layer(t["x"])
     sync()
     assert int(layer.dev_status.item()) == 0
@@ -819,14 +839,18 @@ def test_one_launch_layer(ops, name, over, T):
     assert np.array_equal(layer.view("offsets", torch.int32, (E + 1,)).cpu().numpy(), off)
     assert np.array_equal(layer.view("row_to_flat", torch.int32, (R,)).cpu().numpy(), r2f)
     assert np.array_equal(layer.view("flat_to_row", torch.int32, (R,)).cpu().numpy(), f2r)
-    want = [ops.block_variant(int(m), R, E, -1, 0, ops.W_BF16) for m in np.diff(off)]
+    want = [ops.block_variant(int(m), R, E, -1, 0, U.wdtype_of(ops, spec)) for m in np.diff(off)]
     assert layer.view("block_variant", torch.int32, (E,)).cpu().numpy().tolist() == want
     res = oracle.moe_layer_from_inputs(inp, logits_override=lg.astype(np.float64))
+    rel = 5e-2 if spec.wdtype == "fp8" else 2e-2
     U.assert_bf16_close(U.f64(layer.view("hact", torch.bfloat16, (R, spec.I))), res["hact"],
-                        2e-2, "one-launch hact")
-    U.assert_bf16_close(U.f64(layer.view("y", torch.bfloat16, (R, spec.H))), res["y"], 2e-2,
-                        "one-launch y")
-    U.assert_bf16_close(U.f64(out), res["out"], 2e-2, "one-launch out")
+                        rel, f"{tag} hact")
+    U.assert_bf16_close(U.f64(layer.view("y", torch.bfloat16, (R, spec.H))), res["y"], rel,
+                        f"{tag} y")
+    U.assert_bf16_close(U.f64(out), res["out"], rel, f"{tag} out")
+    if spec.has_shared:
+        U.assert_bf16_close(U.f64(layer.view("shared_y", torch.bfloat16, (T, spec.H))),
+                            res["shared_y"], 2e-2, f"{tag} shared_y")
     again = layer(t["x"])
     sync()
     assert torch.equal(again.view(torch.int16), out.view(torch.int16))
