@@ -1077,6 +1077,8 @@ def workload_spec(args):
     from mixture_experts_layer_07_gb300 import synth
 
     spec = synth.SPECS[args.workload]
+    if args.wdtype:
+        spec = spec.with_(wdtype=args.wdtype)
     if args.act == "fp8":
         spec = spec.with_(wdtype="fp8", act="fp8")
     elif args.act == "bf16":
@@ -1091,6 +1093,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_30b_a3b")
+    ap.add_argument("--wdtype", default=None, choices=["bf16", "fp8", "mxfp4"],
+                    help="expert weight format of the probed workload")
     ap.add_argument("--act", default=None, choices=["bf16", "fp8"],
                     help="expert-GEMM activations of the probed workload (fp8: W8A8, fp8 weights)")
     ap.add_argument("--T", type=int, default=2048)
