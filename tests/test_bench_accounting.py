@@ -30,7 +30,8 @@ def test_gemm_bytes_match_measured_dram_traffic():
     # two grouped-GEMM launches at that size is in profiles/traffic.json
     spec = synth.SPECS["qwen3_30b_a3b"]
     st = _bench().stage_bytes_flops(spec, 2048, None, spec.E)
-    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    recs = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["records"]
+    rec = next(r for r in recs if r["workload_name"] == "qwen3_30b_a3b" and r["T"] == 2048)
     measured = rec["traffic_bytes_per_step"]
     assert abs(st["grouped_gemm"]["bytes"] - measured) <= 0.01 * measured
 
