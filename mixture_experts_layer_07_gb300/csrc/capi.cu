@@ -358,7 +358,13 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
   const bool decode = T <= kRouteDecodeMaxT;
   bool planned = true;  // the grouped-GEMM plan was written by the routing launch
   cudaError_t e;
-  if (decode) {
+  // the matrix-vector path with E <= 128 and T * K <= 32: the logits alone
+  // here, G1's CTAs route the batch themselves
+  const bool gemv_route = decode && gemv && gemv_routes(T, E, K);
+  if (gemv_route) {
+    e = launch_router_gemm(x, w->wg, w->gate_bias, logits, T, H, G, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (decode) {
     // small batch: router + top-K + permute + GEMM plan in one launch
     RouteDecodeArgs a;
     a.x = x; a.wg = w->wg; a.gate_bias = w->gate_bias; a.logits = logits;
@@ -371,10 +377,12 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
     a.done_ctr = reinterpret_cast<unsigned int*>(ws + L.sync);
     e = launch_route_decode(a, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (decode) {
     if (gemv) {
       // the expert GEMMs as matrix-vector products, then the combine
       const moe_plan::PlanView pv = moe_plan::plan_view(ws + L.gemm_scratch, R, E);
-      GemvArgs g;
+      GemvArgs g{};
       g.x = x; g.T = T; g.H = H; g.I = cfg->I; g.K = K; g.Is = Is; g.wdtype = cfg->wdtype;
       g.counts = pv.counts; g.items = pv.items[0];
       g.row_to_flat = r2f; g.flat_to_row = f2r; g.ids = ids; g.weights = wts;
@@ -382,6 +390,17 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
       g.hact = hact; g.y = y; g.sw1 = w->sw1; g.sw3 = w->sw3; g.sw2 = w->sw2;
       g.shared_hact = ws + L.shared_hact; g.shared_y = ws + L.shared_y;
       g.shared_gate = cfg->has_shared ? gsh : nullptr; g.out = out;
+      g.route = gemv_route;
+      if (gemv_route) {
+        GemvRoute& rt = g.rt;
+        rt.logits = logits; rt.G = G; rt.E = E; rt.mode = cfg->mode;
+        rt.scale = cfg->routed_scale; rt.sel_bias = w->sel_bias; rt.ids = ids; rt.weights = wts;
+        rt.shared_gate = cfg->has_shared ? gsh : nullptr; rt.offsets = offsets;
+        rt.row_to_flat = r2f; rt.flat_to_row = f2r; rt.block_variant = bvar;
+        rt.plan_counts = pv.counts; rt.plan_items = pv.items[0]; rt.plan_done = pv.done[0];
+        rt.m_skinny = cfg->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : cfg->m_skinny;
+        rt.dispatch = cfg->dispatch;
+      }
       return cuda_status(launch_gemv_layer(g, stream));
     }
   } else {

@@ -15,14 +15,20 @@
 //      of W1 and W3 once, dots them with the block's token rows (x, staged in
 //      shared memory; the permuted copy xp is not needed) and writes
 //      hact = bf16(silu(g) * u).  The shared expert's features are more
-//      units of the same launch (all T tokens, weights sw1 / sw3).
+//      units of the same launch (all T tokens, weights sw1 / sw3).  With
+//      E <= 128 and T * K <= 32 the launch before G1 computes only the
+//      logits: every G1 CTA routes the batch itself (gemv_route: top-K per
+//      token, the stable permutation and the skinny plan in shared memory),
+//      which replaces the routing launch's serial tail (completion count,
+//      top-K, permute and plan in its last CTA: ~6 us of a 38 us layer at
+//      T = 1, 128 experts).
 //   G2 (gemv_g2_kernel): CTA units of (expert block, 64 output features): the
 //      block's hact rows staged in shared memory, each warp streams W2 rows
-//      two at a time -> y (bf16); the shared expert's rows likewise ->
+//      four at a time (two for T = 4) -> y (bf16); the shared expert's rows likewise ->
 //      shared_y.  Then the combine kernel.
-// Each warp keeps 16 row vectors per lane in flight (two rows, 8 each) before
-// it uses any, so a 2-CTA-per-SM grid holds ~128 KB of weights in flight per
-// SM.  Measured and not kept (Qwen3-30B-A3B shape, T = 1, L2 flushed): a G2
+// Each warp keeps 16 row vectors per lane in flight (G1: two rows, 8 each;
+// G2: four rows, 4 each, or two, 8 each) before it uses any, so a 2-CTA-per-SM grid holds up
+// to ~128 KB of weights in flight per SM.  Measured and not kept (Qwen3-30B-A3B shape, T = 1, L2 flushed): a G2
 // warp per (token, feature) running the token's K picks in turn with the
 // combine fused in (K dependent row loads per warp), and feeding the rows by
 // bulk copies on the TMA engine into per-warp shared-memory slot rings
@@ -35,6 +41,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "plan.cuh"
+#include "topk_warp.cuh"
 
 namespace {
 
@@ -60,52 +67,105 @@ MOE_DEVICE void e4m3x16_to_f32(const uint4& v, float s, float* f) {
   }
 }
 
-// Dot products of one or two weight rows (bf16, or e4m3 with block scales;
-// `two`: rb/sb too) of length n with up to MT activation rows, lane-strided;
-// per-lane partial sums in ga[j] (row a) and gb[j] (row b).  Loads go out in
-// batches of 8 vectors per lane and row (16 in flight per lane for two rows)
-// before any of them is used.  act(j, e0, a) loads 8 activations of token j
-// from element e0.  WQ: 0 bf16 (8 weights per 16-byte vector), 1 e4m3 (16).
-template <int WQ, int MT, typename Act>
-MOE_DEVICE void row_dots(const void* ra, const void* rb, const float* sa, const float* sb,
-                         bool two, int n, int m, Act act, float (&ga)[MT], float (&gb)[MT]) {
-  constexpr int kPer = WQ ? 16 : 8;  // weights per 16-byte vector
-  constexpr int kB = 8;              // vectors per lane and row in one batch
-  const int lane = lane_id();
-  const uint4* a4 = static_cast<const uint4*>(ra);
-  const uint4* b4 = static_cast<const uint4*>(rb);
-  const int nv = n / kPer;
-  for (int v0 = lane; v0 < nv; v0 += 32 * kB) {
-    uint4 va[kB], vb[kB];
+// 8 weights of a 16-byte vector as floats: bf16 (the whole vector), or e4m3
+// codes 8*half .. 8*half+7 times the block scale sc
+template <int WQ>
+MOE_DEVICE void weights8(const uint4& v, int half, float sc, float* f) {
+  if (WQ == 0) {
+    bf16x8_to_f32(v, f);
+  } else {
+    const uint32_t w[2] = {half ? v.z : v.x, half ? v.w : v.y};
 #pragma unroll
-    for (int q = 0; q < kB; ++q) {
-      const int v = v0 + 32 * q;
-      va[q] = v < nv ? __ldcs(a4 + v) : make_uint4(0u, 0u, 0u, 0u);
-      vb[q] = (two && v < nv) ? __ldcs(b4 + v) : make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
+            static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
+        const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        f[4 * i + 2 * h] = p.x * sc;
+        f[4 * i + 2 * h + 1] = p.y * sc;
+      }
+    }
+  }
+}
+
+// Dot products of nr <= NR weight rows (row i at byte r0 + i * rs; bf16, or
+// e4m3 with its block-scale row at s0 + i * ss) of length n with up to MT
+// activation rows, lane-strided 16-byte
+// vectors; per-lane partial sums in acc[i][j] (row i, token j), each summed in
+// element order.  Every lane loads KB vectors of each row (NR * KB in flight)
+// before it uses any.  act(j, e0, a) loads 8 activations of token j from
+// element e0.  WQ: 0 bf16 (8 weights per vector), 1 e4m3 (16).
+template <int WQ, int MT, int NR, int KB, typename Act>
+MOE_DEVICE void rows_dot(const void* r0, ptrdiff_t rs, const float* s0, ptrdiff_t ss, int nr,
+                         int n, int m, Act act, float (&acc)[NR][MT]) {
+  constexpr int kPer = WQ ? 16 : 8;  // weights per 16-byte vector
+  const int lane = lane_id();
+  const int nv = n / kPer;
+  for (int v0 = lane; v0 < nv; v0 += 32 * KB) {
+    uint4 vv[NR][KB];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+#pragma unroll
+      for (int q = 0; q < KB; ++q) {
+        const int v = v0 + 32 * q;
+        const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(r0) + i * rs);
+        vv[i][q] = (i < nr && v < nv) ? __ldcs(row + v) : make_uint4(0u, 0u, 0u, 0u);
+      }
     }
 #pragma unroll
-    for (int q = 0; q < kB; ++q) {
+    for (int q = 0; q < KB; ++q) {
       const int v = v0 + 32 * q;
       if (v >= nv) break;
-      float wa[kPer], wb[kPer];
-      if (WQ) {
-        e4m3x16_to_f32(va[q], __ldg(sa + (kPer * v) / 128), wa);
-        if (two) e4m3x16_to_f32(vb[q], __ldg(sb + (kPer * v) / 128), wb);
-      } else {
-        bf16x8_to_f32(va[q], wa);
-        if (two) bf16x8_to_f32(vb[q], wb);
+      float sc[NR];
+#pragma unroll
+      for (int i = 0; i < NR; ++i) sc[i] = (WQ && i < nr) ? __ldg(s0 + i * ss + (kPer * v) / 128) : 1.f;
+      if constexpr (NR <= 2) {
+        // the rows' weights once, each token's activations once per 8
+        float w[NR][kPer];
+#pragma unroll
+        for (int i = 0; i < NR; ++i)
+#pragma unroll
+          for (int p = 0; p < kPer; p += 8)
+            if (i < nr) weights8<WQ>(vv[i][q], p / 8, sc[i], &w[i][p]);
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+          if (j < m) {
+#pragma unroll
+            for (int p = 0; p < kPer; p += 8) {
+              float a[8];
+              act(j, kPer * v + p, a);
+#pragma unroll
+              for (int i = 0; i < NR; ++i) {
+                if (i < nr) {
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) acc[i][j] = fmaf(w[i][p + c], a[c], acc[i][j]);
+                }
+              }
+            }
+          }
+        }
+        continue;
       }
+      // four rows: every token's 8 activations once, each row's
+      // 8 weights once per 8
 #pragma unroll
-      for (int j = 0; j < MT; ++j) {
-        if (j < m) {
+      for (int p = 0; p < kPer; p += 8) {
+        float a[MT][8];
 #pragma unroll
-          for (int p = 0; p < kPer; p += 8) {
-            float a[8];
-            act(j, kPer * v + p, a);
+        for (int j = 0; j < MT; ++j)
+          if (j < m) act(j, kPer * v + p, a[j]);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              ga[j] = fmaf(wa[p + c], a[c], ga[j]);
-              if (two) gb[j] = fmaf(wb[p + c], a[c], gb[j]);
+        for (int i = 0; i < NR; ++i) {
+          if (i < nr) {
+            float w[8];
+            weights8<WQ>(vv[i][q], p / 8, sc[i], w);
+#pragma unroll
+            for (int j = 0; j < MT; ++j) {
+              if (j < m) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[i][j] = fmaf(w[c], a[j][c], acc[i][j]);
+              }
             }
           }
         }
@@ -121,9 +181,91 @@ MOE_DEVICE float warp_sum(float v) {
   return __shfl_sync(0xffffffffu, v, 0);
 }
 
+// The batch's routing inside a G1 CTA (kRoute): warps 0..T-1 route one token
+// each from the logits (warp_topk, the same selection and weights as the
+// routing kernels), then warp 0 sorts the R = T*K <= 32 replicas stably by
+// expert with lane ballots: replica f (lane f, expert e) goes to row
+// (replicas with a smaller expert) + (earlier replicas with expert e), the
+// counting-sort permutation of the permute stage; each expert's first replica
+// writes its skinny item {e, first row, rows, 0} at (experts below e that
+// occur).  CTA 0 writes everything the later launches and the workspace hold:
+// ids, weights, shared gate, offsets, both permutation maps, per-expert
+// variant and the plan (every occurring expert is skinny: m <= T <= m_skinny).
+struct RouteSmem {
+  int32_t ids[32];
+  float w[32];
+  int4 items[32];
+  int32_t r2f[32];
+  int n_items;
+};
+
+MOE_DEVICE void gemv_route(const GemvRoute& rt, int T, int K, int wdtype, RouteSmem& rs) {
+  const int warp = warp_id(), lane = lane_id();
+  const bool cta0 = blockIdx.x == 0;
+  if (warp < T) {
+    const float* row = rt.logits + (size_t)warp * rt.G;
+    if (cta0)
+      moe_route::warp_topk<4, 4, true>(row, rt.sel_bias, rt.E, K, rt.mode, rt.scale,
+                                       rt.ids + (size_t)warp * K, rt.weights + (size_t)warp * K,
+                                       rs.ids + warp * K);
+    else
+      moe_route::warp_topk<4, 4, true>(row, rt.sel_bias, rt.E, K, rt.mode, rt.scale,
+                                       rs.ids + warp * K, rs.w + warp * K);
+    if (cta0 && rt.shared_gate && lane == 0)
+      rt.shared_gate[warp] = moe_route::sigmoid_key(__ldcg(row + rt.E));
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  const int R = T * K;
+  const int e = lane < R ? rs.ids[lane] : 0x7fffffff;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  const bool lead = lane < R && rank == 0;
+  const unsigned leads = __ballot_sync(0xffffffffu, lead);
+  int less = 0, idx = 0;
+  for (int g = 0; g < R; ++g) {
+    const int eg = __shfl_sync(0xffffffffu, e, g);
+    less += eg < e;
+    idx += (eg < e) && ((leads >> g) & 1u);
+  }
+  const int row = less + rank;
+  if (lane < R) {
+    rs.r2f[row] = lane;
+    if (cta0) {
+      rt.row_to_flat[row] = lane;
+      rt.flat_to_row[lane] = row;
+    }
+  }
+  if (lead) {
+    const int4 it = make_int4(e, less, __popc(peers), 0);
+    rs.items[idx] = it;
+    if (cta0) {
+      rt.plan_items[idx] = it;
+      rt.plan_done[idx] = 0;
+    }
+  }
+  if (lane == 0) rs.n_items = __popc(leads);
+  if (cta0) {
+    if (lane < moe_plan::kLists) rt.plan_counts[lane] = lane == 0 ? __popc(leads) : 0;
+    if (lane < 2 * moe_plan::kLists) rt.plan_counts[moe_plan::kSchedBase + lane] = 0;
+    for (int x = lane; x <= rt.E; x += 32) {
+      int lt = 0, eq = 0;
+      for (int g = 0; g < R; ++g) {
+        const int eg = rs.ids[g];
+        lt += eg < x;
+        eq += eg == x;
+      }
+      rt.offsets[x] = lt;
+      if (x < rt.E)
+        rt.block_variant[x] = moe_variant_of(eq, R, rt.E, rt.m_skinny, rt.dispatch, wdtype);
+    }
+  }
+}
+
 // G1.  units: n_items * I routed (items = the plan's skinny list) + Is shared;
-// MT >= the rows of any block (the batch size T).
-template <int WQ, int MT>
+// MT >= the rows of any block (the batch size T).  kRoute: the CTA routes the
+// batch first (gemv_route) and takes items and rows from that.
+template <int WQ, int MT, bool kRoute>
 __global__ void __launch_bounds__(32 * kWarps, 2)
 gemv_g1_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int I, int K,
                const int32_t* __restrict__ counts, const int4* __restrict__ items,
@@ -131,16 +273,25 @@ gemv_g1_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int I, int K,
                const void* __restrict__ w3, const float* __restrict__ s1,
                const float* __restrict__ s3, __nv_bfloat16* __restrict__ hact, int Is,
                const __nv_bfloat16* __restrict__ sw1, const __nv_bfloat16* __restrict__ sw3,
-               __nv_bfloat16* __restrict__ shared_hact) {
+               __nv_bfloat16* __restrict__ shared_hact, int wdtype, GemvRoute rt) {
   extern __shared__ uint4 xs[];  // the T token rows, H bf16 each
+  __shared__ RouteSmem rs;
   pdl_wait();
   pdl_trigger();
   const int H8 = H / 8;
   const uint4* x4 = reinterpret_cast<const uint4*>(x);
-  for (int i = threadIdx.x; i < T * H8; i += blockDim.x) xs[i] = __ldg(x4 + i);
+  if (kRoute) {
+    // warps T.. stage the token rows while warps 0..T-1 route
+    const int t0 = 32 * T;
+    for (int i = (int)threadIdx.x - t0; i >= 0 && i < T * H8; i += (int)blockDim.x - t0)
+      xs[i] = __ldg(x4 + i);
+    gemv_route(rt, T, K, wdtype, rs);
+  } else {
+    for (int i = threadIdx.x; i < T * H8; i += blockDim.x) xs[i] = __ldg(x4 + i);
+  }
   __syncthreads();
   const int lane = lane_id();
-  const int n_items = counts[0];
+  const int n_items = kRoute ? rs.n_items : counts[0];
   const long long routed = (long long)n_items * I;
   const long long total = routed + Is;
   const int KBh = (H + 127) / 128, NBi = (I + 127) / 128;
@@ -153,12 +304,14 @@ gemv_g1_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int I, int K,
     __nv_bfloat16* dst;
     int ld_dst, row0;
     if (u < routed) {
-      const int4 it = __ldg(items + u / I);  // {expert, first row, rows, -}
+      // {expert, first row, rows, -}
+      const int4 it = kRoute ? rs.items[u / I] : __ldg(items + u / I);
       f = (int)(u % I);
       e = it.x;
       m = it.z < MT ? it.z : MT;
 #pragma unroll
-      for (int j = 0; j < MT; ++j) tok[j] = j < m ? __ldg(row_to_flat + it.y + j) / K : 0;
+      for (int j = 0; j < MT; ++j)
+        tok[j] = j < m ? (kRoute ? rs.r2f[it.y + j] : __ldg(row_to_flat + it.y + j)) / K : 0;
       const size_t row = (size_t)e * I + f;
       ra = WQ ? (const void*)(static_cast<const uint8_t*>(w1) + row * H)
               : (const void*)(static_cast<const __nv_bfloat16*>(w1) + row * H);
@@ -185,18 +338,20 @@ gemv_g1_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int I, int K,
     auto act = [&](int j, int e0, float* a) {
       bf16x8_to_f32(xs[(tok[j] * H + e0) / 8], a);
     };
-    float g[MT], up[MT];
+    float acc[2][MT];  // gate (W1) and up (W3) partial sums per token
 #pragma unroll
-    for (int j = 0; j < MT; ++j) g[j] = up[j] = 0.f;
+    for (int j = 0; j < MT; ++j) acc[0][j] = acc[1][j] = 0.f;
+    // row b and its scales at a fixed distance from row a
+    const ptrdiff_t rs = static_cast<const uint8_t*>(rb) - static_cast<const uint8_t*>(ra);
     if (WQ && u < routed)
-      row_dots<1, MT>(ra, rb, sa, sb, true, H, m, act, g, up);
+      rows_dot<1, MT, 2, 8>(ra, rs, sa, sb - sa, 2, H, m, act, acc);
     else
-      row_dots<0, MT>(ra, rb, nullptr, nullptr, true, H, m, act, g, up);
+      rows_dot<0, MT, 2, 8>(ra, rs, nullptr, 0, 2, H, m, act, acc);
     float hv = 0.f;
 #pragma unroll
     for (int j = 0; j < MT; ++j) {
       if (j < m) {  // m is the same in every lane
-        const float gs = warp_sum(g[j]), us = warp_sum(up[j]);
+        const float gs = warp_sum(acc[0][j]), us = warp_sum(acc[1][j]);
         if (lane == j) hv = silu(gs) * us;
       }
     }
@@ -207,8 +362,13 @@ gemv_g1_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int I, int K,
 // G2.  CTA units: (expert block, 64 output features) routed, then (64 output
 // features) of the shared expert.  The CTA stages the block's hact rows (the
 // shared expert: all T shared_hact rows) in shared memory once; each warp
-// then streams 8 rows of W2, two at a time, dotted with the staged rows.
+// then streams 8 rows of W2, four at a time (two for four tokens), dotted
+// with the staged rows.
 constexpr int kG2Rows = 64;
+// W2 rows a warp streams at once, and vectors per lane and row in a batch
+// (16 in flight per lane); four tokens keep two rows (registers)
+template <int MT>
+constexpr int g2_per() { return MT <= 2 ? 4 : 2; }
 template <int WQ, int MT>
 __global__ void __launch_bounds__(32 * kWarps, 2)
 gemv_g2_kernel(const __nv_bfloat16* __restrict__ hact, int T, int H, int I,
@@ -238,41 +398,51 @@ gemv_g2_kernel(const __nv_bfloat16* __restrict__ hact, int T, int H, int I,
     __syncthreads();
     auto act = [&](int j, int e0, float* a) { bf16x8_to_f32(hs[(j * n + e0) / 8], a); };
     __nv_bfloat16* dst = sh ? shared_y : y + (size_t)it.y * H;
-    for (int r = warp * 2; r < kG2Rows; r += 2 * kWarps) {
+    constexpr int kG2Per = g2_per<MT>(), kG2Batch = 16 / kG2Per;
+    for (int r = warp * kG2Per; r < kG2Rows; r += kG2Per * kWarps) {
       const int h0 = hb * kG2Rows + r;
       if (h0 >= H) break;
-      const bool two = h0 + 1 < H;
-      float a0[MT], a1[MT];
-#pragma unroll
-      for (int j = 0; j < MT; ++j) a0[j] = a1[j] = 0.f;
+      const int nr = H - h0 < kG2Per ? H - h0 : kG2Per;  // the same in every lane
+      // nr consecutive rows h0.. (h0 % 4 == 0: one 128-row scale block)
+      const void* r0;
+      ptrdiff_t rs;
+      const float* s0 = nullptr;
       if (sh) {
-        row_dots<0, MT>(sw2 + (size_t)h0 * Is, sw2 + (size_t)(h0 + (two ? 1 : 0)) * Is, nullptr,
-                        nullptr, two, Is, m, act, a0, a1);
+        r0 = sw2 + (size_t)h0 * Is;
+        rs = (ptrdiff_t)Is * 2;
       } else if (WQ) {
-        const uint8_t* w = static_cast<const uint8_t*>(w2) + ((size_t)it.x * H + h0) * I;
-        const float* sr = s2 + ((size_t)it.x * NBh + h0 / 128) * KBi;
-        const float* sr1 = s2 + ((size_t)it.x * NBh + (h0 + 1) / 128) * KBi;
-        row_dots<1, MT>(w, w + (two ? I : 0), sr, two ? sr1 : sr, two, I, m, act, a0, a1);
+        r0 = static_cast<const uint8_t*>(w2) + ((size_t)it.x * H + h0) * I;
+        rs = I;
+        s0 = s2 + ((size_t)it.x * NBh + h0 / 128) * KBi;
       } else {
-        const __nv_bfloat16* w =
-            static_cast<const __nv_bfloat16*>(w2) + ((size_t)it.x * H + h0) * I;
-        row_dots<0, MT>(w, w + (two ? I : 0), nullptr, nullptr, two, I, m, act, a0, a1);
+        r0 = static_cast<const __nv_bfloat16*>(w2) + ((size_t)it.x * H + h0) * I;
+        rs = (ptrdiff_t)I * 2;
       }
-      float v0 = 0.f, v1 = 0.f;
+      float acc[kG2Per][MT];
 #pragma unroll
-      for (int j = 0; j < MT; ++j) {
-        if (j < m) {
-          const float s0 = warp_sum(a0[j]);
-          const float s1 = two ? warp_sum(a1[j]) : 0.f;
-          if (lane == j) {
-            v0 = s0;
-            v1 = s1;
+      for (int i = 0; i < kG2Per; ++i)
+#pragma unroll
+        for (int j = 0; j < MT; ++j) acc[i][j] = 0.f;
+      if (sh)
+        rows_dot<0, MT, kG2Per, kG2Batch>(r0, rs, nullptr, 0, nr, Is, m, act, acc);
+      else
+        rows_dot<WQ, MT, kG2Per, kG2Batch>(r0, rs, s0, 0, nr, I, m, act, acc);
+      float v[kG2Per];
+#pragma unroll
+      for (int i = 0; i < kG2Per; ++i) {
+        v[i] = 0.f;
+#pragma unroll
+        for (int j = 0; j < MT; ++j) {
+          if (i < nr && j < m) {
+            const float sum = warp_sum(acc[i][j]);
+            if (lane == j) v[i] = sum;
           }
         }
       }
       if (lane < m) {
-        dst[(size_t)lane * H + h0] = __float2bfloat16_rn(v0);
-        if (two) dst[(size_t)lane * H + h0 + 1] = __float2bfloat16_rn(v1);
+#pragma unroll
+        for (int i = 0; i < kG2Per; ++i)
+          if (i < nr) dst[(size_t)lane * H + h0 + i] = __float2bfloat16_rn(v[i]);
       }
     }
   }
@@ -299,21 +469,30 @@ int gemv_grid(Kern kernel, size_t smem) {
   return moe_num_sms() * per_sm;
 }
 
+template <int WQ, int MT, bool kRoute>
+cudaError_t launch_g1(const GemvArgs& a, cudaStream_t stream) {
+  // the limit is raised once, to the largest size a call may stage
+  static std::atomic<unsigned long long> set{0};
+  const cudaError_t e = moe_raise_smem(gemv_g1_kernel<WQ, MT, kRoute>, kMaxSmem, set);
+  if (e != cudaSuccess) return e;
+  const size_t smem = (size_t)a.T * a.H * 2;
+  return moe_launch(gemv_g1_kernel<WQ, MT, kRoute>,
+                    dim3(gemv_grid(gemv_g1_kernel<WQ, MT, kRoute>, smem)), dim3(32 * kWarps), smem,
+                    stream, 1, static_cast<const __nv_bfloat16*>(a.x), a.T, a.H, a.I, a.K,
+                    a.counts, a.items, a.row_to_flat, a.w1, a.w3, a.s1, a.s3,
+                    static_cast<__nv_bfloat16*>(a.hact), a.Is,
+                    static_cast<const __nv_bfloat16*>(a.sw1),
+                    static_cast<const __nv_bfloat16*>(a.sw3),
+                    static_cast<__nv_bfloat16*>(a.shared_hact), a.wdtype, a.rt);
+}
+
 template <int WQ, int MT>
 cudaError_t launch_wq(const GemvArgs& a, cudaStream_t stream) {
-  // the limits are raised once, to the largest sizes a call may stage
-  static std::atomic<unsigned long long> set1{0}, set2{0};
-  cudaError_t e = moe_raise_smem(gemv_g1_kernel<WQ, MT>, kMaxSmem, set1);
+  // the limit is raised once, to the largest size a call may stage
+  static std::atomic<unsigned long long> set2{0};
+  cudaError_t e = moe_raise_smem(gemv_g2_kernel<WQ, MT>, kMaxSmem, set2);
   if (e != cudaSuccess) return e;
-  e = moe_raise_smem(gemv_g2_kernel<WQ, MT>, kMaxSmem, set2);
-  if (e != cudaSuccess) return e;
-  const size_t smem1 = (size_t)a.T * a.H * 2;
-  e = moe_launch(gemv_g1_kernel<WQ, MT>, dim3(gemv_grid(gemv_g1_kernel<WQ, MT>, smem1)),
-                 dim3(32 * kWarps), smem1, stream, 1,
-                 static_cast<const __nv_bfloat16*>(a.x), a.T, a.H, a.I, a.K, a.counts, a.items,
-                 a.row_to_flat, a.w1, a.w3, a.s1, a.s3, static_cast<__nv_bfloat16*>(a.hact), a.Is,
-                 static_cast<const __nv_bfloat16*>(a.sw1), static_cast<const __nv_bfloat16*>(a.sw3),
-                 static_cast<__nv_bfloat16*>(a.shared_hact));
+  e = a.route ? launch_g1<WQ, MT, true>(a, stream) : launch_g1<WQ, MT, false>(a, stream);
   if (e != cudaSuccess) return e;
   const size_t smem2 = (size_t)a.T * (a.I > a.Is ? a.I : a.Is) * 2;
   e = moe_launch(gemv_g2_kernel<WQ, MT>, dim3(gemv_grid(gemv_g2_kernel<WQ, MT>, smem2)),
@@ -343,7 +522,12 @@ bool gemv_supported(int T, int H, int I, int Is, int wdtype, int m_skinny) {
          (wdtype == MOE_W_BF16 || wdtype == MOE_W_FP8E4M3_B128);
 }
 
+bool gemv_routes(int T, int E, int K) {
+  return T >= 1 && T <= kGemvMaxT && E >= 1 && E <= 128 && K >= 1 && T * K <= 32;
+}
+
 cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t stream) {
+  if (a.route && !gemv_routes(a.T, a.rt.E, a.K)) return cudaErrorInvalidValue;
   if (a.wdtype == MOE_W_FP8E4M3_B128) return launch_t<1>(a, stream);
   return launch_t<0>(a, stream);
 }

@@ -74,6 +74,22 @@ constexpr int kRouteDecodeMaxT = 32;
 // matrix-vector products over the plan's skinny list (x rows gathered through
 // row_to_flat), the shared expert riding in both launches, then the combine.
 constexpr int kGemvMaxT = 4;
+// The routing that G1's CTAs run themselves (gemv_routes): every CTA routes
+// the batch from the logits, CTA 0 writes the results below for the later
+// launches and the workspace.
+struct GemvRoute {
+  const float* logits;  // [T][G]
+  int G, E, mode;
+  float scale;
+  const float* sel_bias;
+  int32_t* ids;
+  float *weights, *shared_gate;  // shared_gate nullable
+  int32_t *offsets, *row_to_flat, *flat_to_row, *block_variant;
+  int32_t* plan_counts;  // the plan head, its skinny list and done flags
+  int4* plan_items;
+  int32_t* plan_done;
+  int m_skinny, dispatch;
+};
 struct GemvArgs {
   const void* x;
   int T, H, I, K, Is, wdtype;
@@ -88,8 +104,12 @@ struct GemvArgs {
   void *shared_hact, *shared_y;
   const float* shared_gate;
   void* out;
+  bool route;  // G1 routes the batch itself (rt), after the logits-only router
+  GemvRoute rt;
 };
 bool gemv_supported(int T, int H, int I, int Is, int wdtype, int m_skinny);
+// G1 can route the batch itself: E <= 128 and T * K <= 32
+bool gemv_routes(int T, int E, int K);
 cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t stream);
 
 struct RouteDecodeArgs {
