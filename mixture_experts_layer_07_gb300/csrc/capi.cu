@@ -358,8 +358,8 @@ moe_status_t moe_layer(const moe_config_t* cfg, int T, const void* x, const moe_
   const bool decode = T <= kRouteDecodeMaxT;
   bool planned = true;  // the grouped-GEMM plan was written by the routing launch
   cudaError_t e;
-  // the matrix-vector path with E <= 128 and T * K <= 32: the logits alone
-  // here, G1's CTAs route the batch themselves
+  // the matrix-vector path where G1's CTAs can route the batch themselves
+  // (gemv_routes): the logits alone here
   const bool gemv_route = decode && gemv && gemv_routes(T, E, K);
   if (gemv_route) {
     e = launch_router_gemm(x, w->wg, w->gate_bias, logits, T, H, G, stream);

@@ -108,7 +108,8 @@ struct GemvArgs {
   GemvRoute rt;
 };
 bool gemv_supported(int T, int H, int I, int Is, int wdtype, int m_skinny);
-// G1 can route the batch itself: E <= 128 and T * K <= 32
+// G1 can route the batch itself: T * K <= 32, and E <= 128 or (K <= 16 and
+// E <= 4096 / T', T' = T rounded up to a power of two)
 bool gemv_routes(int T, int E, int K);
 cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t stream);
 

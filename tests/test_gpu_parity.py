@@ -805,7 +805,13 @@ GEMV_CASES = [("qwen3_30b_a3b", {}, 1), ("qwen3_30b_a3b", {}, 2), ("qwen3_30b_a3
               ("high_expert", {}, 1), ("high_expert", {"E": 512, "K": 9}, 4),
               ("tiny", {}, 3), ("tiny", {"H": 2880, "I": 1440, "E": 4, "wdtype": "fp8"}, 2),
               ("tiny", {"E": 40, "K": 3, "mode": 1, "routed_scale": 2.5,
-                        "sel_bias_var": 0.1}, 4)]
+                        "sel_bias_var": 0.1}, 4),
+              # more than 128 experts: the G1 CTAs' sliced routing with 8, 4
+              # and 2 slices per token (T = 1, 2, 3), slices past E
+              ("shared_gate", {}, 2), ("shared_gate", {}, 3), ("high_expert", {}, 2),
+              ("tiny", {"E": 300, "K": 5}, 2),
+              ("tiny", {"E": 257, "K": 7, "mode": 1, "routed_scale": 2.5,
+                        "sel_bias_var": 0.1}, 3)]
 
 
 @pytest.mark.parametrize("name,over,T", GEMV_CASES, ids=case_id)
