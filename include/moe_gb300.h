@@ -357,13 +357,16 @@ moe_status_t moe_workspace_bytes(const moe_config_t* cfg, size_t* bytes);
  *              zero again.
  * Small batches ([router] "why" 1: at low concurrency launches and round trips
  * between them set the time; [permute] performance table):
- *   - T <= 4 with bf16 or W8A16 FP8 experts, cfg->dispatch MOE_DISPATCH_GEMV,
- *     or MOE_DISPATCH_PER_BLOCK with T <= 2 (where it measured fastest): the
- *     fused routing launch, then G1 and G2 as CUDA-core matrix-vector
- *     products (a warp streams whole weight rows, no K split; the shared
- *     expert in the same two launches; [dispatch] "1. gemm.h": tiny blocks
- *     skip the tiled GEMM), then the combine; blocks report the skinny
- *     variant;
+ *   - T <= 4 with bf16, W8A16 FP8 or MXFP4 experts, cfg->dispatch
+ *     MOE_DISPATCH_GEMV, or MOE_DISPATCH_PER_BLOCK with T <= 2 (MXFP4: T = 1;
+ *     where it measured fastest): G1 and G2 as CUDA-core matrix-vector products (a
+ *     warp streams whole weight rows, no K split; the shared expert in the
+ *     same two launches; [dispatch] "1. gemm.h": tiny blocks skip the tiled
+ *     GEMM), then the combine; blocks report the skinny variant.  Where
+ *     T * K <= 32 and E <= 128 (or K <= 16 and E <= 4096 / T rounded up to a
+ *     power of two) the first launch computes only the logits and every G1
+ *     CTA routes the batch itself (top-K, permutation and plan, CTA 0 writing
+ *     them to the workspace); otherwise the fused routing launch comes first;
  *   - the whole layer -- router, top-K, permute, G1/G2, shared expert and the
  *     combine -- runs as ONE cooperative launch of one CTA per SM (bf16 expert
  *     weights, T <= 16) when cfg->dispatch is MOE_DISPATCH_ONE_LAUNCH, or,

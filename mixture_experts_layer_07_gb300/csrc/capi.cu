@@ -64,16 +64,18 @@ size_t decode_sync_offset(const moe_config_t* c) {
 // save (128 experts at T = 1: 53 vs 44 us).
 // The CUDA-core matrix-vector decode path (gemv_decode.cu): forced by
 // MOE_DISPATCH_GEMV, taken under MOE_DISPATCH_PER_BLOCK where it measured
-// faster than the tensor-core paths (L2 flushed): T <= 2, every workload and
-// weight format (T = 1: Qwen3-30B-A3B shape 38.5 vs 42.7 us, GPT-OSS-20B FP8
-// 57.0 vs 66.2, shared-gate 48.8 vs 86.7, 896 experts 265.9 vs 278.2); at
-// T = 3, 4 the tensor-core paths were faster (e.g. 71.3 vs 79.5 us).
+// faster than the tensor-core paths (L2 flushed): T <= 2 for bf16 and FP8
+// weights, T = 1 for MXFP4 (T = 1: Qwen3-30B-A3B shape 33.4 vs 44.7 us,
+// GPT-OSS-20B FP8 54.3 vs 65.8, shared-gate 42.6 vs 86.7, 896 experts 241.3
+// vs 280.2); at T = 3, 4 the tensor-core paths were faster (e.g. 71.3 vs
+// 79.5 us).
 bool use_gemv(const moe_config_t* c, int T) {
   const int ms = c->m_skinny < 0 ? MOE_DEFAULT_M_SKINNY : c->m_skinny;
   if (!gemv_supported(T, c->H, c->I, c->has_shared ? c->I_shared : 0, c->wdtype, ms))
     return false;
   if (c->dispatch == MOE_DISPATCH_GEMV) return true;
-  return c->dispatch == MOE_DISPATCH_PER_BLOCK && T <= 2;
+  // MXFP4 (GPT-OSS-20B shape): T = 1 58.4 vs 66.8 us, T = 2 86.9 vs 85.3
+  return c->dispatch == MOE_DISPATCH_PER_BLOCK && T <= (c->wdtype == MOE_W_MXFP4 ? 1 : 2);
 }
 
 bool one_launch(const moe_config_t* c, int T) {

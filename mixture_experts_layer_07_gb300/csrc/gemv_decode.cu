@@ -15,27 +15,36 @@
 //      of W1 and W3 once, dots them with the block's token rows (x, staged in
 //      shared memory; the permuted copy xp is not needed) and writes
 //      hact = bf16(silu(g) * u).  The shared expert's features are more
-//      units of the same launch (all T tokens, weights sw1 / sw3).  With
-//      E <= 128 and T * K <= 32 the launch before G1 computes only the
-//      logits: every G1 CTA routes the batch itself (gemv_route: top-K per
-//      token, the stable permutation and the skinny plan in shared memory),
-//      which replaces the routing launch's serial tail (completion count,
-//      top-K, permute and plan in its last CTA: ~6 us of a 38 us layer at
-//      T = 1, 128 experts).
+//      units of the same launch (all T tokens, weights sw1 / sw3).  Where
+//      gemv_routes holds (T * K <= 32; E <= 128, or K <= 16 and E <= 4096/T')
+//      the launch before G1 computes only the logits: every G1 CTA routes
+//      the batch itself (gemv_route: top-K per token, the stable permutation
+//      and the skinny plan in shared memory), which replaces the routing
+//      launch's serial tail (completion count, then top-K, permute and plan
+//      in its last CTA: ~6 us of a 38 us layer at T = 1, 128 experts; ~10 us
+//      at 512 experts).
 //   G2 (gemv_g2_kernel): CTA units of (expert block, 64 output features): the
 //      block's hact rows staged in shared memory, each warp streams W2 rows
-//      four at a time (two for T = 4) -> y (bf16); the shared expert's rows likewise ->
-//      shared_y.  Then the combine kernel.
+//      four at a time (two for T = 4) -> y (bf16); the shared expert's rows
+//      likewise -> shared_y.  Then the combine kernel.
 // Each warp keeps 16 row vectors per lane in flight (G1: two rows, 8 each;
-// G2: four rows, 4 each, or two, 8 each) before it uses any, so a 2-CTA-per-SM grid holds up
-// to ~128 KB of weights in flight per SM.  Measured and not kept (Qwen3-30B-A3B shape, T = 1, L2 flushed): a G2
-// warp per (token, feature) running the token's K picks in turn with the
-// combine fused in (K dependent row loads per warp), and feeding the rows by
-// bulk copies on the TMA engine into per-warp shared-memory slot rings
-// (52.9 us against 38.5).
+// G2: four rows, 4 each, or two, 8 each) before it uses any, so a
+// 2-CTA-per-SM grid holds up to ~128 KB of weights in flight per SM.
+// Measured and not kept
+// (Qwen3-30B-A3B shape, L2 flushed): a G2 warp per (token, feature) running
+// the token's K picks in turn with the combine fused in (K dependent row
+// loads per warp), and feeding the rows by bulk copies on the TMA engine into
+// per-warp shared-memory slot rings (T = 1: 52.9 us against 38.5); bulk L2
+// prefetches of each warp's next units' rows (T = 1 38.5 -> 40.6, T = 2
+// 53 -> 65); G2 issuing each warp's first W2 batch before the hact staging
+// barrier (T = 2 50.9 -> 54.9).
 //
-// Weights bf16 or e4m3 with fp32 128 x 128 block scales (the W8A16 format);
-// each weight is widened to fp32 exactly and times its block scale.
+// Weights bf16, e4m3 with fp32 128 x 128 block scales (the W8A16 format), or
+// MXFP4 (e2m1 with a UE8M0 byte per 32 weights of a row): each weight is
+// widened to fp32 exactly: the e4m3 code times its block scale, the e2m1
+// code times 2^(scale byte - 127) (exact unless it overflows fp32, as a bf16
+// weight would).
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
@@ -51,30 +60,24 @@ constexpr size_t kMaxSmem = 200 * 1024;  // the staged token rows: T * H bf16 at
 
 MOE_DEVICE float silu(float g) { return g / (1.f + __expf(-g)); }
 
-// 16 e4m3 codes (a 16-byte vector) -> 16 floats times the block scale
-MOE_DEVICE void e4m3x16_to_f32(const uint4& v, float s, float* f) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
-          static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
-      const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-      f[4 * i + 2 * h] = p.x * s;
-      f[4 * i + 2 * h + 1] = p.y * s;
-    }
-  }
-}
+// A weight vector's scale: the fp32 block scale (e4m3), or 2^(byte - 127)
+// of its UE8M0 byte (e2m1)
+struct WScale {
+  float f;
+};
 
-// 8 weights of a 16-byte vector as floats: bf16 (the whole vector), or e4m3
-// codes 8*half .. 8*half+7 times the block scale sc
+// weights per 16-byte vector: bf16 8, e4m3 16, e2m1 32
 template <int WQ>
-MOE_DEVICE void weights8(const uint4& v, int half, float sc, float* f) {
+constexpr int per_vec() { return WQ == 0 ? 8 : WQ == 1 ? 16 : 32; }
+
+// 8 weights (part p of a 16-byte vector) as floats: bf16; e4m3 codes times
+// the block scale; e2m1 codes times 2^(scale byte - 127), exact
+template <int WQ>
+MOE_DEVICE void weights8(const uint4& v, int part, const WScale& sc, float* f) {
   if (WQ == 0) {
     bf16x8_to_f32(v, f);
-  } else {
-    const uint32_t w[2] = {half ? v.z : v.x, half ? v.w : v.y};
+  } else if (WQ == 1) {
+    const uint32_t w[2] = {part ? v.z : v.x, part ? v.w : v.y};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
 #pragma unroll
@@ -82,24 +85,43 @@ MOE_DEVICE void weights8(const uint4& v, int half, float sc, float* f) {
         const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(
             static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu), __NV_E4M3);
         const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-        f[4 * i + 2 * h] = p.x * sc;
-        f[4 * i + 2 * h + 1] = p.y * sc;
+        f[4 * i + 2 * h] = p.x * sc.f;
+        f[4 * i + 2 * h + 1] = p.y * sc.f;
       }
+    }
+  } else {
+    // byte i holds elements 2i (low nibble) and 2i + 1; each e2m1 value is
+    // exact in f16, and times the power of two sc.f exact in fp32
+    const uint32_t w = part == 0 ? v.x : part == 1 ? v.y : part == 2 ? v.z : v.w;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2(
+          static_cast<__nv_fp4x2_storage_t>((w >> (8 * i)) & 0xFFu), __NV_E2M1);
+      const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+      f[2 * i] = p.x * sc.f;
+      f[2 * i + 1] = p.y * sc.f;
     }
   }
 }
 
-// Dot products of nr <= NR weight rows (row i at byte r0 + i * rs; bf16, or
-// e4m3 with its block-scale row at s0 + i * ss) of length n with up to MT
-// activation rows, lane-strided 16-byte
+// 2^(b - 127) for a UE8M0 scale byte b below 255, as an fp32 (b = 0: the
+// subnormal 2^-127)
+MOE_DEVICE float ue8m0_to_f32(uint32_t b) {
+  return __uint_as_float(b ? b << 23 : 0x00400000u);
+}
+
+// Dot products of nr <= NR weight rows (row i at byte r0 + i * rs; bf16;
+// e4m3 with its fp32 block-scale row at byte s0 + i * ss, one scale per 128
+// weights; e2m1 with its UE8M0 scale row at byte s0 + i * ss, one byte per
+// 32 weights) of length n with up to MT activation rows, lane-strided 16-byte
 // vectors; per-lane partial sums in acc[i][j] (row i, token j), each summed in
 // element order.  Every lane loads KB vectors of each row (NR * KB in flight)
 // before it uses any.  act(j, e0, a) loads 8 activations of token j from
-// element e0.  WQ: 0 bf16 (8 weights per vector), 1 e4m3 (16).
+// element e0.  WQ: 0 bf16, 1 e4m3, 2 e2m1 (per_vec weights per vector).
 template <int WQ, int MT, int NR, int KB, typename Act>
-MOE_DEVICE void rows_dot(const void* r0, ptrdiff_t rs, const float* s0, ptrdiff_t ss, int nr,
+MOE_DEVICE void rows_dot(const void* r0, ptrdiff_t rs, const void* s0, ptrdiff_t ss, int nr,
                          int n, int m, Act act, float (&acc)[NR][MT]) {
-  constexpr int kPer = WQ ? 16 : 8;  // weights per 16-byte vector
+  constexpr int kPer = per_vec<WQ>();
   const int lane = lane_id();
   const int nv = n / kPer;
   for (int v0 = lane; v0 < nv; v0 += 32 * KB) {
@@ -117,10 +139,15 @@ MOE_DEVICE void rows_dot(const void* r0, ptrdiff_t rs, const float* s0, ptrdiff_
     for (int q = 0; q < KB; ++q) {
       const int v = v0 + 32 * q;
       if (v >= nv) break;
-      float sc[NR];
+      WScale sc[NR];
 #pragma unroll
-      for (int i = 0; i < NR; ++i) sc[i] = (WQ && i < nr) ? __ldg(s0 + i * ss + (kPer * v) / 128) : 1.f;
-      if constexpr (NR <= 2) {
+      for (int i = 0; i < NR; ++i) {
+        const uint8_t* srow = static_cast<const uint8_t*>(s0) + i * ss;
+        sc[i].f = 1.f;
+        if (WQ == 1 && i < nr) sc[i].f = __ldg(reinterpret_cast<const float*>(srow) + (kPer * v) / 128);
+        if (WQ == 2 && i < nr) sc[i].f = ue8m0_to_f32(__ldg(srow + v));
+      }
+      if constexpr (NR <= 2 && kPer <= 16) {
         // the rows' weights once, each token's activations once per 8
         float w[NR][kPer];
 #pragma unroll
@@ -147,7 +174,7 @@ MOE_DEVICE void rows_dot(const void* r0, ptrdiff_t rs, const float* s0, ptrdiff_
         }
         continue;
       }
-      // four rows: every token's 8 activations once, each row's
+      // four rows, or e2m1: every token's 8 activations once, each row's
       // 8 weights once per 8
 #pragma unroll
       for (int p = 0; p < kPer; p += 8) {
@@ -479,7 +506,7 @@ gemv_g1_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int I, int K,
     int tok[MT];
     int m, f, e = 0;
     const void *ra, *rb;
-    const float *sa = nullptr, *sb = nullptr;
+    const uint8_t *sa = nullptr, *sb = nullptr;  // the rows' scales (bytes)
     __nv_bfloat16* dst;
     int ld_dst, row0;
     if (u < routed) {
@@ -492,13 +519,15 @@ gemv_g1_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int I, int K,
       for (int j = 0; j < MT; ++j)
         tok[j] = j < m ? (kRoute ? rs.r2f[it.y + j] : __ldg(row_to_flat + it.y + j)) / K : 0;
       const size_t row = (size_t)e * I + f;
-      ra = WQ ? (const void*)(static_cast<const uint8_t*>(w1) + row * H)
-              : (const void*)(static_cast<const __nv_bfloat16*>(w1) + row * H);
-      rb = WQ ? (const void*)(static_cast<const uint8_t*>(w3) + row * H)
-              : (const void*)(static_cast<const __nv_bfloat16*>(w3) + row * H);
-      if (WQ) {
-        sa = s1 + ((size_t)e * NBi + f / 128) * KBh;
-        sb = s3 + ((size_t)e * NBi + f / 128) * KBh;
+      const size_t wrow = (size_t)H * 16 / per_vec<WQ>();  // bytes of a weight row
+      ra = static_cast<const uint8_t*>(w1) + row * wrow;
+      rb = static_cast<const uint8_t*>(w3) + row * wrow;
+      if (WQ == 1) {  // fp32 128 x 128 block scales
+        sa = reinterpret_cast<const uint8_t*>(s1 + ((size_t)e * NBi + f / 128) * KBh);
+        sb = reinterpret_cast<const uint8_t*>(s3 + ((size_t)e * NBi + f / 128) * KBh);
+      } else if (WQ == 2) {  // a UE8M0 byte per 32 weights of the row
+        sa = reinterpret_cast<const uint8_t*>(s1) + row * (H / 32);
+        sb = reinterpret_cast<const uint8_t*>(s3) + row * (H / 32);
       }
       dst = hact;
       ld_dst = I;
@@ -523,7 +552,7 @@ gemv_g1_kernel(const __nv_bfloat16* __restrict__ x, int T, int H, int I, int K,
     // row b and its scales at a fixed distance from row a
     const ptrdiff_t rs = static_cast<const uint8_t*>(rb) - static_cast<const uint8_t*>(ra);
     if (WQ && u < routed)
-      rows_dot<1, MT, 2, 8>(ra, rs, sa, sb - sa, 2, H, m, act, acc);
+      rows_dot<WQ, MT, 2, 8>(ra, rs, sa, sb - sa, 2, H, m, act, acc);
     else
       rows_dot<0, MT, 2, 8>(ra, rs, nullptr, 0, 2, H, m, act, acc);
     float hv = 0.f;
@@ -582,17 +611,23 @@ gemv_g2_kernel(const __nv_bfloat16* __restrict__ hact, int T, int H, int I,
       const int h0 = hb * kG2Rows + r;
       if (h0 >= H) break;
       const int nr = H - h0 < kG2Per ? H - h0 : kG2Per;  // the same in every lane
-      // nr consecutive rows h0.. (h0 % 4 == 0: one 128-row scale block)
+      // nr consecutive rows h0.. (h0 % 4 == 0: e4m3, one 128-row scale
+      // block; e2m1, a scale row per weight row)
       const void* r0;
-      ptrdiff_t rs;
-      const float* s0 = nullptr;
+      ptrdiff_t rs, ss = 0;
+      const void* s0 = nullptr;
       if (sh) {
         r0 = sw2 + (size_t)h0 * Is;
         rs = (ptrdiff_t)Is * 2;
-      } else if (WQ) {
+      } else if (WQ == 1) {
         r0 = static_cast<const uint8_t*>(w2) + ((size_t)it.x * H + h0) * I;
         rs = I;
         s0 = s2 + ((size_t)it.x * NBh + h0 / 128) * KBi;
+      } else if (WQ == 2) {
+        r0 = static_cast<const uint8_t*>(w2) + ((size_t)it.x * H + h0) * (I / 2);
+        rs = I / 2;
+        s0 = reinterpret_cast<const uint8_t*>(s2) + ((size_t)it.x * H + h0) * (I / 32);
+        ss = I / 32;
       } else {
         r0 = static_cast<const __nv_bfloat16*>(w2) + ((size_t)it.x * H + h0) * I;
         rs = (ptrdiff_t)I * 2;
@@ -605,7 +640,7 @@ gemv_g2_kernel(const __nv_bfloat16* __restrict__ hact, int T, int H, int I,
       if (sh)
         rows_dot<0, MT, kG2Per, kG2Batch>(r0, rs, nullptr, 0, nr, Is, m, act, acc);
       else
-        rows_dot<WQ, MT, kG2Per, kG2Batch>(r0, rs, s0, 0, nr, I, m, act, acc);
+        rows_dot<WQ, MT, kG2Per, kG2Batch>(r0, rs, s0, ss, nr, I, m, act, acc);
       float v[kG2Per];
 #pragma unroll
       for (int i = 0; i < kG2Per; ++i) {
@@ -698,7 +733,7 @@ bool gemv_supported(int T, int H, int I, int Is, int wdtype, int m_skinny) {
   const int n = I > Is ? I : Is;
   return T >= 1 && T <= kGemvMaxT && T <= m_skinny && (size_t)T * H * 2 <= kMaxSmem &&
          (size_t)T * n * 2 <= kMaxSmem &&
-         (wdtype == MOE_W_BF16 || wdtype == MOE_W_FP8E4M3_B128);
+         (wdtype == MOE_W_BF16 || wdtype == MOE_W_FP8E4M3_B128 || wdtype == MOE_W_MXFP4);
 }
 
 bool gemv_routes(int T, int E, int K) {
@@ -712,5 +747,6 @@ bool gemv_routes(int T, int E, int K) {
 cudaError_t launch_gemv_layer(const GemvArgs& a, cudaStream_t stream) {
   if (a.route && !gemv_routes(a.T, a.rt.E, a.K)) return cudaErrorInvalidValue;
   if (a.wdtype == MOE_W_FP8E4M3_B128) return launch_t<1>(a, stream);
+  if (a.wdtype == MOE_W_MXFP4) return launch_t<2>(a, stream);
   return launch_t<0>(a, stream);
 }

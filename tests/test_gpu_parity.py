@@ -811,7 +811,11 @@ GEMV_CASES = [("qwen3_30b_a3b", {}, 1), ("qwen3_30b_a3b", {}, 2), ("qwen3_30b_a3
               ("shared_gate", {}, 2), ("shared_gate", {}, 3), ("high_expert", {}, 2),
               ("tiny", {"E": 300, "K": 5}, 2),
               ("tiny", {"E": 257, "K": 7, "mode": 1, "routed_scale": 2.5,
-                        "sel_bias_var": 0.1}, 3)]
+                        "sel_bias_var": 0.1}, 3),
+              # MXFP4 rows (e2m1 decoded exactly, a scale byte per 32 weights)
+              ("gpt_oss_20b", {"wdtype": "mxfp4"}, 1), ("gpt_oss_20b", {"wdtype": "mxfp4"}, 2),
+              ("tiny", {"H": 160, "I": 96, "E": 5, "wdtype": "mxfp4"}, 4),
+              ("shared_gate", {"wdtype": "mxfp4"}, 1)]
 
 
 @pytest.mark.parametrize("name,over,T", GEMV_CASES, ids=case_id)
