@@ -40,7 +40,10 @@
 // per-warp shared-memory slot rings (T = 1: 52.9 us against 38.5); bulk L2
 // prefetches of each warp's next units' rows (T = 1 38.5 -> 40.6, T = 2
 // 53 -> 65); G2 issuing each warp's first W2 batch before the hact staging
-// barrier (T = 2 50.9 -> 54.9).
+// barrier (T = 2 50.9 -> 54.9); G1 fed by a per-lane cp.async ring instead of
+// register batches (T = 1 34.3 -> 36.5); the combine folded into the T = 1 G2
+// through per-row-group arrival counters (32.4 -> 32.6: a fence and an atomic
+// per warp unit cost more than the combine launch).
 //
 // Weights bf16, e4m3 with fp32 128 x 128 block scales (the W8A16 format), or
 // MXFP4 (e2m1 with a UE8M0 byte per 32 weights of a row): each weight is
