@@ -26,9 +26,10 @@
 //   G2 (gemv_g2_kernel): CTA units of (expert block, 64 output features): the
 //      block's hact rows staged in shared memory, each warp streams W2 rows
 //      four at a time (two for T = 4) -> y (bf16); the shared expert's rows
-//      likewise -> shared_y.  At T = 1 (gemv_g2_t1_kernel) warp units of 4 W2
-//      rows instead, the block's single hact row read with the weights (no
-//      staging or barrier; every warp busy: Qwen3-30B-A3B shape 34.4 ->
+//      likewise -> shared_y.  At T <= 2 (gemv_g2_t1_kernel, gemv_g2w_kernel)
+//      warp units of 4 W2 rows instead, the block's hact rows read with the
+//      weights (no staging or barrier; every warp busy: T = 2, GPT-OSS-20B
+//      FP8 80.1 -> 71.3 us; T = 1, Qwen3-30B-A3B shape 34.4 ->
 //      32.2 us, shared-gate shape 42.6 -> 37.8).  Then the combine kernel.
 // Each warp keeps 16 row vectors per lane in flight (G1: two rows, 8 each;
 // G2: four rows, 4 each, or two, 8 each) before it uses any, so a
@@ -786,6 +787,160 @@ gemv_g2_t1_kernel(const __nv_bfloat16* __restrict__ hact, int H, int I,
   }
 }
 
+// G2 for two tokens (MT = 2; an expert block has one or two rows): the
+// T = 1 kernel's warp units of 4 consecutive W2 rows with up to MT hact rows
+// per block (the one-token instance measured ~2 us slower than the kernel
+// above at the Qwen3-30B-A3B shape, so T = 1 keeps its own).  Each lane loads its vectors of the 4 rows and the matching
+// vectors of the block's hact rows together (no staging, no barrier), KB per
+// row in flight; the sums run in the element order of gemv_g2_kernel.
+template <int WQ, int MT>
+constexpr int g2w_batch() {
+  // hact registers grow with the tokens and the weights per vector
+  return (per_vec<WQ>() / 8) * MT <= 2 ? 4 : ((per_vec<WQ>() / 8) * MT <= 4 ? 2 : 1);
+}
+
+template <int WQ, int MT>
+__global__ void __launch_bounds__(32 * kWarps, 2)
+gemv_g2w_kernel(const __nv_bfloat16* __restrict__ hact, int T, int H, int I,
+                const int32_t* __restrict__ counts, const int4* __restrict__ items,
+                const void* __restrict__ w2, const float* __restrict__ s2,
+                __nv_bfloat16* __restrict__ y, int Is,
+                const __nv_bfloat16* __restrict__ shared_hact,
+                const __nv_bfloat16* __restrict__ sw2, __nv_bfloat16* __restrict__ shared_y) {
+  constexpr int kRows = 4;
+  constexpr int kPerR = per_vec<WQ>();
+  pdl_wait();
+  pdl_trigger();
+  const int lane = lane_id();
+  const int ng = H / kRows;  // row groups per block
+  const long long routed = (long long)counts[0] * ng;
+  const long long total = routed + (Is > 0 ? ng : 0);
+  const int KBi = (I + 127) / 128, NBh = (H + 127) / 128;
+  for (long long u = (long long)blockIdx.x * kWarps + warp_id(); u < total;
+       u += (long long)gridDim.x * kWarps) {
+    const bool sh = u >= routed;
+    const int h0 = kRows * (int)(sh ? u - routed : u % ng);
+    float acc[kRows][MT];
+#pragma unroll
+    for (int i = 0; i < kRows; ++i)
+#pragma unroll
+      for (int j = 0; j < MT; ++j) acc[i][j] = 0.f;
+    __nv_bfloat16* dst;
+    int m;
+    if (sh) {
+      // bf16 rows of Is, the shared expert's hact rows (all T tokens)
+      m = T < MT ? T : MT;
+      const int nv = Is / 8;
+      for (int v0 = lane; v0 < nv; v0 += 32 * 4) {
+        uint4 vv[kRows][4], hv[4][MT];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int v = v0 + 32 * q;
+#pragma unroll
+          for (int j = 0; j < MT; ++j)
+            hv[q][j] = (v < nv && j < m)
+                           ? __ldg(reinterpret_cast<const uint4*>(shared_hact + (size_t)j * Is) + v)
+                           : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int i = 0; i < kRows; ++i)
+            vv[i][q] = v < nv ? __ldcs(reinterpret_cast<const uint4*>(sw2 + (size_t)(h0 + i) * Is) + v)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (v0 + 32 * q >= nv) break;
+          float a[MT][8];
+#pragma unroll
+          for (int j = 0; j < MT; ++j) bf16x8_to_f32(hv[q][j], a[j]);
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) {
+            float w[8];
+            bf16x8_to_f32(vv[i][q], w);
+#pragma unroll
+            for (int j = 0; j < MT; ++j)
+              if (j < m) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) acc[i][j] = fmaf(w[c], a[j][c], acc[i][j]);
+              }
+          }
+        }
+      }
+      dst = shared_y;
+    } else {
+      const int4 it = __ldg(items + u / ng);  // {expert, first row, rows, -}
+      m = it.z < MT ? it.z : MT;
+      const size_t rowb = (size_t)I * 16 / kPerR;  // bytes of a W2 row
+      const uint8_t* r0 = static_cast<const uint8_t*>(w2) + ((size_t)it.x * H + h0) * rowb;
+      const uint4* hrow = reinterpret_cast<const uint4*>(hact + (size_t)it.y * I);
+      const int nv = I / kPerR, hstride = I / 8;  // hact row stride in 16-byte vectors
+      constexpr int KB = g2w_batch<WQ, MT>();  // weight vectors per lane and row in a batch
+      for (int v0 = lane; v0 < nv; v0 += 32 * KB) {
+        uint4 vv[kRows][KB], hv[KB][kPerR / 8][MT];
+#pragma unroll
+        for (int q = 0; q < KB; ++q) {
+          const int v = v0 + 32 * q;
+#pragma unroll
+          for (int p = 0; p < kPerR / 8; ++p)
+#pragma unroll
+            for (int j = 0; j < MT; ++j)
+              hv[q][p][j] = (v < nv && j < m)
+                                ? __ldg(hrow + (size_t)j * hstride + (size_t)v * (kPerR / 8) + p)
+                                : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int i = 0; i < kRows; ++i)
+            vv[i][q] = v < nv ? __ldcs(reinterpret_cast<const uint4*>(r0 + i * rowb) + v)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < KB; ++q) {
+          const int v = v0 + 32 * q;
+          if (v >= nv) break;
+          WScale sc[kRows];
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) {
+            sc[i].f = 1.f;
+            if (WQ == 1)  // h0 % 4 == 0: the 4 rows share a 128-row scale block
+              sc[i].f = __ldg(s2 + ((size_t)it.x * NBh + h0 / 128) * KBi + (16 * v) / 128);
+            if (WQ == 2)
+              sc[i].f = ue8m0_to_f32(__ldg(reinterpret_cast<const uint8_t*>(s2) +
+                                           ((size_t)it.x * H + h0 + i) * (I / 32) + v));
+          }
+#pragma unroll
+          for (int p = 0; p < kPerR; p += 8) {
+            float a[MT][8];
+#pragma unroll
+            for (int j = 0; j < MT; ++j) bf16x8_to_f32(hv[q][p / 8][j], a[j]);
+#pragma unroll
+            for (int i = 0; i < kRows; ++i) {
+              float w[8];
+              weights8<WQ>(vv[i][q], p / 8, sc[i], w);
+#pragma unroll
+              for (int j = 0; j < MT; ++j)
+                if (j < m) {
+#pragma unroll
+                  for (int c = 0; c < 8; ++c) acc[i][j] = fmaf(w[c], a[j][c], acc[i][j]);
+                }
+            }
+          }
+        }
+      }
+      dst = y + (size_t)it.y * H;
+    }
+    // lane i + 4 j: row h0 + i of token j
+    float out = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRows; ++i)
+#pragma unroll
+      for (int j = 0; j < MT; ++j) {
+        if (j < m) {
+          const float sum = warp_sum(acc[i][j]);
+          if (lane == i + kRows * j) out = sum;
+        }
+      }
+    if (lane < kRows * m) dst[(size_t)(lane / kRows) * H + h0 + lane % kRows] = __float2bfloat16_rn(out);
+  }
+}
+
 // CTAs that stay resident together (a grid-stride loop shares the units):
 // the kernel's occupancy at this shared-memory size, cached per device for
 // the last size asked
@@ -826,17 +981,41 @@ cudaError_t launch_g1(const GemvArgs& a, cudaStream_t stream) {
 
 template <int WQ, int MT>
 cudaError_t launch_wq(const GemvArgs& a, cudaStream_t stream) {
-  // the limit is raised once, to the largest size a call may stage
-  static std::atomic<unsigned long long> set2{0};
-  cudaError_t e = moe_raise_smem(gemv_g2_kernel<WQ, MT>, kMaxSmem, set2);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if constexpr (MT > 2) {
+    // the limit is raised once, to the largest size a call may stage
+    static std::atomic<unsigned long long> set2{0};
+    e = moe_raise_smem(gemv_g2_kernel<WQ, MT>, kMaxSmem, set2);
+    if (e != cudaSuccess) return e;
+  }
   e = a.route ? launch_g1<WQ, MT, true>(a, stream) : launch_g1<WQ, MT, false>(a, stream);
   if (e != cudaSuccess) return e;
-  if (MT == 1) {
-    // one token: warp units of 4 W2 rows, hact read with the weights
-    e = moe_launch(gemv_g2_t1_kernel<WQ>, dim3(gemv_grid(gemv_g2_t1_kernel<WQ>, 0)),
-                   dim3(32 * kWarps), 0, stream, 1, static_cast<const __nv_bfloat16*>(a.hact),
-                   a.H, a.I, a.counts, a.items, a.w2, a.s2, static_cast<__nv_bfloat16*>(a.y),
+  if constexpr (MT <= 2) {
+    // one or two tokens: warp units of 4 W2 rows, hact read with the weights
+    if constexpr (MT == 1)
+      e = moe_launch(gemv_g2_t1_kernel<WQ>, dim3(gemv_grid(gemv_g2_t1_kernel<WQ>, 0)),
+                     dim3(32 * kWarps), 0, stream, 1, static_cast<const __nv_bfloat16*>(a.hact),
+                     a.H, a.I, a.counts, a.items, a.w2, a.s2, static_cast<__nv_bfloat16*>(a.y),
+                     a.Is, static_cast<const __nv_bfloat16*>(a.shared_hact),
+                     static_cast<const __nv_bfloat16*>(a.sw2),
+                     static_cast<__nv_bfloat16*>(a.shared_y));
+    else
+      e = moe_launch(gemv_g2w_kernel<WQ, MT>, dim3(gemv_grid(gemv_g2w_kernel<WQ, MT>, 0)),
+                     dim3(32 * kWarps), 0, stream, 1, static_cast<const __nv_bfloat16*>(a.hact),
+                     a.T, a.H, a.I, a.counts, a.items, a.w2, a.s2,
+                     static_cast<__nv_bfloat16*>(a.y), a.Is,
+                     static_cast<const __nv_bfloat16*>(a.shared_hact),
+                     static_cast<const __nv_bfloat16*>(a.sw2),
+                     static_cast<__nv_bfloat16*>(a.shared_y));
+    if (e != cudaSuccess) return e;
+    return launch_unpermute(a.y, a.flat_to_row, a.weights, a.T, a.K, a.H,
+                            a.Is > 0 ? a.shared_y : nullptr, a.Is > 0 ? a.shared_gate : nullptr,
+                            a.out, stream);
+  } else {
+    const size_t smem2 = (size_t)a.T * (a.I > a.Is ? a.I : a.Is) * 2;
+    e = moe_launch(gemv_g2_kernel<WQ, MT>, dim3(gemv_grid(gemv_g2_kernel<WQ, MT>, smem2)),
+                   dim3(32 * kWarps), smem2, stream, 1, static_cast<const __nv_bfloat16*>(a.hact),
+                   a.T, a.H, a.I, a.counts, a.items, a.w2, a.s2, static_cast<__nv_bfloat16*>(a.y),
                    a.Is, static_cast<const __nv_bfloat16*>(a.shared_hact),
                    static_cast<const __nv_bfloat16*>(a.sw2),
                    static_cast<__nv_bfloat16*>(a.shared_y));
@@ -845,16 +1024,6 @@ cudaError_t launch_wq(const GemvArgs& a, cudaStream_t stream) {
                             a.Is > 0 ? a.shared_y : nullptr, a.Is > 0 ? a.shared_gate : nullptr,
                             a.out, stream);
   }
-  const size_t smem2 = (size_t)a.T * (a.I > a.Is ? a.I : a.Is) * 2;
-  e = moe_launch(gemv_g2_kernel<WQ, MT>, dim3(gemv_grid(gemv_g2_kernel<WQ, MT>, smem2)),
-                 dim3(32 * kWarps), smem2, stream, 1, static_cast<const __nv_bfloat16*>(a.hact),
-                 a.T, a.H, a.I, a.counts, a.items, a.w2, a.s2, static_cast<__nv_bfloat16*>(a.y),
-                 a.Is, static_cast<const __nv_bfloat16*>(a.shared_hact),
-                 static_cast<const __nv_bfloat16*>(a.sw2), static_cast<__nv_bfloat16*>(a.shared_y));
-  if (e != cudaSuccess) return e;
-  return launch_unpermute(a.y, a.flat_to_row, a.weights, a.T, a.K, a.H,
-                          a.Is > 0 ? a.shared_y : nullptr, a.Is > 0 ? a.shared_gate : nullptr,
-                          a.out, stream);
 }
 
 template <int WQ>
