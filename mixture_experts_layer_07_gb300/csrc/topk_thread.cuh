@@ -6,10 +6,13 @@
 // "FlashInfer MoE routing optimisation" (flashinfer PR #4152), "why" 1: the
 // lane-owned lists spread the top-K registers over a warp.  With a token's
 // <= 128 keys in one thread's registers, most of that work can be skipped:
-//   * tau = min over KT groups (expert e in group e % KT) of the group's
-//     largest key.  The KT group maxima are KT distinct experts with keys
-//     >= tau, so at least KT >= K keys are >= tau, and every expert of the
-//     top K has a key >= tau;
+//   * tau = the KT-th largest of the 2 KT group maxima (expert e in group
+//     e % 2KT; KT groups and their least maximum where 2 KT groups would not
+//     fit the row).  The KT largest group maxima are KT distinct experts with
+//     keys >= tau, so at least KT >= K keys are >= tau, and every expert of
+//     the top K has a key >= tau.  (For random logits, E = 128, K = 8: about
+//     10 candidates a token and 15 for the warp's slowest lane, against 20
+//     and 39 with the least of 8 group maxima.)
 //   * only the experts with key >= tau (a bit mask: for random logits a few
 //     times K of them) are inserted, in rising expert order, into a sorted
 //     list of KT (strictly larger keys move up, so among equal keys the lower
@@ -21,6 +24,28 @@
 #include "topk_warp.cuh"
 
 namespace moe_route {
+
+// N values sorted into descending order in place (bitonic network, N a power
+// of two; NaN-free inputs)
+template <int N>
+MOE_DEVICE void sort_desc(float (&v)[N]) {
+#pragma unroll
+  for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+#pragma unroll
+      for (int i = 0; i < N; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const float x = v[i], y = v[l];
+          const bool down = (i & k) == 0;  // this block ends up descending
+          v[i] = down ? fmaxf(x, y) : fminf(x, y);
+          v[l] = down ? fminf(x, y) : fmaxf(x, y);
+        }
+      }
+    }
+  }
+}
 
 // NV float4 vectors of logits per row (E <= 4 NV); KT >= K list entries, KT a
 // power of two with KT <= E; kVec: the row is 16-byte aligned and E % 4 == 0.
@@ -60,15 +85,35 @@ MOE_DEVICE void thread_topk(const float* __restrict__ row, const float* __restri
     for (int i = 0; i < kN; ++i)
       if (i < E) key[i] = sel_key(key[i], i);
   }
-  // the bound
-  float gmax[KT];
+  // the bound: with 2 KT groups, the KT-th largest of their maxima (KT
+  // distinct experts reach it, so every top-K key does); with KT groups (2 KT
+  // would leave groups of under one row's worth), the least maximum
+  constexpr int kG = 2 * KT <= kN ? 2 * KT : KT;
+  float gmax[kG];
 #pragma unroll
-  for (int g = 0; g < KT; ++g) gmax[g] = kNegInf;
+  for (int g = 0; g < kG; ++g) gmax[g] = kNegInf;
 #pragma unroll
-  for (int i = 0; i < kN; ++i) gmax[i % KT] = fmaxf(gmax[i % KT], key[i]);
-  float tau = gmax[0];
+  for (int i = 0; i < kN; ++i) gmax[i % kG] = fmaxf(gmax[i % kG], key[i]);
+  float tau;
+  if constexpr (kG == 2 * KT) {
+    // each half sorted descending; the half-cleaner max(a_i, b_{KT-1-i})
+    // keeps the KT largest of the union, the least of which is tau
+    float a[KT], b[KT];
 #pragma unroll
-  for (int g = 1; g < KT; ++g) tau = fminf(tau, gmax[g]);
+    for (int g = 0; g < KT; ++g) {
+      a[g] = gmax[g];
+      b[g] = gmax[KT + g];
+    }
+    sort_desc<KT>(a);
+    sort_desc<KT>(b);
+    tau = fmaxf(a[0], b[KT - 1]);
+#pragma unroll
+    for (int g = 1; g < KT; ++g) tau = fminf(tau, fmaxf(a[g], b[KT - 1 - g]));
+  } else {
+    tau = gmax[0];
+#pragma unroll
+    for (int g = 1; g < kG; ++g) tau = fminf(tau, gmax[g]);
+  }
   uint32_t cand[kW];
 #pragma unroll
   for (int w = 0; w < kW; ++w) cand[w] = 0u;

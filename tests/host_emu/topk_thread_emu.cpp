@@ -4,7 +4,7 @@
 // sort of the same keys (larger first, lower expert index first among equal
 // keys) for every (E, K) shape it serves, float4 and scalar rows, both score
 // modes, and random, tie-heavy, all-equal and "top experts in one bound
-// group" logits.  Exit status 0 when every token matches.
+// group" logits (for both groupings the bound may use).  Exit status 0 when every token matches.
 #include <cstdio>
 #include <numeric>
 #include <random>
@@ -26,6 +26,7 @@ int check(int E, int K, int T, int mode, int pattern, unsigned seed) {
       if (pattern == 1) v = (float)((int)(rng() % 3) - 1);
       if (pattern == 2) v = 0.f;
       if (pattern == 3 && e % KT == 0) v += 20.f;  // every pick from bound group 0
+      if (pattern == 4 && e % (2 * KT) == 0) v += 20.f;  // ... of the 2 KT grouping
       lg[(size_t)t * ld + e] = v;
     }
   for (auto& v : bias) v = mode ? 0.3f * nd(rng) : 0.f;
@@ -60,7 +61,7 @@ template <int NV, int KT, bool kVec>
 int sweep(int E, int K) {
   int bad = 0;
   for (int mode = 0; mode < 2; ++mode)
-    for (int pattern = 0; pattern < 4; ++pattern)
+    for (int pattern = 0; pattern < 5; ++pattern)
       bad += check<NV, KT, kVec, false>(E, K, 300, mode, pattern, 1000u * E + 10u * K + pattern) +
              check<NV, KT, kVec, true>(E, K, 100, mode, pattern, 7u * E + 3u * K + pattern);
   return bad;
