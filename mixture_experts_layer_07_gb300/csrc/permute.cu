@@ -295,7 +295,7 @@ namespace {
 
 typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 
-// The driver's current context, to tell a cached address from a stale one.
+// The CUDA context current on this thread, to tell a cached address from a stale one.
 CUcontext current_context() {
   static CtxGetCurrentFn fn = [] {
     void* p = nullptr;
