@@ -192,13 +192,16 @@ def launches_per_layer(spec, T, dispatch=0, m_skinny=16, wide_min=129, num_sms=1
                wide list, per list a G1 and a G2 launch (or one fused); 2 on
                the CUDA-core path
       combine 1; a shared expert adds a grouped GEMM with its own plan.
-      Small batches under per-block dispatch: T <= 2 (bf16 or W8A16 FP8): the
-      routing launch, G1 and G2 as CUDA-core matrix-vector products (the
-      shared expert inside them) and the combine; bf16 with a shared expert at
-      T = 3, 4, or E <= 128 at T = 4..8: the one-launch layer.
+      Small batches under per-block dispatch: T <= 2 (bf16 or W8A16 FP8; MXFP4
+      at T = 1): the logits launch (or the fused routing launch), G1 (routing
+      the batch in its CTAs where it can) and G2 as CUDA-core matrix-vector
+      products (the shared expert inside them) and the combine; bf16 with a
+      shared expert at T = 3, 4, or E <= 128 at T = 4..8: the one-launch
+      layer.
       W8A8: quantise xp, G1, quantise hact, G2 (every block one kernel)."""
     R = T * spec.K
-    if dispatch == 0 and T <= 2 and spec.act == "bf16" and spec.wdtype in ("bf16", "fp8"):
+    if dispatch == 0 and spec.act == "bf16" and (
+            (T <= 2 and spec.wdtype in ("bf16", "fp8")) or (T == 1 and spec.wdtype == "mxfp4")):
         return 4
     if (dispatch == 0 and spec.wdtype == "bf16" and spec.act == "bf16" and
             ((spec.has_shared and T <= 4) or (spec.E <= 128 and 4 <= T <= 8))):
