@@ -823,6 +823,46 @@ def test_gemv_decode_layer(ops, name, over, T):
     check_small_batch_layer(ops, name, over, T, ops.DISPATCH_GEMV, "gemv")
 
 
+# the matrix-vector decode path and the tensor-core path on the same inputs:
+# the routing agrees bit for bit; with bf16 or MXFP4 weights (e2m1 times
+# 2^(byte - 127) is exact in bf16) both read the same weight values, so hact,
+# y and the output agree to the order of the fp32 sums (two bf16 steps).
+# FP8 weights: the tensor-core converter rounds each code * block scale to
+# bf16 for the MMA, the matrix-vector path keeps it in fp32 -- there the two
+# agree to the oracle's FP8 tolerance.
+GEMV_VS_TC_CASES = [("qwen3_30b_a3b", {}, 1), ("qwen3_30b_a3b", {}, 2),
+                    ("gpt_oss_20b", {}, 1), ("gpt_oss_20b", {"wdtype": "mxfp4"}, 1),
+                    ("gpt_oss_20b", {"wdtype": "mxfp4"}, 2), ("shared_gate", {}, 1),
+                    ("high_expert", {}, 2)]
+
+
+@pytest.mark.parametrize("name,over,T", GEMV_VS_TC_CASES, ids=case_id)
+def test_gemv_path_matches_tensor_core_path(ops, name, over, T):
+    spec = SPECS[name].with_(**over)
+    base = synth.host_inputs(spec, T, seed=29, weights=False)
+    _, ids, _ = oracle_routing(spec, base)
+    inp = synth.host_inputs(spec, T, seed=29, experts=sorted(set(ids.ravel().tolist())))
+    t = U.layer_tensors(inp, inp["experts"])
+    E, K, R = spec.E, spec.K, T * spec.K
+    got = {}
+    for tag, disp in (("gemv", ops.DISPATCH_GEMV), ("tensor", ops.DISPATCH_GLOBAL_AVG)):
+        layer = ops.MoELayer(U.config_for(ops, spec, T_max=max(T, 4), dispatch=disp), t)
+        out = layer(t["x"])
+        sync()
+        assert int(layer.dev_status.item()) == 0
+        got[tag] = {"ids": layer.view("ids", torch.int32, (T, K)).cpu().numpy(),
+                    "r2f": layer.view("row_to_flat", torch.int32, (R,)).cpu().numpy(),
+                    "hact": U.f64(layer.view("hact", torch.bfloat16, (R, spec.I))),
+                    "y": U.f64(layer.view("y", torch.bfloat16, (R, spec.H))),
+                    "out": U.f64(out)}
+        del layer
+    g, c = got["gemv"], got["tensor"]
+    assert np.array_equal(g["ids"], c["ids"]) and np.array_equal(g["r2f"], c["r2f"])
+    rel = 5e-2 if spec.wdtype == "fp8" else 8e-3
+    for k in ("hact", "y", "out"):
+        U.assert_bf16_close(g[k], c[k], rel, f"gemv vs tensor cores {k}")
+
+
 def check_small_batch_layer(ops, name, over, T, dispatch, tag):
     spec = SPECS[name].with_(**over)
     base = synth.host_inputs(spec, T, seed=17, weights=False)
