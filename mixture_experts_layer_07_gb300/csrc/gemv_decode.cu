@@ -46,7 +46,10 @@
 // through per-row-group arrival counters (32.4 -> 32.6: a fence and an atomic
 // per warp unit cost more than the combine launch); the T = 1 G2 taking the
 // plan from a flag G1's CTA 0 sets and sending its first units' W2 rows to L2
-// before its grid dependency (30.7 -> 32.7 us).
+// before its grid dependency (30.7 -> 32.7 us); the row batches split into two
+// alternating halves, the next requested before the current one is summed
+// (T = 1 31.8 -> 32.5, T = 2 51.5 -> 54.2: less in flight at each unit's
+// start, and that depth is what this latency-bound path lives on).
 //
 // Weights bf16, e4m3 with fp32 128 x 128 block scales (the W8A16 format), or
 // MXFP4 (e2m1 with a UE8M0 byte per 32 weights of a row): each weight is
