@@ -34,11 +34,12 @@
 // Each warp keeps 16 row vectors per lane in flight (G1: two rows, 8 each;
 // G2: four rows, 4 each, or two, 8 each) before it uses any, so a
 // 2-CTA-per-SM grid holds up to ~128 KB of weights in flight per SM.
-// Measured and not kept
-// (Qwen3-30B-A3B shape, L2 flushed): a G2 warp per (token, feature) running
-// the token's K picks in turn with the combine fused in (K dependent row
-// loads per warp), and feeding the rows by bulk copies on the TMA engine into
-// per-warp shared-memory slot rings (T = 1: 52.9 us against 38.5); bulk L2
+//
+// Measured and not kept (Qwen3-30B-A3B shape, L2 flushed): a G2 warp per
+// (token, feature) running the token's K picks in turn with the combine fused
+// in (K dependent row loads per warp), and feeding the rows by bulk copies on
+// the TMA engine into per-warp shared-memory slot rings (T = 1: 52.9 us
+// against 38.5); bulk L2
 // prefetches of each warp's next units' rows (T = 1 38.5 -> 40.6, T = 2
 // 53 -> 65); G2 issuing each warp's first W2 batch before the hact staging
 // barrier (T = 2 50.9 -> 54.9); G1 fed by a per-lane cp.async ring instead of
