@@ -40,6 +40,12 @@ struct EmuDim { unsigned x, y, z; };
 inline thread_local EmuDim emu_thread_idx;
 #undef threadIdx
 #define threadIdx emu_thread_idx
+// the CTA being run (one at a time; set emu_block_idx before emu_run_cta) and
+// its size.  A program whose device code reads blockIdx / blockDim defines
+// them as these after including common.cuh (whose launch helper names a
+// cudaLaunchConfig_t member blockDim).
+inline EmuDim emu_block_idx = {0, 0, 0};
+inline EmuDim emu_block_dim = {0, 1, 1};
 
 // run fn on one CTA of n threads (n a multiple of 32, at most 1024)
 inline void emu_run_cta(int n, const std::function<void()>& fn) {
@@ -51,6 +57,7 @@ inline void emu_run_cta(int n, const std::function<void()>& fn) {
   }
   std::barrier<> cb(n);
   cta_bar = &cb;
+  emu_block_dim = {(unsigned)n, 1, 1};
   std::vector<std::thread> th;
   for (int i = 0; i < n; ++i)
     th.emplace_back([&, i]() {

@@ -17,7 +17,13 @@ the host:
 * permute_plan_emu.cpp -- csrc/permute_block.cuh and csrc/plan.cuh (the
   one-CTA permute and GEMM plan of the fused routing launches) against a
   stable counting sort and the work lists the variants imply, with
-  out-of-range ids flagged.
+  out-of-range ids flagged;
+* gemv_route_emu.cpp -- csrc/gemv_route.cuh (the matrix-vector decode path's
+  routing inside each G1 CTA: a warp per token for E <= 128, slices of the
+  experts over 8 / T' warps and a merge beyond; a one-warp stable
+  permutation and the skinny plan) against a stable sort, a counting sort,
+  the plan's definition and moe_variant_of, as CTA 0 (writing the workspace)
+  and as another CTA, both score modes, random and tie-heavy logits.
 
 * sigmoid_emu.cpp -- the selection key's float32 sigmoid (sigmoid_key), the
   order-preserving key map (order_key) and its inverse (key_float) of
@@ -60,7 +66,8 @@ def _compile(tmp_path, program):
     return str(exe)
 
 
-@pytest.mark.parametrize("program", ["topk_emu", "topk_thread_emu", "permute_plan_emu"])
+@pytest.mark.parametrize("program", ["topk_emu", "topk_thread_emu", "permute_plan_emu",
+                                     "gemv_route_emu"])
 def test_routing_device_code_on_host(tmp_path, program):
     exe = _compile(tmp_path, program)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
