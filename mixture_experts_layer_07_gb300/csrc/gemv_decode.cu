@@ -73,7 +73,6 @@ using moe_gemv_route::RouteSmem;
 
 constexpr int kWarps = 8;      // per CTA
 static_assert(kWarps == moe_gemv_route::kRouteWarps, "the routing prologue's warps");
-constexpr int kMaxTok = kGemvMaxT;
 constexpr size_t kMaxSmem = 200 * 1024;  // the staged token rows: T * H bf16 at most
 
 MOE_DEVICE float silu(float g) { return g / (1.f + __expf(-g)); }
@@ -190,26 +189,26 @@ MOE_DEVICE void rows_dot(const void* r0, ptrdiff_t rs, const void* s0, ptrdiff_t
             }
           }
         }
-        continue;
-      }
-      // four rows, or e2m1: every token's 8 activations once, each row's
-      // 8 weights once per 8
+      } else {
+        // four rows, or e2m1: every token's 8 activations once, each row's
+        // 8 weights once per 8
 #pragma unroll
-      for (int p = 0; p < kPer; p += 8) {
-        float a[MT][8];
+        for (int p = 0; p < kPer; p += 8) {
+          float a[MT][8];
 #pragma unroll
-        for (int j = 0; j < MT; ++j)
-          if (j < m) act(j, kPer * v + p, a[j]);
+          for (int j = 0; j < MT; ++j)
+            if (j < m) act(j, kPer * v + p, a[j]);
 #pragma unroll
-        for (int i = 0; i < NR; ++i) {
-          if (i < nr) {
-            float w[8];
-            weights8<WQ>(vv[i][q], p / 8, sc[i], w);
+          for (int i = 0; i < NR; ++i) {
+            if (i < nr) {
+              float w[8];
+              weights8<WQ>(vv[i][q], p / 8, sc[i], w);
 #pragma unroll
-            for (int j = 0; j < MT; ++j) {
-              if (j < m) {
+              for (int j = 0; j < MT; ++j) {
+                if (j < m) {
 #pragma unroll
-                for (int c = 0; c < 8; ++c) acc[i][j] = fmaf(w[c], a[j][c], acc[i][j]);
+                  for (int c = 0; c < 8; ++c) acc[i][j] = fmaf(w[c], a[j][c], acc[i][j]);
+                }
               }
             }
           }
